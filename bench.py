@@ -1,0 +1,432 @@
+"""Benchmark of the GatedDeltaNet layer on GB300.
+
+One step = one ``gdn_prefill`` call over the single-sequence workload
+(T = 4096 tokens, H_qk = 16, H_v = 32, d_k = d_v = 128, bf16 streams, fp32
+state, final state returned), inputs resident in HBM, L2 flushed between
+steps.  Prints one JSON line.  Also measured, in ``extra``: the 32768-token
+varlen prefill, the 131072-token long prefill and the 256-sequence decode
+step, each with its roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its
+own GPU (sequences are independent: no data-path collective), the per-step
+time is the max over ranks and ``value`` counts the tokens of all ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(rank 0 only), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gateddeltanet_layer_gb300 import synth  # noqa: E402
+
+METRIC = "GatedDeltaNet prefill tokens/s & decode seqs/s on 1 GB300; % of roofline"
+BYTES_PER_TOKEN = 32896          # q 4096 + k 4096 + v 8192 + z 8192 + a 64 + b 64 + out 8192 (bf16)
+STATE_BYTES = 32 * 128 * 128 * 4  # one sequence's fp32 state, all 32 value heads
+FLOPS_PER_TOKEN = 32 * (10 * 64 * 128 + 6 * 128 * 128)
+DECODE_BYTES_PER_SEQ = 2 * STATE_BYTES + 32896 + 2 * 8192 * 3 * 2
+DECODE_FLOPS_PER_SEQ = 32 * 6 * 128 * 128
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def prefill_work(cfg) -> tuple[int, float]:
+    """Algorithmic bytes and flops of one prefill call (streams, states, no intermediates)."""
+    nbytes = cfg.T * BYTES_PER_TOKEN + cfg.N * STATE_BYTES  # final state written
+    if cfg.init_std > 0:
+        nbytes += cfg.N * STATE_BYTES                        # initial state read
+    return nbytes, float(cfg.T) * FLOPS_PER_TOKEN
+
+
+# ---------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi SM clock / throttle reasons sampled every 200 ms during a timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------- GPU arm
+def _device_inputs(inp, dev):
+    import torch
+    t = {}
+    for key in ("x_q", "x_k", "x_v", "z", "a", "b"):
+        t[key] = torch.from_numpy(inp[key]).to(dev).to(torch.bfloat16)
+    for key in ("conv_w", "A_log", "dt_bias", "norm_w"):
+        t[key] = torch.from_numpy(inp[key]).to(dev)
+    t["cu_seqlens"] = torch.from_numpy(inp["cu_seqlens"]).to(dev)
+    t["init_state"] = None if inp.get("init_state") is None else torch.from_numpy(inp["init_state"]).to(dev)
+    return t
+
+
+def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False):
+    """Per-step device time (CUDA events on the launching stream, L2 flushed
+    between steps) of one gdn_prefill call; optionally the end-to-end time with
+    pinned-host inputs copied in and outputs copied out every step."""
+    import torch
+
+    import gateddeltanet_layer_gb300 as gdn
+    inp = synth.make_prefill(cfg)
+    t = _device_inputs(inp, dev)
+    T, N = cfg.T, cfg.N
+    out = torch.empty((T, cfg.h_v, cfg.d_v), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((N, cfg.h_v, cfg.d_k, cfg.d_v), dtype=torch.float32, device=dev)
+    ws = torch.zeros(gdn.prefill_workspace_bytes(T, N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v, True),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        gdn.prefill(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                    t["dt_bias"], t["norm_w"], t["cu_seqlens"], t["init_state"], out=out, final_state=fs,
+                    workspace=ws, stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        call()
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = [s.elapsed_time(e) for s, e in ev]
+    status = gdn.workspace_status(ws, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed prefill")
+    res = {"ms": ms}
+    if with_e2e:
+        res["e2e"] = _prefill_e2e(t, cfg, steps, warmup, dev, flush, out, fs, ws, stream)
+    del t
+    return res
+
+
+def _prefill_e2e(t, cfg, steps, warmup, dev, flush, out, fs, ws, stream):
+    import torch
+
+    import gateddeltanet_layer_gb300 as gdn
+    keys = ["x_q", "x_k", "x_v", "z", "a", "b", "cu_seqlens"] + (["init_state"] if t["init_state"] is not None else [])
+    host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in keys}
+    for k in keys:
+        host[k].copy_(t[k])
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    fs_h = torch.empty(fs.shape, dtype=fs.dtype, pin_memory=True)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * fs_h.element_size()
+
+    def step():
+        for k in keys:
+            t[k].copy_(host[k], non_blocking=True)
+        gdn.prefill(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                    t["dt_bias"], t["norm_w"], t["cu_seqlens"], t["init_state"], out=out, final_state=fs,
+                    workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        fs_h.copy_(fs, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        step()
+        e.record(stream)
+        e.synchronize()
+        ms.append(s.elapsed_time(e))
+    return {"ms": statistics.mean(ms), "h2d": h2d, "d2h": d2h}
+
+
+def time_decode(cfg, steps, warmup, dev, flush):
+    import torch
+
+    import gateddeltanet_layer_gb300 as gdn
+    inp = synth.make_decode(cfg)
+    t = {}
+    for key in ("x_q", "x_k", "x_v", "z", "a", "b", "conv_state"):
+        t[key] = torch.from_numpy(inp[key]).to(dev).to(torch.bfloat16)
+    for key in ("conv_w", "A_log", "dt_bias", "norm_w", "state"):
+        t[key] = torch.from_numpy(inp[key]).to(dev)
+    out = torch.empty((cfg.batch, cfg.h_v, cfg.d_v), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        gdn.decode_step(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                        t["dt_bias"], t["norm_w"], t["conv_state"], t["state"], out=out, stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        ms.append(s.elapsed_time(e))
+    return {"ms": ms}
+
+
+def roofline_of(nbytes, flops, ms, pk, peak_key="hbm_gbs"):
+    t = ms * 1e-3
+    gbs = nbytes / t / 1e9
+    tfl = flops / t / 1e12
+    t_roof = max(nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+    return {"achieved_gbs": gbs, "achieved_tflops": tfl, "roofline_frac": t_roof / t,
+            "hbm_frac": gbs / pk["hbm_gbs"]}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import gateddeltanet_layer_gb300 as gdn
+    gdn.library()
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    cfg = synth.SINGLE_4K
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- the headline: T=4096 prefill
+    barrier()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = time.perf_counter()
+        res = time_prefill(cfg, args.steps, args.warmup, dev, flush, with_e2e=True)
+        barrier()
+        wall = time.perf_counter() - t0
+    ms = statistics.mean(res["ms"])
+    e2e_ms = res["e2e"]["ms"]
+    if world > 1:
+        tt = torch.tensor([ms, e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(tt[0]), float(tt[1])
+    nbytes, flops = prefill_work(cfg)
+    rf = roofline_of(nbytes, flops, ms, pk)
+
+    extra = {}
+    if not args.quick:
+        for c in (synth.VARLEN_32K, synth.LONG_128K):
+            r = time_prefill(c, max(3, args.steps // 4), args.warmup, dev, flush)
+            m = statistics.mean(r["ms"])
+            b_, f_ = prefill_work(c)
+            extra[c.name] = {"tokens_per_s": c.T / (m * 1e-3), "ms": m, **roofline_of(b_, f_, m, pk)}
+        dc = synth.DECODE_256
+        r = time_decode(dc, args.steps, args.warmup, dev, flush)
+        m = statistics.mean(r["ms"])
+        extra[dc.name] = {"seqs_per_s": dc.batch / (m * 1e-3), "ms": m,
+                          **roofline_of(dc.batch * DECODE_BYTES_PER_SEQ, dc.batch * DECODE_FLOPS_PER_SEQ, m, pk)}
+    if rank != 0:
+        return
+    cpu = cpu_baseline(cfg, args)
+    line = {
+        "metric": METRIC,
+        "value": world * cfg.T / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; distributions of the workload definitions)",
+        "config": {"workload": cfg.name, "tokens": cfg.T, "seqs": cfg.N, "h_qk": cfg.h_qk, "h_v": cfg.h_v,
+                   "d_k": cfg.d_k, "d_v": cfg.d_v, "state": "fp32", "final_state": True,
+                   "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": rf["achieved_gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": rf["achieved_gbs"] / pk["hbm_gbs"], "traffic": None,
+                     "peak_source": pk["source"], "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                     "kernel": "gdn_prefill (all launches of one call)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * cfg.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"]},
+        "gpu_launches": args.steps * LAUNCHES_PER_PREFILL,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+        "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+LAUNCHES_PER_PREFILL = 1
+
+
+# ---------------------------------------------------------------------- CPU oracle
+def cpu_baseline(cfg, args, budget_chains=None):
+    """The fp64 oracle, as it is, on the host cores: a bounded sample of the
+    workload's (sequence, head) chains, scaled to tokens/s of the whole layer."""
+    from oracle import oracle as ref
+    cores = os.cpu_count() or 1
+    inp = synth.make_prefill(cfg)
+    n_chains = budget_chains or min(cfg.h_v * cfg.N, max(cores, 8))
+    chains = [(0, h) for h in range(n_chains)]
+    t0 = time.perf_counter()
+    ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], chains=chains, threads=cores)
+    dt = time.perf_counter() - t0
+    tokens_equiv = cfg.T * n_chains / cfg.h_v
+    return {"value": tokens_equiv / dt, "unit": "tokens/s", "cores": min(cores, n_chains), "kind": "oracle",
+            "sample": f"{n_chains} of {cfg.h_v * cfg.N} (sequence, head) chains of {cfg.name}, all {cfg.T} tokens "
+                      f"each, {dt:.2f} s wall"}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = synth.SINGLE_4K
+    from oracle import oracle as ref
+    ref.build()
+    cores = os.cpu_count() or 1
+    inp = synth.make_prefill(cfg)
+    n_chains = min(cfg.h_v, cores)
+    chains = [(0, h) for h in range(n_chains)]
+    for _ in range(min(args.warmup, 1)):
+        ref.prefill(inp, inp["cu_seqlens"], chains=chains[:1], threads=1)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        ref.prefill(inp, inp["cu_seqlens"], chains=chains, threads=cores)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    value = cfg.T * n_chains / cfg.h_v / dt
+    sample = f"{n_chains} of {cfg.h_v} (sequence, head) chains of {cfg.name} per step, all {cfg.T} tokens each"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 * cfg.h_v / n_chains,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": cfg.name, "tokens": cfg.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, n_chains), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_case(args):
+    """Only the GPU call of one workload (warm-up + steps), for profilers."""
+    import torch
+
+    import gateddeltanet_layer_gb300 as gdn
+    gdn.library()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    cfg = synth.CONFIGS[args.case]
+    if isinstance(cfg, synth.DecodeConfig):
+        r = time_decode(cfg, args.steps, args.warmup, dev, flush)
+    else:
+        r = time_prefill(cfg, args.steps, args.warmup, dev, flush)
+    print(json.dumps({"case": args.case, "ms": r["ms"]}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--case", choices=sorted(synth.CONFIGS), help="run only this workload's GPU call")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,193 @@
-"""GatedDeltaNet layer on GB300 (placeholder; binding added with the C-ABI)."""
+"""GatedDeltaNet layer on GB300: thin Python binding of the C-ABI library.
+
+Every step of the layer runs in the CUDA kernels of ``libgdn.so``; this module
+only marshals torch tensors (device memory) and the current CUDA stream into
+the C entry points of ``include/gdn.h`` under the same names.  There is no
+Python or CPU implementation of the layer here: if ``libgdn.so`` is missing or
+fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["prefill", "decode_step", "prefill_workspace_bytes", "workspace_status", "library",
+           "GdnError", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+GDN_BF16, GDN_FP32 = 0, 1
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE",
+          4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_CHECK", 6: "GDN_ERR_TIMEOUT"}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("h_qk", ctypes.c_int32),
+                ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("io_dtype", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def library() -> ctypes.CDLL:
+    """Load libgdn.so (built by ``gateddeltanet_layer_gb300.build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is not built: run `python -m gateddeltanet_layer_gb300.build` "
+                                  "(nvcc, sm_103a); there is no fallback implementation")
+            lib = ctypes.CDLL(LIB_PATH)
+            dp = ctypes.POINTER(Dims)
+            lib.gdn_prefill_workspace_bytes.argtypes = [dp]
+            lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+            lib.gdn_prefill.argtypes = [dp] + [_vp] * 15 + [ctypes.c_size_t, _vp]
+            lib.gdn_prefill.restype = ctypes.c_int
+            lib.gdn_decode_step.argtypes = [dp] + [_vp] * 14
+            lib.gdn_decode_step.restype = ctypes.c_int
+            lib.gdn_workspace_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
+            lib.gdn_workspace_status.restype = ctypes.c_int
+            lib.gdn_status_string.argtypes = [ctypes.c_int]
+            lib.gdn_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = library().gdn_status_string(status).decode()
+        raise GdnError(status, f"{what}: {msg}")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _io_dtype(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_FP32
+    raise TypeError(f"unsupported stream dtype {t.dtype} (bf16 or fp32)")
+
+
+def _req(t, name, dtype=None, cuda=True):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def dims_of(q, v, num_seqs: int) -> Dims:
+    T, h_qk, d_k = q.shape
+    _, h_v, d_v = v.shape
+    return Dims(T, num_seqs, h_qk, h_v, d_k, d_v, _io_dtype(q))
+
+
+def prefill_workspace_bytes(T: int, N: int, h_qk: int, h_v: int, d_k: int, d_v: int, bf16: bool = True) -> int:
+    d = Dims(T, N, h_qk, h_v, d_k, d_v, GDN_BF16 if bf16 else GDN_FP32)
+    return int(library().gdn_prefill_workspace_bytes(ctypes.byref(d)))
+
+
+def prefill(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state=None, *,
+            out=None, final_state=None, return_final_state=True, workspace=None, stream=None):
+    """``gdn_prefill``: the layer over packed sequences.
+
+    q, k [T, h_qk, d_k]; v, z [T, h_v, d_v]; a, b [T, h_v] (bf16 or fp32, one
+    dtype); conv_w [Cc, 4], A_log, dt_bias [h_v], norm_w [d_v] fp32;
+    cu_seqlens int32 [N+1]; init_state fp32 [N, h_v, d_k, d_v] or None.
+    Returns (out [T, h_v, d_v], final_state or None).
+    """
+    torch = _torch()
+    lib = library()
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("z", z)):
+        _req(t, name, dt)
+    for name, t in (("conv_w", conv_w), ("A_log", A_log), ("dt_bias", dt_bias), ("norm_w", norm_w)):
+        _req(t, name, torch.float32)
+    _req(cu_seqlens, "cu_seqlens", torch.int32)
+    N = cu_seqlens.numel() - 1
+    d = dims_of(q, v, N)
+    T, h_v, d_v = v.shape
+    if init_state is not None:
+        _req(init_state, "init_state", torch.float32)
+    if out is None:
+        out = torch.empty((T, h_v, d_v), dtype=dt, device=q.device)
+    _req(out, "out", dt)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((N, h_v, d.d_k, d_v), dtype=torch.float32, device=q.device)
+    if final_state is not None:
+        _req(final_state, "final_state", torch.float32)
+    ws_bytes = 0
+    if workspace is not None:
+        _req(workspace, "workspace", torch.uint8)
+        ws_bytes = workspace.numel()
+    st = lib.gdn_prefill(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(conv_w),
+                         _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(cu_seqlens), _ptr(init_state),
+                         _ptr(out), _ptr(final_state), _ptr(workspace), ws_bytes,
+                         _stream_handle(stream, q.device))
+    _check(st, "gdn_prefill")
+    return out, final_state
+
+
+def decode_step(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, conv_state, state, *, out=None,
+                stream=None):
+    """``gdn_decode_step``: one token per sequence; updates ``state`` (fp32
+    [B, h_v, d_k, d_v]) and ``conv_state`` ([B, Cc, 3], stream dtype) in place.
+    Returns out [B, h_v, d_v]."""
+    torch = _torch()
+    lib = library()
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("z", z), ("conv_state", conv_state)):
+        _req(t, name, dt)
+    for name, t in (("conv_w", conv_w), ("A_log", A_log), ("dt_bias", dt_bias), ("norm_w", norm_w),
+                    ("state", state)):
+        _req(t, name, torch.float32)
+    d = dims_of(q, v, 1)
+    B, h_v, d_v = v.shape
+    if out is None:
+        out = torch.empty((B, h_v, d_v), dtype=dt, device=q.device)
+    _req(out, "out", dt)
+    st = lib.gdn_decode_step(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z),
+                             _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(conv_state),
+                             _ptr(state), _ptr(out), _stream_handle(stream, q.device))
+    _check(st, "gdn_decode_step")
+    return out
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """Read and clear the device status word of a prefill workspace (synchronises the stream)."""
+    lib = library()
+    res = ctypes.c_int(0)
+    _check(lib.gdn_workspace_status(_ptr(workspace), _stream_handle(stream, workspace.device),
+                                    ctypes.byref(res)), "gdn_workspace_status")
+    return res.value

@@ -1,0 +1,197 @@
+// Decode step: one token per sequence against a carried fp32 state.
+//
+// The step is a pure stream over the state (4 MiB read + 4 MiB written per
+// 32-head sequence at d = 128): per value head it needs p = H^T k and
+// s = H^T q from one read pass, then u = beta (v - alpha p),
+// o = scale (alpha s + (k . q) u) (equal to (alpha H + k u^T)^T q * scale), and
+// writes H <- alpha H + k u^T back in place.
+//
+// One CTA per (sequence, query/key head): the CTA owns the conv-cache channels
+// of that q/k head and of its h_v / h_qk value heads, so no two CTAs touch
+// the same cache entry.  Thread layout per value head: warp w owns rows
+// [w*R, (w+1)*R) of H (R = d_k / 8), lane l owns columns [4l, 4l+4); each
+// thread keeps its R x 4 block in registers between the read and the write.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxRows = 16;  // d_k / kWarps for d_k <= 128
+
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
+  const int h_qk = p.h_qk, h_v = p.h_v, dk = p.d_k, dv = p.d_v;
+  const int rep = h_v / h_qk;
+  const int b = blockIdx.x / h_qk;
+  const int hq = blockIdx.x % h_qk;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Cc = 2 * h_qk * dk + h_v * dv;
+
+  const IO *__restrict__ xq = static_cast<const IO *>(p.q);
+  const IO *__restrict__ xk = static_cast<const IO *>(p.k);
+  const IO *__restrict__ xv = static_cast<const IO *>(p.v);
+  const IO *__restrict__ xa = static_cast<const IO *>(p.a);
+  const IO *__restrict__ xb = static_cast<const IO *>(p.b);
+  const IO *__restrict__ xz = static_cast<const IO *>(p.z);
+  IO *__restrict__ cache = static_cast<IO *>(p.conv_state);
+  IO *__restrict__ out = static_cast<IO *>(p.out);
+
+  __shared__ float sq[128], sk[128], sv[128], su[128], so[128];
+  __shared__ float red_p[kWarps][128], red_s[kWarps][128];
+  __shared__ float sred[kWarps];
+  __shared__ float s_kq, s_alpha, s_beta, s_inv;
+
+  // conv with the cache + SiLU for the q and k channels of this head
+  for (int c = tid; c < 2 * dk; c += kThreads) {
+    const bool isq = c < dk;
+    const int i = isq ? c : c - dk;
+    const int ch = (isq ? 0 : h_qk * dk) + hq * dk + i;
+    const float x = to_f((isq ? xq : xk)[((size_t)b * h_qk + hq) * dk + i]);
+    IO *cc = cache + ((size_t)b * Cc + ch) * 3;
+    const float c0 = to_f(cc[0]), c1 = to_f(cc[1]), c2 = to_f(cc[2]);
+    const float *w = p.conv_w + (size_t)ch * 4;
+    const float pre = fmaf(w[0], c0, fmaf(w[1], c1, fmaf(w[2], c2, w[3] * x)));
+    cc[0] = cc[1];
+    cc[1] = cc[2];
+    cc[2] = (isq ? xq : xk)[((size_t)b * h_qk + hq) * dk + i];
+    (isq ? sq : sk)[i] = silu_f(pre);
+  }
+  __syncthreads();
+  // L2 norms of q, k and their dot product
+  if (warp < 2) {
+    float *x = warp == 0 ? sq : sk;
+    float ss = 0.0f;
+    for (int i = lane; i < dk; i += 32) ss = fmaf(x[i], x[i], ss);
+    const float inv = rsqrtf(warp_sum(ss) + kEpsL2);
+    for (int i = lane; i < dk; i += 32) x[i] *= inv;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float s = 0.0f;
+    for (int i = lane; i < dk; i += 32) s = fmaf(sq[i], sk[i], s);
+    s = warp_sum(s);
+    if (lane == 0) s_kq = s;
+  }
+
+  const int rows = (dk + kWarps - 1) / kWarps;
+  const int i0 = warp * rows;
+  const int j0 = lane * 4;
+  const bool col_ok = j0 < dv;
+  const float scale = rsqrtf((float)dk);
+
+  for (int vv = 0; vv < rep; ++vv) {
+    const int h = hq * rep + vv;
+    float *Hg = p.state + ((size_t)b * h_v + h) * dk * dv;
+    // issue the state loads first: they are the stream this kernel exists for
+    float4 Hr[kMaxRows];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      const int i = i0 + r;
+      Hr[r] = (r < rows && i < dk && col_ok) ? *reinterpret_cast<const float4 *>(Hg + (size_t)i * dv + j0)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // conv + SiLU of this head's v channels; gates
+    for (int j = tid; j < dv; j += kThreads) {
+      const int ch = 2 * h_qk * dk + h * dv + j;
+      const size_t xi = ((size_t)b * h_v + h) * dv + j;
+      const float x = to_f(xv[xi]);
+      IO *cc = cache + ((size_t)b * Cc + ch) * 3;
+      const float c0 = to_f(cc[0]), c1 = to_f(cc[1]), c2 = to_f(cc[2]);
+      const float *w = p.conv_w + (size_t)ch * 4;
+      const float pre = fmaf(w[0], c0, fmaf(w[1], c1, fmaf(w[2], c2, w[3] * x)));
+      cc[0] = cc[1];
+      cc[1] = cc[2];
+      cc[2] = xv[xi];
+      sv[j] = silu_f(pre);
+    }
+    if (tid == 0) {
+      const size_t gi = (size_t)b * h_v + h;
+      s_alpha = expf(gate_g(to_f(xa[gi]), expf(p.A_log[h]), p.dt_bias[h]));
+      s_beta = sigmoid_f(to_f(xb[gi]));
+    }
+    __syncthreads();
+    // partial H^T k and H^T q over this warp's rows
+    float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      if (r < rows && i0 + r < dk) {
+        const float kv = sk[i0 + r], qv = sq[i0 + r];
+        pk[0] = fmaf(Hr[r].x, kv, pk[0]); pk[1] = fmaf(Hr[r].y, kv, pk[1]);
+        pk[2] = fmaf(Hr[r].z, kv, pk[2]); pk[3] = fmaf(Hr[r].w, kv, pk[3]);
+        pq[0] = fmaf(Hr[r].x, qv, pq[0]); pq[1] = fmaf(Hr[r].y, qv, pq[1]);
+        pq[2] = fmaf(Hr[r].z, qv, pq[2]); pq[3] = fmaf(Hr[r].w, qv, pq[3]);
+      }
+    }
+    if (col_ok) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        red_p[warp][j0 + c] = pk[c];
+        red_s[warp][j0 + c] = pq[c];
+      }
+    }
+    __syncthreads();
+    const float al = s_alpha, be = s_beta;
+    float o_j = 0.0f;
+    if (tid < dv) {
+      float pj = 0.f, sj = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        pj += red_p[w][tid];
+        sj += red_s[w][tid];
+      }
+      const float u = be * (sv[tid] - al * pj);
+      su[tid] = u;
+      o_j = scale * fmaf(al, sj, s_kq * u);
+      so[tid] = o_j;
+    }
+    // RMSNormGated needs sum_j o_j^2
+    float ss = warp_sum(tid < dv ? o_j * o_j : 0.0f);
+    if (lane == 0) sred[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < kWarps; ++w) t += sred[w];
+      s_inv = rsqrtf(t / (float)dv + kEpsRms);
+    }
+    __syncthreads();
+    if (tid < dv) {
+      const size_t oi = ((size_t)b * h_v + h) * dv + tid;
+      out[oi] = from_f<IO>(so[tid] * s_inv * p.norm_w[tid] * silu_f(to_f(xz[oi])));
+    }
+    // H <- alpha H + k u^T, written back in place
+    if (col_ok) {
+      const float u0 = su[j0], u1 = su[j0 + 1], u2 = su[j0 + 2], u3 = su[j0 + 3];
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        const int i = i0 + r;
+        if (r < rows && i < dk) {
+          const float kv = sk[i];
+          float4 hn;
+          hn.x = fmaf(kv, u0, al * Hr[r].x);
+          hn.y = fmaf(kv, u1, al * Hr[r].y);
+          hn.z = fmaf(kv, u2, al * Hr[r].z);
+          hn.w = fmaf(kv, u3, al * Hr[r].w);
+          *reinterpret_cast<float4 *>(Hg + (size_t)i * dv + j0) = hn;
+        }
+      }
+    }
+    __syncthreads();  // sv, su, so, red_* are reused by the next value head
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s) {
+  const unsigned grid = (unsigned)p.B * (unsigned)p.h_qk;
+  if (grid == 0) return cudaSuccess;
+  if (bf16)
+    decode_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(p);
+  else
+    decode_kernel<float><<<grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

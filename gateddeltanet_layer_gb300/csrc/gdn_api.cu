@@ -1,0 +1,129 @@
+// C ABI of the GatedDeltaNet layer library: argument validation and dispatch.
+// Everything here runs on the host and only enqueues work; the layer itself
+// is computed by the kernels in this directory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;  // status word, padded to keep what follows aligned
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
+
+// Checks shared by prefill and decode.  Returns GDN_OK or a status.
+int check_dims(const gdn_dims *d) {
+  if (!d) return GDN_ERR_INVALID_ARG;
+  if (d->num_tokens < 0 || d->h_qk <= 0 || d->h_v <= 0 || d->d_k <= 0 || d->d_v <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (d->h_v % d->h_qk != 0) return GDN_ERR_INVALID_ARG;
+  if (d->io_dtype != GDN_BF16 && d->io_dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+  if (!head_dim_ok(d->d_k) || !head_dim_ok(d->d_v)) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+bool use_tensor_core_prefill(const gdn_dims *) { return false; }
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_prefill_workspace_bytes(const gdn_dims *d) {
+  if (check_dims(d) != GDN_OK || d->num_seqs <= 0) return 0;
+  size_t bytes = kStatusBytes;
+  return bytes;
+}
+
+int gdn_prefill(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
+                const void *b, const void *z, const float *conv_w, const float *A_log,
+                const float *dt_bias, const float *norm_w, const int32_t *cu_seqlens,
+                const float *init_state, void *out, float *final_state, void *workspace,
+                size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (d->num_seqs <= 0) return GDN_ERR_INVALID_ARG;
+  if (!conv_w || !A_log || !dt_bias || !norm_w || !cu_seqlens) return GDN_ERR_INVALID_ARG;
+  if (d->num_tokens > 0 && (!q || !k || !v || !a || !b || !z || !out)) return GDN_ERR_INVALID_ARG;
+  const void *streams[] = {q, k, v, a, b, z, out, init_state, final_state, conv_w};
+  for (const void *p : streams)
+    if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_prefill_workspace_bytes(d);
+  if (workspace && (ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GDN_ERR_WORKSPACE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void *ws = workspace;
+  bool owned = false;
+  if (!ws) {
+    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return GDN_ERR_CUDA;
+    owned = true;
+  }
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return GDN_ERR_CUDA;
+
+  gdn::PrefillParams p{};
+  p.T = d->num_tokens; p.N = d->num_seqs; p.h_qk = d->h_qk; p.h_v = d->h_v;
+  p.d_k = d->d_k; p.d_v = d->d_v;
+  p.q = q; p.k = k; p.v = v; p.a = a; p.b = b; p.z = z;
+  p.conv_w = conv_w; p.A_log = A_log; p.dt_bias = dt_bias; p.norm_w = norm_w;
+  p.cu_seqlens = cu_seqlens; p.init_state = init_state; p.out = out; p.final_state = final_state;
+  p.status = static_cast<int *>(ws);
+  p.ws = static_cast<uint8_t *>(ws) + kStatusBytes;
+  p.ws_bytes = need - kStatusBytes;
+
+  cudaError_t e;
+  e = gdn::launch_prefill_simt(p, d->io_dtype == GDN_BF16, s);
+  if (owned) cudaFreeAsync(ws, s);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_decode_step(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
+                    const void *b, const void *z, const float *conv_w, const float *A_log,
+                    const float *dt_bias, const float *norm_w, void *conv_state, float *state,
+                    void *out, void *stream) {
+  int st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (!conv_w || !A_log || !dt_bias || !norm_w) return GDN_ERR_INVALID_ARG;
+  if (d->num_tokens > 0 && (!q || !k || !v || !a || !b || !z || !out || !conv_state || !state))
+    return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, a, b, z, out, state, conv_w};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
+  gdn::DecodeParams p{};
+  p.B = d->num_tokens; p.h_qk = d->h_qk; p.h_v = d->h_v; p.d_k = d->d_k; p.d_v = d->d_v;
+  p.q = q; p.k = k; p.v = v; p.a = a; p.b = b; p.z = z;
+  p.conv_w = conv_w; p.A_log = A_log; p.dt_bias = dt_bias; p.norm_w = norm_w;
+  p.conv_state = conv_state; p.state = state; p.out = out;
+  cudaError_t e = gdn::launch_decode(p, d->io_dtype == GDN_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_workspace_status(void *workspace, void *stream, int *device_status) {
+  if (!workspace || !device_status) return GDN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  *device_status = host;
+  return GDN_OK;
+}
+
+const char *gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: unsupported shape or dtype";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace too small or misaligned";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA runtime or launch failure";
+    case GDN_ERR_DEVICE_CHECK: return "GDN_ERR_DEVICE_CHECK: device-side validation failed (cu_seqlens)";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait ran out";
+    default: return "GDN_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

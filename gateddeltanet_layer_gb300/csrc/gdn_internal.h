@@ -1,0 +1,39 @@
+// Internal launch interface between the C ABI (gdn_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct PrefillParams {
+  int T, N, h_qk, h_v, d_k, d_v;
+  const void *q, *k, *v, *a, *b, *z;
+  const float *conv_w, *A_log, *dt_bias, *norm_w;
+  const int32_t *cu_seqlens;
+  const float *init_state;
+  void *out;
+  float *final_state;
+  int *status;       // device status word (workspace), may be null
+  uint8_t *ws;       // workspace base (256-byte aligned)
+  size_t ws_bytes;
+};
+
+struct DecodeParams {
+  int B, h_qk, h_v, d_k, d_v;
+  const void *q, *k, *v, *a, *b, *z;
+  const float *conv_w, *A_log, *dt_bias, *norm_w;
+  void *conv_state;
+  float *state;
+  void *out;
+};
+
+// Token-sequential fp32 prefill (any supported shape, bf16 or fp32 streams).
+cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t s);
+// Chunked tensor-core prefill (bf16 streams, d_k = d_v = 128).
+cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
+size_t prefill_tc_workspace_bytes(int N, int h_v);
+// Decode step.
+cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s);
+
+}  // namespace gdn

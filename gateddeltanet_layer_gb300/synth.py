@@ -25,10 +25,12 @@ import numpy as np
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
     """Round fp32 values to the nearest bf16 (ties to even); returns fp32."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    x = np.array(x, dtype=np.float32, copy=True, order="C")
+    u = x.view(np.uint32)
+    # finite inputs: u + 0x8000 <= 0xFF807FFF, so 32-bit arithmetic cannot wrap
+    u += np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    u &= np.uint32(0xFFFF0000)
+    return x
 
 
 @dataclass(frozen=True)

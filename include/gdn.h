@@ -1,0 +1,158 @@
+/*
+ * gdn.h -- C ABI of the GatedDeltaNet layer library (libgdn.so), GB300 / sm_103a.
+ *
+ * The library computes one GatedDeltaNet linear-attention layer of a hybrid
+ * Qwen3.5 decoder from its post-projection streams to the gated-normed output:
+ * the "GatedDeltaNet" module with its "RMSNormGated" output norm, its
+ * depthwise conv1d and softplus gate ("[Qwen3.5 MoE] Add hybrid decoder model
+ * (GatedDeltaNet + full attention + MoE)", Summary: model.py and
+ * parallelize.py bullets), over packed variable-length sequences described by
+ * cu_seqlens ("Support Qwen35 SFT", XTuner changes: GatedDeltaNet in varlen
+ * mode; "feat(models): dense Qwen3.5 custom attention", Summary: varlen
+ * cu_seqlens, one packed row).  The pages name these pieces without formulas;
+ * the library computes, per sequence n and value head h (query/key head
+ * h' = h / (h_v / h_qk)), the gated delta rule of Yang et al., "Gated Delta
+ * Networks" (ICLR 2025):
+ *
+ *   x^  = silu(conv1d_4(x)) for x in {q, k, v}   causal depthwise, width 4,
+ *         conv_w[c][3] multiplies the current token, no bias, zero history at
+ *         each sequence start (prefill) or the carried cache (decode)
+ *   q^, k^ <- x / sqrt(sum x^2 + 1e-6)
+ *   g_t = -exp(A_log[h]) softplus(a_t + dt_bias[h]),  beta_t = sigmoid(b_t)
+ *   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *   o_t = S_t q_t / sqrt(d_k)
+ *   y_t = o_t / sqrt(mean(o_t^2) + 1e-6) * norm_w * silu(z_t)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensors are dense, row-major, token-major, caller-owned DEVICE memory
+ *    on the current CUDA device; the library keeps no pointer after a call
+ *    returns.  Stream tensors start on a 16-byte boundary.
+ *  - Streams (dtype = io_dtype): q, k [T, h_qk, d_k]; v, z, out [T, h_v, d_v];
+ *    a, b [T, h_v].  Parameters (always fp32): conv_w [Cc, 4] with
+ *    Cc = 2 h_qk d_k + h_v d_v, channels ordered [q heads | k heads | v heads],
+ *    each head-major then dim; A_log, dt_bias [h_v]; norm_w [d_v] (shared by
+ *    all heads).
+ *  - States (fp32): [N, h_v, d_k, d_v]; element [n][h][i][j] = S[j][i], i over
+ *    d_k, j over d_v.
+ *  - Supported shapes: 1 <= h_qk, h_v % h_qk == 0; d_k, d_v multiples of 16 in
+ *    [16, 128].  The tensor-core prefill runs bf16 streams with
+ *    d_k = d_v = 128; every other supported shape runs a token-sequential fp32
+ *    kernel.  Anything else returns GDN_ERR_UNSUPPORTED.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *    asynchronous: they enqueue kernels and return without synchronising.
+ *  - Errors.  Invalid arguments (NULL required pointer, non-positive size,
+ *    misalignment, h_v not a multiple of h_qk, short workspace) return a status
+ *    before anything is launched.  A failed launch returns GDN_ERR_CUDA.
+ *    Problems only the device can see (cu_seqlens not non-decreasing within
+ *    [0, T]; a bounded wait inside a kernel running out) are recorded in the
+ *    workspace's status word and read back with gdn_workspace_status().  No
+ *    entry point aborts, throws or traps.
+ *  - Thread safety: entry points hold no global state and may be called from
+ *    several host threads at once (with distinct workspaces).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,  /* NULL / non-positive / misaligned / inconsistent argument */
+  GDN_ERR_UNSUPPORTED = 2,  /* valid but unsupported shape or dtype */
+  GDN_ERR_WORKSPACE = 3,    /* workspace given but smaller than gdn_prefill_workspace_bytes() */
+  GDN_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+  GDN_ERR_DEVICE_CHECK = 5, /* device-side validation failed (bad cu_seqlens) */
+  GDN_ERR_TIMEOUT = 6       /* a bounded device-side wait ran out */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
+
+typedef struct {
+  int32_t num_tokens; /* T: packed tokens (prefill) or batch size B (decode)      */
+  int32_t num_seqs;   /* N: sequences in cu_seqlens (prefill); ignored by decode  */
+  int32_t h_qk;       /* query/key heads                                          */
+  int32_t h_v;        /* value heads, a multiple of h_qk                          */
+  int32_t d_k;        /* query/key head dim                                       */
+  int32_t d_v;        /* value head dim                                           */
+  int32_t io_dtype;   /* gdn_dtype of the streams q, k, v, a, b, z, out, conv cache */
+} gdn_dims;
+
+/*
+ * Bytes of device workspace gdn_prefill needs for `dims` (0 if dims is NULL or
+ * invalid).  The workspace holds the device status word and the schedule of
+ * (sequence, head) chains.  It is scratch: its contents need not be preserved
+ * between calls, but a call's status word stays readable until the next call
+ * that uses the same workspace.
+ */
+GDN_API size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
+
+/*
+ * Prefill: run the layer over N packed sequences of T tokens in total.
+ *
+ * cu_seqlens  int32 [N+1] on the device: sequence n owns tokens
+ *             [cu_seqlens[n], cu_seqlens[n+1]); cu_seqlens[0] = 0,
+ *             cu_seqlens[N] = T, non-decreasing (an empty sequence is allowed:
+ *             its final state equals its initial state).
+ * init_state  fp32 [N, h_v, d_k, d_v] or NULL (= zeros).
+ * out         io_dtype [T, h_v, d_v]: y, rounded to nearest (even) for bf16.
+ * final_state fp32 [N, h_v, d_k, d_v] or NULL (= not returned).  It may equal
+ *             init_state (in-place update): each chain reads its state before
+ *             it writes it.
+ * workspace   device scratch of ws_bytes >= gdn_prefill_workspace_bytes(dims)
+ *             bytes, 256-byte aligned; or NULL, in which case the library takes
+ *             and returns stream-ordered memory (cudaMallocAsync /
+ *             cudaFreeAsync) around the launch.
+ * Returns a gdn_status.
+ */
+GDN_API int gdn_prefill(const gdn_dims *dims, const void *q, const void *k, const void *v, const void *a,
+                const void *b, const void *z, const float *conv_w, const float *A_log,
+                const float *dt_bias, const float *norm_w, const int32_t *cu_seqlens,
+                const float *init_state, void *out, float *final_state, void *workspace,
+                size_t ws_bytes, void *stream);
+
+/*
+ * Decode step: one new token for each of B = dims->num_tokens independent
+ * sequences, against a carried state; the state and the conv cache are
+ * updated in place.
+ *
+ * q, k, v, a, b, z  the B new tokens, layouts as above with T = B.
+ * conv_state  io_dtype [B, Cc, 3], in/out: the raw (pre-conv) inputs of the
+ *             three previous tokens of each sequence, oldest first; after the
+ *             call it holds the last three including this token.
+ * state       fp32 [B, h_v, d_k, d_v], in/out.
+ * out         io_dtype [B, h_v, d_v].
+ * Returns a gdn_status.
+ */
+GDN_API int gdn_decode_step(const gdn_dims *dims, const void *q, const void *k, const void *v,
+                    const void *a, const void *b, const void *z, const float *conv_w,
+                    const float *A_log, const float *dt_bias, const float *norm_w,
+                    void *conv_state, float *state, void *out, void *stream);
+
+/*
+ * Read and clear the device status word of a prefill workspace.  Enqueued on
+ * `stream` and waits for it (the one synchronising call of the library).
+ * Writes GDN_OK, GDN_ERR_DEVICE_CHECK or GDN_ERR_TIMEOUT to *device_status
+ * and returns GDN_OK, or returns GDN_ERR_INVALID_ARG / GDN_ERR_CUDA.
+ */
+GDN_API int gdn_workspace_status(void *workspace, void *stream, int *device_status);
+
+/* Human-readable name of a gdn_status (never NULL). */
+GDN_API const char *gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

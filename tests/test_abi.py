@@ -1,0 +1,90 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point that
+include/gdn.h declares, and rejects invalid arguments on the host before
+touching the GPU (so these run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gateddeltanet_layer_gb300 as gdn
+from gateddeltanet_layer_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
+                 "gdn_workspace_status"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in gdn.STATUS.items():
+        assert lib.gdn_status_string(code).decode().startswith(name)
+    assert lib.gdn_status_string(99) == b"GDN_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    assert gdn.prefill_workspace_bytes(4096, 1, 16, 32, 128, 128) >= 256
+    assert gdn.prefill_workspace_bytes(64, 1, 2, 2, 16, 16, bf16=False) >= 256
+    assert gdn.prefill_workspace_bytes(64, 1, 2, 3, 16, 16) == 0        # h_v % h_qk != 0
+    assert gdn.prefill_workspace_bytes(64, 1, 2, 2, 24, 16) == 0        # unsupported head dim
+    assert lib.gdn_prefill_workspace_bytes(None) == 0
+
+
+def _call_prefill(lib, dims, ptr=1 << 20, ws=None, ws_bytes=0, cu=1 << 20):
+    p = ctypes.c_void_p(ptr)
+    return lib.gdn_prefill(None if dims is None else ctypes.byref(dims), p, p, p, p, p, p, p, p, p, p,
+                           ctypes.c_void_p(cu), None, p, None, ws, ws_bytes, None)
+
+
+def test_prefill_rejects_bad_arguments_without_a_gpu(lib):
+    D = gdn.Dims
+    assert _call_prefill(lib, None) == 1
+    assert _call_prefill(lib, D(64, 1, 2, 3, 128, 128, 0)) == 1          # h_v % h_qk
+    assert _call_prefill(lib, D(-1, 1, 2, 2, 128, 128, 0)) == 1          # negative T
+    assert _call_prefill(lib, D(64, 0, 2, 2, 128, 128, 0)) == 1          # no sequences
+    assert _call_prefill(lib, D(64, 1, 2, 2, 128, 128, 7)) == 1          # bad dtype
+    assert _call_prefill(lib, D(64, 1, 2, 2, 96 + 8, 128, 0)) == 2       # unsupported d_k
+    assert _call_prefill(lib, D(64, 1, 2, 2, 128, 128, 0), ptr=(1 << 20) + 2) == 1  # misaligned
+    assert _call_prefill(lib, D(64, 1, 2, 2, 128, 128, 0), cu=0) == 1    # NULL cu_seqlens
+    ws = ctypes.c_void_p(1 << 24)
+    assert _call_prefill(lib, D(64, 1, 2, 2, 128, 128, 0), ws=ws, ws_bytes=8) == 3  # short workspace
+
+
+def test_decode_rejects_bad_arguments_without_a_gpu(lib):
+    D = gdn.Dims
+    p = ctypes.c_void_p(1 << 20)
+    args = [p] * 14
+    assert lib.gdn_decode_step(ctypes.byref(D(4, 1, 2, 3, 128, 128, 0)), *args) == 1
+    assert lib.gdn_decode_step(ctypes.byref(D(4, 1, 2, 2, 100, 128, 0)), *args) == 2
+    bad = list(args)
+    bad[11] = None  # state
+    assert lib.gdn_decode_step(ctypes.byref(D(4, 1, 2, 2, 128, 128, 0)), *bad) == 1
+
+
+def test_library_fails_loudly_when_missing(monkeypatch, tmp_path):
+    """No fallback: a missing libgdn.so raises instead of computing anything."""
+    monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "libgdn.so"))
+    monkeypatch.setattr(gdn, "_lib", None)
+    with pytest.raises(ImportError):
+        gdn.library()

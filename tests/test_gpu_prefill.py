@@ -1,0 +1,138 @@
+"""GPU parity of gdn_prefill against the fp64 oracle.
+
+Small cases run the oracle on every chain; the full-size workloads run the
+whole GPU call exactly as the benchmark launches it and compare the chains the
+oracle computes (sampled (sequence, head) pairs, every token and the final
+state of each).
+"""
+import numpy as np
+import pytest
+
+from gateddeltanet_layer_gb300 import synth
+from oracle import oracle as ref
+from tests.helpers import parity, to_torch
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _gdn():
+    import gateddeltanet_layer_gb300 as gdn
+    gdn.library()
+    return gdn
+
+
+def run_gpu(inp, bf16, *, workspace=None, in_place=False):
+    gdn = _gdn()
+    t = to_torch(inp, bf16)
+    init = t.get("init_state")
+    fs = init if (in_place and init is not None) else None
+    out, fs = gdn.prefill(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                          t["dt_bias"], t["norm_w"], t["cu_seqlens"], init, final_state=fs,
+                          workspace=workspace)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), fs.cpu().numpy()
+
+
+def check(inp, cfg_dtype, chains=None, **kw):
+    bf16 = cfg_dtype == "bf16"
+    y, fs = run_gpu(inp, bf16, **kw)
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], chains=chains)
+    parity(y, r["y"], cfg_dtype, "out")
+    parity(fs, r["final_state"], cfg_dtype, "final_state")
+    return y, fs, r
+
+
+def test_tiny_fp32_config():
+    """T=64, H=2/2, d=16, fp32: every output and the final state within 1e-4."""
+    check(synth.make_prefill(synth.TINY), "fp32")
+
+
+@pytest.mark.parametrize("case", ["ragged_single", "varlen_edges", "long_memory", "gqa4", "fp32_d128"])
+def test_small_cases(case):
+    if case == "ragged_single":      # several chunks plus a ragged tail
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(200,), h_qk=2, h_v=4)
+    elif case == "varlen_edges":     # empty, 1-token, exact-chunk and straddling sequences
+        cfg = synth.scaled(synth.VARLEN_32K, lengths=(64, 1, 0, 130, 63, 65), h_qk=1, h_v=2, seed=3)
+    elif case == "long_memory":      # slow decay: dt_bias = -6 keeps alpha near 1
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(300,), h_qk=1, h_v=2, a_log_range=(1.0, 1.5),
+                           init_std=0.02, seed=5)
+    elif case == "gqa4":             # 4 value heads per q/k head
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(97, 31), h_qk=1, h_v=4, seed=7)
+    else:                            # fp32 streams at d = 128 (token-sequential fp32 kernel)
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(130, 7), h_qk=1, h_v=2, dtype="fp32", init_std=0.02)
+    inp = synth.make_prefill(cfg)
+    if case == "long_memory":
+        inp["dt_bias"][:] = -6.0
+    check(inp, cfg.dtype)
+
+
+def _sample_chains(cfg, picks):
+    return [(n, h) for n, h in picks if n < cfg.N and h < cfg.h_v]
+
+
+@pytest.mark.slow
+def test_full_single_4k():
+    cfg = synth.SINGLE_4K
+    check(synth.make_prefill(cfg), "bf16", chains=_sample_chains(cfg, [(0, 0), (0, 1), (0, 17), (0, 31)]))
+
+
+@pytest.mark.slow
+def test_full_varlen_32k():
+    cfg = synth.VARLEN_32K
+    lengths = np.array(cfg.lengths)
+    longest, shortest = int(lengths.argmax()), int(lengths.argmin())
+    picks = [(longest, 0), (longest, 31), (shortest, 5), (shortest, 6), (cfg.N - 1, 30), (3, 14)]
+    check(synth.make_prefill(cfg), "bf16", chains=_sample_chains(cfg, picks))
+
+
+@pytest.mark.slow
+def test_full_long_128k():
+    cfg = synth.LONG_128K
+    check(synth.make_prefill(cfg), "bf16", chains=_sample_chains(cfg, [(0, 0), (7, 13), (15, 31)]))
+
+
+def test_deterministic_and_workspace_equivalent():
+    """Bitwise-identical results run to run, with and without a caller workspace."""
+    gdn = _gdn()
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=(150, 77), h_qk=2, h_v=4, seed=11)
+    inp = synth.make_prefill(cfg)
+    y1, f1 = run_gpu(inp, True)
+    y2, f2 = run_gpu(inp, True)
+    nbytes = gdn.prefill_workspace_bytes(cfg.T, cfg.N, cfg.h_qk, cfg.h_v, 128, 128, True)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    y3, f3 = run_gpu(inp, True, workspace=ws)
+    assert np.array_equal(y1, y2) and np.array_equal(f1, f2)
+    assert np.array_equal(y1, y3) and np.array_equal(f1, f3)
+    assert gdn.workspace_status(ws) == 0
+
+
+def test_in_place_state_update():
+    """final_state may be the init_state buffer."""
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=(100, 64), h_qk=1, h_v=2, seed=12)
+    inp = synth.make_prefill(cfg)
+    y_a, f_a = run_gpu(inp, True)
+    y_b, f_b = run_gpu(inp, True, in_place=True)
+    assert np.array_equal(y_a, y_b) and np.array_equal(f_a, f_b)
+
+
+def test_bad_cu_seqlens_sets_device_status():
+    """Decreasing cu_seqlens is caught on the device and reported through the workspace."""
+    gdn = _gdn()
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=(64, 64), h_qk=1, h_v=2, seed=13)
+    inp = synth.make_prefill(cfg)
+    inp["cu_seqlens"] = np.array([0, 100, 64], dtype=np.int32)  # sequence 1 has negative length
+    nbytes = gdn.prefill_workspace_bytes(cfg.T, cfg.N, 1, 2, 128, 128, True)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    run_gpu(inp, True, workspace=ws)
+    assert gdn.workspace_status(ws) == 5
+    assert gdn.workspace_status(ws) == 0  # reading clears it
+
+
+def test_invalid_arguments_raise():
+    gdn = _gdn()
+    t = to_torch(synth.make_prefill(synth.scaled(synth.SINGLE_4K, lengths=(8,), h_qk=2, h_v=3)), True)
+    with pytest.raises(gdn.GdnError) as e:   # h_v not a multiple of h_qk
+        gdn.prefill(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                    t["dt_bias"], t["norm_w"], t["cu_seqlens"])
+    assert e.value.status == 1
