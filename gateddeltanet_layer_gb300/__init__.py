@@ -13,7 +13,7 @@ import os
 import threading
 
 __all__ = ["prefill", "decode_step", "prefill_workspace_bytes", "workspace_status", "library",
-           "GdnError", "STATUS"]
+           "GdnError", "STATUS", "prefill_noalloc", "NOALLOC_SCRATCH_BYTES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
@@ -191,3 +191,42 @@ def workspace_status(workspace, stream=None) -> int:
     _check(lib.gdn_workspace_status(_ptr(workspace), _stream_handle(stream, workspace.device),
                                     ctypes.byref(res)), "gdn_workspace_status")
     return res.value
+
+
+# Size of the library's fixed scratch array used by gdn_prefill_noalloc
+# (GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h).
+NOALLOC_SCRATCH_BYTES = 65536
+
+
+def prefill_noalloc(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state=None, *,
+                    out=None, final_state=None, stream=None):
+    """``gdn_prefill_noalloc``: the prefill for callers that cannot allocate
+    device memory (an engine whose memory planner owns all of HBM, a serving
+    loop that forbids allocation after warm-up, code running inside another
+    allocator's callback).  The library takes its workspace from a fixed
+    device array of NOALLOC_SCRATCH_BYTES instead of allocating one.  ``out``
+    and ``final_state`` must be passed in (this wrapper does not create them
+    either).  Calls that overlap on the GPU share that array and race: order
+    them on one stream.  Returns (out, final_state)."""
+    torch = _torch()
+    lib = library()
+    fn = lib.gdn_prefill_noalloc
+    fn.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 15
+    fn.restype = ctypes.c_int
+    if out is None:
+        raise ValueError("prefill_noalloc allocates nothing: pass `out`")
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("z", z), ("out", out)):
+        _req(t, name, dt)
+    for name, t in (("conv_w", conv_w), ("A_log", A_log), ("dt_bias", dt_bias), ("norm_w", norm_w)):
+        _req(t, name, torch.float32)
+    _req(cu_seqlens, "cu_seqlens", torch.int32)
+    for name, t in (("init_state", init_state), ("final_state", final_state)):
+        if t is not None:
+            _req(t, name, torch.float32)
+    d = dims_of(q, v, cu_seqlens.numel() - 1)
+    st = fn(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(conv_w), _ptr(A_log),
+            _ptr(dt_bias), _ptr(norm_w), _ptr(cu_seqlens), _ptr(init_state), _ptr(out), _ptr(final_state),
+            _stream_handle(stream, q.device))
+    _check(st, "gdn_prefill_noalloc")
+    return out, final_state

@@ -49,7 +49,8 @@
  *    workspace's status word and read back with gdn_workspace_status().  No
  *    entry point aborts, throws or traps.
  *  - Thread safety: entry points hold no global state and may be called from
- *    several host threads at once (with distinct workspaces).
+ *    several host threads at once (with distinct workspaces); the one
+ *    exception is gdn_prefill_noalloc, whose comment says how it shares state.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -147,6 +148,43 @@ GDN_API int gdn_decode_step(const gdn_dims *dims, const void *q, const void *k, 
  * and returns GDN_OK, or returns GDN_ERR_INVALID_ARG / GDN_ERR_CUDA.
  */
 GDN_API int gdn_workspace_status(void *workspace, void *stream, int *device_status);
+
+/*
+ * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate.
+ *
+ * (An addition of this library; the pages have no counterpart.)
+ *
+ * Some callers cannot call cudaMalloc or hand out a workspace: an inference
+ * engine whose memory planner owns all of HBM from start-up, a serving loop
+ * that forbids allocation after warm-up (an allocation there can stall on the
+ * driver or fail under memory pressure), or code running inside another
+ * allocator's callback, where allocating would re-enter it.  This entry point
+ * is gdn_prefill with the workspace taken from a fixed array of
+ * GDN_NOALLOC_SCRATCH_BYTES in the library's own device memory; it calls no
+ * cudaMalloc, cudaMallocAsync, cudaFree or other allocating routine.  The
+ * caller still passes every input and output, with the meaning, layout and
+ * error behaviour of gdn_prefill.
+ *
+ *  - Limit: problems whose gdn_prefill_workspace_bytes() exceeds
+ *    GDN_NOALLOC_SCRATCH_BYTES are rejected with GDN_ERR_WORKSPACE before
+ *    anything is launched.
+ *  - The array is a device global of the library: every GPU that loads the
+ *    library holds it until the process exits.  The first call on a device
+ *    looks up its device address (cudaGetSymbolAddress, on the current
+ *    device); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind; each call clears the part that must start at zero.  Calls whose
+ *    kernels overlap on the GPU (different streams, or different host threads
+ *    without ordering) race on it: order them on one stream or serialise them.
+ *  - The device status word of this entry point is not readable by the caller
+ *    (gdn_workspace_status needs a caller-owned workspace).
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES 65536
+GDN_API int gdn_prefill_noalloc(const gdn_dims *dims, const void *q, const void *k, const void *v,
+                                const void *a, const void *b, const void *z, const float *conv_w,
+                                const float *A_log, const float *dt_bias, const float *norm_w,
+                                const int32_t *cu_seqlens, const float *init_state, void *out,
+                                float *final_state, void *stream);
 
 /* Human-readable name of a gdn_status (never NULL). */
 GDN_API const char *gdn_status_string(int status);
