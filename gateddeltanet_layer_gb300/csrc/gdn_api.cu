@@ -26,7 +26,9 @@ int check_dims(const gdn_dims *d) {
   return GDN_OK;
 }
 
-bool use_tensor_core_prefill(const gdn_dims *) { return false; }
+bool use_tensor_core_prefill(const gdn_dims *d) {
+  return d->io_dtype == GDN_BF16 && d->d_k == 128 && d->d_v == 128;
+}
 
 }  // namespace
 
@@ -35,6 +37,7 @@ extern "C" {
 size_t gdn_prefill_workspace_bytes(const gdn_dims *d) {
   if (check_dims(d) != GDN_OK || d->num_seqs <= 0) return 0;
   size_t bytes = kStatusBytes;
+  if (use_tensor_core_prefill(d)) bytes += gdn::prefill_tc_workspace_bytes(d->num_seqs, d->h_v);
   return bytes;
 }
 
@@ -75,7 +78,10 @@ int gdn_prefill(const gdn_dims *d, const void *q, const void *k, const void *v, 
   p.ws_bytes = need - kStatusBytes;
 
   cudaError_t e;
-  e = gdn::launch_prefill_simt(p, d->io_dtype == GDN_BF16, s);
+  if (use_tensor_core_prefill(d))
+    e = gdn::launch_prefill_tc(p, s);
+  else
+    e = gdn::launch_prefill_simt(p, d->io_dtype == GDN_BF16, s);
   if (owned) cudaFreeAsync(ws, s);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -20,9 +20,14 @@ def lib():
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", src)))
+    """Every gdn_* function declared by a header under include/."""
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            src = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_declares_the_entry_points():
