@@ -14,7 +14,7 @@
 //                                      A_Q = e^(G_r-G_s) (q_r.k_s)          (s <= r)
 //             P^T = S K^T           (P = K H: the entering state seen by each key)
 //             D2a = S Q^T
-//   inverse   T = (I + A)^-1        (fp32, blocked 16 x 16 forward substitution)
+//   inverse   T = (I + A)^-1        (fp32: 16 x 16 diagonal blocks, then 32 x 32 halves)
 //   group 2   U^T = V^T (T diag(beta))^T - P^T (T diag(beta gamma))^T
 //             (= U' - W H with W = T diag(beta gamma) K: the per-token u_r of the rule)
 //   group 3   D2b = U^T A_Q^T;   S <- gamma_C S + U^T K~,   K~ = diag(e^(G_C - G)) K
@@ -71,8 +71,8 @@ constexpr uint32_t OFF_PT = OFF_US + 16384;      // -P^T         [128 j][64 m]
 constexpr uint32_t OFF_KQL = OFF_PT + 16384;     // [K; Q] lo    (P1 only) ...
 constexpr uint32_t OFF_AF = OFF_KQL;             // ... then A fp32 [64][65]
 constexpr uint32_t OFF_TF = OFF_AF + 64 * kPad * 4;  // and T fp32 [64][65]
-constexpr uint32_t OFF_XF = OFF_TF + 64 * kPad * 4;  // block products, 3 x 16 x 16 fp32
-constexpr uint32_t OFF_VEC = OFF_XF + 3 * 256 * 4;   // G, gamma, beta, decay-to-end: 4 x 64 fp32
+constexpr uint32_t OFF_XF = OFF_TF + 64 * kPad * 4;  // block products of the inverse, 32 x 32 fp32
+constexpr uint32_t OFF_VEC = OFF_XF + 1024 * 4;      // G, gamma, beta, decay-to-end: 4 x 64 fp32
 constexpr uint32_t OFF_RED = OFF_VEC + 4 * 64 * 4;   // reductions: 16 x 32 fp32
 constexpr uint32_t OFF_INV = OFF_RED + 8 * 64 * 4;   // per-row inverse norms: 64 fp32
 constexpr uint32_t OFF_MISC = OFF_INV + 64 * 4;      // mbarriers, TMEM base, scan carry
@@ -134,8 +134,18 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
   return v[0];
 }
 
-// SiLU with the fast exponential and division (the result feeds fp16 operands).
-__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+// SiLU x sigmoid(x) with one special-function op: e^-x by the fast exponential,
+// then 1 / (1 + e^-x) by two Newton-Raphson steps y <- y (2 - d y) from the
+// classic bit-pattern reciprocal seed (relative error < 1e-5 after the two
+// steps, far below the fp16 rounding of the result).  The reciprocal runs on
+// the FMA pipe, which has 8x the throughput of the special-function unit.
+__device__ __forceinline__ float silu_fast(float x) {
+  const float d = fminf(1.0f + __expf(-x), 1e30f);
+  float y = __int_as_float(0x7EF311C7 - __float_as_int(d));
+  y = y * (2.0f - d * y);
+  y = y * (2.0f - d * y);
+  return x * y;
+}
 
 // All threads: wait for an MMA commit (or a TMA transaction) phase; true if it
 // ran out (every thread then takes the exit path).
@@ -439,49 +449,89 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---------------- T = (I + A)^-1: diagonal 16x16 blocks by forward substitution
+    // ---------------- T = (I + A)^-1 by recursive doubling on the unit lower-triangular L = I + A
+    // (a) the four diagonal 16x16 blocks by forward substitution, one column per thread
     if (tid < 64) {
       const int bb = tid >> 4, s = tid & 15;
       float x[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        float acc = (r == s) ? 1.0f : 0.0f;
         const float *arow = AF + (16 * bb + r) * kPad + 16 * bb;
+        float acc0 = (r == s) ? 1.0f : 0.0f, acc1 = 0.0f;
 #pragma unroll
-        for (int m = 0; m < r; ++m) acc = fmaf(-arow[m], x[m], acc);
-        x[r] = acc;
+        for (int m = 0; m + 1 < r; m += 2) {
+          acc0 = fmaf(-arow[m], x[m], acc0);
+          acc1 = fmaf(-arow[m + 1], x[m + 1], acc1);
+        }
+        if (r & 1) acc0 = fmaf(-arow[r - 1], x[r - 1], acc0);
+        x[r] = acc0 + acc1;
       }
 #pragma unroll
       for (int r = 0; r < 16; ++r) TF[(16 * bb + r) * kPad + 16 * bb + s] = x[r];
     }
     __syncthreads();
-    // off-diagonal blocks, one block row at a time: T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj
-    for (int i = 1; i < 4; ++i) {
-      for (int e = tid; e < 256 * i; e += kThreads) {
-        const int j = e >> 8, r = (e >> 4) & 15, s = e & 15;
-        float acc = 0.0f;
-        for (int m = j; m < i; ++m) {
-          const float *arow = AF + (16 * i + r) * kPad + 16 * m;
-          const float *tcol = TF + (16 * m) * kPad + 16 * j + s;
+    // (b) the 32x32 halves: T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22)
+    {
+      const int blk = tid >> 8, r = (tid >> 4) & 15, s = tid & 15;
+      const int o = 32 * blk;
+      const float *arow = AF + (o + 16 + r) * kPad + o;
+      float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) acc = fmaf(arow[kk], tcol[kk * kPad], acc);
-        }
-        XF[j * 256 + r * 16 + s] = acc;
+      for (int k = 0; k < 16; k += 2) {  // T_00 is lower triangular: rows k < s do not contribute
+        const float t0 = (k >= s) ? TF[(o + k) * kPad + o + s] : 0.0f;
+        const float t1 = (k + 1 >= s) ? TF[(o + k + 1) * kPad + o + s] : 0.0f;
+        acc0 = fmaf(arow[k], t0, acc0);
+        acc1 = fmaf(arow[k + 1], t1, acc1);
       }
+      XF[blk * 256 + r * 16 + s] = acc0 + acc1;
       __syncthreads();
-      for (int e = tid; e < 256 * i; e += kThreads) {
-        const int j = e >> 8, r = (e >> 4) & 15, s = e & 15;
-        const float *trow = TF + (16 * i + r) * kPad + 16 * i;
-        float acc = 0.0f;
+      const float *trow = TF + (o + 16 + r) * kPad + o + 16;
+      acc0 = 0.0f;
+      acc1 = 0.0f;
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) acc = fmaf(trow[kk], XF[j * 256 + kk * 16 + s], acc);
-        TF[(16 * i + r) * kPad + 16 * j + s] = -acc;
+      for (int k = 0; k < 16; k += 2) {  // T_11 is lower triangular: columns k > r do not contribute
+        const float t0 = (k <= r) ? trow[k] : 0.0f;
+        const float t1 = (k + 1 <= r) ? trow[k + 1] : 0.0f;
+        acc0 = fmaf(t0, XF[blk * 256 + k * 16 + s], acc0);
+        acc1 = fmaf(t1, XF[blk * 256 + (k + 1) * 16 + s], acc1);
       }
-      __syncthreads();
+      TF[(o + 16 + r) * kPad + o + s] = -(acc0 + acc1);
     }
+    __syncthreads();
+    // (c) the lower-left 32x32 block: T_21 = -T_2 (A_21 T_1), two rows per thread
+    {
+      const int r = tid >> 5, s = tid & 31;
+      const float *a0 = AF + (32 + r) * kPad, *a1 = AF + (48 + r) * kPad;
+      float y0 = 0.0f, y1 = 0.0f, y2 = 0.0f, y3 = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {  // T_1 is lower triangular: rows k < s do not contribute
+        const float t0 = (k >= s) ? TF[k * kPad + s] : 0.0f;
+        const float t1 = (k + 1 >= s) ? TF[(k + 1) * kPad + s] : 0.0f;
+        y0 = fmaf(a0[k], t0, y0);
+        y1 = fmaf(a1[k], t0, y1);
+        y2 = fmaf(a0[k + 1], t1, y2);
+        y3 = fmaf(a1[k + 1], t1, y3);
+      }
+      XF[r * 32 + s] = y0 + y2;
+      XF[(r + 16) * 32 + s] = y1 + y3;
+      __syncthreads();
+      const float *t0r = TF + (32 + r) * kPad + 32, *t1r = TF + (48 + r) * kPad + 32;
+      float z0 = 0.0f, z1 = 0.0f, z2 = 0.0f, z3 = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {  // T_2 is lower triangular: columns k > row do not contribute
+        const float yk0 = XF[k * 32 + s], yk1 = XF[(k + 1) * 32 + s];
+        z0 = fmaf((k <= r) ? t0r[k] : 0.0f, yk0, z0);
+        z2 = fmaf((k + 1 <= r) ? t0r[k + 1] : 0.0f, yk1, z2);
+        z1 = fmaf((k <= r + 16) ? t1r[k] : 0.0f, yk0, z1);
+        z3 = fmaf((k + 1 <= r + 16) ? t1r[k + 1] : 0.0f, yk1, z3);
+      }
+      TF[(32 + r) * kPad + s] = -(z0 + z2);
+      TF[(48 + r) * kPad + s] = -(z1 + z3);
+    }
+    __syncthreads();
     // T diag(beta gamma) and T diag(beta) as fp16 operands (rows r, columns m)
     {
-      const int r = tid >> 3, oq = tid & 7;
+      const int r = tid & 63, oq = tid >> 6;
       float a8[8], b8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
