@@ -195,7 +195,7 @@ def workspace_status(workspace, stream=None) -> int:
 
 # Size of the library's fixed scratch array used by gdn_prefill_noalloc
 # (GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h).
-NOALLOC_SCRATCH_BYTES = 65536
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def prefill_noalloc(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state=None, *,

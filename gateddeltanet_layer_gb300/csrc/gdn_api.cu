@@ -3,6 +3,7 @@
 // is computed by the kernels in this directory.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "../../include/gdn.h"
 #include "gdn_internal.h"
@@ -37,7 +38,8 @@ extern "C" {
 size_t gdn_prefill_workspace_bytes(const gdn_dims *d) {
   if (check_dims(d) != GDN_OK || d->num_seqs <= 0) return 0;
   size_t bytes = kStatusBytes;
-  if (use_tensor_core_prefill(d)) bytes += gdn::prefill_tc_workspace_bytes(d->num_seqs, d->h_v);
+  if (use_tensor_core_prefill(d))
+    bytes += gdn::prefill_tc_workspace_bytes(d->num_tokens, d->num_seqs, d->h_qk, d->h_v);
   return bytes;
 }
 
@@ -79,7 +81,7 @@ int gdn_prefill(const gdn_dims *d, const void *q, const void *k, const void *v, 
 
   cudaError_t e;
   if (use_tensor_core_prefill(d))
-    e = gdn::launch_prefill_tc(p, s);
+    e = getenv("GDN_PREFILL_FUSED") ? gdn::launch_prefill_fused(p, s) : gdn::launch_prefill_tc(p, s);
   else
     e = gdn::launch_prefill_simt(p, d->io_dtype == GDN_BF16, s);
   if (owned) cudaFreeAsync(ws, s);

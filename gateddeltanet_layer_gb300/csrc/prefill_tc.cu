@@ -1,43 +1,50 @@
 // Chunked prefill on the 5th-generation tensor cores (bf16 streams, d_k = d_v = 128).
 //
-// One CTA per (sequence, value head) chain walks the sequence in chunks of
-// C = 64 tokens.  The state H = S^T (d_k x d_v, fp32) stays in tensor memory
-// for the whole sequence as S (lane j over d_v, column i over d_k); an fp16
-// copy of it in shared memory is the MMA operand.  Per chunk, with G_r the
-// running sum of the gates g inside the chunk and gamma_r = exp(G_r)
-// (the chunked WY/UT form of the gated delta rule: Yang et al., "Gated Delta
-// Networks", ICLR 2025; "Parallelizing Linear Transformers with the Delta
-// Rule over Sequence Length", NeurIPS 2024):
+// The chunked WY/UT form of the gated delta rule (Yang et al., "Gated Delta
+// Networks", ICLR 2025; "Parallelizing Linear Transformers with the Delta Rule
+// over Sequence Length", NeurIPS 2024).  A sequence is cut into chunks of
+// C = 64 tokens.  With G_r the running sum of the gates g inside a chunk,
+// gamma_r = exp(G_r), H = S^T the state entering the chunk (d_k x d_v):
 //
-//   prologue  q, k, v <- silu(conv4(x)); q, k L2-normalised; g, beta per token
-//   group 1   P1  = [K; Q] K^T      -> A   = beta_r e^(G_r-G_s) (k_r.k_s)   (s < r)
-//                                      A_Q = e^(G_r-G_s) (q_r.k_s)          (s <= r)
-//             P^T = S K^T           (P = K H: the entering state seen by each key)
-//             D2a = S Q^T
-//   inverse   T = (I + A)^-1        (fp32: 16 x 16 diagonal blocks, then 32 x 32 halves)
-//   group 2   U^T = V^T (T diag(beta))^T - P^T (T diag(beta gamma))^T
-//             (= U' - W H with W = T diag(beta gamma) K: the per-token u_r of the rule)
-//   group 3   D2b = U^T A_Q^T;   S <- gamma_C S + U^T K~,   K~ = diag(e^(G_C - G)) K
-//   output    o_r = d_k^-1/2 (gamma_r D2a + D2b)[:, r];  y = RMSNorm(o) w silu(z)
+//   A   = strict_lower(beta_r e^(G_r - G_s) k_r.k_s),   T = (I + A)^-1
+//   U   = T diag(beta) V - T diag(beta gamma) K H         (row r = the u_r of the rule)
+//   O   = d_k^-1/2 (diag(gamma) Q H + (Q K^T o D) U),       D_rs = e^(G_r - G_s), s <= r
+//   H  <- gamma_C H + K~^T U,                               K~ = diag(e^(G_C - G)) K
+//   y   = RMSNorm(O) w silu(z)
+//
+// Everything that does not depend on H is computed for all chunks at once, and
+// only the H-dependent products run sequentially per chain:
+//
+//   chunk_table_kernel  cu_seqlens -> chunk list (sequence, first token) and
+//                       each sequence's first chunk; validates cu_seqlens.
+//   chunk_prep_kernel   one CTA per (chunk, q/k head), all chunks in parallel:
+//                       conv(4) + SiLU + L2 norm of q, k (shared by the value
+//                       heads of the q/k head) and v, the gates, P1 = [K; Q] K^T
+//                       on the tensor cores, A and A_Q, the blocked inverse T,
+//                       U' = T diag(beta) V on the tensor cores; writes the
+//                       state pass's MMA operands, already in their shared-
+//                       memory image, to the workspace.
+//   state_kernel        one CTA per (sequence, value head) chain: H lives in
+//                       tensor memory (as S, lane j over d_v); per chunk three
+//                       MMA groups  (P^T = S K^T, D2a = S Q^T),  U^T = U'^T -
+//                       P^T (T diag(beta gamma))^T,  (D2b = U^T A_Q^T,
+//                       S += U^T K~), and the RMSNormGated epilogue; the next
+//                       chunk's operands stream in by TMA while it works.
 //
 // Every dense contraction is a tcgen05.mma chain with M = 128 (the transposed
-// forms above keep M at d_k or d_v), fp16 operands in 128-byte-swizzled
-// K-major shared memory and fp32 accumulators in tensor memory; one thread
-// issues, tcgen05.commit signals an mbarrier, and every wait is bounded.  Raw
-// stream rows reach shared memory by TMA tensor copies one chunk ahead.
-// Decays between two tokens are always exp(G_r - G_s) with r >= s.
+// forms keep M at d_k or d_v), fp16 operands in 128-byte-swizzled K-major
+// shared memory, fp32 accumulators in tensor memory; one thread issues,
+// tcgen05.commit signals an mbarrier, and every wait is bounded.  Decays
+// between two tokens are always exp(G_r - G_s) with r >= s.
 //
-// Operand precision.  The streams arrive in bf16, but every value the kernel
-// computes (conv outputs, T, P, U, the state copy) is rounded to fp16 for the
-// tensor cores: 3 more mantissa bits than bf16 at the same MMA rate and
-// operand size.  The layer's output is normalised per token (RMSNorm), which
-// magnifies the rounding error of rows whose o is small; with bf16 operands
+// Operand precision.  Every computed operand is rounded to fp16 (3 more
+// mantissa bits than bf16, same MMA rate and size).  The per-token RMSNorm
+// magnifies the rounding error of rows whose o is small: with bf16 operands
 // single outputs drifted by up to 6 % of max(1, |y|), with fp16 by under 1 %.
-// Every operand is bounded well inside the fp16 range (|x| <= ~4 for unit-
-// normalised q, k, the SiLU-conv'd v of O(1) inputs, T diag(beta), P and the
-// state).  The q.k and k.k products of P1 additionally use a hi + lo split
-// (q = q_hi + q_lo, both fp16; P1 = hi.hi + hi.lo + lo.hi), which recovers
-// ~22 bits for the entries of A and A_Q.
+// All operands are bounded well inside the fp16 range (|x| <= ~4: unit-norm
+// q, k, the SiLU-conv'd v of O(1) inputs, T diag(beta), P and the state).  The
+// q.k and k.k products of P1 use a hi + lo split (P1 = hi.hi + hi.lo + lo.hi),
+// which recovers ~22 bits for A and A_Q.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -53,57 +60,41 @@ namespace {
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 512;
-constexpr int kPad = 65;  // fp32 64x64 matrices are stored with a padded row
-constexpr int kStageRows = kC + 3;
+constexpr int kPad = 65;  // fp32 64 x 64 matrices: padded rows
 
-// Shared-memory map (bytes from a 1024-aligned base).  Operand tiles are fp16,
-// 128-byte-swizzled K-major, each on a 1024-byte boundary.
-constexpr uint32_t OFF_SB = 0;                   // S            [128 j][128 i]
-constexpr uint32_t OFF_KQ = OFF_SB + 32768;      // [K; Q] hi    [128 rows][128 i]; later z rows
-constexpr uint32_t OFF_VT = OFF_KQ + 32768;      // V^T          [128 j][64 m]
-constexpr uint32_t OFF_KTT = OFF_VT + 16384;     // K~^T         [128 i][64 r]
-constexpr uint32_t OFF_AQ = OFF_KTT + 16384;     // A_Q          [64 r][64 s]
-constexpr uint32_t OFF_TBG = OFF_AQ + 8192;      // T diag(beta gamma) [64 r][64 m]
-constexpr uint32_t OFF_TB = OFF_TBG + 8192;      // T diag(beta)       [64 r][64 m]
-constexpr uint32_t OFF_US = OFF_TB + 8192;       // U^T          [128 j][64 r]
-constexpr uint32_t OFF_PT = OFF_US + 16384;      // -P^T         [128 j][64 m]
-constexpr uint32_t OFF_KQL = OFF_PT + 16384;     // [K; Q] lo    (P1 only) ...
-constexpr uint32_t OFF_AF = OFF_KQL;             // ... then A fp32 [64][65]
-constexpr uint32_t OFF_TF = OFF_AF + 64 * kPad * 4;  // and T fp32 [64][65]
-constexpr uint32_t OFF_XF = OFF_TF + 64 * kPad * 4;  // block products of the inverse, 32 x 32 fp32
-constexpr uint32_t OFF_VEC = OFF_XF + 1024 * 4;      // G, gamma, beta, decay-to-end: 4 x 64 fp32
-constexpr uint32_t OFF_RED = OFF_VEC + 4 * 64 * 4;   // reductions: 16 x 32 fp32
-constexpr uint32_t OFF_INV = OFF_RED + 8 * 64 * 4;   // per-row inverse norms: 64 fp32
-constexpr uint32_t OFF_MISC = OFF_INV + 64 * 4;      // mbarriers, TMEM base, scan carry
-constexpr uint32_t SMEM_USED = OFF_MISC + 64;
-constexpr size_t kSmemBytes = SMEM_USED + 1024;      // + alignment slack
-// Raw stream rows, staged by TMA in tiles idle at the time:
-//   x rows [3][67][256 B] (q, k, v of rows t0-3 .. t0+63) over A_Q .. -P^T,
-//   loaded once the previous chunk's group 3 is done;
-//   z rows [64][256 B] over [K; Q], loaded once group 1 is done.
-constexpr uint32_t OFF_XST = OFF_AQ;
-constexpr uint32_t OFF_ZST = OFF_KQ;
-constexpr uint32_t kXTileBytes = kStageRows * 256;
+// ---------------------------------------------------------------- workspace
+// Per (chunk, q/k head): the K and Q images ([64 rows][128 cols] fp16 SW128).
+// Per (chunk, value head): A_Q [64][64], T diag(beta gamma) [64][64],
+// U'^T [128][64], K~^T [128][64] (fp16 SW128 images) and gamma [64] fp32.
+constexpr uint32_t kQkSlot = 32768;
+constexpr uint32_t kQkK = 0, kQkQ = 16384;
+constexpr uint32_t kVSlot = 50176;
+constexpr uint32_t kVAq = 0, kVTbg = 8192, kVUp = 16384, kVKt = 32768, kVGam = 49152;
 
-static_assert(OFF_PT % 1024 == 0 && OFF_KQL % 1024 == 0 && OFF_US % 1024 == 0, "SW128 tiles must be 1024-aligned");
-static_assert(OFF_KQL + 32768 <= OFF_XF, "the low-part tile fits in the A/T scratch");
-static_assert(OFF_XST + 3 * kXTileBytes <= OFF_KQL, "x staging fits in A_Q .. -P^T");
-static_assert(kXTileBytes % 128 == 0 && OFF_XST % 128 == 0, "TMA destinations 128-byte aligned");
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-// Tensor-memory columns (512 allocated).
-constexpr int COL_S = 0, COL_D2A = 128, COL_D2B = 192, COL_P1 = 256, COL_PM = 320, COL_X = 384;
-constexpr uint32_t kTmemCols = 512;
-
-constexpr uint32_t kIdN64 = tc::idesc_f16(128, 64);
-constexpr uint32_t kIdN128 = tc::idesc_f16(128, 128);
-
-struct TcMaps {
-  CUtensorMap xq, xk, xv, z;  // [T][heads * 128] bf16, boxes of 128 columns x 67 (x) / 64 (z) rows
+struct Ws {
+  int *chunk_base;   // [N + 1]: first chunk of each sequence; [N] = number of chunks
+  int2 *chunk_info;  // [max_chunks]: (sequence, first token)
+  uint8_t *qk;       // [max_chunks][h_qk] x kQkSlot
+  uint8_t *vs;       // [max_chunks][h_v] x kVSlot
+  int max_chunks;
 };
 
-// K-steps of one MMA chain: D (+)= A[rows a_row0..] * B[rows b_row0..]^T over k16 in [0, ksteps).
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t base, info, qk, vs, total;
+  int max_chunks;
+  WsLayout(int T, int N, int h_qk, int h_v) {
+    max_chunks = (T + kC - 1) / kC + N;
+    base = 0;
+    info = align_up(sizeof(int) * (size_t)(N + 1), 1024);
+    qk = align_up(info + sizeof(int2) * (size_t)max_chunks, 1024);
+    vs = qk + (size_t)max_chunks * h_qk * kQkSlot;
+    total = vs + (size_t)max_chunks * h_v * kVSlot;
+  }
+};
+
+// ---------------------------------------------------------------- helpers
 __device__ __forceinline__ void mma_chain(uint32_t d, uint32_t a, int a_rows, int a_row0, uint32_t b, int b_rows,
                                           int b_row0, int ksteps, uint32_t idesc, bool acc) {
   for (int k = 0; k < ksteps; ++k)
@@ -137,8 +128,7 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
 // SiLU x sigmoid(x) with one special-function op: e^-x by the fast exponential,
 // then 1 / (1 + e^-x) by two Newton-Raphson steps y <- y (2 - d y) from the
 // classic bit-pattern reciprocal seed (relative error < 1e-5 after the two
-// steps, far below the fp16 rounding of the result).  The reciprocal runs on
-// the FMA pipe, which has 8x the throughput of the special-function unit.
+// steps, far below the fp16 rounding of the result).
 __device__ __forceinline__ float silu_fast(float x) {
   const float d = fminf(1.0f + __expf(-x), 1e30f);
   float y = __int_as_float(0x7EF311C7 - __float_as_int(d));
@@ -147,8 +137,6 @@ __device__ __forceinline__ float silu_fast(float x) {
   return x * y;
 }
 
-// All threads: wait for an MMA commit (or a TMA transaction) phase; true if it
-// ran out (every thread then takes the exit path).
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t &phase) {
   const bool ok = tc::mbar_wait(bar, phase & 1);
   ++phase;
@@ -156,8 +144,6 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t &phase) {
   return __syncthreads_or(!ok) != 0;
 }
 
-// Make this thread's shared-memory operand writes and tensor-memory accesses
-// visible to the next MMA, then synchronise the CTA.
 __device__ __forceinline__ void publish_operands() {
   tc::fence_async_smem();
   tc::fence_before_sync();
@@ -165,286 +151,317 @@ __device__ __forceinline__ void publish_operands() {
   tc::fence_after_sync();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p,
-                                                                  const __grid_constant__ TcMaps maps) {
+__device__ __forceinline__ uint2 pack4_f16(float a, float b, float c, float d) {
+  return make_uint2(tc::pack_f16x2(a, b), tc::pack_f16x2(c, d));
+}
+__device__ __forceinline__ void st_chunk_f16_global(uint8_t *dst, const float *x) {
+  uint4 u;
+  u.x = tc::pack_f16x2(x[0], x[1]);
+  u.y = tc::pack_f16x2(x[2], x[3]);
+  u.z = tc::pack_f16x2(x[4], x[5]);
+  u.w = tc::pack_f16x2(x[6], x[7]);
+  *reinterpret_cast<uint4 *>(dst) = u;
+}
+
+// ================================================================ chunk table
+__global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p, Ws ws) {
+  __shared__ int scan[1024];
+  __shared__ int bad;
+  const int N = p.N, tid = threadIdx.x;
+  if (tid == 0) bad = 0;
+  const int per = (N + 1023) / 1024;
+  const int n0 = min(N, tid * per), n1 = min(N, n0 + per);
+  int cnt = 0;
+  for (int n = n0; n < n1; ++n) {
+    const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+    if (s0 >= 0 && s1 >= s0 && s1 <= p.T) cnt += (s1 - s0 + kC - 1) / kC;
+  }
+  scan[tid] = cnt;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan
+    const int v = tid >= off ? scan[tid - off] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  const int total = scan[1023];
+  const bool overflow = total > ws.max_chunks;  // only possible with invalid cu_seqlens
+  int run = scan[tid] - cnt;
+  for (int n = n0; n < n1; ++n) {
+    const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+    const bool ok = s0 >= 0 && s1 >= s0 && s1 <= p.T;
+    if (!ok) bad = 1;
+    ws.chunk_base[n] = overflow ? 0 : run;
+    if (ok) run += (s1 - s0 + kC - 1) / kC;
+  }
+  if (tid == 1023) ws.chunk_base[N] = overflow ? 0 : total;
+  __syncthreads();
+  if (tid == 0 && (bad || overflow)) set_status(p.status, kDevBadSeqlens);
+  if (overflow) return;
+  for (int g = tid; g < total; g += 1024) {  // sequence of chunk g by binary search
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ws.chunk_base[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    ws.chunk_info[g] = make_int2(lo, p.cu_seqlens[lo] + kC * (g - ws.chunk_base[lo]));
+  }
+}
+
+// ================================================================ chunk prep
+constexpr int kPrepThreads = 256;
+// shared memory (from a 1024-aligned base)
+constexpr uint32_t P_KQ = 0;                          // [K; Q] hi fp16 [128][128]
+constexpr uint32_t P_KQL = 32768;                     // [K; Q] lo, later A and T fp32 [64][65]
+constexpr uint32_t P_AF = P_KQL;
+constexpr uint32_t P_TF = P_AF + 64 * kPad * 4;
+constexpr uint32_t P_VT = 66560;                      // V^T fp16 [128 j][64 m]
+constexpr uint32_t P_TB = P_VT + 16384;               // T diag(beta) fp16 [64 r][64 m]
+constexpr uint32_t P_XF = P_TB + 8192;                // inverse block products 32 x 32 fp32
+constexpr int kMaxRep = 8;                            // value heads per q/k head
+constexpr uint32_t P_VEC = P_XF + 4096;               // per value head: G, gamma, beta, decay-to-end
+constexpr uint32_t P_RED = P_VEC + kMaxRep * 1024;
+constexpr uint32_t P_MISC = P_RED + 64;
+constexpr size_t kPrepSmem = P_MISC + 64 + 1024;
+static_assert(P_TF + 64 * kPad * 4 <= P_VT, "A and T fit over the lo tile");
+static_assert(P_VT % 1024 == 0 && P_TB % 1024 == 0, "SW128 tiles 1024-aligned");
+static_assert(2 * kPrepSmem <= 232448, "two prep CTAs per SM");
+
+constexpr uint32_t kIdN64 = tc::idesc_f16(128, 64);
+constexpr uint32_t kIdN128 = tc::idesc_f16(128, 128);
+
+// conv(4) + SiLU of 8 rows x 4 channels of one head: rows r0 .. r0+7 of the
+// chunk, channels c0 .. c0+3 (x points at channel c0 of token 0; bf16 row
+// pitch `stride` elements; conv_w rows from `ch`).  Rows before the sequence
+// start or past the chunk's end are 0.
+__device__ __forceinline__ void conv_rows(const __nv_bfloat16 *x, size_t stride, const float *conv_w, int ch,
+                                          int t0, int s0, int Lc, int r0, float (&y)[8][4]) {
+  float4 w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const float4 *>(conv_w + (size_t)(ch + c) * 4);
+  uint2 xr[11];  // packed bf16 rows
+#pragma unroll
+  for (int rr = 0; rr < 11; ++rr) {
+    const int row = r0 - 3 + rr;
+    const int t = t0 + row;
+    xr[rr] = (t >= s0 && row < Lc) ? *reinterpret_cast<const uint2 *>(x + (size_t)t * stride) : make_uint2(0u, 0u);
+  }
+  auto val = [&](int rr, int c) {
+    const uint32_t w32 = (c < 2) ? xr[rr].x : xr[rr].y;
+    return __uint_as_float((c & 1) ? (w32 & 0xFFFF0000u) : (w32 << 16));
+  };
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const bool ok = r0 + r < Lc;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float a = w[c].x * val(r, c);
+      a = fmaf(w[c].y, val(r + 1, c), a);
+      a = fmaf(w[c].z, val(r + 2, c), a);
+      a = fmaf(w[c].w, val(r + 3, c), a);
+      y[r][c] = ok ? silu_fast(a) : 0.0f;
+    }
+  }
+}
+
+// L2-normalise the 8 rows held by a warp (each lane holds 4 of the 128 channels).
+__device__ __forceinline__ void l2norm_rows(float (&y)[8][4], int lane) {
+  float ss[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) ss[r] = y[r][0] * y[r][0] + y[r][1] * y[r][1] + y[r][2] * y[r][2] + y[r][3] * y[r][3];
+  const float mine = reduce_scatter<8>(ss, lane);  // lane l: row l >> 2
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const float inv = rsqrtf(__shfl_sync(0xffffffffu, mine, 4 * r) + kEpsL2);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) y[r][c] *= inv;
+  }
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const PrefillParams p, const Ws ws) {
+  const int g = blockIdx.x, hq = blockIdx.y;
+  const int total = ws.chunk_base[p.N];
+  if (g >= total) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = tc::smem_u32(sm);
-
-  const int h_v = p.h_v, h_qk = p.h_qk;
-  const int n = blockIdx.x / h_v;
-  const int h = blockIdx.x % h_v;
-  const int hq = h / (h_v / h_qk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lr = tid & 127;    // tensor-memory lane of this thread
-  const int gq = tid >> 7;     // which quarter of the columns this thread takes
+  const int lr = tid & 127, gh = tid >> 7;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  const int h_v = p.h_v, h_qk = p.h_qk, rep = h_v / h_qk;
 
+  const int2 info = ws.chunk_info[g];
+  const int n = info.x, t0 = info.y;
   const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
-  if (s0 < 0 || s1 < s0 || s1 > p.T) {
-    if (tid == 0) set_status(p.status, kDevBadSeqlens);
-    return;
-  }
+  const int Lc = min(kC, s1 - t0);
 
-  float *AF = reinterpret_cast<float *>(sm + OFF_AF);
-  float *TF = reinterpret_cast<float *>(sm + OFF_TF);
-  float *XF = reinterpret_cast<float *>(sm + OFF_XF);
-  float *sG = reinterpret_cast<float *>(sm + OFF_VEC);
-  float *sGam = sG + 64;
-  float *sBeta = sG + 128;
-  float *sDec = sG + 192;
-  float *red = reinterpret_cast<float *>(sm + OFF_RED);
-  float *sInv = reinterpret_cast<float *>(sm + OFF_INV);
-  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_MISC);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 8);
-  float *carry = reinterpret_cast<float *>(sm + OFF_MISC + 16);
-  uint64_t *bar_x = reinterpret_cast<uint64_t *>(sm + OFF_MISC + 24);
-  uint64_t *bar_z = reinterpret_cast<uint64_t *>(sm + OFF_MISC + 32);
+  float *AF = reinterpret_cast<float *>(sm + P_AF);
+  float *TF = reinterpret_cast<float *>(sm + P_TF);
+  float *XF = reinterpret_cast<float *>(sm + P_XF);
+  // per value head vv: G at sG[256 vv], gamma at +64, beta at +128, decay-to-end at +192
+  float *sG = reinterpret_cast<float *>(sm + P_VEC);
+  float *const sGall = sG;
+  float *carry = reinterpret_cast<float *>(sm + P_RED);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P_MISC);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + P_MISC + 8);
 
+  const __nv_bfloat16 *xq = static_cast<const __nv_bfloat16 *>(p.q);
+  const __nv_bfloat16 *xk = static_cast<const __nv_bfloat16 *>(p.k);
+  const __nv_bfloat16 *xv = static_cast<const __nv_bfloat16 *>(p.v);
   const __nv_bfloat16 *xa = static_cast<const __nv_bfloat16 *>(p.a);
   const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(p.b);
-  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+  const size_t qk_stride = (size_t)h_qk * kD, v_stride = (size_t)h_v * kD;
 
   if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_alloc(tmem_slot, 128);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
     tc::mbar_init(bar, 1);
-    tc::mbar_init(bar_x, 1);
-    tc::mbar_init(bar_z, 1);
     tc::fence_mbar_init();
-    tc::prefetch_tmap(&maps.xq);
-    tc::prefetch_tmap(&maps.xk);
-    tc::prefetch_tmap(&maps.xv);
-    tc::prefetch_tmap(&maps.z);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  uint32_t phase = 0, phase_x = 0, phase_z = 0;
-  bool failed = false, x_pending = false, z_pending = false;
+  constexpr int COL_P1 = 0, COL_UP = 64;
+  uint32_t phase = 0;
+  bool failed = false;
 
-  // q, k, v rows t_next-3 .. t_next+63 -> x staging (rows outside the tensor
-  // read as zero; rows of neighbouring sequences are masked where used).
-  auto issue_x = [&](int t_next) {
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(bar_x, 3 * kXTileBytes);
-      tc::tma_load_2d(sm + OFF_XST, &maps.xq, hq * kD, t_next - 3, bar_x);
-      tc::tma_load_2d(sm + OFF_XST + kXTileBytes, &maps.xk, hq * kD, t_next - 3, bar_x);
-      tc::tma_load_2d(sm + OFF_XST + 2 * kXTileBytes, &maps.xv, h * kD, t_next - 3, bar_x);
-    }
-  };
-  auto issue_z = [&](int t0_) {
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(bar_z, kC * 256);
-      tc::tma_load_2d(sm + OFF_ZST, &maps.z, h * kD, t0_, bar_z);
-    }
-  };
+  uint8_t *qk_slot = ws.qk + ((size_t)g * h_qk + hq) * kQkSlot;
+  const int r0 = 8 * warp, c0 = 4 * lane;  // prologue: this thread's rows and channels
+  auto v_slot_of = [&](int vv) { return ws.vs + ((size_t)g * h_v + hq * rep + vv) * kVSlot; };
 
-  // ---------------- initial state -> TMEM S (fp32) and its fp16 copy
-  const size_t st_off = ((size_t)n * h_v + h) * kD * kD;
+  // ---------------- gates of every value head and their running sums inside the chunk
+  for (int v0 = 0; v0 < rep; v0 += 4) {
+    const int vv = v0 + (tid >> 6), r = tid & 63;
+    float gsum = 0.0f;
+    if (vv < rep) {
+      const int h = hq * rep + vv;
+      float gg = 0.0f, be = 0.0f;
+      if (r < Lc) {
+        const size_t gi = (size_t)(t0 + r) * h_v + h;
+        gg = gate_g(__bfloat162float(xa[gi]), expf(p.A_log[h]), p.dt_bias[h]);
+        be = sigmoid_f(__bfloat162float(xb[gi]));
+      }
+      gsum = gg;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, gsum, off);
+        if (lane >= off) gsum += y;
+      }
+      if (r == 31) carry[vv & 3] = gsum;
+      sG[vv * 256 + 128 + r] = be;
+    }
+    __syncthreads();
+    if (vv < rep) {
+      if (r >= 32) gsum += carry[vv & 3];
+      sG[vv * 256 + r] = gsum;
+      const float gm = expf(gsum);
+      sG[vv * 256 + 64 + r] = gm;
+      *reinterpret_cast<float *>(v_slot_of(vv) + kVGam + 4 * r) = gm;
+    }
+    __syncthreads();
+    if (vv < rep) sG[vv * 256 + 192 + r] = expf(sG[vv * 256 + 63] - sG[vv * 256 + r]);
+    __syncthreads();
+  }
+
+  // ---------------- q and k: conv + SiLU + L2 norm -> [K; Q] hi / lo tiles, K and Q images,
+  //                  and K~^T = (diag(e^(G_C - G)) K)^T images of every value head
   {
-    const int j = lr;
-    float v[32];
+    float y[8][4], kreg[8][4];
+    conv_rows(xq + hq * kD + c0, qk_stride, p.conv_w, hq * kD + c0, t0, s0, Lc, r0, y);
+    l2norm_rows(y, lane);
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      const int i = 32 * gq + q;
-      v[q] = p.init_state ? p.init_state[st_off + (size_t)i * kD + j] : 0.0f;
+    for (int r = 0; r < 8; ++r) {
+      const uint2 hi = pack4_f16(y[r][0], y[r][1], y[r][2], y[r][3]);
+      const __half2 h01 = *reinterpret_cast<const __half2 *>(&hi.x), h23 = *reinterpret_cast<const __half2 *>(&hi.y);
+      const uint2 lo = pack4_f16(y[r][0] - __low2float(h01), y[r][1] - __high2float(h01),
+                                 y[r][2] - __low2float(h23), y[r][3] - __high2float(h23));
+      const uint32_t off = tc::sw128_offset(128, 64 + r0 + r, c0);
+      *reinterpret_cast<uint2 *>(sm + P_KQ + off) = hi;
+      *reinterpret_cast<uint2 *>(sm + P_KQL + off) = lo;
+      *reinterpret_cast<uint2 *>(qk_slot + kQkQ + tc::sw128_offset(64, r0 + r, c0)) = hi;
     }
-    tc::tmem_st32(tmem + lane_off + COL_S + 32 * gq, v);
+    conv_rows(xk + hq * kD + c0, qk_stride, p.conv_w, h_qk * kD + hq * kD + c0, t0, s0, Lc, r0, kreg);
+    l2norm_rows(kreg, lane);
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) tc::st_chunk_f16(sm + OFF_SB + tc::sw128_chunk(128, j, 4 * gq + cc), v + 8 * cc);
+    for (int r = 0; r < 8; ++r) {
+      const uint2 hi = pack4_f16(kreg[r][0], kreg[r][1], kreg[r][2], kreg[r][3]);
+      const __half2 h01 = *reinterpret_cast<const __half2 *>(&hi.x), h23 = *reinterpret_cast<const __half2 *>(&hi.y);
+      const uint2 lo = pack4_f16(kreg[r][0] - __low2float(h01), kreg[r][1] - __high2float(h01),
+                                 kreg[r][2] - __low2float(h23), kreg[r][3] - __high2float(h23));
+      const uint32_t off = tc::sw128_offset(128, r0 + r, c0);
+      *reinterpret_cast<uint2 *>(sm + P_KQ + off) = hi;
+      *reinterpret_cast<uint2 *>(sm + P_KQL + off) = lo;
+      *reinterpret_cast<uint2 *>(qk_slot + kQkK + tc::sw128_offset(64, r0 + r, c0)) = hi;
+    }
+    for (int vv = 0; vv < rep; ++vv) {
+      const float *dec = sG + vv * 256 + 192;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float kt[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) kt[r] = kreg[r][c] * dec[r0 + r];
+        st_chunk_f16_global(v_slot_of(vv) + kVKt + tc::sw128_chunk(128, c0 + c, warp), kt);
+      }
+    }
   }
   publish_operands();
 
-  const float A_exp = expf(p.A_log[h]);
-  const float dtb = p.dt_bias[h];
-  const float scale = rsqrtf((float)kD);
-
-  // the first chunk's raw rows and gate inputs
-  float a_in = 0.0f, b_in = 0.0f;
-  if (s1 > s0) {
-    issue_x(s0);
-    x_pending = true;
-    if (tid < 64 && s0 + tid < s1) {
-      a_in = __bfloat162float(xa[(size_t)(s0 + tid) * h_v + h]);
-      b_in = __bfloat162float(xb[(size_t)(s0 + tid) * h_v + h]);
-    }
+  // ---------------- P1 = [K; Q] K^T (hi.hi + hi.lo + lo.hi): rows 0..63 K K^T, 64..127 Q K^T
+  if (tid == 0) {
+    mma_chain(tmem + COL_P1, sbase + P_KQ, 128, 0, sbase + P_KQ, 128, 0, 8, kIdN64, false);
+    mma_chain(tmem + COL_P1, sbase + P_KQ, 128, 0, sbase + P_KQL, 128, 0, 8, kIdN64, true);
+    mma_chain(tmem + COL_P1, sbase + P_KQL, 128, 0, sbase + P_KQ, 128, 0, 8, kIdN64, true);
+    tc::mma_commit(bar);
   }
 
-  for (int t0 = s0; t0 < s1 && !failed; t0 += kC) {
-    const int Lc = min(kC, s1 - t0);
+  for (int vv = 0; vv < rep && !failed; ++vv) {
+    const int h = hq * rep + vv;
+    uint8_t *v_slot = v_slot_of(vv);
 
-    // ---------------- gates and their running sum inside the chunk
-    {
-      float gsum = 0.0f;
-      if (tid < 64) {
-        const int r = tid;
-        float g = 0.0f, be = 0.0f;
-        if (r < Lc) {
-          g = gate_g(a_in, A_exp, dtb);
-          be = sigmoid_f(b_in);
-        }
-        gsum = g;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, gsum, off);
-          if (lane >= off) gsum += y;
-        }
-        if (tid == 31) carry[0] = gsum;
-        sBeta[r] = be;
-      }
-      __syncthreads();
-      if (tid < 64) {
-        if (tid >= 32) gsum += carry[0];
-        sG[tid] = gsum;
-        sGam[tid] = expf(gsum);
-      }
-      __syncthreads();
-      if (tid < 64) sDec[tid] = expf(sG[63] - sG[tid]);
-    }
-    if (wait_all(bar_x, phase_x)) { failed = true; break; }
-    x_pending = false;
+    const float *sG = sGall + vv * 256, *sGam = sG + 64, *sBeta = sG + 128;
 
-    // ---------------- prologue: conv(4) + SiLU (+ L2 norm) of q, k, v
-    // thread -> channels (2cp, 2cp+1), rows [8 rb, 8 rb + 8)
+    // ---------------- v: conv + SiLU -> V^T tile
     {
-      const int cp = tid & 63, rb = tid >> 6;
-      for (int mat = 0; mat < 3; ++mat) {
-        const int ch = mat == 0 ? hq * kD + 2 * cp
-                       : mat == 1 ? h_qk * kD + hq * kD + 2 * cp
-                                  : 2 * h_qk * kD + h * kD + 2 * cp;
-        const uint8_t *stage = sm + OFF_XST + (uint32_t)mat * kXTileBytes + 4 * cp;
-        const float4 w0 = *reinterpret_cast<const float4 *>(p.conv_w + (size_t)ch * 4);
-        const float4 w1 = *reinterpret_cast<const float4 *>(p.conv_w + (size_t)(ch + 1) * 4);
-        float x0[11], x1[11];
+      float y[8][4];
+      conv_rows(xv + h * kD + c0, v_stride, p.conv_w, 2 * h_qk * kD + h * kD + c0, t0, s0, Lc, r0, y);
 #pragma unroll
-        for (int rr = 0; rr < 11; ++rr) {
-          const int row = 8 * rb - 3 + rr;
-          if (t0 + row >= s0 && row < Lc) {
-            const float2 f =
-                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(stage + (row + 3) * 256));
-            x0[rr] = f.x;
-            x1[rr] = f.y;
-          } else {
-            x0[rr] = 0.0f;
-            x1[rr] = 0.0f;
-          }
-        }
-        float y0[8], y1[8], ss[8];
+      for (int c = 0; c < 4; ++c) {
+        float col[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const bool ok = 8 * rb + r < Lc;
-          float a0 = w0.x * x0[r];
-          a0 = fmaf(w0.y, x0[r + 1], a0);
-          a0 = fmaf(w0.z, x0[r + 2], a0);
-          a0 = fmaf(w0.w, x0[r + 3], a0);
-          float a1 = w1.x * x1[r];
-          a1 = fmaf(w1.y, x1[r + 1], a1);
-          a1 = fmaf(w1.z, x1[r + 2], a1);
-          a1 = fmaf(w1.w, x1[r + 3], a1);
-          y0[r] = ok ? silu_fast(a0) : 0.0f;
-          y1[r] = ok ? silu_fast(a1) : 0.0f;
-          ss[r] = y0[r] * y0[r] + y1[r] * y1[r];
-        }
-        if (mat < 2) {  // L2 norm over the 128 channels of each row: 64 threads, 2 warps
-          const float part = reduce_scatter<8>(ss, lane);
-          if ((lane & 3) == 0) red[warp * 8 + (lane >> 2)] = part;
-          __syncthreads();
-          if (tid < 64) {
-            const int rbb = tid >> 3, rr = tid & 7;
-            sInv[tid] = rsqrtf(red[(2 * rbb) * 8 + rr] + red[(2 * rbb + 1) * 8 + rr] + kEpsL2);
-          }
-          __syncthreads();
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const float inv = sInv[8 * rb + r];
-            y0[r] *= inv;
-            y1[r] *= inv;
-          }
-          // [K; Q] rows (K: 0..63, Q: 64..127), high and low fp16 parts
-          const int row0 = mat == 0 ? 64 : 0;
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const __half2 hi = __floats2half2_rn(y0[r], y1[r]);
-            const __half2 lo = __floats2half2_rn(y0[r] - __low2float(hi), y1[r] - __high2float(hi));
-            const uint32_t off = tc::sw128_offset(128, row0 + 8 * rb + r, 2 * cp);
-            *reinterpret_cast<__half2 *>(sm + OFF_KQ + off) = hi;
-            *reinterpret_cast<__half2 *>(sm + OFF_KQL + off) = lo;
-          }
-        }
-        if (mat == 1) {  // K~^T = (diag(e^(G_C - G)) K)^T
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const float dcy = sDec[8 * rb + r];
-            y0[r] *= dcy;
-            y1[r] *= dcy;
-          }
-          tc::st_chunk_f16(sm + OFF_KTT + tc::sw128_chunk(128, 2 * cp, rb), y0);
-          tc::st_chunk_f16(sm + OFF_KTT + tc::sw128_chunk(128, 2 * cp + 1, rb), y1);
-        }
-        if (mat == 2) {  // V^T
-          tc::st_chunk_f16(sm + OFF_VT + tc::sw128_chunk(128, 2 * cp, rb), y0);
-          tc::st_chunk_f16(sm + OFF_VT + tc::sw128_chunk(128, 2 * cp + 1, rb), y1);
-        }
+        for (int r = 0; r < 8; ++r) col[r] = y[r][c];
+        tc::st_chunk_f16(sm + P_VT + tc::sw128_chunk(128, c0 + c, warp), col);
       }
     }
-    publish_operands();
-
-    // ---------------- group 1: P1 = [K; Q] K^T (hi.hi + hi.lo + lo.hi), P^T = S K^T, D2a = S Q^T
-    if (tid == 0) {
-      mma_chain(tmem + COL_P1, sbase + OFF_KQ, 128, 0, sbase + OFF_KQ, 128, 0, 8, kIdN64, false);
-      mma_chain(tmem + COL_P1, sbase + OFF_KQ, 128, 0, sbase + OFF_KQL, 128, 0, 8, kIdN64, true);
-      mma_chain(tmem + COL_P1, sbase + OFF_KQL, 128, 0, sbase + OFF_KQ, 128, 0, 8, kIdN64, true);
-      mma_chain(tmem + COL_PM, sbase + OFF_SB, 128, 0, sbase + OFF_KQ, 128, 0, 8, kIdN64, false);
-      mma_chain(tmem + COL_D2A, sbase + OFF_SB, 128, 0, sbase + OFF_KQ, 128, 64, 8, kIdN64, false);
-      tc::mma_commit(bar);
+    if (vv == 0) {
+      if (wait_all(bar, phase)) { failed = true; break; }
     }
-    // meanwhile: S <- gamma_C S in tensor memory (the MMAs above read the fp16 copy)
+
+    // ---------------- A (fp32, strictly lower) and A_Q (image)
     {
-      const float gC = sGam[63];
       float v[32];
-      tc::tmem_ld32(tmem + lane_off + COL_S + 32 * gq, v);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) v[q] *= gC;
-      tc::tmem_st32(tmem + lane_off + COL_S + 32 * gq, v);
-    }
-    if (wait_all(bar, phase)) { failed = true; break; }
-    // [K; Q] is consumed: stage this chunk's z rows over it
-    tc::fence_async_smem();
-    issue_z(t0);
-    z_pending = true;
-
-    // ---------------- A (fp32, strictly lower), A_Q and -P^T (fp16 operands)
-    {
-      float v[16];
-      tc::tmem_ld16(tmem + lane_off + COL_P1 + 16 * gq, v);
+      tc::tmem_ld32(tmem + lane_off + COL_P1 + 32 * gh, v);
       if (lr < 64) {
         const int r = lr;
         const float Gr = sG[r], br = sBeta[r];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int s = 16 * gq + q;
+        for (int q = 0; q < 32; ++q) {
+          const int s = 32 * gh + q;
           AF[r * kPad + s] = (s < r) ? br * __expf(Gr - sG[s]) * v[q] : 0.0f;
         }
       } else {
         const int r = lr - 64;
         const float Gr = sG[r];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int s = 16 * gq + q;
+        for (int q = 0; q < 32; ++q) {
+          const int s = 32 * gh + q;
           v[q] = (s <= r) ? __expf(Gr - sG[s]) * v[q] : 0.0f;
         }
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) tc::st_chunk_f16(sm + OFF_AQ + tc::sw128_chunk(64, r, 2 * gq + cc), v + 8 * cc);
+        for (int cc = 0; cc < 4; ++cc) st_chunk_f16_global(v_slot + kVAq + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
       }
-      tc::tmem_ld16(tmem + lane_off + COL_PM + 16 * gq, v);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = -v[q];
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) tc::st_chunk_f16(sm + OFF_PT + tc::sw128_chunk(128, lr, 2 * gq + cc), v + 8 * cc);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -470,180 +487,387 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       for (int r = 0; r < 16; ++r) TF[(16 * bb + r) * kPad + 16 * bb + s] = x[r];
     }
     __syncthreads();
-    // (b) the 32x32 halves: T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22)
+    // (b) T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22): two elements per thread
     {
-      const int blk = tid >> 8, r = (tid >> 4) & 15, s = tid & 15;
-      const int o = 32 * blk;
-      const float *arow = AF + (o + 16 + r) * kPad + o;
-      float acc0 = 0.0f, acc1 = 0.0f;
+      float xv2[2];
 #pragma unroll
-      for (int k = 0; k < 16; k += 2) {  // T_00 is lower triangular: rows k < s do not contribute
-        const float t0 = (k >= s) ? TF[(o + k) * kPad + o + s] : 0.0f;
-        const float t1 = (k + 1 >= s) ? TF[(o + k + 1) * kPad + o + s] : 0.0f;
-        acc0 = fmaf(arow[k], t0, acc0);
-        acc1 = fmaf(arow[k + 1], t1, acc1);
+      for (int it = 0; it < 2; ++it) {
+        const int e = tid + kPrepThreads * it;
+        const int blk = e >> 8, r = (e >> 4) & 15, s = e & 15, o = 32 * blk;
+        const float *arow = AF + (o + 16 + r) * kPad + o;
+        float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {  // T_00 is lower triangular
+          const float ta = (k >= s) ? TF[(o + k) * kPad + o + s] : 0.0f;
+          const float tb = (k + 1 >= s) ? TF[(o + k + 1) * kPad + o + s] : 0.0f;
+          acc0 = fmaf(arow[k], ta, acc0);
+          acc1 = fmaf(arow[k + 1], tb, acc1);
+        }
+        xv2[it] = acc0 + acc1;
       }
-      XF[blk * 256 + r * 16 + s] = acc0 + acc1;
+#pragma unroll
+      for (int it = 0; it < 2; ++it) XF[tid + kPrepThreads * it] = xv2[it];
       __syncthreads();
-      const float *trow = TF + (o + 16 + r) * kPad + o + 16;
-      acc0 = 0.0f;
-      acc1 = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 16; k += 2) {  // T_11 is lower triangular: columns k > r do not contribute
-        const float t0 = (k <= r) ? trow[k] : 0.0f;
-        const float t1 = (k + 1 <= r) ? trow[k + 1] : 0.0f;
-        acc0 = fmaf(t0, XF[blk * 256 + k * 16 + s], acc0);
-        acc1 = fmaf(t1, XF[blk * 256 + (k + 1) * 16 + s], acc1);
+      for (int it = 0; it < 2; ++it) {
+        const int e = tid + kPrepThreads * it;
+        const int blk = e >> 8, r = (e >> 4) & 15, s = e & 15, o = 32 * blk;
+        const float *trow = TF + (o + 16 + r) * kPad + o + 16;
+        float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {  // T_11 is lower triangular
+          acc0 = fmaf((k <= r) ? trow[k] : 0.0f, XF[blk * 256 + k * 16 + s], acc0);
+          acc1 = fmaf((k + 1 <= r) ? trow[k + 1] : 0.0f, XF[blk * 256 + (k + 1) * 16 + s], acc1);
+        }
+        TF[(o + 16 + r) * kPad + o + s] = -(acc0 + acc1);
       }
-      TF[(o + 16 + r) * kPad + o + s] = -(acc0 + acc1);
     }
     __syncthreads();
-    // (c) the lower-left 32x32 block: T_21 = -T_2 (A_21 T_1), two rows per thread
+    // (c) the lower-left 32x32 block T_21 = -T_2 (A_21 T_1): four rows per thread
     {
-      const int r = tid >> 5, s = tid & 31;
-      const float *a0 = AF + (32 + r) * kPad, *a1 = AF + (48 + r) * kPad;
-      float y0 = 0.0f, y1 = 0.0f, y2 = 0.0f, y3 = 0.0f;
+      const int rb = tid >> 5, s = tid & 31;  // rows rb, rb+8, rb+16, rb+24
+      float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {  // T_1 is lower triangular: rows k < s do not contribute
-        const float t0 = (k >= s) ? TF[k * kPad + s] : 0.0f;
-        const float t1 = (k + 1 >= s) ? TF[(k + 1) * kPad + s] : 0.0f;
-        y0 = fmaf(a0[k], t0, y0);
-        y1 = fmaf(a1[k], t0, y1);
-        y2 = fmaf(a0[k + 1], t1, y2);
-        y3 = fmaf(a1[k + 1], t1, y3);
+      for (int k = 0; k < 32; ++k) {  // T_1 is lower triangular
+        const float t = (k >= s) ? TF[k * kPad + s] : 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) y[q] = fmaf(AF[(32 + rb + 8 * q) * kPad + k], t, y[q]);
       }
-      XF[r * 32 + s] = y0 + y2;
-      XF[(r + 16) * 32 + s] = y1 + y3;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) XF[(rb + 8 * q) * 32 + s] = y[q];
       __syncthreads();
-      const float *t0r = TF + (32 + r) * kPad + 32, *t1r = TF + (48 + r) * kPad + 32;
-      float z0 = 0.0f, z1 = 0.0f, z2 = 0.0f, z3 = 0.0f;
+      float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {  // T_2 is lower triangular: columns k > row do not contribute
-        const float yk0 = XF[k * 32 + s], yk1 = XF[(k + 1) * 32 + s];
-        z0 = fmaf((k <= r) ? t0r[k] : 0.0f, yk0, z0);
-        z2 = fmaf((k + 1 <= r) ? t0r[k + 1] : 0.0f, yk1, z2);
-        z1 = fmaf((k <= r + 16) ? t1r[k] : 0.0f, yk0, z1);
-        z3 = fmaf((k + 1 <= r + 16) ? t1r[k + 1] : 0.0f, yk1, z3);
+      for (int k = 0; k < 32; ++k) {  // T_2 is lower triangular
+        const float yk = XF[k * 32 + s];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = rb + 8 * q;
+          z[q] = fmaf((k <= r) ? TF[(32 + r) * kPad + 32 + k] : 0.0f, yk, z[q]);
+        }
       }
-      TF[(32 + r) * kPad + s] = -(z0 + z2);
-      TF[(48 + r) * kPad + s] = -(z1 + z3);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) TF[(32 + rb + 8 * q) * kPad + s] = -z[q];
     }
     __syncthreads();
-    // T diag(beta gamma) and T diag(beta) as fp16 operands (rows r, columns m)
+    // T diag(beta) (shared-memory operand) and T diag(beta gamma) (image)
     {
-      const int r = tid & 63, oq = tid >> 6;
-      float a8[8], b8[8];
+      const int r = tid & 63, oq = tid >> 6;  // columns [16 oq, 16 oq + 16)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int m = 8 * oq + e;
-        const float t = (m <= r) ? TF[r * kPad + m] : 0.0f;
-        b8[e] = t * sBeta[m];
-        a8[e] = b8[e] * sGam[m];
+      for (int hh = 0; hh < 2; ++hh) {
+        float a8[8], b8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int m = 16 * oq + 8 * hh + e;
+          const float t = (m <= r) ? TF[r * kPad + m] : 0.0f;
+          b8[e] = t * sBeta[m];
+          a8[e] = b8[e] * sGam[m];
+        }
+        tc::st_chunk_f16(sm + P_TB + tc::sw128_chunk(64, r, 2 * oq + hh), b8);
+        st_chunk_f16_global(v_slot + kVTbg + tc::sw128_chunk(64, r, 2 * oq + hh), a8);
       }
-      tc::st_chunk_f16(sm + OFF_TBG + tc::sw128_chunk(64, r, oq), a8);
-      tc::st_chunk_f16(sm + OFF_TB + tc::sw128_chunk(64, r, oq), b8);
     }
     publish_operands();
 
-    // ---------------- group 2: U^T = V^T (T diag(beta))^T + (-P^T) (T diag(beta gamma))^T
+    // ---------------- U'^T = V^T (T diag(beta))^T -> image
     if (tid == 0) {
-      mma_chain(tmem + COL_X, sbase + OFF_VT, 128, 0, sbase + OFF_TB, 64, 0, 4, kIdN64, false);
-      mma_chain(tmem + COL_X, sbase + OFF_PT, 128, 0, sbase + OFF_TBG, 64, 0, 4, kIdN64, true);
+      mma_chain(tmem + COL_UP, sbase + P_VT, 128, 0, sbase + P_TB, 64, 0, 4, kIdN64, false);
       tc::mma_commit(bar);
     }
     if (wait_all(bar, phase)) { failed = true; break; }
-    // U^T (lane j) -> fp16 operand rows j, columns r
     {
-      float u[16];
-      tc::tmem_ld16(tmem + lane_off + COL_X + 16 * gq, u);
+      float u[32];
+      tc::tmem_ld32(tmem + lane_off + COL_UP + 32 * gh, u);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) tc::st_chunk_f16(sm + OFF_US + tc::sw128_chunk(128, lr, 2 * gq + cc), u + 8 * cc);
+      for (int cc = 0; cc < 4; ++cc) st_chunk_f16_global(v_slot + kVUp + tc::sw128_chunk(128, lr, 4 * gh + cc), u + 8 * cc);
+    }
+    tc::fence_before_sync();
+    __syncthreads();  // V^T, T, A are reused by the next value head
+  }
+  if (failed && tid == 0) set_status(p.status, kDevTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+}
+
+// ================================================================ state pass
+constexpr int kStateThreads = 256;
+constexpr uint32_t S_SB = 0;          // S fp16 [128 j][128 i]
+constexpr uint32_t S_KH = 32768;      // K image [64][128]    } one bulk set (with gamma)
+constexpr uint32_t S_QH = 49152;      // Q image [64][128]    }
+constexpr uint32_t S_AQ = 65536;      // A_Q image            } one bulk set
+constexpr uint32_t S_KTT = 73728;     // K~^T image           }
+constexpr uint32_t S_TBG = 90112;     // T diag(beta gamma)   } one bulk set
+constexpr uint32_t S_UP = 98304;      // U'^T image           }
+constexpr uint32_t S_Z = 114688;      // z rows [64][256 B] (TMA tensor copy)
+constexpr uint32_t S_PT = 131072;     // -P^T fp16 [128 j][64 m]
+constexpr uint32_t S_US = 147456;     // U^T fp16 [128 j][64 r]
+constexpr uint32_t S_GAM = 163840;    // gamma [64] (bulk, with K and Q)
+constexpr uint32_t S_GAML = S_GAM + 256;  // this chunk's gamma, kept while the next loads
+constexpr uint32_t S_RED = S_GAML + 256;
+constexpr uint32_t S_INV = S_RED + 2048;
+constexpr uint32_t S_MISC = S_INV + 256;
+constexpr size_t kStateSmem = S_MISC + 128 + 1024;
+static_assert(S_US % 1024 == 0 && S_KTT % 1024 == 0 && S_TBG % 1024 == 0, "SW128 tiles 1024-aligned");
+static_assert(kStateSmem <= 232448, "shared memory budget");
+
+constexpr int COL_S = 0, COL_PM = 128, COL_D2A = 192, COL_D2B = 256, COL_X = 320;
+
+__global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillParams p, const Ws ws,
+                                                                 const __grid_constant__ CUtensorMap zmap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = tc::smem_u32(sm);
+  const int h_v = p.h_v, h_qk = p.h_qk;
+  const int n = blockIdx.x / h_v, h = blockIdx.x % h_v;
+  const int hq = h / (h_v / h_qk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lr = tid & 127, gh = tid >> 7;
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+
+  const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+  if (s0 < 0 || s1 < s0 || s1 > p.T) return;  // reported by the chunk table
+  const int g0 = ws.chunk_base[n], g1 = ws.chunk_base[n + 1];
+  if (g1 - g0 != (s1 - s0 + kC - 1) / kC) return;  // table overflow (invalid cu_seqlens), reported
+
+  float *sGamL = reinterpret_cast<float *>(sm + S_GAML);
+  float *red = reinterpret_cast<float *>(sm + S_RED);
+  float *sInv = reinterpret_cast<float *>(sm + S_INV);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_MISC);
+  uint64_t *bar_kq = bar + 1, *bar_aq = bar + 2, *bar_tu = bar + 3, *bar_z = bar + 4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) tc::mbar_init(bar + i, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&zmap);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  uint32_t ph = 0, ph_kq = 0, ph_aq = 0, ph_tu = 0, ph_z = 0;
+  bool failed = false;
+  int pend_kq = 0, pend_aq = 0, pend_tu = 0, pend_z = 0;
+
+  auto qk_slot = [&](int gg) { return ws.qk + ((size_t)gg * h_qk + hq) * kQkSlot; };
+  auto v_slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
+  auto issue_kq = [&](int gg) {
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(bar_kq, 2 * 16384 + 256);
+      tc::bulk_g2s(sm + S_KH, qk_slot(gg) + kQkK, 16384, bar_kq);
+      tc::bulk_g2s(sm + S_QH, qk_slot(gg) + kQkQ, 16384, bar_kq);
+      tc::bulk_g2s(sm + S_GAM, v_slot(gg) + kVGam, 256, bar_kq);
+    }
+  };
+  auto issue_aq = [&](int gg) {
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(bar_aq, 8192 + 16384);
+      tc::bulk_g2s(sm + S_AQ, v_slot(gg) + kVAq, 8192, bar_aq);
+      tc::bulk_g2s(sm + S_KTT, v_slot(gg) + kVKt, 16384, bar_aq);
+    }
+  };
+  auto issue_tu = [&](int gg) {
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(bar_tu, 8192 + 16384);
+      tc::bulk_g2s(sm + S_TBG, v_slot(gg) + kVTbg, 8192, bar_tu);
+      tc::bulk_g2s(sm + S_UP, v_slot(gg) + kVUp, 16384, bar_tu);
+    }
+  };
+  auto issue_z = [&](int t0_) {
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(bar_z, kC * 256);
+      tc::tma_load_2d(sm + S_Z, &zmap, h * kD, t0_, bar_z);
+    }
+  };
+
+  // ---------------- initial state -> TMEM S (fp32) and its fp16 copy
+  const size_t st_off = ((size_t)n * h_v + h) * kD * kD;
+  {
+    float v[32];
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int i = 64 * gh + c0 + q;
+        v[q] = p.init_state ? p.init_state[st_off + (size_t)i * kD + lr] : 0.0f;
+      }
+      tc::tmem_st32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        tc::st_chunk_f16(sm + S_SB + tc::sw128_chunk(128, lr, 8 * gh + (c0 >> 3) + cc), v + 8 * cc);
+    }
+  }
+  publish_operands();
+  if (g1 > g0) {
+    issue_kq(g0);
+    issue_tu(g0);
+    issue_aq(g0);
+    issue_z(s0);
+    pend_kq = pend_tu = pend_aq = pend_z = 1;
+  }
+  const float scale = rsqrtf((float)kD);
+
+  for (int g = g0; g < g1 && !failed; ++g) {
+    const int t0 = s0 + kC * (g - g0);
+    const int Lc = min(kC, s1 - t0);
+    const bool more = g + 1 < g1;
+
+    // ---------------- group 1: P^T = S K^T, D2a = S Q^T
+    if (wait_all(bar_kq, ph_kq)) { failed = true; break; }
+    pend_kq = 0;
+    if (tid == 0) {
+      mma_chain(tmem + COL_PM, sbase + S_SB, 128, 0, sbase + S_KH, 64, 0, 8, kIdN64, false);
+      mma_chain(tmem + COL_D2A, sbase + S_SB, 128, 0, sbase + S_QH, 64, 0, 8, kIdN64, false);
+      tc::mma_commit(bar);
+    }
+    if (tid < 64) sGamL[tid] = reinterpret_cast<const float *>(sm + S_GAM)[tid];
+    {  // meanwhile: S <- gamma_C S in tensor memory (the MMAs read the fp16 copy)
+      const float gC = reinterpret_cast<const float *>(sm + S_GAM)[63];
+      float v[32];
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] *= gC;
+        tc::tmem_st32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+      }
+    }
+    if (wait_all(bar, ph)) { failed = true; break; }
+    if (more) {
+      tc::fence_async_smem();
+      issue_kq(g + 1);
+      pend_kq = 1;
+    }
+    {  // -P^T -> fp16 operand
+      float v[32];
+      tc::tmem_ld32(tmem + lane_off + COL_PM + 32 * gh, v);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) v[q] = -v[q];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tc::st_chunk_f16(sm + S_PT + tc::sw128_chunk(128, lr, 4 * gh + cc), v + 8 * cc);
     }
     publish_operands();
+
+    // ---------------- group 2: X = -P^T (T diag(beta gamma))^T;  U^T = U'^T + X
+    if (wait_all(bar_tu, ph_tu)) { failed = true; break; }
+    pend_tu = 0;
+    if (tid == 0) {
+      mma_chain(tmem + COL_X, sbase + S_PT, 128, 0, sbase + S_TBG, 64, 0, 4, kIdN64, false);
+      tc::mma_commit(bar);
+    }
+    if (wait_all(bar, ph)) { failed = true; break; }
+    {
+      float u[32];
+      tc::tmem_ld32(tmem + lane_off + COL_X + 32 * gh, u);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(sm + S_UP + tc::sw128_chunk(128, lr, 4 * gh + cc));
+        const __half2 *hp = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(hp[e]);
+          u[8 * cc + 2 * e] += f.x;
+          u[8 * cc + 2 * e + 1] += f.y;
+        }
+        tc::st_chunk_f16(sm + S_US + tc::sw128_chunk(128, lr, 4 * gh + cc), u + 8 * cc);
+      }
+    }
+    publish_operands();
+    if (more) {
+      tc::fence_async_smem();
+      issue_tu(g + 1);
+      pend_tu = 1;
+    }
 
     // ---------------- group 3: D2b = U^T A_Q^T;  S += U^T K~
+    if (wait_all(bar_aq, ph_aq)) { failed = true; break; }
+    pend_aq = 0;
     if (tid == 0) {
-      mma_chain(tmem + COL_D2B, sbase + OFF_US, 128, 0, sbase + OFF_AQ, 64, 0, 4, kIdN64, false);
-      mma_chain(tmem + COL_S, sbase + OFF_US, 128, 0, sbase + OFF_KTT, 128, 0, 4, kIdN128, true);
+      mma_chain(tmem + COL_D2B, sbase + S_US, 128, 0, sbase + S_AQ, 64, 0, 4, kIdN64, false);
+      mma_chain(tmem + COL_S, sbase + S_US, 128, 0, sbase + S_KTT, 128, 0, 4, kIdN128, true);
       tc::mma_commit(bar);
     }
-    if (wait_all(bar, phase)) { failed = true; break; }
-    // A_Q .. -P^T are consumed: stage the next chunk's raw rows there
-    if (t0 + kC < s1) {
+    if (wait_all(bar, ph)) { failed = true; break; }
+    if (more) {
       tc::fence_async_smem();
-      issue_x(t0 + kC);
-      x_pending = true;
-      if (tid < 64 && t0 + kC + tid < s1) {
-        a_in = __bfloat162float(xa[(size_t)(t0 + kC + tid) * h_v + h]);
-        b_in = __bfloat162float(xb[(size_t)(t0 + kC + tid) * h_v + h]);
-      }
+      issue_aq(g + 1);
+      pend_aq = 1;
     }
 
     // ---------------- output: o = scale (gamma_r D2a + D2b), RMSNormGated, store
     {
-      const int j = lr;
-      float o[16], d2b[16];
-      tc::tmem_ld16(tmem + lane_off + COL_D2A + 16 * gq, o);
-      tc::tmem_ld16(tmem + lane_off + COL_D2B + 16 * gq, d2b);
-      float sq[16];
+      float o[32], d2b[32], sq[32];
+      tc::tmem_ld32(tmem + lane_off + COL_D2A + 32 * gh, o);
+      tc::tmem_ld32(tmem + lane_off + COL_D2B + 32 * gh, d2b);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        o[q] = scale * fmaf(sGam[16 * gq + q], o[q], d2b[q]);
+      for (int q = 0; q < 32; ++q) {
+        o[q] = scale * fmaf(sGamL[32 * gh + q], o[q], d2b[q]);
         sq[q] = o[q] * o[q];
       }
-      const float part = reduce_scatter<16>(sq, lane);
-      // warp w (quarter gq = w / 4) covers j in [32 (w & 3), +32) and tokens [16 gq, +16)
-      if ((lane & 1) == 0) red[warp * 16 + (lane >> 1)] = part;
+      const float part = reduce_scatter<32>(sq, lane);
+      red[warp * 32 + lane] = part;  // warp w of half gh: j in [32 (w & 3), +32), tokens [32 gh, +32)
       __syncthreads();
       if (tid < 64) {
-        const int qq = tid >> 4, q = tid & 15;
-        const float ssum = red[(4 * qq) * 16 + q] + red[(4 * qq + 1) * 16 + q] + red[(4 * qq + 2) * 16 + q] +
-                           red[(4 * qq + 3) * 16 + q];
+        const int hh = tid >> 5, q = tid & 31;
+        const float ssum = red[(4 * hh) * 32 + q] + red[(4 * hh + 1) * 32 + q] + red[(4 * hh + 2) * 32 + q] +
+                           red[(4 * hh + 3) * 32 + q];
         sInv[tid] = rsqrtf(ssum * (1.0f / kD) + kEpsRms);
       }
-      const bool zok = tc::mbar_wait(bar_z, phase_z & 1);
-      ++phase_z;
-      if (__syncthreads_or(!zok)) { failed = true; break; }
-      z_pending = false;
-      const float wj = p.norm_w[j];
-      const __nv_bfloat16 *zst = reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_ZST);
+      if (wait_all(bar_z, ph_z)) { failed = true; break; }
+      pend_z = 0;
+      const float wj = p.norm_w[lr];
+      const __nv_bfloat16 *zst = reinterpret_cast<const __nv_bfloat16 *>(sm + S_Z);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int r = 16 * gq + q;
+      for (int q = 0; q < 32; ++q) {
+        const int r = 32 * gh + q;
         if (r < Lc) {
-          const float zz = __bfloat162float(zst[r * kD + j]);
-          out[((size_t)(t0 + r) * h_v + h) * kD + j] = __float2bfloat16_rn(o[q] * sInv[r] * wj * silu_fast(zz));
+          const float zz = __bfloat162float(zst[r * kD + lr]);
+          out[((size_t)(t0 + r) * h_v + h) * kD + lr] = __float2bfloat16_rn(o[q] * sInv[r] * wj * silu_fast(zz));
         }
       }
     }
-    // next chunk's fp16 copy of S
-    {
+    {  // next chunk's fp16 copy of S
       float v[32];
-      tc::tmem_ld32(tmem + lane_off + COL_S + 32 * gq, v);
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tc::st_chunk_f16(sm + OFF_SB + tc::sw128_chunk(128, lr, 4 * gq + cc), v + 8 * cc);
+        for (int cc = 0; cc < 4; ++cc)
+          tc::st_chunk_f16(sm + S_SB + tc::sw128_chunk(128, lr, 8 * gh + (c0 >> 3) + cc), v + 8 * cc);
+      }
     }
     publish_operands();
+    if (more) {
+      tc::fence_async_smem();
+      issue_z(t0 + kC);
+      pend_z = 1;
+    }
   }
 
   if (failed) {
     if (tid == 0) set_status(p.status, kDevTimeout);
     // copies still in flight must land before the CTA's shared memory goes away
-    if (x_pending) tc::mbar_wait(bar_x, phase_x & 1);
-    if (z_pending) tc::mbar_wait(bar_z, phase_z & 1);
+    if (pend_kq) tc::mbar_wait(bar_kq, ph_kq & 1);
+    if (pend_aq) tc::mbar_wait(bar_aq, ph_aq & 1);
+    if (pend_tu) tc::mbar_wait(bar_tu, ph_tu & 1);
+    if (pend_z) tc::mbar_wait(bar_z, ph_z & 1);
   } else if (p.final_state) {
-    const int j = lr;
     float v[32];
-    tc::tmem_ld32(tmem + lane_off + COL_S + 32 * gq, v);
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
 #pragma unroll
-    for (int q = 0; q < 32; ++q) p.final_state[st_off + (size_t)(32 * gq + q) * kD + j] = v[q];
+      for (int q = 0; q < 32; ++q) p.final_state[st_off + (size_t)(64 * gh + c0 + q) * kD + lr] = v[q];
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-// ------------------------------------------------------------------ host side
+// ================================================================ host side
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -674,24 +898,35 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 
 }  // namespace
 
-size_t prefill_tc_workspace_bytes(int, int) { return 0; }
+size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v) { return WsLayout(T, N, h_qk, h_v).total; }
 
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
-  const unsigned grid = (unsigned)p.N * (unsigned)p.h_v;
-  if (grid == 0) return cudaSuccess;
-  TcMaps maps;
-  std::memset(&maps, 0, sizeof(maps));
-  if (p.T > 0) {  // with no tokens every chain is empty and no copy is issued
-    const bool ok = make_map(&maps.xq, p.q, (uint64_t)p.T, (uint64_t)p.h_qk * kD, kStageRows) &&
-                    make_map(&maps.xk, p.k, (uint64_t)p.T, (uint64_t)p.h_qk * kD, kStageRows) &&
-                    make_map(&maps.xv, p.v, (uint64_t)p.T, (uint64_t)p.h_v * kD, kStageRows) &&
-                    make_map(&maps.z, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, kC);
-    if (!ok) return cudaErrorInvalidValue;
-  }
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  if (p.N <= 0) return cudaSuccess;
+  const WsLayout L(p.T, p.N, p.h_qk, p.h_v);
+  if (p.ws_bytes < L.total) return cudaErrorInvalidValue;
+  Ws ws;
+  ws.chunk_base = reinterpret_cast<int *>(p.ws + L.base);
+  ws.chunk_info = reinterpret_cast<int2 *>(p.ws + L.info);
+  ws.qk = p.ws + L.qk;
+  ws.vs = p.ws + L.vs;
+  ws.max_chunks = L.max_chunks;
+  CUtensorMap zmap;
+  std::memset(&zmap, 0, sizeof(zmap));
+  if (p.T > 0 && !make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, kC)) return cudaErrorInvalidValue;
+
+  chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prefill_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, maps);
+  if (p.T > 0) {
+    e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+    if (e != cudaSuccess) return e;
+    chunk_prep_kernel<<<dim3((unsigned)L.max_chunks, (unsigned)p.h_qk), kPrepThreads, kPrepSmem, s>>>(p, ws);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
+  if (e != cudaSuccess) return e;
+  state_kernel<<<(unsigned)p.N * (unsigned)p.h_v, kStateThreads, kStateSmem, s>>>(p, ws, zmap);
   return cudaGetLastError();
 }
 

@@ -179,7 +179,7 @@ GDN_API int gdn_workspace_status(void *workspace, void *stream, int *device_stat
  *  - The device status word of this entry point is not readable by the caller
  *    (gdn_workspace_status needs a caller-owned workspace).
  */
-#define GDN_NOALLOC_SCRATCH_BYTES 65536
+#define GDN_NOALLOC_SCRATCH_BYTES (8u << 20)
 GDN_API int gdn_prefill_noalloc(const gdn_dims *dims, const void *q, const void *k, const void *v,
                                 const void *a, const void *b, const void *z, const float *conv_w,
                                 const float *A_log, const float *dt_bias, const float *norm_w,
