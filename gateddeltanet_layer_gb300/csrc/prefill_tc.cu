@@ -443,21 +443,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     {
       float v[32];
       tc::tmem_ld32(tmem + lane_off + COL_P1 + 32 * gh, v);
+      float Gs[32];  // shared-memory reads before the stores below
+#pragma unroll
+      for (int q = 0; q < 32; ++q) Gs[q] = sG[32 * gh + q];
       if (lr < 64) {
         const int r = lr;
         const float Gr = sG[r], br = sBeta[r];
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const int s = 32 * gh + q;
-          AF[r * kPad + s] = (s < r) ? br * __expf(Gr - sG[s]) * v[q] : 0.0f;
+          v[q] = (s < r) ? br * __expf(Gr - Gs[q]) * v[q] : 0.0f;
         }
+#pragma unroll
+        for (int q = 0; q < 32; ++q) AF[r * kPad + 32 * gh + q] = v[q];
       } else {
         const int r = lr - 64;
         const float Gr = sG[r];
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const int s = 32 * gh + q;
-          v[q] = (s <= r) ? __expf(Gr - sG[s]) * v[q] : 0.0f;
+          v[q] = (s <= r) ? __expf(Gr - Gs[q]) * v[q] : 0.0f;
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) st_chunk_f16_global(v_slot + kVAq + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
@@ -553,18 +558,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     // T diag(beta) (shared-memory operand) and T diag(beta gamma) (image)
     {
       const int r = tid & 63, oq = tid >> 6;  // columns [16 oq, 16 oq + 16)
+      float a16[16], b16[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {  // shared-memory reads before the stores below
+        const int m = 16 * oq + e;
+        const float t = (m <= r) ? TF[r * kPad + m] : 0.0f;
+        b16[e] = t * sBeta[m];
+        a16[e] = b16[e] * sGam[m];
+      }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        float a8[8], b8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int m = 16 * oq + 8 * hh + e;
-          const float t = (m <= r) ? TF[r * kPad + m] : 0.0f;
-          b8[e] = t * sBeta[m];
-          a8[e] = b8[e] * sGam[m];
-        }
-        tc::st_chunk_f16(sm + P_TB + tc::sw128_chunk(64, r, 2 * oq + hh), b8);
-        st_chunk_f16_global(v_slot + kVTbg + tc::sw128_chunk(64, r, 2 * oq + hh), a8);
+        tc::st_chunk_f16(sm + P_TB + tc::sw128_chunk(64, r, 2 * oq + hh), b16 + 8 * hh);
+        st_chunk_f16_global(v_slot + kVTbg + tc::sw128_chunk(64, r, 2 * oq + hh), a16 + 8 * hh);
       }
     }
     publish_operands();
@@ -591,7 +596,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 }
 
 // ================================================================ state pass
-constexpr int kStateThreads = 256;
+// Warps 0-7 (256 threads) run the state chain; warps 8-11 (128 threads) run
+// the RMSNormGated epilogue of the previous chunk at the same time, handed
+// over through two mbarriers (o-ready: main -> epilogue; o-done: back).
+constexpr int kMainThreads = 256;
+constexpr int kOutThreads = 128;
+constexpr int kStateThreads = kMainThreads + kOutThreads;
+constexpr int kBarMain = 1, kBarOut = 2;  // named barriers of the two groups
 constexpr uint32_t S_SB = 0;          // S fp16 [128 j][128 i]
 constexpr uint32_t S_KH = 32768;      // K image [64][128]    } one bulk set (with gamma)
 constexpr uint32_t S_QH = 49152;      // Q image [64][128]    }
@@ -602,19 +613,24 @@ constexpr uint32_t S_UP = 98304;      // U'^T image           }
 constexpr uint32_t S_Z = 114688;      // z rows [64][256 B] (TMA tensor copy)
 constexpr uint32_t S_PT = 131072;     // -P^T fp16 [128 j][64 m]
 constexpr uint32_t S_US = 147456;     // U^T fp16 [128 j][64 r]
-constexpr uint32_t S_GAM = 163840;    // gamma [64] (bulk, with K and Q)
-constexpr uint32_t S_GAML = S_GAM + 256;  // this chunk's gamma, kept while the next loads
-constexpr uint32_t S_RED = S_GAML + 256;
+constexpr uint32_t S_OUT = 163840;    // y rows [64][256 B] bf16, stored by TMA
+constexpr uint32_t S_GAM = 180224;    // gamma [64] (bulk, with K and Q)
+constexpr uint32_t S_GAML = S_GAM + 256;  // gamma of the last two chunks [2][64]
+constexpr uint32_t S_RED = S_GAML + 512;
 constexpr uint32_t S_INV = S_RED + 2048;
 constexpr uint32_t S_MISC = S_INV + 256;
 constexpr size_t kStateSmem = S_MISC + 128 + 1024;
 static_assert(S_US % 1024 == 0 && S_KTT % 1024 == 0 && S_TBG % 1024 == 0, "SW128 tiles 1024-aligned");
+static_assert(S_OUT % 128 == 0 && S_Z % 128 == 0, "TMA boxes 128-byte aligned");
 static_assert(kStateSmem <= 232448, "shared memory budget");
 
-constexpr int COL_S = 0, COL_PM = 128, COL_D2A = 192, COL_D2B = 256, COL_X = 320;
+// tensor memory: S, P^T, D2a (two buffers: chunk c's epilogue reads one while
+// chunk c+1's first MMA group writes the other), D2b, X
+constexpr int COL_S = 0, COL_PM = 128, COL_D2A = 192, COL_D2B = 320, COL_X = 384;
 
 __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillParams p, const Ws ws,
-                                                                 const __grid_constant__ CUtensorMap zmap) {
+                                                                 const __grid_constant__ CUtensorMap zmap,
+                                                                 const __grid_constant__ CUtensorMap omap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = tc::smem_u32(sm);
@@ -622,19 +638,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
   const int n = blockIdx.x / h_v, h = blockIdx.x % h_v;
   const int hq = h / (h_v / h_qk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lr = tid & 127, gh = tid >> 7;
+  const int lr = tid & 127;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  const bool is_main = tid < kMainThreads;
 
   const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
   if (s0 < 0 || s1 < s0 || s1 > p.T) return;  // reported by the chunk table
   const int g0 = ws.chunk_base[n], g1 = ws.chunk_base[n + 1];
   if (g1 - g0 != (s1 - s0 + kC - 1) / kC) return;  // table overflow (invalid cu_seqlens), reported
 
+  const float *sGamIn = reinterpret_cast<const float *>(sm + S_GAM);
   float *sGamL = reinterpret_cast<float *>(sm + S_GAML);
   float *red = reinterpret_cast<float *>(sm + S_RED);
   float *sInv = reinterpret_cast<float *>(sm + S_INV);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_MISC);
   uint64_t *bar_kq = bar + 1, *bar_aq = bar + 2, *bar_tu = bar + 3, *bar_z = bar + 4;
+  uint64_t *bar_oready = bar + 5, *bar_odone = bar + 6;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
   __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 
@@ -643,223 +662,317 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) tc::mbar_init(bar + i, 1);
+    for (int i = 0; i < 7; ++i) tc::mbar_init(bar + i, 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&zmap);
+    tc::prefetch_tmap(&omap);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  uint32_t ph = 0, ph_kq = 0, ph_aq = 0, ph_tu = 0, ph_z = 0;
   bool failed = false;
-  int pend_kq = 0, pend_aq = 0, pend_tu = 0, pend_z = 0;
 
-  auto qk_slot = [&](int gg) { return ws.qk + ((size_t)gg * h_qk + hq) * kQkSlot; };
-  auto v_slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
-  auto issue_kq = [&](int gg) {
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(bar_kq, 2 * 16384 + 256);
-      tc::bulk_g2s(sm + S_KH, qk_slot(gg) + kQkK, 16384, bar_kq);
-      tc::bulk_g2s(sm + S_QH, qk_slot(gg) + kQkQ, 16384, bar_kq);
-      tc::bulk_g2s(sm + S_GAM, v_slot(gg) + kVGam, 256, bar_kq);
-    }
-  };
-  auto issue_aq = [&](int gg) {
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(bar_aq, 8192 + 16384);
-      tc::bulk_g2s(sm + S_AQ, v_slot(gg) + kVAq, 8192, bar_aq);
-      tc::bulk_g2s(sm + S_KTT, v_slot(gg) + kVKt, 16384, bar_aq);
-    }
-  };
-  auto issue_tu = [&](int gg) {
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(bar_tu, 8192 + 16384);
-      tc::bulk_g2s(sm + S_TBG, v_slot(gg) + kVTbg, 8192, bar_tu);
-      tc::bulk_g2s(sm + S_UP, v_slot(gg) + kVUp, 16384, bar_tu);
-    }
-  };
-  auto issue_z = [&](int t0_) {
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(bar_z, kC * 256);
-      tc::tma_load_2d(sm + S_Z, &zmap, h * kD, t0_, bar_z);
-    }
-  };
-
-  // ---------------- initial state -> TMEM S (fp32) and its fp16 copy
-  const size_t st_off = ((size_t)n * h_v + h) * kD * kD;
-  {
-    float v[32];
-    for (int c0 = 0; c0 < 64; c0 += 32) {
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int i = 64 * gh + c0 + q;
-        v[q] = p.init_state ? p.init_state[st_off + (size_t)i * kD + lr] : 0.0f;
+  if (is_main) {
+    // ======================= state chain (warps 0-7)
+    const int gh = tid >> 7;
+    uint32_t ph = 0, ph_kq = 0, ph_aq = 0, ph_tu = 0, ph_odone = 0;
+    int pend_kq = 0, pend_aq = 0, pend_tu = 0;
+    auto qk_slot = [&](int gg) { return ws.qk + ((size_t)gg * h_qk + hq) * kQkSlot; };
+    auto v_slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
+    auto issue_kq = [&](int gg) {
+      if (tid == 0) {
+        tc::mbar_arrive_expect_tx(bar_kq, 2 * 16384 + 256);
+        tc::bulk_g2s(sm + S_KH, qk_slot(gg) + kQkK, 16384, bar_kq);
+        tc::bulk_g2s(sm + S_QH, qk_slot(gg) + kQkQ, 16384, bar_kq);
+        tc::bulk_g2s(sm + S_GAM, v_slot(gg) + kVGam, 256, bar_kq);
       }
-      tc::tmem_st32(tmem + lane_off + COL_S + 64 * gh + c0, v);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        tc::st_chunk_f16(sm + S_SB + tc::sw128_chunk(128, lr, 8 * gh + (c0 >> 3) + cc), v + 8 * cc);
-    }
-  }
-  publish_operands();
-  if (g1 > g0) {
-    issue_kq(g0);
-    issue_tu(g0);
-    issue_aq(g0);
-    issue_z(s0);
-    pend_kq = pend_tu = pend_aq = pend_z = 1;
-  }
-  const float scale = rsqrtf((float)kD);
-
-  for (int g = g0; g < g1 && !failed; ++g) {
-    const int t0 = s0 + kC * (g - g0);
-    const int Lc = min(kC, s1 - t0);
-    const bool more = g + 1 < g1;
-
-    // ---------------- group 1: P^T = S K^T, D2a = S Q^T
-    if (wait_all(bar_kq, ph_kq)) { failed = true; break; }
-    pend_kq = 0;
-    if (tid == 0) {
-      mma_chain(tmem + COL_PM, sbase + S_SB, 128, 0, sbase + S_KH, 64, 0, 8, kIdN64, false);
-      mma_chain(tmem + COL_D2A, sbase + S_SB, 128, 0, sbase + S_QH, 64, 0, 8, kIdN64, false);
-      tc::mma_commit(bar);
-    }
-    if (tid < 64) sGamL[tid] = reinterpret_cast<const float *>(sm + S_GAM)[tid];
-    {  // meanwhile: S <- gamma_C S in tensor memory (the MMAs read the fp16 copy)
-      const float gC = reinterpret_cast<const float *>(sm + S_GAM)[63];
-      float v[32];
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] *= gC;
-        tc::tmem_st32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+    };
+    auto issue_aq = [&](int gg) {
+      if (tid == 0) {
+        tc::mbar_arrive_expect_tx(bar_aq, 8192 + 16384);
+        tc::bulk_g2s(sm + S_AQ, v_slot(gg) + kVAq, 8192, bar_aq);
+        tc::bulk_g2s(sm + S_KTT, v_slot(gg) + kVKt, 16384, bar_aq);
       }
-    }
-    if (wait_all(bar, ph)) { failed = true; break; }
-    if (more) {
+    };
+    auto issue_tu = [&](int gg) {
+      if (tid == 0) {
+        tc::mbar_arrive_expect_tx(bar_tu, 8192 + 16384);
+        tc::bulk_g2s(sm + S_TBG, v_slot(gg) + kVTbg, 8192, bar_tu);
+        tc::bulk_g2s(sm + S_UP, v_slot(gg) + kVUp, 16384, bar_tu);
+      }
+    };
+    // wait (all 256 main threads) for a phase; true if it ran out
+    auto wait_main = [&](uint64_t *b, uint32_t &phase) {
+      const bool ok = tc::mbar_wait(b, phase & 1);
+      ++phase;
+      tc::fence_after_sync();
+      return tc::named_barrier_or(kBarMain, kMainThreads, !ok);
+    };
+    auto publish_main = [&]() {
       tc::fence_async_smem();
-      issue_kq(g + 1);
-      pend_kq = 1;
-    }
-    {  // -P^T -> fp16 operand
-      float v[32];
-      tc::tmem_ld32(tmem + lane_off + COL_PM + 32 * gh, v);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) v[q] = -v[q];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tc::st_chunk_f16(sm + S_PT + tc::sw128_chunk(128, lr, 4 * gh + cc), v + 8 * cc);
-    }
-    publish_operands();
-
-    // ---------------- group 2: X = -P^T (T diag(beta gamma))^T;  U^T = U'^T + X
-    if (wait_all(bar_tu, ph_tu)) { failed = true; break; }
-    pend_tu = 0;
-    if (tid == 0) {
-      mma_chain(tmem + COL_X, sbase + S_PT, 128, 0, sbase + S_TBG, 64, 0, 4, kIdN64, false);
-      tc::mma_commit(bar);
-    }
-    if (wait_all(bar, ph)) { failed = true; break; }
-    {
-      float u[32];
-      tc::tmem_ld32(tmem + lane_off + COL_X + 32 * gh, u);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(sm + S_UP + tc::sw128_chunk(128, lr, 4 * gh + cc));
-        const __half2 *hp = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(hp[e]);
-          u[8 * cc + 2 * e] += f.x;
-          u[8 * cc + 2 * e + 1] += f.y;
-        }
-        tc::st_chunk_f16(sm + S_US + tc::sw128_chunk(128, lr, 4 * gh + cc), u + 8 * cc);
-      }
-    }
-    publish_operands();
-    if (more) {
-      tc::fence_async_smem();
-      issue_tu(g + 1);
-      pend_tu = 1;
-    }
-
-    // ---------------- group 3: D2b = U^T A_Q^T;  S += U^T K~
-    if (wait_all(bar_aq, ph_aq)) { failed = true; break; }
-    pend_aq = 0;
-    if (tid == 0) {
-      mma_chain(tmem + COL_D2B, sbase + S_US, 128, 0, sbase + S_AQ, 64, 0, 4, kIdN64, false);
-      mma_chain(tmem + COL_S, sbase + S_US, 128, 0, sbase + S_KTT, 128, 0, 4, kIdN128, true);
-      tc::mma_commit(bar);
-    }
-    if (wait_all(bar, ph)) { failed = true; break; }
-    if (more) {
-      tc::fence_async_smem();
-      issue_aq(g + 1);
-      pend_aq = 1;
-    }
-
-    // ---------------- output: o = scale (gamma_r D2a + D2b), RMSNormGated, store
-    {
-      float o[32], d2b[32], sq[32];
-      tc::tmem_ld32(tmem + lane_off + COL_D2A + 32 * gh, o);
-      tc::tmem_ld32(tmem + lane_off + COL_D2B + 32 * gh, d2b);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        o[q] = scale * fmaf(sGamL[32 * gh + q], o[q], d2b[q]);
-        sq[q] = o[q] * o[q];
-      }
-      const float part = reduce_scatter<32>(sq, lane);
-      red[warp * 32 + lane] = part;  // warp w of half gh: j in [32 (w & 3), +32), tokens [32 gh, +32)
-      __syncthreads();
-      if (tid < 64) {
-        const int hh = tid >> 5, q = tid & 31;
-        const float ssum = red[(4 * hh) * 32 + q] + red[(4 * hh + 1) * 32 + q] + red[(4 * hh + 2) * 32 + q] +
-                           red[(4 * hh + 3) * 32 + q];
-        sInv[tid] = rsqrtf(ssum * (1.0f / kD) + kEpsRms);
-      }
-      if (wait_all(bar_z, ph_z)) { failed = true; break; }
-      pend_z = 0;
-      const float wj = p.norm_w[lr];
-      const __nv_bfloat16 *zst = reinterpret_cast<const __nv_bfloat16 *>(sm + S_Z);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int r = 32 * gh + q;
-        if (r < Lc) {
-          const float zz = __bfloat162float(zst[r * kD + lr]);
-          out[((size_t)(t0 + r) * h_v + h) * kD + lr] = __float2bfloat16_rn(o[q] * sInv[r] * wj * silu_fast(zz));
-        }
-      }
-    }
-    {  // next chunk's fp16 copy of S
+      tc::fence_before_sync();
+      tc::named_barrier(kBarMain, kMainThreads);
+      tc::fence_after_sync();
+    };
+    // S (fp32, tensor memory) -> its fp16 copy, then S <- gamma_C S for the
+    // coming chunk's update (gamma_C from the freshly loaded gamma vector).
+    auto copy_and_scale_state = [&]() {
+      const float gC = sGamIn[63];
       float v[32];
       for (int c0 = 0; c0 < 64; c0 += 32) {
         tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
           tc::st_chunk_f16(sm + S_SB + tc::sw128_chunk(128, lr, 8 * gh + (c0 >> 3) + cc), v + 8 * cc);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] *= gC;
+        tc::tmem_st32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+      }
+    };
+
+    // ---------------- initial state -> TMEM S (fp32)
+    const size_t st_off = ((size_t)n * h_v + h) * kD * kD;
+    {
+      float v[32];
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int i = 64 * gh + c0 + q;
+          v[q] = p.init_state ? p.init_state[st_off + (size_t)i * kD + lr] : 0.0f;
+        }
+        tc::tmem_st32(tmem + lane_off + COL_S + 64 * gh + c0, v);
       }
     }
-    publish_operands();
-    if (more) {
-      tc::fence_async_smem();
-      issue_z(t0 + kC);
+    tc::fence_before_sync();
+    tc::named_barrier(kBarMain, kMainThreads);
+    tc::fence_after_sync();
+    if (g1 > g0) {
+      issue_kq(g0);
+      issue_tu(g0);
+      issue_aq(g0);
+      pend_kq = pend_tu = pend_aq = 1;
+      if (wait_main(bar_kq, ph_kq)) failed = true;
+      if (!failed) {
+        pend_kq = 0;
+        if (tid < 64) sGamL[tid] = sGamIn[tid];
+        copy_and_scale_state();
+      }
+    }
+    publish_main();
+
+    for (int g = g0; g < g1 && !failed; ++g) {
+      const int buf = (g - g0) & 1;
+      const bool more = g + 1 < g1;
+
+      // ---------------- group 1: P^T = S K^T, D2a = S Q^T (S entering the chunk, fp16 copy)
+      if (tid == 0) {
+        mma_chain(tmem + COL_PM, sbase + S_SB, 128, 0, sbase + S_KH, 64, 0, 8, kIdN64, false);
+        mma_chain(tmem + COL_D2A + 64 * buf, sbase + S_SB, 128, 0, sbase + S_QH, 64, 0, 8, kIdN64, false);
+        tc::mma_commit(bar);
+      }
+      if (wait_main(bar, ph)) { failed = true; break; }
+      if (more) {
+        tc::fence_async_smem();
+        issue_kq(g + 1);
+        pend_kq = 1;
+      }
+      {  // -P^T -> fp16 operand
+        float v[32];
+        tc::tmem_ld32(tmem + lane_off + COL_PM + 32 * gh, v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = -v[q];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tc::st_chunk_f16(sm + S_PT + tc::sw128_chunk(128, lr, 4 * gh + cc), v + 8 * cc);
+      }
+      publish_main();
+
+      // ---------------- group 2: X = -P^T (T diag(beta gamma))^T;  U^T = U'^T + X
+      if (wait_main(bar_tu, ph_tu)) { failed = true; break; }
+      pend_tu = 0;
+      if (tid == 0) {
+        mma_chain(tmem + COL_X, sbase + S_PT, 128, 0, sbase + S_TBG, 64, 0, 4, kIdN64, false);
+        tc::mma_commit(bar);
+      }
+      if (wait_main(bar, ph)) { failed = true; break; }
+      {
+        float u[32];
+        tc::tmem_ld32(tmem + lane_off + COL_X + 32 * gh, u);
+        uint4 raw[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          raw[cc] = *reinterpret_cast<const uint4 *>(sm + S_UP + tc::sw128_chunk(128, lr, 4 * gh + cc));
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const __half2 *hp = reinterpret_cast<const __half2 *>(&raw[cc]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(hp[e]);
+            u[8 * cc + 2 * e] += f.x;
+            u[8 * cc + 2 * e + 1] += f.y;
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tc::st_chunk_f16(sm + S_US + tc::sw128_chunk(128, lr, 4 * gh + cc), u + 8 * cc);
+      }
+      publish_main();
+      if (more) {
+        tc::fence_async_smem();
+        issue_tu(g + 1);
+        pend_tu = 1;
+      }
+
+      // ---------------- group 3: D2b = U^T A_Q^T;  S += U^T K~   (S already scaled by gamma_C)
+      if (g > g0) {  // the epilogue has read the previous chunk's D2b
+        if (wait_main(bar_odone, ph_odone)) { failed = true; break; }
+      }
+      if (wait_main(bar_aq, ph_aq)) { failed = true; break; }
+      pend_aq = 0;
+      if (tid == 0) {
+        mma_chain(tmem + COL_D2B, sbase + S_US, 128, 0, sbase + S_AQ, 64, 0, 4, kIdN64, false);
+        mma_chain(tmem + COL_S, sbase + S_US, 128, 0, sbase + S_KTT, 128, 0, 4, kIdN128, true);
+        tc::mma_commit(bar);
+      }
+      if (wait_main(bar, ph)) { failed = true; break; }
+      if (tid == 0) {  // this chunk's D2a, D2b and gamma are ready for the epilogue
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_oready);
+      }
+      if (more) {
+        tc::fence_async_smem();
+        issue_aq(g + 1);
+        pend_aq = 1;
+      }
+
+      // ---------------- next chunk's fp16 state copy (and gamma_C scaling of S)
+      if (more) {
+        if (wait_main(bar_kq, ph_kq)) { failed = true; break; }
+        pend_kq = 0;
+        if (tid < 64) sGamL[64 * (buf ^ 1) + tid] = sGamIn[tid];
+        copy_and_scale_state();
+      }
+      publish_main();
+    }
+
+    if (failed) {
+      if (tid == 0) set_status(p.status, kDevTimeout);
+      // copies still in flight must land before the CTA's shared memory goes away
+      if (pend_kq) tc::mbar_wait(bar_kq, ph_kq & 1);
+      if (pend_aq) tc::mbar_wait(bar_aq, ph_aq & 1);
+      if (pend_tu) tc::mbar_wait(bar_tu, ph_tu & 1);
+    } else if (p.final_state) {
+      float v[32];
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) p.final_state[st_off + (size_t)(64 * gh + c0 + q) * kD + lr] = v[q];
+      }
+    }
+  } else {
+    // ======================= RMSNormGated epilogue (warps 8-11), one chunk behind
+    const int otid = tid - kMainThreads, ow = warp - 8;  // lane j = otid
+    uint32_t ph_oready = 0, ph_z = 0;
+    int pend_z = 0;
+    const float scale = rsqrtf((float)kD);
+    const float wj = p.norm_w[lr];
+    auto issue_z = [&](int t0_) {
+      if (otid == 0) {
+        tc::mbar_arrive_expect_tx(bar_z, kC * 256);
+        tc::tma_load_2d(sm + S_Z, &zmap, h * kD, t0_, bar_z);
+      }
+    };
+    auto wait_out = [&](uint64_t *b, uint32_t &phase) {
+      const bool ok = tc::mbar_wait(b, phase & 1);
+      ++phase;
+      tc::fence_after_sync();
+      return tc::named_barrier_or(kBarOut, kOutThreads, !ok);
+    };
+    if (g1 > g0) {
+      issue_z(s0);
       pend_z = 1;
     }
-  }
-
-  if (failed) {
-    if (tid == 0) set_status(p.status, kDevTimeout);
-    // copies still in flight must land before the CTA's shared memory goes away
-    if (pend_kq) tc::mbar_wait(bar_kq, ph_kq & 1);
-    if (pend_aq) tc::mbar_wait(bar_aq, ph_aq & 1);
-    if (pend_tu) tc::mbar_wait(bar_tu, ph_tu & 1);
-    if (pend_z) tc::mbar_wait(bar_z, ph_z & 1);
-  } else if (p.final_state) {
-    float v[32];
-    for (int c0 = 0; c0 < 64; c0 += 32) {
-      tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+    for (int g = g0; g < g1; ++g) {
+      const int t0 = s0 + kC * (g - g0);
+      const int Lc = min(kC, s1 - t0);
+      const int buf = (g - g0) & 1;
+      if (wait_out(bar_oready, ph_oready)) { failed = true; break; }
+      // o = scale (gamma_r D2a + D2b) for this lane j and the chunk's 64 tokens
+      float o[64];
+      {
+        float d[32];
+        const float *gam = sGamL + 64 * buf;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) p.final_state[st_off + (size_t)(64 * gh + c0 + q) * kD + lr] = v[q];
+        for (int hh = 0; hh < 2; ++hh) {
+          float a32[32];
+          tc::tmem_ld32(tmem + lane_off + COL_D2A + 64 * buf + 32 * hh, a32);
+          tc::tmem_ld32(tmem + lane_off + COL_D2B + 32 * hh, d);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) o[32 * hh + q] = scale * fmaf(gam[32 * hh + q], a32[q], d[q]);
+        }
+      }
+      // D2a, D2b and gamma are read: the state chain may overwrite them
+      tc::fence_before_sync();
+      tc::named_barrier(kBarOut, kOutThreads);
+      if (otid == 0) tc::mbar_arrive(bar_odone);
+      // per-token sum of squares over j (the 128 lanes of the four epilogue warps)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float sq[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) sq[q] = o[32 * hh + q] * o[32 * hh + q];
+        red[(hh * 4 + ow) * 32 + lane] = reduce_scatter<32>(sq, lane);
+      }
+      if (otid < 64) tc::bulk_wait_read();  // the previous chunk's y rows have left S_OUT
+      tc::named_barrier(kBarOut, kOutThreads);
+      if (otid < 64) {
+        const int hh = otid >> 5, q = otid & 31;
+        const float ssum = red[(hh * 4) * 32 + q] + red[(hh * 4 + 1) * 32 + q] + red[(hh * 4 + 2) * 32 + q] +
+                           red[(hh * 4 + 3) * 32 + q];
+        sInv[otid] = rsqrtf(ssum * (1.0f / kD) + kEpsRms);
+      }
+      if (wait_out(bar_z, ph_z)) { failed = true; break; }
+      pend_z = 0;
+      const __nv_bfloat16 *zst = reinterpret_cast<const __nv_bfloat16 *>(sm + S_Z);
+      __nv_bfloat16 *yst = reinterpret_cast<__nv_bfloat16 *>(sm + S_OUT);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float zz[32], iv[32];  // shared-memory reads before the stores
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          zz[q] = __bfloat162float(zst[(32 * hh + q) * kD + lr]);
+          iv[q] = sInv[32 * hh + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          // silu(z) = z (1 + tanh(z / 2)) / 2 with the hardware tanh: its ~2^-11
+          // error scales one output element, well inside the output rounding
+          const float th = tc::tanh_approx(0.5f * zz[q]);
+          o[32 * hh + q] = o[32 * hh + q] * iv[q] * wj * (0.5f * zz[q]) * (1.0f + th);
+        }
+#pragma unroll
+        for (int q = 0; q < 32; ++q) yst[(32 * hh + q) * kD + lr] = __float2bfloat16_rn(o[32 * hh + q]);
+      }
+      tc::fence_async_smem();
+      tc::named_barrier(kBarOut, kOutThreads);
+      if (Lc == kC) {
+        if (otid == 0) {
+          tc::tma_store_2d(&omap, h * kD, t0, sm + S_OUT);
+          tc::bulk_commit();
+        }
+      } else if (otid < Lc) {  // a sequence's last, short chunk: only its own rows
+        tc::bulk_s2g(out + ((size_t)(t0 + otid) * h_v + h) * kD, sm + S_OUT + otid * 256, 256);
+        tc::bulk_commit();
+      }
+      if (g + 1 < g1) {  // the z rows of the next chunk, over the ones just used
+        tc::fence_async_smem();
+        issue_z(t0 + kC);
+        pend_z = 1;
+      }
+    }
+    if (otid < 64) tc::bulk_wait_all();
+    if (failed) {
+      if (otid == 0) set_status(p.status, kDevTimeout);
+      if (pend_z) tc::mbar_wait(bar_z, ph_z & 1);
     }
   }
   tc::fence_before_sync();
@@ -910,9 +1023,12 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   ws.qk = p.ws + L.qk;
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
-  CUtensorMap zmap;
+  CUtensorMap zmap, omap;
   std::memset(&zmap, 0, sizeof(zmap));
-  if (p.T > 0 && !make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, kC)) return cudaErrorInvalidValue;
+  std::memset(&omap, 0, sizeof(omap));
+  if (p.T > 0 && !(make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, kC) &&
+                   make_map(&omap, p.out, (uint64_t)p.T, (uint64_t)p.h_v * kD, kC)))
+    return cudaErrorInvalidValue;
 
   chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
   cudaError_t e = cudaGetLastError();
@@ -926,7 +1042,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   }
   e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
   if (e != cudaSuccess) return e;
-  state_kernel<<<(unsigned)p.N * (unsigned)p.h_v, kStateThreads, kStateSmem, s>>>(p, ws, zmap);
+  state_kernel<<<(unsigned)p.N * (unsigned)p.h_v, kStateThreads, kStateSmem, s>>>(p, ws, zmap, omap);
   return cudaGetLastError();
 }
 
