@@ -135,10 +135,12 @@ def _device_inputs(inp, dev):
     return t
 
 
-def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False):
+def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False, trace=False):
     """Per-step device time (CUDA events on the launching stream, L2 flushed
     between steps) of one gdn_prefill call; optionally the end-to-end time with
-    pinned-host inputs copied in and outputs copied out every step."""
+    pinned-host inputs copied in and outputs copied out every step, and the
+    library's per-kernel trace (CUDA events around each of its launches, on the
+    same stream) over the timed steps."""
     import torch
 
     import gateddeltanet_layer_gb300 as gdn
@@ -161,17 +163,24 @@ def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False):
         call()
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if trace:
+        gdn.trace_enable(True)
+        gdn.trace_read()
     for s, e in ev:
         flush.zero_()
         s.record(stream)
         call()
         e.record(stream)
     torch.cuda.synchronize(dev)
+    kernels = None
+    if trace:
+        kernels = gdn.trace_read()
+        gdn.trace_enable(False)
     ms = [s.elapsed_time(e) for s, e in ev]
     status = gdn.workspace_status(ws, stream)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed prefill")
-    res = {"ms": ms}
+    res = {"ms": ms, "kernels": kernels}
     if with_e2e:
         res["e2e"] = _prefill_e2e(t, cfg, steps, warmup, dev, flush, out, fs, ws, stream)
     del t
@@ -282,7 +291,7 @@ def run_ours(args):
     barrier()
     with ClockSampler(torch.cuda.current_device()) as clk:
         t0 = time.perf_counter()
-        res = time_prefill(cfg, args.steps, args.warmup, dev, flush, with_e2e=True)
+        res = time_prefill(cfg, args.steps, args.warmup, dev, flush, with_e2e=True, trace=True)
         barrier()
         wall = time.perf_counter() - t0
     ms = statistics.mean(res["ms"])
@@ -293,14 +302,27 @@ def run_ours(args):
         ms, e2e_ms = float(tt[0]), float(tt[1])
     nbytes, flops = prefill_work(cfg)
     rf = roofline_of(nbytes, flops, ms, pk)
+    # the dominant kernel: most device time over the timed steps (library trace)
+    kernels = res["kernels"]
+    top = max(kernels, key=lambda k: kernels[k][1])
+    top_n, top_ms_total = kernels[top]
+    top_ms = top_ms_total / top_n
+    if world > 1:
+        tt = torch.tensor([top_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        top_ms = float(tt[0])
+    top_gbs = nbytes / (top_ms * 1e-3) / 1e9
+    launches = sum(n for n, _ in kernels.values())
 
     extra = {}
     if not args.quick:
         for c in (synth.VARLEN_32K, synth.LONG_128K):
-            r = time_prefill(c, max(3, args.steps // 4), args.warmup, dev, flush)
+            n_steps = max(3, args.steps // 4)
+            r = time_prefill(c, n_steps, args.warmup, dev, flush, trace=True)
             m = statistics.mean(r["ms"])
             b_, f_ = prefill_work(c)
-            extra[c.name] = {"tokens_per_s": c.T / (m * 1e-3), "ms": m, **roofline_of(b_, f_, m, pk)}
+            extra[c.name] = {"tokens_per_s": c.T / (m * 1e-3), "ms": m, **roofline_of(b_, f_, m, pk),
+                             "kernels_ms_per_step": {k: v[1] / n_steps for k, v in r["kernels"].items()}}
         dc = synth.DECODE_256
         r = time_decode(dc, args.steps, args.warmup, dev, flush)
         m = statistics.mean(r["ms"])
@@ -325,14 +347,16 @@ def run_ours(args):
         "config": {"workload": cfg.name, "tokens": cfg.T, "seqs": cfg.N, "h_qk": cfg.h_qk, "h_v": cfg.h_v,
                    "d_k": cfg.d_k, "d_v": cfg.d_v, "state": "fp32", "final_state": True,
                    "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": rf["achieved_gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": rf["achieved_gbs"] / pk["hbm_gbs"], "traffic": None,
-                     "peak_source": pk["source"], "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                     "kernel": "gdn_prefill (all launches of one call)"},
+        "roofline": {"bound": "hbm", "achieved": top_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": top_gbs / pk["hbm_gbs"], "traffic": profiled_traffic(top),
+                     "peak_source": pk["source"] + " (burst copy)", "kernel": top,
+                     "kernel_ms": top_ms, "algorithmic_bytes_per_launch": nbytes,
+                     "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kernels.items()},
+                     "whole_call": {"achieved": rf["achieved_gbs"], "frac": rf["roofline_frac"]}},
         "cpu_baseline": cpu,
         "e2e": {"value": world * cfg.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"]},
-        "gpu_launches": args.steps * LAUNCHES_PER_PREFILL,
+        "gpu_launches": launches,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
         "extra": extra,
@@ -340,7 +364,25 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
-LAUNCHES_PER_PREFILL = 1
+def profiled_traffic(kernel):
+    """DRAM bytes (read + write) per launch of `kernel` on the headline workload,
+    from the committed ncu summary, or None when that summary is missing or was
+    taken on another version of the kernel's source file."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_prefill_T4096.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_bytes", "source_")))
+    try:
+        src = fields["source_file"].strip()
+        digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()
+        if digest != fields["source_sha256"].strip():
+            return None
+        return int(fields["traffic_bytes_per_launch"].strip())
+    except (KeyError, OSError, ValueError):
+        return None
 
 
 # ---------------------------------------------------------------------- CPU oracle

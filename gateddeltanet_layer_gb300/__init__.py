@@ -60,6 +60,13 @@ def library() -> ctypes.CDLL:
             lib.gdn_workspace_status.restype = ctypes.c_int
             lib.gdn_status_string.argtypes = [ctypes.c_int]
             lib.gdn_status_string.restype = ctypes.c_char_p
+            lib.gdn_trace_enable.argtypes = [ctypes.c_int]
+            lib.gdn_trace_enable.restype = ctypes.c_int
+            lib.gdn_trace_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                           ctypes.POINTER(ctypes.c_double)]
+            lib.gdn_trace_read.restype = ctypes.c_int
+            lib.gdn_trace_kernel_name.argtypes = [ctypes.c_int]
+            lib.gdn_trace_kernel_name.restype = ctypes.c_char_p
             _lib = lib
     return _lib
 
@@ -191,6 +198,24 @@ def workspace_status(workspace, stream=None) -> int:
     _check(lib.gdn_workspace_status(_ptr(workspace), _stream_handle(stream, workspace.device),
                                     ctypes.byref(res)), "gdn_workspace_status")
     return res.value
+
+
+# Number of kernel kinds the trace distinguishes (GDN_K_COUNT in include/gdn_trace.h).
+TRACE_KINDS = 5
+
+
+def trace_enable(on: bool = True) -> None:
+    """Start (or stop) recording CUDA events around every kernel the library launches."""
+    _check(library().gdn_trace_enable(1 if on else 0), "gdn_trace_enable")
+
+
+def trace_read() -> dict:
+    """Per kernel name: (launches, total device ms) recorded since the last read; clears the record."""
+    lib = library()
+    n = (ctypes.c_int * TRACE_KINDS)()
+    ms = (ctypes.c_double * TRACE_KINDS)()
+    _check(lib.gdn_trace_read(TRACE_KINDS, n, ms), "gdn_trace_read")
+    return {lib.gdn_trace_kernel_name(k).decode(): (n[k], ms[k]) for k in range(TRACE_KINDS) if n[k]}
 
 
 # Size of the library's fixed scratch array used by gdn_prefill_noalloc

@@ -12,6 +12,7 @@
 // [w*R, (w+1)*R) of H (R = d_k / 8), lane l owns columns [4l, 4l+4); each
 // thread keeps its R x 4 block in registers between the read and the write.
 #include "gdn_common.cuh"
+#include "../../include/gdn_trace.h"
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -187,10 +188,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
 cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s) {
   const unsigned grid = (unsigned)p.B * (unsigned)p.h_qk;
   if (grid == 0) return cudaSuccess;
+  trace_begin(s, GDN_K_DECODE);
   if (bf16)
     decode_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(p);
   else
     decode_kernel<float><<<grid, kThreads, 0, s>>>(p);
+  trace_end(s);
   return cudaGetLastError();
 }
 

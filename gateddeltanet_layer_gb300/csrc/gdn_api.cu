@@ -3,7 +3,6 @@
 // is computed by the kernels in this directory.
 #include <cuda_runtime.h>
 #include <stdint.h>
-#include <stdlib.h>
 
 #include "../../include/gdn.h"
 #include "gdn_internal.h"
@@ -81,7 +80,7 @@ int gdn_prefill(const gdn_dims *d, const void *q, const void *k, const void *v, 
 
   cudaError_t e;
   if (use_tensor_core_prefill(d))
-    e = getenv("GDN_PREFILL_FUSED") ? gdn::launch_prefill_fused(p, s) : gdn::launch_prefill_tc(p, s);
+    e = gdn::launch_prefill_tc(p, s);
   else
     e = gdn::launch_prefill_simt(p, d->io_dtype == GDN_BF16, s);
   if (owned) cudaFreeAsync(ws, s);

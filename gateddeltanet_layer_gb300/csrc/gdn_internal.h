@@ -33,8 +33,12 @@ cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t 
 // Chunked tensor-core prefill (bf16 streams, d_k = d_v = 128).
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
 size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v);
-cudaError_t launch_prefill_fused(const PrefillParams &p, cudaStream_t s);
 // Decode step.
 cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s);
+
+// Kernel timing trace (gdn_trace.cu): events around one launch on its stream;
+// no-ops while tracing is off.  `kind` is a gdn_kernel_kind.
+void trace_begin(cudaStream_t s, int kind);
+void trace_end(cudaStream_t s);
 
 }  // namespace gdn

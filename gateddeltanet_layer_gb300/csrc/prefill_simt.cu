@@ -10,6 +10,7 @@
 // waiting for the others; only the RMSNormGated epilogue needs every column,
 // and it runs once per batch of kTB tokens.
 #include "gdn_common.cuh"
+#include "../../include/gdn_trace.h"
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -193,12 +194,16 @@ cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t 
     auto kern = prefill_simt_kernel<__nv_bfloat16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    trace_begin(s, GDN_K_PREFILL_SIMT);
     kern<<<grid, threads, smem, s>>>(p);
+    trace_end(s);
   } else {
     auto kern = prefill_simt_kernel<float>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    trace_begin(s, GDN_K_PREFILL_SIMT);
     kern<<<grid, threads, smem, s>>>(p);
+    trace_end(s);
   }
   return cudaGetLastError();
 }

@@ -52,6 +52,7 @@
 #include <mutex>
 
 #include "gdn_common.cuh"
+#include "../../include/gdn_trace.h"
 #include "gdn_internal.h"
 #include "tc_ptx.cuh"
 
@@ -1030,19 +1031,25 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
                    make_map(&omap, p.out, (uint64_t)p.T, (uint64_t)p.h_v * kD, kC)))
     return cudaErrorInvalidValue;
 
+  trace_begin(s, GDN_K_CHUNK_TABLE);
   chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
+  trace_end(s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.T > 0) {
     e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
+    trace_begin(s, GDN_K_CHUNK_PREP);
     chunk_prep_kernel<<<dim3((unsigned)L.max_chunks, (unsigned)p.h_qk), kPrepThreads, kPrepSmem, s>>>(p, ws);
+    trace_end(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
   if (e != cudaSuccess) return e;
+  trace_begin(s, GDN_K_STATE);
   state_kernel<<<(unsigned)p.N * (unsigned)p.h_v, kStateThreads, kStateSmem, s>>>(p, ws, zmap, omap);
+  trace_end(s);
   return cudaGetLastError();
 }
 

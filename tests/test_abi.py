@@ -93,3 +93,13 @@ def test_library_fails_loudly_when_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "_lib", None)
     with pytest.raises(ImportError):
         gdn.library()
+
+
+def test_trace_read_without_launches(lib):
+    """The kernel trace reads back empty (and names its kernel kinds) without a GPU."""
+    assert gdn.trace_read() == {}
+    names = [lib.gdn_trace_kernel_name(k).decode() for k in range(gdn.TRACE_KINDS)]
+    assert names == ["chunk_table_kernel", "chunk_prep_kernel", "state_kernel", "prefill_simt_kernel",
+                     "decode_kernel"]
+    assert lib.gdn_trace_kernel_name(gdn.TRACE_KINDS) == b""
+    assert lib.gdn_trace_read(0, None, None) == 1

@@ -136,3 +136,22 @@ def test_invalid_arguments_raise():
         gdn.prefill(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
                     t["dt_bias"], t["norm_w"], t["cu_seqlens"])
     assert e.value.status == 1
+
+
+def test_kernel_trace_counts_each_launch():
+    """With tracing on, each prefill records its three launches (chunk table,
+    chunk prep, state pass) with positive device times; tracing off records nothing."""
+    gdn = _gdn()
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=(130, 64), h_qk=2, h_v=4, seed=14)
+    inp = synth.make_prefill(cfg)
+    gdn.trace_enable(True)
+    gdn.trace_read()
+    run_gpu(inp, True)
+    run_gpu(inp, True)
+    rec = gdn.trace_read()
+    gdn.trace_enable(False)
+    assert set(rec) == {"chunk_table_kernel", "chunk_prep_kernel", "state_kernel"}
+    for name, (n, ms) in rec.items():
+        assert n == 2 and ms > 0, (name, n, ms)
+    run_gpu(inp, True)
+    assert gdn.trace_read() == {}
