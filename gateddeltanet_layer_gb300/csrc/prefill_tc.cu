@@ -21,15 +21,18 @@
 //                       conv(4) + SiLU + L2 norm of q, k (shared by the value
 //                       heads of the q/k head) and v, the gates, P1 = [K; Q] K^T
 //                       on the tensor cores, A and A_Q, the blocked inverse T,
-//                       U' = T diag(beta) V on the tensor cores; writes the
-//                       state pass's MMA operands, already in their shared-
-//                       memory image, to the workspace.
-//   state_kernel        one CTA per (sequence, value head) chain: H lives in
-//                       tensor memory (as S, lane j over d_v); per chunk three
-//                       MMA groups  (P^T = S K^T, D2a = S Q^T),  U^T = U'^T -
-//                       P^T (T diag(beta gamma))^T,  (D2b = U^T A_Q^T,
-//                       S += U^T K~), and the RMSNormGated epilogue; the next
-//                       chunk's operands stream in by TMA while it works.
+//                       and on the tensor cores W = T diag(beta gamma) K and
+//                       U' = T diag(beta) V; writes the state pass's operands
+//                       ([Q^; W] with Q^ = diag(gamma) Q, K~^T, U', -A_Q,
+//                       gamma), already in their shared-memory image.
+//   state_kernel        per (sequence, value head) chain a cluster of CTAs,
+//                       each owning a slice of the columns of H (d_v), held in
+//                       tensor memory.  Per chunk two MMA steps: U = U' - W H
+//                       (with -Q^ H in the same 128-row product), then
+//                       H <- gamma_C H + K~^T U and O += A_Q U; an epilogue
+//                       warp pair forms y, exchanging the per-token sums of
+//                       o^2 across the cluster; a producer warp streams the
+//                       next chunk's operands in by TMA.
 //
 // Every dense contraction is a tcgen05.mma chain with M = 128 (the transposed
 // forms keep M at d_k or d_v), fp16 operands in 128-byte-swizzled K-major
@@ -42,7 +45,7 @@
 // magnifies the rounding error of rows whose o is small: with bf16 operands
 // single outputs drifted by up to 6 % of max(1, |y|), with fp16 by under 1 %.
 // All operands are bounded well inside the fp16 range (|x| <= ~4: unit-norm
-// q, k, the SiLU-conv'd v of O(1) inputs, T diag(beta), P and the state).  The
+// q, k, the SiLU-conv'd v of O(1) inputs, T diag(beta), W and the state).  The
 // q.k and k.k products of P1 use a hi + lo split (P1 = hi.hi + hi.lo + lo.hi),
 // which recovers ~22 bits for A and A_Q.
 #include <cuda.h>
@@ -64,18 +67,22 @@ constexpr int kD = 128;
 constexpr int kPad = 65;  // fp32 64 x 64 matrices: padded rows
 
 // ---------------------------------------------------------------- workspace
-// Per (chunk, q/k head): the K and Q images ([64 rows][128 cols] fp16 SW128).
-// Per (chunk, value head): A_Q [64][64], T diag(beta gamma) [64][64],
-// U'^T [128][64], K~^T [128][64] (fp16 SW128 images) and gamma [64] fp32.
-constexpr uint32_t kQkSlot = 32768;
-constexpr uint32_t kQkK = 0, kQkQ = 16384;
-constexpr uint32_t kVSlot = 50176;
-constexpr uint32_t kVAq = 0, kVTbg = 8192, kVUp = 16384, kVKt = 32768, kVGam = 49152;
+// Per (chunk, value head), operand images the state pass copies straight into
+// shared memory (fp16; SW128 K-major unless noted):
+//   [Q^; W]  [128 rows][128 cols]: rows 0-63 Q^ = diag(gamma) Q, rows 64-127
+//            W = T diag(beta gamma) K (one 128-row MMA operand)
+//   K~^T     [128 i][64 m] = (diag(e^(G_C - G)) K)^T
+//   U'       T diag(beta) V, plain row-major per state slice: [kSlices][64 m][kBV]
+//   -A_Q     [64 r][64 s], A_Q = D o (Q K^T), lower triangle with the diagonal
+//   gamma    [64] fp32
+constexpr int kSlices = 4;                 // state column slices (CTAs) per (sequence, value head)
+constexpr int kBV = 128 / kSlices;         // state columns per slice
+constexpr uint32_t kVWQ = 0, kVKt = 32768, kVUp = 49152, kVAq = 65536, kVGam = 73728;
+constexpr uint32_t kVSlot = 73984;
 
 struct Ws {
   int *chunk_base;   // [N + 1]: first chunk of each sequence; [N] = number of chunks
   int2 *chunk_info;  // [max_chunks]: (sequence, first token)
-  uint8_t *qk;       // [max_chunks][h_qk] x kQkSlot
   uint8_t *vs;       // [max_chunks][h_v] x kVSlot
   int max_chunks;
 };
@@ -83,14 +90,14 @@ struct Ws {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t base, info, qk, vs, total;
+  size_t base, info, vs, total;
   int max_chunks;
   WsLayout(int T, int N, int h_qk, int h_v) {
+    (void)h_qk;
     max_chunks = (T + kC - 1) / kC + N;
     base = 0;
     info = align_up(sizeof(int) * (size_t)(N + 1), 1024);
-    qk = align_up(info + sizeof(int2) * (size_t)max_chunks, 1024);
-    vs = qk + (size_t)max_chunks * h_qk * kQkSlot;
+    vs = align_up(info + sizeof(int2) * (size_t)max_chunks, 1024);
     total = vs + (size_t)max_chunks * h_v * kVSlot;
   }
 };
@@ -126,17 +133,15 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
   return v[0];
 }
 
-// SiLU x sigmoid(x) with one special-function op: e^-x by the fast exponential,
-// then 1 / (1 + e^-x) by two Newton-Raphson steps y <- y (2 - d y) from the
-// classic bit-pattern reciprocal seed (relative error < 1e-5 after the two
-// steps, far below the fp16 rounding of the result).
-__device__ __forceinline__ float silu_fast(float x) {
-  const float d = fminf(1.0f + __expf(-x), 1e30f);
-  float y = __int_as_float(0x7EF311C7 - __float_as_int(d));
-  y = y * (2.0f - d * y);
-  y = y * (2.0f - d * y);
-  return x * y;
+// SiLU x sigmoid(x) from the fast exponential and the hardware reciprocal
+// (rcp.approx: a few ulp of fp32, far below the fp16 rounding of the result;
+// 1 / inf = 0 gives the right limit for very negative x).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
+__device__ __forceinline__ float silu_fast(float x) { return x * rcp_approx(1.0f + __expf(-x)); }
 
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t &phase) {
   const bool ok = tc::mbar_wait(bar, phase & 1);
@@ -212,20 +217,21 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p
 // ================================================================ chunk prep
 constexpr int kPrepThreads = 256;
 // shared memory (from a 1024-aligned base)
-constexpr uint32_t P_KQ = 0;                          // [K; Q] hi fp16 [128][128]
+constexpr uint32_t P_KQ = 0;                          // [K; Q] hi fp16 [128][128]; after K K^T and Q K^T:
+constexpr uint32_t P_VTT = P_KQ;                      //   V^T fp16 [128 j][64 m] (B operand of U')
+constexpr uint32_t P_TBS = P_KQ + 16384;              //   [T diag(beta gamma); T diag(beta)] fp16 [128][64]
 constexpr uint32_t P_KQL = 32768;                     // [K; Q] lo, later A and T fp32 [64][65]
 constexpr uint32_t P_AF = P_KQL;
 constexpr uint32_t P_TF = P_AF + 64 * kPad * 4;
-constexpr uint32_t P_VT = 66560;                      // V^T fp16 [128 j][64 m]
-constexpr uint32_t P_TB = P_VT + 16384;               // T diag(beta) fp16 [64 r][64 m]
-constexpr uint32_t P_XF = P_TB + 8192;                // inverse block products 32 x 32 fp32
+constexpr uint32_t P_VT = 66560;                      // K^T fp16 [128 i][64 m] (B operand of W)
+constexpr uint32_t P_XF = P_VT + 16384;               // inverse block products 32 x 32 fp32
 constexpr int kMaxRep = 8;                            // value heads per q/k head
 constexpr uint32_t P_VEC = P_XF + 4096;               // per value head: G, gamma, beta, decay-to-end
 constexpr uint32_t P_RED = P_VEC + kMaxRep * 1024;
 constexpr uint32_t P_MISC = P_RED + 64;
 constexpr size_t kPrepSmem = P_MISC + 64 + 1024;
 static_assert(P_TF + 64 * kPad * 4 <= P_VT, "A and T fit over the lo tile");
-static_assert(P_VT % 1024 == 0 && P_TB % 1024 == 0, "SW128 tiles 1024-aligned");
+static_assert(P_VT % 1024 == 0 && P_TBS % 1024 == 0, "SW128 tiles 1024-aligned");
 static_assert(2 * kPrepSmem <= 232448, "two prep CTAs per SM");
 
 constexpr uint32_t kIdN64 = tc::idesc_f16(128, 64);
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const size_t qk_stride = (size_t)h_qk * kD, v_stride = (size_t)h_v * kD;
 
   if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, 128);
+    tc::tmem_alloc(tmem_slot, 256);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -325,11 +331,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  constexpr int COL_P1 = 0, COL_UP = 64;
+  constexpr int COL_P1 = 0, COL_W = 64;
   uint32_t phase = 0;
   bool failed = false;
 
-  uint8_t *qk_slot = ws.qk + ((size_t)g * h_qk + hq) * kQkSlot;
   const int r0 = 8 * warp, c0 = 4 * lane;  // prologue: this thread's rows and channels
   auto v_slot_of = [&](int vv) { return ws.vs + ((size_t)g * h_v + hq * rep + vv) * kVSlot; };
 
@@ -382,7 +387,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       const uint32_t off = tc::sw128_offset(128, 64 + r0 + r, c0);
       *reinterpret_cast<uint2 *>(sm + P_KQ + off) = hi;
       *reinterpret_cast<uint2 *>(sm + P_KQL + off) = lo;
-      *reinterpret_cast<uint2 *>(qk_slot + kQkQ + tc::sw128_offset(64, r0 + r, c0)) = hi;
+    }
+    for (int vv = 0; vv < rep; ++vv) {  // Q^ = diag(gamma) Q: rows 0-63 of the [Q^; W] image
+      const float *gam = sG + vv * 256 + 64;
+      uint8_t *dst = v_slot_of(vv) + kVWQ;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float gr = gam[r0 + r];
+        *reinterpret_cast<uint2 *>(dst + tc::sw128_offset(128, r0 + r, c0)) =
+            pack4_f16(gr * y[r][0], gr * y[r][1], gr * y[r][2], gr * y[r][3]);
+      }
     }
     conv_rows(xk + hq * kD + c0, qk_stride, p.conv_w, h_qk * kD + hq * kD + c0, t0, s0, Lc, r0, kreg);
     l2norm_rows(kreg, lane);
@@ -395,7 +409,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       const uint32_t off = tc::sw128_offset(128, r0 + r, c0);
       *reinterpret_cast<uint2 *>(sm + P_KQ + off) = hi;
       *reinterpret_cast<uint2 *>(sm + P_KQL + off) = lo;
-      *reinterpret_cast<uint2 *>(qk_slot + kQkK + tc::sw128_offset(64, r0 + r, c0)) = hi;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {  // K^T tile (B operand of W = T diag(beta gamma) K)
+      float kt[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) kt[r] = kreg[r][c];
+      tc::st_chunk_f16(sm + P_VT + tc::sw128_chunk(128, c0 + c, warp), kt);
     }
     for (int vv = 0; vv < rep; ++vv) {
       const float *dec = sG + vv * 256 + 192;
@@ -424,23 +444,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 
     const float *sG = sGall + vv * 256, *sGam = sG + 64, *sBeta = sG + 128;
 
-    // ---------------- v: conv + SiLU -> V^T tile
+    // ---------------- v: conv + SiLU -> V^T tile (over the [K; Q] tile, once K K^T and Q K^T are done)
     {
       float y[8][4];
       conv_rows(xv + h * kD + c0, v_stride, p.conv_w, 2 * h_qk * kD + h * kD + c0, t0, s0, Lc, r0, y);
+      if (vv == 0) {
+        if (wait_all(bar, phase)) { failed = true; break; }
+      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float col[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) col[r] = y[r][c];
-        tc::st_chunk_f16(sm + P_VT + tc::sw128_chunk(128, c0 + c, warp), col);
+        tc::st_chunk_f16(sm + P_VTT + tc::sw128_chunk(128, c0 + c, warp), col);
       }
     }
-    if (vv == 0) {
-      if (wait_all(bar, phase)) { failed = true; break; }
-    }
 
-    // ---------------- A (fp32, strictly lower) and A_Q (image)
+    // ---------------- A (fp32, strictly lower) and -A_Q (image)
     {
       float v[32];
       tc::tmem_ld32(tmem + lane_off + COL_P1 + 32 * gh, v);
@@ -463,7 +483,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const int s = 32 * gh + q;
-          v[q] = (s <= r) ? __expf(Gr - Gs[q]) * v[q] : 0.0f;
+          v[q] = (s <= r) ? -__expf(Gr - Gs[q]) * v[q] : 0.0f;  // -A_Q
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) st_chunk_f16_global(v_slot + kVAq + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
@@ -556,7 +576,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       for (int q = 0; q < 4; ++q) TF[(32 + rb + 8 * q) * kPad + s] = -z[q];
     }
     __syncthreads();
-    // T diag(beta) (shared-memory operand) and T diag(beta gamma) (image)
+    // [T diag(beta gamma); T diag(beta)] (one 128-row shared-memory operand)
     {
       const int r = tid & 63, oq = tid >> 6;  // columns [16 oq, 16 oq + 16)
       float a16[16], b16[16];
@@ -569,141 +589,169 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        tc::st_chunk_f16(sm + P_TB + tc::sw128_chunk(64, r, 2 * oq + hh), b16 + 8 * hh);
-        st_chunk_f16_global(v_slot + kVTbg + tc::sw128_chunk(64, r, 2 * oq + hh), a16 + 8 * hh);
+        tc::st_chunk_f16(sm + P_TBS + tc::sw128_chunk(128, r, 2 * oq + hh), a16 + 8 * hh);
+        tc::st_chunk_f16(sm + P_TBS + tc::sw128_chunk(128, 64 + r, 2 * oq + hh), b16 + 8 * hh);
       }
     }
     publish_operands();
 
-    // ---------------- U'^T = V^T (T diag(beta))^T -> image
+    // ---------------- W = T diag(beta gamma) K -> rows 64-127 of the [Q^; W] image
+    //                  (rows 0-63 of [T diag(beta gamma); T diag(beta)] K^T^T)
     if (tid == 0) {
-      mma_chain(tmem + COL_UP, sbase + P_VT, 128, 0, sbase + P_TB, 64, 0, 4, kIdN64, false);
+      mma_chain(tmem + COL_W, sbase + P_TBS, 128, 0, sbase + P_VT, 128, 0, 4, kIdN128, false);
       tc::mma_commit(bar);
     }
     if (wait_all(bar, phase)) { failed = true; break; }
-    {
-      float u[32];
-      tc::tmem_ld32(tmem + lane_off + COL_UP + 32 * gh, u);
+    if ((warp & 3) < 2) {  // TMEM lanes 0-63
+      const int r = 32 * (warp & 3) + lane, hh = warp >> 2;  // columns [64 hh, 64 hh + 64)
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) st_chunk_f16_global(v_slot + kVUp + tc::sw128_chunk(128, lr, 4 * gh + cc), u + 8 * cc);
+      for (int c32 = 0; c32 < 2; ++c32) {
+        float w[32];
+        tc::tmem_ld32(tmem + lane_off + COL_W + 64 * hh + 32 * c32, w);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          st_chunk_f16_global(v_slot + kVWQ + tc::sw128_offset(128, 64 + r, 64 * hh + 32 * c32 + 8 * cc), w + 8 * cc);
+      }
     }
     tc::fence_before_sync();
-    __syncthreads();  // V^T, T, A are reused by the next value head
+    __syncthreads();  // W is read: the accumulator takes U'
+    tc::fence_after_sync();
+
+    // ---------------- U' = T diag(beta) V -> image (rows 64-127 of [T diag(beta gamma); T diag(beta)] V)
+    if (tid == 0) {
+      mma_chain(tmem + COL_W, sbase + P_TBS, 128, 0, sbase + P_VTT, 128, 0, 4, kIdN128, false);
+      tc::mma_commit(bar);
+    }
+    if (wait_all(bar, phase)) { failed = true; break; }
+    if ((warp & 3) >= 2) {  // TMEM lanes 64-127
+      const int m = 32 * (warp & 3) - 64 + lane, hh = warp >> 2;  // columns [64 hh, 64 hh + 64)
+#pragma unroll
+      for (int c32 = 0; c32 < 2; ++c32) {
+        float u[32];
+        tc::tmem_ld32(tmem + lane_off + COL_W + 64 * hh + 32 * c32, u);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int j = 64 * hh + 32 * c32 + 8 * cc;  // state column of this 16-byte chunk
+          st_chunk_f16_global(v_slot + kVUp + ((size_t)(j / kBV) * 64 + m) * (kBV * 2) + (j % kBV) * 2, u + 8 * cc);
+        }
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();  // A, T, V^T and the accumulator are reused by the next value head
   }
   if (failed && tid == 0) set_status(p.status, kDevTimeout);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
 // ================================================================ state pass
-// Warps 0-7 (256 threads) run the state chain; warps 8-11 (128 threads) run
-// the RMSNormGated epilogue of the previous chunk at the same time, handed
-// over through two mbarriers (o-ready: main -> epilogue; o-done: back).
-constexpr int kMainThreads = 256;
-constexpr int kOutThreads = 128;
-constexpr int kStateThreads = kMainThreads + kOutThreads;
-constexpr int kBarMain = 1, kBarOut = 2;  // named barriers of the two groups
-constexpr uint32_t S_SB = 0;          // S fp16 [128 j][128 i]
-constexpr uint32_t S_KH = 32768;      // K image [64][128]    } one bulk set (with gamma)
-constexpr uint32_t S_QH = 49152;      // Q image [64][128]    }
-constexpr uint32_t S_AQ = 65536;      // A_Q image            } one bulk set
-constexpr uint32_t S_KTT = 73728;     // K~^T image           }
-constexpr uint32_t S_TBG = 90112;     // T diag(beta gamma)   } one bulk set
-constexpr uint32_t S_UP = 98304;      // U'^T image           }
-constexpr uint32_t S_Z = 114688;      // z rows [64][256 B] (TMA tensor copy)
-constexpr uint32_t S_PT = 131072;     // -P^T fp16 [128 j][64 m]
-constexpr uint32_t S_US = 147456;     // U^T fp16 [128 j][64 r]
-constexpr uint32_t S_OUT = 163840;    // y rows [64][256 B] bf16, stored by TMA
-constexpr uint32_t S_GAM = 180224;    // gamma [64] (bulk, with K and Q)
-constexpr uint32_t S_GAML = S_GAM + 256;  // gamma of the last two chunks [2][64]
-constexpr uint32_t S_RED = S_GAML + 512;
-constexpr uint32_t S_INV = S_RED + 2048;
-constexpr uint32_t S_MISC = S_INV + 256;
+// The columns j of H = S^T (d_v) evolve independently, so each (sequence,
+// value head) chain is split over a cluster of kSlices CTAs, CTA `sv` owning
+// columns [kBV sv, kBV sv + kBV).  Per chunk, with H the slice entering it:
+//   MMA 1:  D_U  = [Q^; W] (-H)            rows 0-63: -Q^ H,  rows 64-127: -W H
+//           U    = U' + D_U[64:128]         (fp32, then the fp16 operand U^T)
+//   MMA 2:  D_H += K~^T U                   (D_H scaled by gamma_C before)
+//           D_U += [-A_Q; *] U              (rows 0-63 become -O; rows 64-127 unused)
+// Every product has M = 128 rows and N = kBV columns.  A single thread issues
+// tcgen05.mma at a fixed cost per instruction, so the critical path per chunk
+// is kept to MMA 1 (8 instructions) and the K~^T U half of MMA 2 (4); the
+// A_Q U half is issued by a second thread.  Warps 0-7 run the chain (each TMEM
+// lane by two warps, one per half of the columns), warps 8-9 the epilogue one
+// chunk behind (exchanging per-token partial sums of o^2 with the other CTAs
+// of the cluster through st.async into their shared memory), warp 10 issues
+// the operand copies.
+constexpr int kStateThreads = 352;
+constexpr int kMainThreads = 256, kEpiThreads = 64;
+constexpr int kBarMain = 1, kBarEpi = 2;
+constexpr int kHalf = kBV / 2;                         // columns per chain thread
+constexpr uint32_t S_WQ = 0;                           // [Q^; W] image (32 KB)
+constexpr uint32_t S_KT = 32768;                       // K~^T [128 i][64 m] (16 KB)
+constexpr uint32_t S_AQ = 49152;                       // -A_Q [64][64] (8 KB), rows 64-127 of its
+constexpr uint32_t S_NH = S_AQ + 8192;                 //   operand read the first 8 KB here (unused)
+constexpr uint32_t S_NU = S_NH + kBV * 256;            // U^T fp16 [kBV j][64 m]
+constexpr uint32_t S_UP = S_NU + kBV * 128;            // U' [64 m][kBV] fp16 (plain)
+constexpr uint32_t S_Z = S_UP + kBV * 128;             // z [64 t][kBV] bf16 (TMA)
+constexpr uint32_t S_Y = S_Z + kBV * 128;              // y [64 t][kBV] bf16 (TMA store)
+constexpr uint32_t S_GAM = S_Y + kBV * 128;            // gamma [64]
+constexpr uint32_t S_WN = S_GAM + 256;                 // norm_w of this slice [kBV]
+constexpr uint32_t S_PART = S_WN + kBV * 4;            // partial sums of o^2 [2][kSlices][64]
+constexpr uint32_t S_MISC = S_PART + 2 * kSlices * 64 * 4;
 constexpr size_t kStateSmem = S_MISC + 128 + 1024;
-static_assert(S_US % 1024 == 0 && S_KTT % 1024 == 0 && S_TBG % 1024 == 0, "SW128 tiles 1024-aligned");
-static_assert(S_OUT % 128 == 0 && S_Z % 128 == 0, "TMA boxes 128-byte aligned");
-static_assert(kStateSmem <= 232448, "shared memory budget");
+static_assert(S_NH % 1024 == 0 && S_NU % 1024 == 0 && S_KT % 1024 == 0 && S_AQ % 1024 == 0, "SW128 tiles");
+static_assert(kBV * 256 >= 8192, "rows 64-127 of the -A_Q operand stay inside -H^T");
+static_assert(S_Z % 128 == 0 && S_Y % 128 == 0 && S_UP % 16 == 0, "TMA boxes 128-byte aligned");
+static_assert(2 * kStateSmem <= 232448, "two state CTAs per SM");
 
-// tensor memory: S, P^T, D2a (two buffers: chunk c's epilogue reads one while
-// chunk c+1's first MMA group writes the other), D2b, X
-constexpr int COL_S = 0, COL_PM = 128, COL_D2A = 192, COL_D2B = 320, COL_X = 384;
+// tensor memory: H slice (fp32, lanes i), D_U in two buffers (chunk c's
+// epilogue reads one while chunk c+1's first product writes the other)
+constexpr int COL_H = 0, COL_U = kBV;
+constexpr uint32_t kStateTmemCols = 3 * kBV <= 128 ? 128 : 256;
+constexpr uint32_t kIdNBV = tc::idesc_f16(128, kBV);
 
-__global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillParams p, const Ws ws,
-                                                                 const __grid_constant__ CUtensorMap zmap,
-                                                                 const __grid_constant__ CUtensorMap omap) {
+// tcgen05.ld / st of NC consecutive columns (32 lanes x 32 bit), NC = 16 or 32
+[[maybe_unused]] __device__ __forceinline__ void tmem_ld_cols(uint32_t a, float (&v)[32]) { tc::tmem_ld32(a, v); }
+[[maybe_unused]] __device__ __forceinline__ void tmem_ld_cols(uint32_t a, float (&v)[16]) { tc::tmem_ld16(a, v); }
+[[maybe_unused]] __device__ __forceinline__ void tmem_st_cols(uint32_t a, const float (&v)[32]) { tc::tmem_st32(a, v); }
+[[maybe_unused]] __device__ __forceinline__ void tmem_st_cols(uint32_t a, const float (&v)[16]) { tc::tmem_st16(a, v); }
+[[maybe_unused]] __device__ __forceinline__ void tmem_st_cols_nowait(uint32_t a, const float (&v)[32]) {
+  tc::tmem_st32_nowait(a, v);
+}
+[[maybe_unused]] __device__ __forceinline__ void tmem_st_cols_nowait(uint32_t a, const float (&v)[16]) {
+  tc::tmem_st16_nowait(a, v);
+}
+
+__global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads, 2)
+    state_kernel(const PrefillParams p, const Ws ws, const __grid_constant__ CUtensorMap zmap,
+                 const __grid_constant__ CUtensorMap omap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = tc::smem_u32(sm);
-  const int h_v = p.h_v, h_qk = p.h_qk;
-  const int n = blockIdx.x / h_v, h = blockIdx.x % h_v;
-  const int hq = h / (h_v / h_qk);
+  const int h_v = p.h_v;
+  const int chain = blockIdx.x / kSlices;
+  const int sv = (int)tc::cluster_ctarank();
+  const int n = chain / h_v, h = chain % h_v;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lr = tid & 127;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-  const bool is_main = tid < kMainThreads;
+  const int j0 = kBV * sv;  // first state column of this CTA
 
   const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
-  if (s0 < 0 || s1 < s0 || s1 > p.T) return;  // reported by the chunk table
-  const int g0 = ws.chunk_base[n], g1 = ws.chunk_base[n + 1];
-  if (g1 - g0 != (s1 - s0 + kC - 1) / kC) return;  // table overflow (invalid cu_seqlens), reported
+  bool valid = s0 >= 0 && s1 >= s0 && s1 <= p.T;  // else reported by the chunk table
+  const int g0 = valid ? ws.chunk_base[n] : 0, g1 = valid ? ws.chunk_base[n + 1] : 0;
+  if (valid && g1 - g0 != (s1 - s0 + kC - 1) / kC) valid = false;  // table overflow, reported
+  const int nch = valid ? g1 - g0 : 0;
 
-  const float *sGamIn = reinterpret_cast<const float *>(sm + S_GAM);
-  float *sGamL = reinterpret_cast<float *>(sm + S_GAML);
-  float *red = reinterpret_cast<float *>(sm + S_RED);
-  float *sInv = reinterpret_cast<float *>(sm + S_INV);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_MISC);
-  uint64_t *bar_kq = bar + 1, *bar_aq = bar + 2, *bar_tu = bar + 3, *bar_z = bar + 4;
-  uint64_t *bar_oready = bar + 5, *bar_odone = bar + 6;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
+  uint64_t *bar_s1 = bar, *bar_s2 = bar + 1, *bar_m1 = bar + 2, *bar_m2 = bar + 3, *bar_m2b = bar + 4;
+  uint64_t *bar_udone = bar + 5, *bar_z = bar + 6;
+  uint64_t *bar_oready = bar + 7, *bar_odone = bar + 9, *bar_part = bar + 11;  // [2] each
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_MISC + 112);
+  const float *sGam = reinterpret_cast<const float *>(sm + S_GAM);
+  float *sWn = reinterpret_cast<float *>(sm + S_WN);
   __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 
   if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_alloc(tmem_slot, kStateTmemCols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 7; ++i) tc::mbar_init(bar + i, 1);
+    for (int i = 0; i < 13; ++i) tc::mbar_init(bar + i, 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&zmap);
     tc::prefetch_tmap(&omap);
   }
+  for (int j = tid; j < kBV; j += kStateThreads) sWn[j] = p.norm_w[j0 + j];
   tc::fence_before_sync();
-  __syncthreads();
+  tc::cluster_sync();  // every CTA's barriers are initialised before any peer signals them
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
+  auto slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
 
-  if (is_main) {
-    // ======================= state chain (warps 0-7)
-    const int gh = tid >> 7;
-    uint32_t ph = 0, ph_kq = 0, ph_aq = 0, ph_tu = 0, ph_odone = 0;
-    int pend_kq = 0, pend_aq = 0, pend_tu = 0;
-    auto qk_slot = [&](int gg) { return ws.qk + ((size_t)gg * h_qk + hq) * kQkSlot; };
-    auto v_slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
-    auto issue_kq = [&](int gg) {
-      if (tid == 0) {
-        tc::mbar_arrive_expect_tx(bar_kq, 2 * 16384 + 256);
-        tc::bulk_g2s(sm + S_KH, qk_slot(gg) + kQkK, 16384, bar_kq);
-        tc::bulk_g2s(sm + S_QH, qk_slot(gg) + kQkQ, 16384, bar_kq);
-        tc::bulk_g2s(sm + S_GAM, v_slot(gg) + kVGam, 256, bar_kq);
-      }
-    };
-    auto issue_aq = [&](int gg) {
-      if (tid == 0) {
-        tc::mbar_arrive_expect_tx(bar_aq, 8192 + 16384);
-        tc::bulk_g2s(sm + S_AQ, v_slot(gg) + kVAq, 8192, bar_aq);
-        tc::bulk_g2s(sm + S_KTT, v_slot(gg) + kVKt, 16384, bar_aq);
-      }
-    };
-    auto issue_tu = [&](int gg) {
-      if (tid == 0) {
-        tc::mbar_arrive_expect_tx(bar_tu, 8192 + 16384);
-        tc::bulk_g2s(sm + S_TBG, v_slot(gg) + kVTbg, 8192, bar_tu);
-        tc::bulk_g2s(sm + S_UP, v_slot(gg) + kVUp, 16384, bar_tu);
-      }
-    };
-    // wait (all 256 main threads) for a phase; true if it ran out
+  if (warp < 8) {
+    // ======================= state chain (warps 0-7): TMEM lane i, columns [kHalf gh, kHalf gh + kHalf)
+    const int i = 32 * (warp & 3) + lane, gh = warp >> 2, jc = kHalf * gh;
+    uint32_t ph_s1 = 0, ph_s2 = 0, ph_m1 = 0, ph_m2 = 0;
     auto wait_main = [&](uint64_t *b, uint32_t &phase) {
       const bool ok = tc::mbar_wait(b, phase & 1);
       ++phase;
@@ -716,269 +764,254 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
       tc::named_barrier(kBarMain, kMainThreads);
       tc::fence_after_sync();
     };
-    // S (fp32, tensor memory) -> its fp16 copy, then S <- gamma_C S for the
-    // coming chunk's update (gamma_C from the freshly loaded gamma vector).
-    auto copy_and_scale_state = [&]() {
-      const float gC = sGamIn[63];
-      float v[32];
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+    // H (fp32, TMEM) -> -H^T fp16 operand; then H <- gamma_C H for the coming update
+    auto copy_and_scale = [&](float gC) {
+      float v[kHalf], w[kHalf];
+      tmem_ld_cols(tmem + lane_off + COL_H + jc, v);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          tc::st_chunk_f16(sm + S_SB + tc::sw128_chunk(128, lr, 8 * gh + (c0 >> 3) + cc), v + 8 * cc);
+      for (int j = 0; j < kHalf; ++j) w[j] = v[j] * gC;
+      tmem_st_cols_nowait(tmem + lane_off + COL_H + jc, w);  // completes while the copy is written
+      __half *nh = reinterpret_cast<__half *>(sm + S_NH);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] *= gC;
-        tc::tmem_st32(tmem + lane_off + COL_S + 64 * gh + c0, v);
-      }
+      for (int j = 0; j < kHalf; ++j) nh[tc::sw128_offset(kBV, jc + j, i) >> 1] = __float2half_rn(-v[j]);
+      tc::tmem_st_wait();
     };
 
-    // ---------------- initial state -> TMEM S (fp32)
-    const size_t st_off = ((size_t)n * h_v + h) * kD * kD;
+    // ---------------- initial state slice -> TMEM H
+    const size_t st_off = ((size_t)n * h_v + h) * kD * kD + (size_t)i * kD + j0 + jc;
     {
-      float v[32];
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      float v[kHalf];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int i = 64 * gh + c0 + q;
-          v[q] = p.init_state ? p.init_state[st_off + (size_t)i * kD + lr] : 0.0f;
-        }
-        tc::tmem_st32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+      for (int q = 0; q < kHalf; q += 4) {
+        const float4 f = p.init_state ? *reinterpret_cast<const float4 *>(p.init_state + st_off + q)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[q] = f.x; v[q + 1] = f.y; v[q + 2] = f.z; v[q + 3] = f.w;
       }
+      tmem_st_cols(tmem + lane_off + COL_H + jc, v);
     }
-    tc::fence_before_sync();
-    tc::named_barrier(kBarMain, kMainThreads);
-    tc::fence_after_sync();
-    if (g1 > g0) {
-      issue_kq(g0);
-      issue_tu(g0);
-      issue_aq(g0);
-      pend_kq = pend_tu = pend_aq = 1;
-      if (wait_main(bar_kq, ph_kq)) failed = true;
-      if (!failed) {
-        pend_kq = 0;
-        if (tid < 64) sGamL[tid] = sGamIn[tid];
-        copy_and_scale_state();
-      }
+    if (nch > 0) {
+      if (wait_main(bar_s1, ph_s1)) failed = true;
+      else copy_and_scale(sGam[63]);
     }
     publish_main();
 
-    for (int g = g0; g < g1 && !failed; ++g) {
-      const int buf = (g - g0) & 1;
-      const bool more = g + 1 < g1;
+    for (int c = 0; c < nch && !failed; ++c) {
+      const int buf = c & 1;
+      const uint32_t d_u = tmem + COL_U + kBV * buf;
+      if (c >= 2) {  // the epilogue has read chunk c-2's -O from this buffer
+        uint32_t par = ((c - 2) >> 1) & 1;
+        if (wait_main(bar_odone + buf, par)) { failed = true; break; }
+      }
 
-      // ---------------- group 1: P^T = S K^T, D2a = S Q^T (S entering the chunk, fp16 copy)
+      // ---------------- MMA 1: D_U = [Q^; W] (-H)
       if (tid == 0) {
-        mma_chain(tmem + COL_PM, sbase + S_SB, 128, 0, sbase + S_KH, 64, 0, 8, kIdN64, false);
-        mma_chain(tmem + COL_D2A + 64 * buf, sbase + S_SB, 128, 0, sbase + S_QH, 64, 0, 8, kIdN64, false);
-        tc::mma_commit(bar);
+        for (int k = 0; k < 8; ++k)
+          tc::mma16(d_u, tc::sdesc_kstep(sbase + S_WQ, 128, 0, k), tc::sdesc_kstep(sbase + S_NH, kBV, 0, k), kIdNBV,
+                    k > 0 ? 1u : 0u);
+        tc::mma_commit(bar_m1);
       }
-      if (wait_main(bar, ph)) { failed = true; break; }
-      if (more) {
-        tc::fence_async_smem();
-        issue_kq(g + 1);
-        pend_kq = 1;
-      }
-      {  // -P^T -> fp16 operand
-        float v[32];
-        tc::tmem_ld32(tmem + lane_off + COL_PM + 32 * gh, v);
+      if (wait_main(bar_m1, ph_m1)) { failed = true; break; }
+      if (warp & 2) {  // U = U' + D_U rows 64-127 -> U^T fp16 operand
+        const int m = i - 64;
+        float u[kHalf];
+        tmem_ld_cols(d_u + lane_off + jc, u);
+        const uint4 *up = reinterpret_cast<const uint4 *>(sm + S_UP + m * kBV * 2 + jc * 2);
+        __half *nu = reinterpret_cast<__half *>(sm + S_NU);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = -v[q];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tc::st_chunk_f16(sm + S_PT + tc::sw128_chunk(128, lr, 4 * gh + cc), v + 8 * cc);
-      }
-      publish_main();
-
-      // ---------------- group 2: X = -P^T (T diag(beta gamma))^T;  U^T = U'^T + X
-      if (wait_main(bar_tu, ph_tu)) { failed = true; break; }
-      pend_tu = 0;
-      if (tid == 0) {
-        mma_chain(tmem + COL_X, sbase + S_PT, 128, 0, sbase + S_TBG, 64, 0, 4, kIdN64, false);
-        tc::mma_commit(bar);
-      }
-      if (wait_main(bar, ph)) { failed = true; break; }
-      {
-        float u[32];
-        tc::tmem_ld32(tmem + lane_off + COL_X + 32 * gh, u);
-        uint4 raw[4];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          raw[cc] = *reinterpret_cast<const uint4 *>(sm + S_UP + tc::sw128_chunk(128, lr, 4 * gh + cc));
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const __half2 *hp = reinterpret_cast<const __half2 *>(&raw[cc]);
+        for (int q = 0; q < kHalf / 8; ++q) {
+          const uint4 raw = up[q];
+          const __half2 *hp = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 f = __half22float2(hp[e]);
-            u[8 * cc + 2 * e] += f.x;
-            u[8 * cc + 2 * e + 1] += f.y;
+            u[8 * q + 2 * e] += f.x;
+            u[8 * q + 2 * e + 1] += f.y;
           }
         }
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tc::st_chunk_f16(sm + S_US + tc::sw128_chunk(128, lr, 4 * gh + cc), u + 8 * cc);
+        for (int j = 0; j < kHalf; ++j) nu[tc::sw128_offset(kBV, jc + j, m) >> 1] = __float2half_rn(u[j]);
       }
       publish_main();
-      if (more) {
-        tc::fence_async_smem();
-        issue_tu(g + 1);
-        pend_tu = 1;
-      }
+      if (tid == 0) tc::mbar_arrive(bar_udone);  // U' and [Q^; W] of this chunk are consumed
 
-      // ---------------- group 3: D2b = U^T A_Q^T;  S += U^T K~   (S already scaled by gamma_C)
-      if (g > g0) {  // the epilogue has read the previous chunk's D2b
-        if (wait_main(bar_odone, ph_odone)) { failed = true; break; }
-      }
-      if (wait_main(bar_aq, ph_aq)) { failed = true; break; }
-      pend_aq = 0;
+      // ---------------- MMA 2: D_H += K~^T U (critical);  D_U += [-A_Q; *] U (second issuer)
+      if (wait_main(bar_s2, ph_s2)) { failed = true; break; }
       if (tid == 0) {
-        mma_chain(tmem + COL_D2B, sbase + S_US, 128, 0, sbase + S_AQ, 64, 0, 4, kIdN64, false);
-        mma_chain(tmem + COL_S, sbase + S_US, 128, 0, sbase + S_KTT, 128, 0, 4, kIdN128, true);
-        tc::mma_commit(bar);
+        for (int k = 0; k < 4; ++k)
+          tc::mma16(tmem + COL_H, tc::sdesc_kstep(sbase + S_KT, 128, 0, k), tc::sdesc_kstep(sbase + S_NU, kBV, 0, k),
+                    kIdNBV, 1u);
+        tc::mma_commit(bar_m2);
+      } else if (tid == 32) {
+        for (int k = 0; k < 4; ++k)
+          tc::mma16(d_u, tc::sdesc_kstep(sbase + S_AQ, 128, 0, k), tc::sdesc_kstep(sbase + S_NU, kBV, 0, k), kIdNBV,
+                    1u);
+        tc::mma_commit(bar_m2b);
+        tc::mma_commit(bar_oready + buf);
       }
-      if (wait_main(bar, ph)) { failed = true; break; }
-      if (tid == 0) {  // this chunk's D2a, D2b and gamma are ready for the epilogue
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar_oready);
-      }
-      if (more) {
-        tc::fence_async_smem();
-        issue_aq(g + 1);
-        pend_aq = 1;
-      }
-
-      // ---------------- next chunk's fp16 state copy (and gamma_C scaling of S)
-      if (more) {
-        if (wait_main(bar_kq, ph_kq)) { failed = true; break; }
-        pend_kq = 0;
-        if (tid < 64) sGamL[64 * (buf ^ 1) + tid] = sGamIn[tid];
-        copy_and_scale_state();
+      if (wait_main(bar_m2, ph_m2)) { failed = true; break; }
+      if (c + 1 < nch) {
+        if (wait_main(bar_s1, ph_s1)) { failed = true; break; }
+        copy_and_scale(sGam[63]);
       }
       publish_main();
     }
 
     if (failed) {
       if (tid == 0) set_status(p.status, kDevTimeout);
-      // copies still in flight must land before the CTA's shared memory goes away
-      if (pend_kq) tc::mbar_wait(bar_kq, ph_kq & 1);
-      if (pend_aq) tc::mbar_wait(bar_aq, ph_aq & 1);
-      if (pend_tu) tc::mbar_wait(bar_tu, ph_tu & 1);
-    } else if (p.final_state) {
-      float v[32];
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        tc::tmem_ld32(tmem + lane_off + COL_S + 64 * gh + c0, v);
+    } else if (valid && p.final_state) {
+      float v[kHalf];
+      tmem_ld_cols(tmem + lane_off + COL_H + jc, v);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) p.final_state[st_off + (size_t)(64 * gh + c0 + q) * kD + lr] = v[q];
-      }
+      for (int q = 0; q < kHalf; q += 4)
+        *reinterpret_cast<float4 *>(p.final_state + st_off + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
     }
-  } else {
-    // ======================= RMSNormGated epilogue (warps 8-11), one chunk behind
-    const int otid = tid - kMainThreads, ow = warp - 8;  // lane j = otid
-    uint32_t ph_oready = 0, ph_z = 0;
-    int pend_z = 0;
+  } else if (warp < 10) {
+    // ======================= RMSNormGated epilogue (warps 8-9; thread m owns token row m of the chunk)
+    // buffer c & 1 of each two-buffer barrier completes for chunk c in phase (c >> 1) & 1
+    const int m = tid - kMainThreads;
+    uint32_t ph_z = 0;
+    int z_pend = 0;
     const float scale = rsqrtf((float)kD);
-    const float wj = p.norm_w[lr];
-    auto issue_z = [&](int t0_) {
-      if (otid == 0) {
-        tc::mbar_arrive_expect_tx(bar_z, kC * 256);
-        tc::tma_load_2d(sm + S_Z, &zmap, h * kD, t0_, bar_z);
+    auto issue_z = [&](int cc) {
+      if (m == 0) {
+        tc::mbar_arrive_expect_tx(bar_z, 64 * kBV * 2);
+        tc::tma_load_2d(sm + S_Z, &zmap, h * kD + j0, s0 + kC * cc, bar_z);
       }
+      z_pend = 1;
     };
-    auto wait_out = [&](uint64_t *b, uint32_t &phase) {
-      const bool ok = tc::mbar_wait(b, phase & 1);
-      ++phase;
+    auto wait_epi = [&](uint64_t *b, uint32_t parity, bool cluster) {
+      const bool ok = cluster ? tc::mbar_wait_cluster(b, parity) : tc::mbar_wait(b, parity);
       tc::fence_after_sync();
-      return tc::named_barrier_or(kBarOut, kOutThreads, !ok);
+      return tc::named_barrier_or(kBarEpi, kEpiThreads, !ok);
     };
-    if (g1 > g0) {
-      issue_z(s0);
-      pend_z = 1;
-    }
-    for (int g = g0; g < g1; ++g) {
-      const int t0 = s0 + kC * (g - g0);
+    // this thread's partial sum goes to slot [buf][sv][m] of every CTA of the cluster
+    const uint32_t part_local = tc::smem_u32(sm + S_PART) + 4u * (uint32_t)(sv * 64 + m);
+    if (nch > 0) issue_z(0);
+    for (int c = 0; c < nch; ++c) {
+      const int buf = c & 1;
+      const uint32_t par = (c >> 1) & 1;
+      const uint32_t d_u = tmem + lane_off + COL_U + kBV * buf;
+      const int t0 = s0 + kC * c;
       const int Lc = min(kC, s1 - t0);
-      const int buf = (g - g0) & 1;
-      if (wait_out(bar_oready, ph_oready)) { failed = true; break; }
-      // o = scale (gamma_r D2a + D2b) for this lane j and the chunk's 64 tokens
-      float o[64];
-      {
-        float d[32];
-        const float *gam = sGamL + 64 * buf;
+      if (wait_epi(bar_oready + buf, par, false)) { failed = true; break; }
+      float ss = 0.0f;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float a32[32];
-          tc::tmem_ld32(tmem + lane_off + COL_D2A + 64 * buf + 32 * hh, a32);
-          tc::tmem_ld32(tmem + lane_off + COL_D2B + 32 * hh, d);
+      for (int c32 = 0; c32 < kBV; c32 += 32) {
+        float o[32];
+        tc::tmem_ld32(d_u + c32, o);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) o[32 * hh + q] = scale * fmaf(gam[32 * hh + q], a32[q], d[q]);
+        for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
+      }
+      ss *= scale * scale;
+      if (m == 0) tc::mbar_arrive_expect_tx(bar_part + buf, kSlices * 64 * 4);
+      const uint32_t off = 4u * (uint32_t)(buf * kSlices * 64);
+      for (int r = 0; r < kSlices; ++r)
+        tc::st_async_f32(tc::mapa(part_local + off, r), ss, tc::mapa(tc::smem_u32(bar_part + buf), r));
+      if (wait_epi(bar_part + buf, par, true)) { failed = true; break; }
+      const float *part = reinterpret_cast<const float *>(sm + S_PART) + buf * kSlices * 64;
+      float tot = 0.0f;
+#pragma unroll
+      for (int r = 0; r < kSlices; ++r) tot += part[r * 64 + m];
+      const float inv = -scale * rsqrtf(tot * (1.0f / kD) + kEpsRms);  // o = -scale D_U
+      if (wait_epi(bar_z, ph_z & 1, false)) { failed = true; break; }
+      ++ph_z;
+      z_pend = 0;
+      tc::bulk_wait_read();  // this thread's earlier y copies have left S_Y
+      tc::named_barrier(kBarEpi, kEpiThreads);
+#pragma unroll
+      for (int c32 = 0; c32 < kBV; c32 += 32) {
+        float o[32];
+        tc::tmem_ld32(d_u + c32, o);
+        const uint4 *zrow = reinterpret_cast<const uint4 *>(sm + S_Z + m * kBV * 2 + c32 * 2);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 zz = zrow[q];
+          const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
+          float y8[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float za = __uint_as_float(zw[e] << 16), zb = __uint_as_float(zw[e] & 0xFFFF0000u);
+            const int j = c32 + 8 * q + 2 * e;
+            // silu(z) = z (1 + tanh(z / 2)) / 2 with the hardware tanh: its ~2^-11
+            // error scales one output element, well inside the output rounding
+            y8[2 * e] = o[8 * q + 2 * e] * inv * sWn[j] * (0.5f * za) * (1.0f + tc::tanh_approx(0.5f * za));
+            y8[2 * e + 1] = o[8 * q + 2 * e + 1] * inv * sWn[j + 1] * (0.5f * zb) * (1.0f + tc::tanh_approx(0.5f * zb));
+          }
+          *reinterpret_cast<uint4 *>(sm + S_Y + m * kBV * 2 + (c32 + 8 * q) * 2) =
+              make_uint4(tc::pack_bf16x2(y8[0], y8[1]), tc::pack_bf16x2(y8[2], y8[3]), tc::pack_bf16x2(y8[4], y8[5]),
+                         tc::pack_bf16x2(y8[6], y8[7]));
         }
       }
-      // D2a, D2b and gamma are read: the state chain may overwrite them
       tc::fence_before_sync();
-      tc::named_barrier(kBarOut, kOutThreads);
-      if (otid == 0) tc::mbar_arrive(bar_odone);
-      // per-token sum of squares over j (the 128 lanes of the four epilogue warps)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float sq[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) sq[q] = o[32 * hh + q] * o[32 * hh + q];
-        red[(hh * 4 + ow) * 32 + lane] = reduce_scatter<32>(sq, lane);
-      }
-      if (otid < 64) tc::bulk_wait_read();  // the previous chunk's y rows have left S_OUT
-      tc::named_barrier(kBarOut, kOutThreads);
-      if (otid < 64) {
-        const int hh = otid >> 5, q = otid & 31;
-        const float ssum = red[(hh * 4) * 32 + q] + red[(hh * 4 + 1) * 32 + q] + red[(hh * 4 + 2) * 32 + q] +
-                           red[(hh * 4 + 3) * 32 + q];
-        sInv[otid] = rsqrtf(ssum * (1.0f / kD) + kEpsRms);
-      }
-      if (wait_out(bar_z, ph_z)) { failed = true; break; }
-      pend_z = 0;
-      const __nv_bfloat16 *zst = reinterpret_cast<const __nv_bfloat16 *>(sm + S_Z);
-      __nv_bfloat16 *yst = reinterpret_cast<__nv_bfloat16 *>(sm + S_OUT);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float zz[32], iv[32];  // shared-memory reads before the stores
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          zz[q] = __bfloat162float(zst[(32 * hh + q) * kD + lr]);
-          iv[q] = sInv[32 * hh + q];
-        }
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          // silu(z) = z (1 + tanh(z / 2)) / 2 with the hardware tanh: its ~2^-11
-          // error scales one output element, well inside the output rounding
-          const float th = tc::tanh_approx(0.5f * zz[q]);
-          o[32 * hh + q] = o[32 * hh + q] * iv[q] * wj * (0.5f * zz[q]) * (1.0f + th);
-        }
-#pragma unroll
-        for (int q = 0; q < 32; ++q) yst[(32 * hh + q) * kD + lr] = __float2bfloat16_rn(o[32 * hh + q]);
-      }
       tc::fence_async_smem();
-      tc::named_barrier(kBarOut, kOutThreads);
+      tc::named_barrier(kBarEpi, kEpiThreads);
+      if (m == 0) tc::mbar_arrive(bar_odone + buf);  // -O of this buffer is read; z is consumed
+      if (c + 1 < nch) issue_z(c + 1);
       if (Lc == kC) {
-        if (otid == 0) {
-          tc::tma_store_2d(&omap, h * kD, t0, sm + S_OUT);
+        if (m == 0) {
+          tc::tma_store_2d(&omap, h * kD + j0, t0, sm + S_Y);
           tc::bulk_commit();
         }
-      } else if (otid < Lc) {  // a sequence's last, short chunk: only its own rows
-        tc::bulk_s2g(out + ((size_t)(t0 + otid) * h_v + h) * kD, sm + S_OUT + otid * 256, 256);
+      } else if (m < Lc) {  // a sequence's last, short chunk: only its own rows
+        tc::bulk_s2g(out + ((size_t)(t0 + m) * h_v + h) * kD + j0, sm + S_Y + m * kBV * 2, kBV * 2);
         tc::bulk_commit();
       }
-      if (g + 1 < g1) {  // the z rows of the next chunk, over the ones just used
-        tc::fence_async_smem();
-        issue_z(t0 + kC);
-        pend_z = 1;
-      }
     }
-    if (otid < 64) tc::bulk_wait_all();
+    tc::bulk_wait_all();
     if (failed) {
-      if (otid == 0) set_status(p.status, kDevTimeout);
-      if (pend_z) tc::mbar_wait(bar_z, ph_z & 1);
+      if (m == 0) set_status(p.status, kDevTimeout);
+      if (z_pend) tc::mbar_wait(bar_z, ph_z & 1);
+    }
+  } else if (warp == 10) {
+    // ======================= operand copies (warp 10, one lane), each set as soon as its buffers are free
+    uint32_t ph = 0;
+    int n1 = 0, n2 = 0;  // sets issued
+    auto issue_s1 = [&](int gg) {  // [Q^; W], U' slice, gamma
+      tc::mbar_arrive_expect_tx(bar_s1, 32768 + 64 * kBV * 2 + 256);
+      tc::bulk_g2s(sm + S_WQ, slot(gg) + kVWQ, 32768, bar_s1);
+      tc::bulk_g2s(sm + S_UP, slot(gg) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2, bar_s1);
+      tc::bulk_g2s(sm + S_GAM, slot(gg) + kVGam, 256, bar_s1);
+      ++n1;
+    };
+    auto issue_s2 = [&](int gg) {  // K~^T, -A_Q
+      tc::mbar_arrive_expect_tx(bar_s2, 16384 + 8192);
+      tc::bulk_g2s(sm + S_KT, slot(gg) + kVKt, 16384, bar_s2);
+      tc::bulk_g2s(sm + S_AQ, slot(gg) + kVAq, 8192, bar_s2);
+      ++n2;
+    };
+    if (lane == 0 && nch > 0) {
+      issue_s1(g0);
+      issue_s2(g0);
+      if (nch > 1) {
+        tc::prefetch_l2(slot(g0 + 1) + kVWQ, 32768 + 16384);
+        tc::prefetch_l2(slot(g0 + 1) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2);
+        tc::prefetch_l2(slot(g0 + 1) + kVAq, 8192 + 256);
+      }
+      for (int c = 0; c + 1 < nch; ++c) {
+        // chunk c's MMA 1 and U' are consumed (the chain signals after MMA 1 and the U step)
+        if (!tc::mbar_wait(bar_udone, ph & 1)) { failed = true; break; }
+        issue_s1(g0 + c + 1);
+        if (c + 2 < nch) {  // the chunk after: into L2 now, so its copies later come from there
+          tc::prefetch_l2(slot(g0 + c + 2) + kVWQ, 32768 + 16384);
+          tc::prefetch_l2(slot(g0 + c + 2) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2);
+          tc::prefetch_l2(slot(g0 + c + 2) + kVAq, 8192 + 256);
+        }
+        // chunk c's MMA 2 (both halves) has read K~^T and -A_Q
+        if (!tc::mbar_wait(bar_m2, ph & 1) || !tc::mbar_wait(bar_m2b, ph & 1)) { failed = true; break; }
+        issue_s2(g0 + c + 1);
+        ++ph;
+      }
+      if (failed) set_status(p.status, kDevTimeout);
+      // copies in flight must land before the CTA's shared memory goes away
+      // (the last set of each kind; set k completes phase k of its barrier)
+      if (n1 > 0) tc::mbar_wait(bar_s1, (uint32_t)(n1 - 1) & 1);
+      if (n2 > 0) tc::mbar_wait(bar_s2, (uint32_t)(n2 - 1) & 1);
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+  if (warp == 0) tc::tmem_dealloc(tmem, kStateTmemCols);
+  tc::cluster_sync();  // no CTA leaves while a peer may still store into its shared memory
 }
 
 // ================================================================ host side
@@ -996,14 +1029,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D map over a [rows][cols] bf16 tensor, boxes of 128 columns x box_rows rows;
-// out-of-range rows read as zero.
-bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D map over a [rows][cols] bf16 tensor, boxes of box_cols columns x box_rows
+// rows; out-of-range rows read as zero.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+              uint32_t box_rows) {
   auto encode = tensor_map_encoder();
   if (!encode) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1021,14 +1055,13 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   Ws ws;
   ws.chunk_base = reinterpret_cast<int *>(p.ws + L.base);
   ws.chunk_info = reinterpret_cast<int2 *>(p.ws + L.info);
-  ws.qk = p.ws + L.qk;
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
   CUtensorMap zmap, omap;
   std::memset(&zmap, 0, sizeof(zmap));
   std::memset(&omap, 0, sizeof(omap));
-  if (p.T > 0 && !(make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, kC) &&
-                   make_map(&omap, p.out, (uint64_t)p.T, (uint64_t)p.h_v * kD, kC)))
+  if (p.T > 0 && !(make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, kBV, kC) &&
+                   make_map(&omap, p.out, (uint64_t)p.T, (uint64_t)p.h_v * kD, kBV, kC)))
     return cudaErrorInvalidValue;
 
   trace_begin(s, GDN_K_CHUNK_TABLE);
@@ -1048,7 +1081,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
   if (e != cudaSuccess) return e;
   trace_begin(s, GDN_K_STATE);
-  state_kernel<<<(unsigned)p.N * (unsigned)p.h_v, kStateThreads, kStateSmem, s>>>(p, ws, zmap, omap);
+  state_kernel<<<(unsigned)p.N * (unsigned)p.h_v * kSlices, kStateThreads, kStateSmem, s>>>(p, ws, zmap, omap);
   trace_end(s);
   return cudaGetLastError();
 }

@@ -85,7 +85,8 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const uint16_t *__re
 extern "C" int gdn_selftest_umma(const void *A, const void *B, float *D, int *flag, int N, int K, int b_row0,
                                  int fp16, void *stream) {
   if (!A || !B || !D || !flag) return GDN_ERR_INVALID_ARG;
-  if ((N != 64 && N != 128) || (K != 64 && K != 128) || (b_row0 != 0 && b_row0 != 64) || b_row0 + N > 128)
+  if ((N != 32 && N != 64 && N != 128) || (K != 64 && K != 128) || (b_row0 != 0 && b_row0 != 64) ||
+      b_row0 + N > 128)
     return GDN_ERR_INVALID_ARG;
   const size_t smem = 1024 + (size_t)128 * K * 2 + (size_t)(b_row0 + N) * K * 2;
   auto kern = gdn::umma_selftest_kernel;
