@@ -30,7 +30,9 @@ struct DecodeParams {
 
 // Token-sequential fp32 prefill (any supported shape, bf16 or fp32 streams).
 cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t s);
-// Chunked tensor-core prefill (bf16 streams, d_k = d_v = 128).
+// Chunked tensor-core prefill (bf16 streams, d_k = d_v = 128, at most
+// kTcMaxRep value heads per q/k head).
+constexpr int kTcMaxRep = 8;
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
 size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v);
 // Decode step.

@@ -64,7 +64,7 @@ namespace {
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kPad = 65;  // fp32 64 x 64 matrices: padded rows
+constexpr int kPad = 66;  // fp32 64 x 64 matrices: padded rows (even: 8-byte aligned pairs)
 
 // ---------------------------------------------------------------- workspace
 // Per (chunk, value head), operand images the state pass copies straight into
@@ -82,7 +82,7 @@ constexpr uint32_t kVSlot = 73984;
 
 struct Ws {
   int *chunk_base;   // [N + 1]: first chunk of each sequence; [N] = number of chunks
-  int2 *chunk_info;  // [max_chunks]: (sequence, first token)
+  int4 *chunk_info;  // [max_chunks]: (sequence, first token, sequence start, tokens in the chunk)
   uint8_t *vs;       // [max_chunks][h_v] x kVSlot
   int max_chunks;
 };
@@ -97,7 +97,7 @@ struct WsLayout {
     max_chunks = (T + kC - 1) / kC + N;
     base = 0;
     info = align_up(sizeof(int) * (size_t)(N + 1), 1024);
-    vs = align_up(info + sizeof(int2) * (size_t)max_chunks, 1024);
+    vs = align_up(info + sizeof(int4) * (size_t)max_chunks, 1024);
     total = vs + (size_t)max_chunks * h_v * kVSlot;
   }
 };
@@ -210,7 +210,8 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p
       const int mid = (lo + hi + 1) >> 1;
       if (ws.chunk_base[mid] <= g) lo = mid; else hi = mid - 1;
     }
-    ws.chunk_info[g] = make_int2(lo, p.cu_seqlens[lo] + kC * (g - ws.chunk_base[lo]));
+    const int sq0 = p.cu_seqlens[lo], tq0 = sq0 + kC * (g - ws.chunk_base[lo]);
+    ws.chunk_info[g] = make_int4(lo, tq0, sq0, min(kC, p.cu_seqlens[lo + 1] - tq0));
   }
 }
 
@@ -225,7 +226,7 @@ constexpr uint32_t P_AF = P_KQL;
 constexpr uint32_t P_TF = P_AF + 64 * kPad * 4;
 constexpr uint32_t P_VT = 66560;                      // K^T fp16 [128 i][64 m] (B operand of W)
 constexpr uint32_t P_XF = P_VT + 16384;               // inverse block products 32 x 32 fp32
-constexpr int kMaxRep = 8;                            // value heads per q/k head
+constexpr int kMaxRep = kTcMaxRep;                    // value heads per q/k head
 constexpr uint32_t P_VEC = P_XF + 4096;               // per value head: G, gamma, beta, decay-to-end
 constexpr uint32_t P_RED = P_VEC + kMaxRep * 1024;
 constexpr uint32_t P_MISC = P_RED + 64;
@@ -237,22 +238,25 @@ static_assert(2 * kPrepSmem <= 232448, "two prep CTAs per SM");
 constexpr uint32_t kIdN64 = tc::idesc_f16(128, 64);
 constexpr uint32_t kIdN128 = tc::idesc_f16(128, 128);
 
-// conv(4) + SiLU of 8 rows x 4 channels of one head: rows r0 .. r0+7 of the
-// chunk, channels c0 .. c0+3 (x points at channel c0 of token 0; bf16 row
-// pitch `stride` elements; conv_w rows from `ch`).  Rows before the sequence
-// start or past the chunk's end are 0.
-__device__ __forceinline__ void conv_rows(const __nv_bfloat16 *x, size_t stride, const float *conv_w, int ch,
-                                          int t0, int s0, int Lc, int r0, float (&y)[8][4]) {
-  float4 w[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const float4 *>(conv_w + (size_t)(ch + c) * 4);
-  uint2 xr[11];  // packed bf16 rows
+// Raw rows for conv(4) of 8 output rows r0 .. r0+7 of the chunk: input rows
+// r0-3 .. r0+7, 4 channels (x points at the first channel of token 0; bf16 row
+// pitch `stride` elements) as packed bf16; rows before the sequence start or
+// past the chunk's end are 0.
+__device__ __forceinline__ void load_rows(const __nv_bfloat16 *x, size_t stride, int t0, int s0, int Lc, int r0,
+                                          uint2 (&xr)[11]) {
 #pragma unroll
   for (int rr = 0; rr < 11; ++rr) {
     const int row = r0 - 3 + rr;
     const int t = t0 + row;
     xr[rr] = (t >= s0 && row < Lc) ? *reinterpret_cast<const uint2 *>(x + (size_t)t * stride) : make_uint2(0u, 0u);
   }
+}
+// conv(4) + SiLU of the rows of load_rows, channels from conv_w row `ch`.
+__device__ __forceinline__ void conv_silu(const uint2 (&xr)[11], const float *conv_w, int ch, int Lc, int r0,
+                                          float (&y)[8][4]) {
+  float4 w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const float4 *>(conv_w + (size_t)(ch + c) * 4);
   auto val = [&](int rr, int c) {
     const uint32_t w32 = (c < 2) ? xr[rr].x : xr[rr].y;
     return __uint_as_float((c & 1) ? (w32 & 0xFFFF0000u) : (w32 << 16));
@@ -269,6 +273,12 @@ __device__ __forceinline__ void conv_rows(const __nv_bfloat16 *x, size_t stride,
       y[r][c] = ok ? silu_fast(a) : 0.0f;
     }
   }
+}
+__device__ __forceinline__ void conv_rows(const __nv_bfloat16 *x, size_t stride, const float *conv_w, int ch,
+                                          int t0, int s0, int Lc, int r0, float (&y)[8][4]) {
+  uint2 xr[11];
+  load_rows(x, stride, t0, s0, Lc, r0, xr);
+  conv_silu(xr, conv_w, ch, Lc, r0, y);
 }
 
 // L2-normalise the 8 rows held by a warp (each lane holds 4 of the 128 channels).
@@ -297,10 +307,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   const int h_v = p.h_v, h_qk = p.h_qk, rep = h_v / h_qk;
 
-  const int2 info = ws.chunk_info[g];
-  const int n = info.x, t0 = info.y;
-  const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
-  const int Lc = min(kC, s1 - t0);
+  const int4 info = ws.chunk_info[g];
+  const int t0 = info.y, s0 = info.z, Lc = info.w;
 
   float *AF = reinterpret_cast<float *>(sm + P_AF);
   float *TF = reinterpret_cast<float *>(sm + P_TF);
@@ -337,6 +345,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 
   const int r0 = 8 * warp, c0 = 4 * lane;  // prologue: this thread's rows and channels
   auto v_slot_of = [&](int vv) { return ws.vs + ((size_t)g * h_v + hq * rep + vv) * kVSlot; };
+
+  // the first value head's v rows into L2 while the q/k rows are worked on
+  auto prefetch_v = [&](int vv) {
+    const int t = t0 - 3 + tid;
+    if (tid < kC + 3 && t >= s0 && t < t0 + Lc)
+      tc::prefetch_l2(xv + (size_t)t * v_stride + (size_t)(hq * rep + vv) * kD, kD * 2);
+  };
+  prefetch_v(0);
 
   // ---------------- gates of every value head and their running sums inside the chunk
   for (int v0 = 0; v0 < rep; v0 += 4) {
@@ -376,7 +392,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   //                  and K~^T = (diag(e^(G_C - G)) K)^T images of every value head
   {
     float y[8][4], kreg[8][4];
-    conv_rows(xq + hq * kD + c0, qk_stride, p.conv_w, hq * kD + c0, t0, s0, Lc, r0, y);
+    uint2 xrk[11];
+    {  // both heads' rows in flight at once
+      uint2 xrq[11];
+      load_rows(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, xrq);
+      load_rows(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, xrk);
+      conv_silu(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
+    }
     l2norm_rows(y, lane);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -398,7 +420,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
             pack4_f16(gr * y[r][0], gr * y[r][1], gr * y[r][2], gr * y[r][3]);
       }
     }
-    conv_rows(xk + hq * kD + c0, qk_stride, p.conv_w, h_qk * kD + hq * kD + c0, t0, s0, Lc, r0, kreg);
+    conv_silu(xrk, p.conv_w, h_qk * kD + hq * kD + c0, Lc, r0, kreg);
     l2norm_rows(kreg, lane);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -443,6 +465,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     uint8_t *v_slot = v_slot_of(vv);
 
     const float *sG = sGall + vv * 256, *sGam = sG + 64, *sBeta = sG + 128;
+    if (vv + 1 < rep) prefetch_v(vv + 1);
 
     // ---------------- v: conv + SiLU -> V^T tile (over the [K; Q] tile, once K K^T and Q K^T are done)
     {
@@ -450,6 +473,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       conv_rows(xv + h * kD + c0, v_stride, p.conv_w, 2 * h_qk * kD + h * kD + c0, t0, s0, Lc, r0, y);
       if (vv == 0) {
         if (wait_all(bar, phase)) { failed = true; break; }
+        // the [K; Q] lo tile under A and T is dead: zero the two 16 x 16 blocks of
+        // T above its diagonal blocks that the inverse never writes, once
+        {
+          const int blk = tid >> 7, r = (tid >> 3) & 15, c2 = 2 * (tid & 7);
+          *reinterpret_cast<float2 *>(TF + (32 * blk + r) * kPad + 32 * blk + 16 + c2) = make_float2(0.f, 0.f);
+        }
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -514,6 +543,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     }
     __syncthreads();
     // (b) T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22): two elements per thread
+    //     (the diagonal blocks of T hold zeros above their diagonal)
     {
       float xv2[2];
 #pragma unroll
@@ -523,11 +553,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         const float *arow = AF + (o + 16 + r) * kPad + o;
         float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {  // T_00 is lower triangular
-          const float ta = (k >= s) ? TF[(o + k) * kPad + o + s] : 0.0f;
-          const float tb = (k + 1 >= s) ? TF[(o + k + 1) * kPad + o + s] : 0.0f;
-          acc0 = fmaf(arow[k], ta, acc0);
-          acc1 = fmaf(arow[k + 1], tb, acc1);
+        for (int k = 0; k < 16; k += 2) {
+          acc0 = fmaf(arow[k], TF[(o + k) * kPad + o + s], acc0);
+          acc1 = fmaf(arow[k + 1], TF[(o + k + 1) * kPad + o + s], acc1);
         }
         xv2[it] = acc0 + acc1;
       }
@@ -541,39 +569,45 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         const float *trow = TF + (o + 16 + r) * kPad + o + 16;
         float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {  // T_11 is lower triangular
-          acc0 = fmaf((k <= r) ? trow[k] : 0.0f, XF[blk * 256 + k * 16 + s], acc0);
-          acc1 = fmaf((k + 1 <= r) ? trow[k + 1] : 0.0f, XF[blk * 256 + (k + 1) * 16 + s], acc1);
+        for (int k = 0; k < 16; k += 2) {
+          acc0 = fmaf(trow[k], XF[blk * 256 + k * 16 + s], acc0);
+          acc1 = fmaf(trow[k + 1], XF[blk * 256 + (k + 1) * 16 + s], acc1);
         }
         TF[(o + 16 + r) * kPad + o + s] = -(acc0 + acc1);
       }
     }
     __syncthreads();
-    // (c) the lower-left 32x32 block T_21 = -T_2 (A_21 T_1): four rows per thread
+    // (c) the lower-left 32x32 block T_21 = -T_2 (A_21 T_1), a 2 x 2 tile per thread
+    //     (T_1 and T_2 are whole lower-triangular blocks: zeros above the diagonal)
     {
-      const int rb = tid >> 5, s = tid & 31;  // rows rb, rb+8, rb+16, rb+24
-      float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const int rr = 2 * (tid >> 4), ss = 2 * (tid & 15);
+      const float *a0 = AF + (32 + rr) * kPad, *a1 = a0 + kPad;
+      float y00 = 0.0f, y01 = 0.0f, y10 = 0.0f, y11 = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {  // T_1 is lower triangular
-        const float t = (k >= s) ? TF[k * kPad + s] : 0.0f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) y[q] = fmaf(AF[(32 + rb + 8 * q) * kPad + k], t, y[q]);
+      for (int k = 0; k < 32; ++k) {
+        const float2 t = *reinterpret_cast<const float2 *>(TF + k * kPad + ss);
+        const float av = a0[k], bv = a1[k];
+        y00 = fmaf(av, t.x, y00);
+        y01 = fmaf(av, t.y, y01);
+        y10 = fmaf(bv, t.x, y10);
+        y11 = fmaf(bv, t.y, y11);
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) XF[(rb + 8 * q) * 32 + s] = y[q];
+      *reinterpret_cast<float2 *>(XF + rr * 32 + ss) = make_float2(y00, y01);
+      *reinterpret_cast<float2 *>(XF + (rr + 1) * 32 + ss) = make_float2(y10, y11);
       __syncthreads();
-      float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const float *t0r = TF + (32 + rr) * kPad + 32, *t1r = t0r + kPad;
+      float z00 = 0.0f, z01 = 0.0f, z10 = 0.0f, z11 = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {  // T_2 is lower triangular
-        const float yk = XF[k * 32 + s];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = rb + 8 * q;
-          z[q] = fmaf((k <= r) ? TF[(32 + r) * kPad + 32 + k] : 0.0f, yk, z[q]);
-        }
+      for (int k = 0; k < 32; ++k) {
+        const float2 yk = *reinterpret_cast<const float2 *>(XF + k * 32 + ss);
+        const float p0 = t0r[k], p1 = t1r[k];
+        z00 = fmaf(p0, yk.x, z00);
+        z01 = fmaf(p0, yk.y, z01);
+        z10 = fmaf(p1, yk.x, z10);
+        z11 = fmaf(p1, yk.y, z11);
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) TF[(32 + rb + 8 * q) * kPad + s] = -z[q];
+      *reinterpret_cast<float2 *>(TF + (32 + rr) * kPad + ss) = make_float2(-z00, -z01);
+      *reinterpret_cast<float2 *>(TF + (33 + rr) * kPad + ss) = make_float2(-z10, -z11);
     }
     __syncthreads();
     // [T diag(beta gamma); T diag(beta)] (one 128-row shared-memory operand)
@@ -1054,7 +1088,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   if (p.ws_bytes < L.total) return cudaErrorInvalidValue;
   Ws ws;
   ws.chunk_base = reinterpret_cast<int *>(p.ws + L.base);
-  ws.chunk_info = reinterpret_cast<int2 *>(p.ws + L.info);
+  ws.chunk_info = reinterpret_cast<int4 *>(p.ws + L.info);
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
   CUtensorMap zmap, omap;

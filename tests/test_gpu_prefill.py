@@ -48,7 +48,8 @@ def test_tiny_fp32_config():
     check(synth.make_prefill(synth.TINY), "fp32")
 
 
-@pytest.mark.parametrize("case", ["ragged_single", "varlen_edges", "long_memory", "gqa4", "fp32_d128"])
+@pytest.mark.parametrize("case", ["ragged_single", "varlen_edges", "long_memory", "gqa4", "gqa8", "gqa16",
+                                  "fp32_d128"])
 def test_small_cases(case):
     if case == "ragged_single":      # several chunks plus a ragged tail
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(200,), h_qk=2, h_v=4)
@@ -59,6 +60,10 @@ def test_small_cases(case):
                            init_std=0.02, seed=5)
     elif case == "gqa4":             # 4 value heads per q/k head
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(97, 31), h_qk=1, h_v=4, seed=7)
+    elif case == "gqa8":             # the most value heads per q/k head the chunked path takes
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(70,), h_qk=1, h_v=8, seed=8)
+    elif case == "gqa16":            # beyond it: served by the token-sequential kernel
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(70,), h_qk=1, h_v=16, seed=9)
     else:                            # fp32 streams at d = 128 (token-sequential fp32 kernel)
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(130, 7), h_qk=1, h_v=2, dtype="fp32", init_std=0.02)
     inp = synth.make_prefill(cfg)
