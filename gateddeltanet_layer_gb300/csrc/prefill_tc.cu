@@ -72,11 +72,10 @@ constexpr int kPad = 66;  // fp32 64 x 64 matrices: padded rows (even: 8-byte al
 //   [Q^; W]  [128 rows][128 cols]: rows 0-63 Q^ = diag(gamma) Q, rows 64-127
 //            W = T diag(beta gamma) K (one 128-row MMA operand)
 //   K~^T     [128 i][64 m] = (diag(e^(G_C - G)) K)^T
-//   U'       T diag(beta) V, plain row-major per state slice: [kSlices][64 m][kBV]
+//   U'       T diag(beta) V, plain row-major per state slice: [128 / bv][64 m][bv]
+//            (bv = the state pass's slice width)
 //   -A_Q     [64 r][64 s], A_Q = D o (Q K^T), lower triangle with the diagonal
 //   gamma    [64] fp32
-constexpr int kSlices = 4;                 // state column slices (CTAs) per (sequence, value head)
-constexpr int kBV = 128 / kSlices;         // state columns per slice
 constexpr uint32_t kVWQ = 0, kVKt = 32768, kVUp = 49152, kVAq = 65536, kVGam = 73728;
 constexpr uint32_t kVSlot = 73984;
 
@@ -85,6 +84,7 @@ struct Ws {
   int4 *chunk_info;  // [max_chunks]: (sequence, first token, sequence start, tokens in the chunk)
   uint8_t *vs;       // [max_chunks][h_v] x kVSlot
   int max_chunks;
+  int up_bv_log2;    // log2 of the column width of the U' image slices (the state pass's slice width)
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -666,7 +666,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int j = 64 * hh + 32 * c32 + 8 * cc;  // state column of this 16-byte chunk
-          st_chunk_f16_global(v_slot + kVUp + ((size_t)(j / kBV) * 64 + m) * (kBV * 2) + (j % kBV) * 2, u + 8 * cc);
+          const int lb = ws.up_bv_log2;
+          st_chunk_f16_global(v_slot + kVUp + ((size_t)(j >> lb) * 64 + m) * (2u << lb) + (j & ((1 << lb) - 1)) * 2,
+                              u + 8 * cc);
         }
       }
     }
@@ -695,33 +697,42 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 // chunk behind (exchanging per-token partial sums of o^2 with the other CTAs
 // of the cluster through st.async into their shared memory), warp 10 issues
 // the operand copies.
-constexpr int kStateThreads = 352;
-constexpr int kMainThreads = 256, kEpiThreads = 64;
+template <int NS>
+struct StateCfg {
+  static constexpr int kSlices = NS;                    // CTAs per chain
+  static constexpr int kBV = kD / NS;                   // state columns per CTA
+  static constexpr int kCG = 2;                         // column groups of the chain warps
+  static constexpr int kCols = kBV / kCG;               // columns per chain thread
+  static constexpr int kMainWarps = 4 * kCG;            // TMEM lane quarters x column groups
+  static constexpr int kMainThreads = 32 * kMainWarps, kEpiThreads = 64;
+  static constexpr int kEpiWarp = kMainWarps, kProdWarp = kMainWarps + 2;
+  static constexpr int kThreads = 32 * (kMainWarps + 3);
+  static constexpr int kMinBlocks = 2;
+  static constexpr uint32_t S_WQ = 0;                   // [Q^; W] image (32 KB)
+  static constexpr uint32_t S_KT = 32768;               // K~^T [128 i][64 m] (16 KB)
+  static constexpr uint32_t S_AQ = 49152;               // -A_Q [64][64] (8 KB), rows 64-127 of its
+  static constexpr uint32_t S_NH = S_AQ + 8192;         //   operand read the first 8 KB here (unused)
+  static constexpr uint32_t S_NU = S_NH + kBV * 256;    // U^T fp16 [kBV j][64 m]
+  static constexpr uint32_t S_UP = S_NU + kBV * 128;    // U' [64 m][kBV] fp16 (plain)
+  static constexpr uint32_t S_Z = S_UP + kBV * 128;     // z [64 t][kBV] bf16 (TMA)
+  static constexpr uint32_t S_Y = S_Z + kBV * 128;      // y [64 t][kBV] bf16 (TMA store)
+  static constexpr uint32_t S_GAM = S_Y + kBV * 128;    // gamma [64]
+  static constexpr uint32_t S_WN = S_GAM + 256;         // norm_w of this slice [kBV]
+  static constexpr uint32_t S_PART = S_WN + kBV * 4;    // partial sums of o^2 [2][kSlices][64]
+  static constexpr uint32_t S_MISC = S_PART + 2 * kSlices * 64 * 4;
+  static constexpr size_t kSmem = S_MISC + 128 + 1024;
+  // tensor memory: H slice (fp32, lanes i), D_U in two buffers (chunk c's
+  // epilogue reads one while chunk c+1's first product writes the other)
+  static constexpr int COL_H = 0, COL_U = kBV;
+  static constexpr uint32_t kTmemCols = 3 * kBV <= 128 ? 128 : 3 * kBV <= 256 ? 256 : 512;
+  static constexpr uint32_t kIdN = tc::idesc_f16(128, kBV);
+  static_assert(S_NH % 1024 == 0 && S_NU % 1024 == 0 && S_KT % 1024 == 0 && S_AQ % 1024 == 0, "SW128 tiles");
+  static_assert(kBV * 256 >= 8192, "rows 64-127 of the -A_Q operand stay inside -H^T");
+  static_assert(S_Z % 128 == 0 && S_Y % 128 == 0 && S_UP % 16 == 0, "TMA boxes 128-byte aligned");
+  static_assert(kMinBlocks * kSmem <= 232448, "shared memory budget");
+  static_assert(kCols == 16 || kCols == 32, "TMEM access widths");
+};
 constexpr int kBarMain = 1, kBarEpi = 2;
-constexpr int kHalf = kBV / 2;                         // columns per chain thread
-constexpr uint32_t S_WQ = 0;                           // [Q^; W] image (32 KB)
-constexpr uint32_t S_KT = 32768;                       // K~^T [128 i][64 m] (16 KB)
-constexpr uint32_t S_AQ = 49152;                       // -A_Q [64][64] (8 KB), rows 64-127 of its
-constexpr uint32_t S_NH = S_AQ + 8192;                 //   operand read the first 8 KB here (unused)
-constexpr uint32_t S_NU = S_NH + kBV * 256;            // U^T fp16 [kBV j][64 m]
-constexpr uint32_t S_UP = S_NU + kBV * 128;            // U' [64 m][kBV] fp16 (plain)
-constexpr uint32_t S_Z = S_UP + kBV * 128;             // z [64 t][kBV] bf16 (TMA)
-constexpr uint32_t S_Y = S_Z + kBV * 128;              // y [64 t][kBV] bf16 (TMA store)
-constexpr uint32_t S_GAM = S_Y + kBV * 128;            // gamma [64]
-constexpr uint32_t S_WN = S_GAM + 256;                 // norm_w of this slice [kBV]
-constexpr uint32_t S_PART = S_WN + kBV * 4;            // partial sums of o^2 [2][kSlices][64]
-constexpr uint32_t S_MISC = S_PART + 2 * kSlices * 64 * 4;
-constexpr size_t kStateSmem = S_MISC + 128 + 1024;
-static_assert(S_NH % 1024 == 0 && S_NU % 1024 == 0 && S_KT % 1024 == 0 && S_AQ % 1024 == 0, "SW128 tiles");
-static_assert(kBV * 256 >= 8192, "rows 64-127 of the -A_Q operand stay inside -H^T");
-static_assert(S_Z % 128 == 0 && S_Y % 128 == 0 && S_UP % 16 == 0, "TMA boxes 128-byte aligned");
-static_assert(2 * kStateSmem <= 232448, "two state CTAs per SM");
-
-// tensor memory: H slice (fp32, lanes i), D_U in two buffers (chunk c's
-// epilogue reads one while chunk c+1's first product writes the other)
-constexpr int COL_H = 0, COL_U = kBV;
-constexpr uint32_t kStateTmemCols = 3 * kBV <= 128 ? 128 : 256;
-constexpr uint32_t kIdNBV = tc::idesc_f16(128, kBV);
 
 // tcgen05.ld / st of NC consecutive columns (32 lanes x 32 bit), NC = 16 or 32
 [[maybe_unused]] __device__ __forceinline__ void tmem_ld_cols(uint32_t a, float (&v)[32]) { tc::tmem_ld32(a, v); }
@@ -735,9 +746,18 @@ constexpr uint32_t kIdNBV = tc::idesc_f16(128, kBV);
   tc::tmem_st16_nowait(a, v);
 }
 
-__global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads, 2)
+template <int NS>
+__global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBlocks)
     state_kernel(const PrefillParams p, const Ws ws, const __grid_constant__ CUtensorMap zmap,
                  const __grid_constant__ CUtensorMap omap) {
+  using C = StateCfg<NS>;
+  constexpr int kSlices = C::kSlices, kBV = C::kBV, kCols = C::kCols;
+  constexpr int kMainThreads = C::kMainThreads, kEpiThreads = C::kEpiThreads, kStateThreads = C::kThreads;
+  constexpr uint32_t S_WQ = C::S_WQ, S_KT = C::S_KT, S_AQ = C::S_AQ, S_NH = C::S_NH, S_NU = C::S_NU, S_UP = C::S_UP,
+                     S_Z = C::S_Z, S_Y = C::S_Y, S_GAM = C::S_GAM, S_WN = C::S_WN, S_PART = C::S_PART,
+                     S_MISC = C::S_MISC;
+  constexpr int COL_H = C::COL_H, COL_U = C::COL_U;
+  constexpr uint32_t kStateTmemCols = C::kTmemCols, kIdNBV = C::kIdN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = tc::smem_u32(sm);
@@ -782,9 +802,9 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads,
   bool failed = false;
   auto slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
 
-  if (warp < 8) {
-    // ======================= state chain (warps 0-7): TMEM lane i, columns [kHalf gh, kHalf gh + kHalf)
-    const int i = 32 * (warp & 3) + lane, gh = warp >> 2, jc = kHalf * gh;
+  if (warp < C::kMainWarps) {
+    // ======================= state chain: TMEM lane i, columns [kCols gh, kCols gh + kCols)
+    const int i = 32 * (warp & 3) + lane, gh = warp >> 2, jc = kCols * gh;
     uint32_t ph_s1 = 0, ph_s2 = 0, ph_m1 = 0, ph_m2 = 0;
     auto wait_main = [&](uint64_t *b, uint32_t &phase) {
       const bool ok = tc::mbar_wait(b, phase & 1);
@@ -800,23 +820,23 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads,
     };
     // H (fp32, TMEM) -> -H^T fp16 operand; then H <- gamma_C H for the coming update
     auto copy_and_scale = [&](float gC) {
-      float v[kHalf], w[kHalf];
+      float v[kCols], w[kCols];
       tmem_ld_cols(tmem + lane_off + COL_H + jc, v);
 #pragma unroll
-      for (int j = 0; j < kHalf; ++j) w[j] = v[j] * gC;
+      for (int j = 0; j < kCols; ++j) w[j] = v[j] * gC;
       tmem_st_cols_nowait(tmem + lane_off + COL_H + jc, w);  // completes while the copy is written
       __half *nh = reinterpret_cast<__half *>(sm + S_NH);
 #pragma unroll
-      for (int j = 0; j < kHalf; ++j) nh[tc::sw128_offset(kBV, jc + j, i) >> 1] = __float2half_rn(-v[j]);
+      for (int j = 0; j < kCols; ++j) nh[tc::sw128_offset(kBV, jc + j, i) >> 1] = __float2half_rn(-v[j]);
       tc::tmem_st_wait();
     };
 
     // ---------------- initial state slice -> TMEM H
     const size_t st_off = ((size_t)n * h_v + h) * kD * kD + (size_t)i * kD + j0 + jc;
     {
-      float v[kHalf];
+      float v[kCols];
 #pragma unroll
-      for (int q = 0; q < kHalf; q += 4) {
+      for (int q = 0; q < kCols; q += 4) {
         const float4 f = p.init_state ? *reinterpret_cast<const float4 *>(p.init_state + st_off + q)
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
         v[q] = f.x; v[q + 1] = f.y; v[q + 2] = f.z; v[q + 3] = f.w;
@@ -847,12 +867,12 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads,
       if (wait_main(bar_m1, ph_m1)) { failed = true; break; }
       if (warp & 2) {  // U = U' + D_U rows 64-127 -> U^T fp16 operand
         const int m = i - 64;
-        float u[kHalf];
+        float u[kCols];
         tmem_ld_cols(d_u + lane_off + jc, u);
         const uint4 *up = reinterpret_cast<const uint4 *>(sm + S_UP + m * kBV * 2 + jc * 2);
         __half *nu = reinterpret_cast<__half *>(sm + S_NU);
 #pragma unroll
-        for (int q = 0; q < kHalf / 8; ++q) {
+        for (int q = 0; q < kCols / 8; ++q) {
           const uint4 raw = up[q];
           const __half2 *hp = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
@@ -863,7 +883,7 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads,
           }
         }
 #pragma unroll
-        for (int j = 0; j < kHalf; ++j) nu[tc::sw128_offset(kBV, jc + j, m) >> 1] = __float2half_rn(u[j]);
+        for (int j = 0; j < kCols; ++j) nu[tc::sw128_offset(kBV, jc + j, m) >> 1] = __float2half_rn(u[j]);
       }
       publish_main();
       if (tid == 0) tc::mbar_arrive(bar_udone);  // U' and [Q^; W] of this chunk are consumed
@@ -893,14 +913,14 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads,
     if (failed) {
       if (tid == 0) set_status(p.status, kDevTimeout);
     } else if (valid && p.final_state) {
-      float v[kHalf];
+      float v[kCols];
       tmem_ld_cols(tmem + lane_off + COL_H + jc, v);
 #pragma unroll
-      for (int q = 0; q < kHalf; q += 4)
+      for (int q = 0; q < kCols; q += 4)
         *reinterpret_cast<float4 *>(p.final_state + st_off + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
     }
-  } else if (warp < 10) {
-    // ======================= RMSNormGated epilogue (warps 8-9; thread m owns token row m of the chunk)
+  } else if (warp < C::kEpiWarp + 2) {
+    // ======================= RMSNormGated epilogue (two warps; thread m owns token row m of the chunk)
     // buffer c & 1 of each two-buffer barrier completes for chunk c in phase (c >> 1) & 1
     const int m = tid - kMainThreads;
     uint32_t ph_z = 0;
@@ -996,8 +1016,8 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads,
       if (m == 0) set_status(p.status, kDevTimeout);
       if (z_pend) tc::mbar_wait(bar_z, ph_z & 1);
     }
-  } else if (warp == 10) {
-    // ======================= operand copies (warp 10, one lane), each set as soon as its buffers are free
+  } else if (warp == C::kProdWarp) {
+    // ======================= operand copies (one lane), each set as soon as its buffers are free
     uint32_t ph = 0;
     int n1 = 0, n2 = 0;  // sets issued
     auto issue_s1 = [&](int gg) {  // [Q^; W], U' slice, gamma
@@ -1082,6 +1102,47 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 
 size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v) { return WsLayout(T, N, h_qk, h_v).total; }
 
+namespace {
+
+// Slices per chain.  The pass is bound by each chain's per-chunk latency, and
+// 4 slices of 32 columns give the shortest chunk (~2 us on GB300).  Measured
+// alternatives: 2 slices of 64 columns (~2.8 us per chunk, half the CTAs per
+// chain) and one 128-column CTA per chain were no faster with many chains
+// (32768-token varlen: 0.630 and 0.732 ms against 0.618) and slower with few.
+constexpr int kStateSlices = 4;
+
+template <int NS>
+cudaError_t launch_state(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
+  using C = StateCfg<NS>;
+  CUtensorMap zmap, omap;
+  std::memset(&zmap, 0, sizeof(zmap));
+  std::memset(&omap, 0, sizeof(omap));
+  if (p.T > 0 && !(make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, C::kBV, kC) &&
+                   make_map(&omap, p.out, (uint64_t)p.T, (uint64_t)p.h_v * kD, C::kBV, kC)))
+    return cudaErrorInvalidValue;
+  auto kern = state_kernel<NS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.N * (unsigned)p.h_v * NS);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = NS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  trace_begin(s, GDN_K_STATE);
+  e = cudaLaunchKernelEx(&cfg, kern, p, ws, zmap, omap);
+  trace_end(s);
+  return e;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
   const WsLayout L(p.T, p.N, p.h_qk, p.h_v);
@@ -1091,12 +1152,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   ws.chunk_info = reinterpret_cast<int4 *>(p.ws + L.info);
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
-  CUtensorMap zmap, omap;
-  std::memset(&zmap, 0, sizeof(zmap));
-  std::memset(&omap, 0, sizeof(omap));
-  if (p.T > 0 && !(make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, kBV, kC) &&
-                   make_map(&omap, p.out, (uint64_t)p.T, (uint64_t)p.h_v * kD, kBV, kC)))
-    return cudaErrorInvalidValue;
+  ws.up_bv_log2 = kStateSlices == 4 ? 5 : kStateSlices == 2 ? 6 : 7;
 
   trace_begin(s, GDN_K_CHUNK_TABLE);
   chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
@@ -1112,12 +1168,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
-  if (e != cudaSuccess) return e;
-  trace_begin(s, GDN_K_STATE);
-  state_kernel<<<(unsigned)p.N * (unsigned)p.h_v * kSlices, kStateThreads, kStateSmem, s>>>(p, ws, zmap, omap);
-  trace_end(s);
-  return cudaGetLastError();
+  return launch_state<kStateSlices>(p, ws, s);
 }
 
 }  // namespace gdn

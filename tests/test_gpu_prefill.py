@@ -72,6 +72,25 @@ def test_small_cases(case):
     check(inp, cfg.dtype)
 
 
+@pytest.mark.parametrize("lengths,h_qk,h_v", [
+    ((150, 1, 64), 2, 8),                  # 24 chains: every CTA of the state pass resident at once
+    ((65, 1, 128, 30, 64, 100, 7, 64, 129, 3), 16, 32),  # 320 chains: more CTAs than fit at once
+], ids=["chains24", "chains320"])
+def test_state_pass_chain_counts(lengths, h_qk, h_v):
+    """Few and many (sequence, value head) chains, sampled chains against the oracle."""
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=lengths, h_qk=h_qk, h_v=h_v, init_std=0.02, seed=21)
+    inp = synth.make_prefill(cfg)
+    chains = [(n, h) for n in range(cfg.N) for h in (0, 5, h_v - 1) if h < h_v]
+    y, fs = run_gpu(inp, True)
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], chains=chains)
+    cu = inp["cu_seqlens"]
+    for n, h in chains:
+        sl = slice(cu[n], cu[n + 1])
+        if cu[n + 1] > cu[n]:
+            parity(y[sl, h], r["y"][sl, h], "bf16", f"out chain {(n, h)}")
+        parity(fs[n, h], r["final_state"][n, h], "bf16", f"final_state chain {(n, h)}")
+
+
 def _sample_chains(cfg, picks):
     return [(n, h) for n, h in picks if n < cfg.N and h < cfg.h_v]
 
