@@ -60,6 +60,10 @@ def library() -> ctypes.CDLL:
             lib.gdn_workspace_status.restype = ctypes.c_int
             lib.gdn_status_string.argtypes = [ctypes.c_int]
             lib.gdn_status_string.restype = ctypes.c_char_p
+            lib.gdn_decode_step_slots.argtypes = [dp] + [_vp] * 13 + [ctypes.c_int] + [_vp] * 3
+            lib.gdn_decode_step_slots.restype = ctypes.c_int
+            lib.gdn_conv_cache_from_prefill.argtypes = [dp] + [_vp] * 6
+            lib.gdn_conv_cache_from_prefill.restype = ctypes.c_int
             lib.gdn_trace_enable.argtypes = [ctypes.c_int]
             lib.gdn_trace_enable.restype = ctypes.c_int
             lib.gdn_trace_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
@@ -188,6 +192,62 @@ def decode_step(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, conv_state, st
                              _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(conv_state),
                              _ptr(state), _ptr(out), _stream_handle(stream, q.device))
     _check(st, "gdn_decode_step")
+    return out
+
+
+def decode_step_slots(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, conv_state, state, slots, *, out=None,
+                      status=None, stream=None):
+    """``gdn_decode_step_slots``: one token per sequence against pools of conv
+    caches ([P, Cc, 3]) and states (fp32 [P, h_v, d_k, d_v]); sequence b uses
+    pool entry ``slots[b]`` (int32, device).  An entry outside [0, P) writes
+    zeros for that sequence and sets ``status`` (int32 [1] device tensor, if
+    given) to 5.  Returns out [B, h_v, d_v]."""
+    torch = _torch()
+    lib = library()
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("z", z), ("conv_state", conv_state)):
+        _req(t, name, dt)
+    for name, t in (("conv_w", conv_w), ("A_log", A_log), ("dt_bias", dt_bias), ("norm_w", norm_w),
+                    ("state", state)):
+        _req(t, name, torch.float32)
+    _req(slots, "slots", torch.int32)
+    if status is not None:
+        _req(status, "status", torch.int32)
+    d = dims_of(q, v, 1)
+    B, h_v, d_v = v.shape
+    if slots.numel() != B:
+        raise ValueError("slots must hold one entry per sequence")
+    if out is None:
+        out = torch.empty((B, h_v, d_v), dtype=dt, device=q.device)
+    _req(out, "out", dt)
+    st = lib.gdn_decode_step_slots(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z),
+                                   _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(conv_state),
+                                   _ptr(state), _ptr(slots), int(state.shape[0]), _ptr(out), _ptr(status),
+                                   _stream_handle(stream, q.device))
+    _check(st, "gdn_decode_step_slots")
+    return out
+
+
+def conv_cache_from_prefill(q, k, v, cu_seqlens, *, out=None, stream=None):
+    """``gdn_conv_cache_from_prefill``: the decode conv cache [N, Cc, 3] (stream
+    dtype) that the sequences of a prefill call leave: their last three raw
+    q, k, v inputs per channel, oldest first, zeros before a sequence start."""
+    torch = _torch()
+    lib = library()
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _req(t, name, dt)
+    _req(cu_seqlens, "cu_seqlens", torch.int32)
+    N = cu_seqlens.numel() - 1
+    d = dims_of(q, v, N)
+    T, h_qk, d_k = q.shape
+    _, h_v, d_v = v.shape
+    Cc = 2 * h_qk * d_k + h_v * d_v
+    if out is None:
+        out = torch.empty((N, Cc, 3), dtype=dt, device=q.device)
+    _req(out, "out", dt)
+    _check(lib.gdn_conv_cache_from_prefill(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(out),
+                                           _stream_handle(stream, q.device)), "gdn_conv_cache_from_prefill")
     return out
 
 

@@ -30,6 +30,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
   const int hq = blockIdx.x % h_qk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Cc = 2 * h_qk * dk + h_v * dv;
+  // pool entry of this sequence's state and conv cache
+  const int sb = p.slots ? p.slots[b] : b;
+  if (p.slots && (sb < 0 || sb >= p.num_slots)) {  // no pool access: zero output, report
+    IO *o = static_cast<IO *>(p.out);
+    for (int j = tid; j < (h_v / h_qk) * dv; j += kThreads)
+      o[((size_t)b * h_v + hq * (h_v / h_qk)) * dv + j] = from_f<IO>(0.0f);
+    if (tid == 0 && p.status) set_status(p.status, kDevBadSeqlens);
+    return;
+  }
 
   const IO *__restrict__ xq = static_cast<const IO *>(p.q);
   const IO *__restrict__ xk = static_cast<const IO *>(p.k);
@@ -51,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
     const int i = isq ? c : c - dk;
     const int ch = (isq ? 0 : h_qk * dk) + hq * dk + i;
     const float x = to_f((isq ? xq : xk)[((size_t)b * h_qk + hq) * dk + i]);
-    IO *cc = cache + ((size_t)b * Cc + ch) * 3;
+    IO *cc = cache + ((size_t)sb * Cc + ch) * 3;
     const float c0 = to_f(cc[0]), c1 = to_f(cc[1]), c2 = to_f(cc[2]);
     const float *w = p.conv_w + (size_t)ch * 4;
     const float pre = fmaf(w[0], c0, fmaf(w[1], c1, fmaf(w[2], c2, w[3] * x)));
@@ -85,7 +94,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
 
   for (int vv = 0; vv < rep; ++vv) {
     const int h = hq * rep + vv;
-    float *Hg = p.state + ((size_t)b * h_v + h) * dk * dv;
+    float *Hg = p.state + ((size_t)sb * h_v + h) * dk * dv;
     // issue the state loads first: they are the stream this kernel exists for
     float4 Hr[kMaxRows];
 #pragma unroll
@@ -99,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
       const int ch = 2 * h_qk * dk + h * dv + j;
       const size_t xi = ((size_t)b * h_v + h) * dv + j;
       const float x = to_f(xv[xi]);
-      IO *cc = cache + ((size_t)b * Cc + ch) * 3;
+      IO *cc = cache + ((size_t)sb * Cc + ch) * 3;
       const float c0 = to_f(cc[0]), c1 = to_f(cc[1]), c2 = to_f(cc[2]);
       const float *w = p.conv_w + (size_t)ch * 4;
       const float pre = fmaf(w[0], c0, fmaf(w[1], c1, fmaf(w[2], c2, w[3] * x)));
@@ -183,7 +192,47 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
   }
 }
 
+// Conv cache after a prefill: for sequence n and conv channel c, the raw
+// inputs of its last three tokens, oldest first, zero where the sequence is
+// shorter (the prefill's conv sees zeros before a sequence start).  One thread
+// per (sequence, channel); an invalid cu_seqlens range gives zeros.
+template <typename IO>
+__global__ void __launch_bounds__(256) conv_cache_kernel(ConvCacheParams p) {
+  const int n = blockIdx.y;
+  const int ch = blockIdx.x * blockDim.x + threadIdx.x;
+  const int cq = p.h_qk * p.d_k, Cc = 2 * cq + p.h_v * p.d_v;
+  if (ch >= Cc) return;
+  const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+  const bool ok = s0 >= 0 && s1 >= s0 && s1 <= p.T;
+  const IO *src;
+  size_t stride, col;
+  if (ch < cq) {
+    src = static_cast<const IO *>(p.q); stride = cq; col = ch;
+  } else if (ch < 2 * cq) {
+    src = static_cast<const IO *>(p.k); stride = cq; col = ch - cq;
+  } else {
+    src = static_cast<const IO *>(p.v); stride = (size_t)p.h_v * p.d_v; col = ch - 2 * cq;
+  }
+  IO *dst = static_cast<IO *>(p.conv_cache) + ((size_t)n * Cc + ch) * 3;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int t = s1 - 3 + j;
+    dst[j] = (ok && t >= s0) ? src[(size_t)t * stride + col] : from_f<IO>(0.0f);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_conv_cache(const ConvCacheParams &p, bool bf16, cudaStream_t s) {
+  const int Cc = 2 * p.h_qk * p.d_k + p.h_v * p.d_v;
+  if (p.N <= 0) return cudaSuccess;
+  const dim3 grid((unsigned)((Cc + 255) / 256), (unsigned)p.N);
+  if (bf16)
+    conv_cache_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
+  else
+    conv_cache_kernel<float><<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s) {
   const unsigned grid = (unsigned)p.B * (unsigned)p.h_qk;

@@ -91,6 +91,15 @@ int gdn_decode_step(const gdn_dims *d, const void *q, const void *k, const void 
                     const void *b, const void *z, const float *conv_w, const float *A_log,
                     const float *dt_bias, const float *norm_w, void *conv_state, float *state,
                     void *out, void *stream) {
+  return gdn_decode_step_slots(d, q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, conv_state, state, nullptr, 0,
+                               out, nullptr, stream);
+}
+
+int gdn_decode_step_slots(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
+                          const void *b, const void *z, const float *conv_w, const float *A_log,
+                          const float *dt_bias, const float *norm_w, void *conv_state, float *state,
+                          const int32_t *slots, int num_slots, void *out, int *device_status, void *stream) {
+  if (slots && num_slots <= 0) return GDN_ERR_INVALID_ARG;
   int st = check_dims(d);
   if (st != GDN_OK) return st;
   if (!conv_w || !A_log || !dt_bias || !norm_w) return GDN_ERR_INVALID_ARG;
@@ -104,7 +113,21 @@ int gdn_decode_step(const gdn_dims *d, const void *q, const void *k, const void 
   p.q = q; p.k = k; p.v = v; p.a = a; p.b = b; p.z = z;
   p.conv_w = conv_w; p.A_log = A_log; p.dt_bias = dt_bias; p.norm_w = norm_w;
   p.conv_state = conv_state; p.state = state; p.out = out;
+  p.slots = slots; p.num_slots = num_slots; p.status = device_status;
   cudaError_t e = gdn::launch_decode(p, d->io_dtype == GDN_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_conv_cache_from_prefill(const gdn_dims *d, const void *q, const void *k, const void *v,
+                                const int32_t *cu_seqlens, void *conv_cache, void *stream) {
+  int st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (d->num_seqs <= 0 || !cu_seqlens || !conv_cache) return GDN_ERR_INVALID_ARG;
+  if (d->num_tokens > 0 && (!q || !k || !v)) return GDN_ERR_INVALID_ARG;
+  gdn::ConvCacheParams p{};
+  p.T = d->num_tokens; p.N = d->num_seqs; p.h_qk = d->h_qk; p.h_v = d->h_v; p.d_k = d->d_k; p.d_v = d->d_v;
+  p.q = q; p.k = k; p.v = v; p.cu_seqlens = cu_seqlens; p.conv_cache = conv_cache;
+  cudaError_t e = gdn::launch_conv_cache(p, d->io_dtype == GDN_BF16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -26,6 +26,16 @@ struct DecodeParams {
   void *conv_state;
   float *state;
   void *out;
+  const int32_t *slots;  // [B] pool entry of each sequence, or null (entry b)
+  int num_slots;         // entries in the conv_state / state pools when slots is set
+  int *status;           // device status word for out-of-range slots, may be null
+};
+
+struct ConvCacheParams {
+  int T, N, h_qk, h_v, d_k, d_v;
+  const void *q, *k, *v;
+  const int32_t *cu_seqlens;
+  void *conv_cache;      // [N, Cc, 3]
 };
 
 // Token-sequential fp32 prefill (any supported shape, bf16 or fp32 streams).
@@ -37,6 +47,8 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
 size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v);
 // Decode step.
 cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s);
+// Conv cache of each sequence after a prefill (its last three raw inputs).
+cudaError_t launch_conv_cache(const ConvCacheParams &p, bool bf16, cudaStream_t s);
 
 // Kernel timing trace (gdn_trace.cu): events around one launch on its stream;
 // no-ops while tracing is off.  `kind` is a gdn_kernel_kind.

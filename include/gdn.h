@@ -142,6 +142,38 @@ GDN_API int gdn_decode_step(const gdn_dims *dims, const void *q, const void *k, 
                     void *conv_state, float *state, void *out, void *stream);
 
 /*
+ * Prefill -> decode hand-off, for serving (an addition of this library: the
+ * pages name varlen prefill and the layer, not a serving interface).
+ *
+ * gdn_conv_cache_from_prefill: the decode conv cache each sequence of a
+ * prefill call leaves behind.  With the prefill's dims (num_tokens = T,
+ * num_seqs = N), q, k, v and cu_seqlens, writes conv_cache io_dtype
+ * [N, Cc, 3]: per sequence and conv channel (order [q | k | v], as conv_w)
+ * the raw inputs of its last three tokens, oldest first, zero where the
+ * sequence has fewer than three (the prefill's conv sees zeros before a
+ * sequence start).  Together with the prefill's final_state this is exactly
+ * what gdn_decode_step continues from.  An invalid cu_seqlens range gives
+ * zeros for that sequence.  Returns a gdn_status (GDN_ERR_INVALID_ARG for null
+ * pointers or num_seqs < 1).
+ *
+ * gdn_decode_step_slots: gdn_decode_step over pools of states and conv
+ * caches, for paged / batched serving.  Sequence b of the batch reads and
+ * updates entry slots[b] (int32, device) of conv_state [num_slots, Cc, 3] and
+ * state [num_slots, h_v, d_k, d_v]; B = dims->num_tokens.  The slots of one
+ * call must be distinct (two sequences on one entry race).  An entry outside
+ * [0, num_slots) leaves every pool untouched, writes zeros to that sequence's
+ * out rows and sets *device_status (device int, may be NULL) to
+ * GDN_ERR_DEVICE_CHECK.  slots == NULL is gdn_decode_step (entry b).
+ */
+GDN_API int gdn_conv_cache_from_prefill(const gdn_dims *dims, const void *q, const void *k, const void *v,
+                                        const int32_t *cu_seqlens, void *conv_cache, void *stream);
+GDN_API int gdn_decode_step_slots(const gdn_dims *dims, const void *q, const void *k, const void *v,
+                                  const void *a, const void *b, const void *z, const float *conv_w,
+                                  const float *A_log, const float *dt_bias, const float *norm_w,
+                                  void *conv_state, float *state, const int32_t *slots, int num_slots,
+                                  void *out, int *device_status, void *stream);
+
+/*
  * Read and clear the device status word of a prefill workspace.  Enqueued on
  * `stream` and waits for it (the one synchronising call of the library).
  * Writes GDN_OK, GDN_ERR_DEVICE_CHECK or GDN_ERR_TIMEOUT to *device_status

@@ -249,3 +249,24 @@ def decode_step(inp: dict, conv_state, state, threads=None, **kw):
                             np.asarray(inp["x_v"], np.float64).reshape(B, -1)], axis=1)
     new_cs = np.concatenate([cs[:, :, 1:], x_all[:, :, None]], axis=2)
     return dict(y=y, state=new_state, conv_state=new_cs)
+
+
+def conv_cache_after_prefill(inp: dict, cu_seqlens):
+    """The decode conv cache [N, Cc, 3] a prefill leaves: per sequence and conv
+    channel ([q | k | v], as conv_w) the raw inputs of its last three tokens,
+    oldest first, zero before the sequence start (the zero conv history of the
+    prefill, reading of the depthwise-conv bullet of "[Qwen3.5 MoE] Add hybrid
+    decoder model ...", Summary).  Plain slicing, written from that definition."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    T = inp["x_q"].shape[0]
+    x_all = np.concatenate([np.asarray(inp["x_q"], np.float64).reshape(T, -1),
+                            np.asarray(inp["x_k"], np.float64).reshape(T, -1),
+                            np.asarray(inp["x_v"], np.float64).reshape(T, -1)], axis=1)
+    N, Cc = len(cu) - 1, x_all.shape[1]
+    cache = np.zeros((N, Cc, 3))
+    for n in range(N):
+        for j in range(3):
+            t = cu[n + 1] - 3 + j
+            if t >= cu[n]:
+                cache[n, :, j] = x_all[t]
+    return cache

@@ -103,3 +103,17 @@ def test_trace_read_without_launches(lib):
                      "decode_kernel"]
     assert lib.gdn_trace_kernel_name(gdn.TRACE_KINDS) == b""
     assert lib.gdn_trace_read(0, None, None) == 1
+
+
+def test_hand_off_calls_reject_bad_arguments_without_a_gpu(lib):
+    D = gdn.Dims
+    p = ctypes.c_void_p(1 << 20)
+    d = ctypes.byref(D(64, 2, 2, 2, 128, 128, 0))
+    assert lib.gdn_conv_cache_from_prefill(None, p, p, p, p, p, None) == 1
+    assert lib.gdn_conv_cache_from_prefill(d, p, p, p, None, p, None) == 1       # no cu_seqlens
+    assert lib.gdn_conv_cache_from_prefill(d, p, p, p, p, None, None) == 1       # no cache
+    assert lib.gdn_conv_cache_from_prefill(ctypes.byref(D(64, 0, 2, 2, 128, 128, 0)), p, p, p, p, p, None) == 1
+    args = [p] * 12
+    dd = ctypes.byref(D(4, 1, 2, 2, 128, 128, 0))
+    assert lib.gdn_decode_step_slots(dd, *args, p, 0, p, None, None) == 1        # slots without a pool size
+    assert lib.gdn_decode_step_slots(ctypes.byref(D(4, 1, 2, 3, 128, 128, 0)), *args, p, 4, p, None, None) == 1

@@ -367,3 +367,40 @@ def test_synth_bf16_rounding():
     x[:4] = [1.00390625, 1.01171875, -1.00390625, 3.0e-39]  # ties and a subnormal
     np.testing.assert_array_equal(synth.round_bf16(x),
                                   torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+
+
+def test_conv_cache_after_prefill_equals_stepping_decode():
+    """The conv cache a prefill leaves (the last three raw inputs, zeros before
+    the sequence start) equals the cache that decoding the same tokens one by
+    one from an empty cache builds up -- for sequences of 0, 1, 2 and 5 tokens."""
+    lengths = (0, 1, 2, 5)
+    inp = _tiny_inputs(lengths, h_qk=1, h_v=2, seed=8)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    cache = ref.conv_cache_after_prefill(inp, cu)
+    h_qk, dk = inp["x_q"].shape[1:]
+    h_v, dv = inp["x_v"].shape[1:]
+    Cc = 2 * h_qk * dk + h_v * dv
+    for n, L in enumerate(lengths):
+        cs = np.zeros((1, Cc, 3))
+        st = np.zeros((1, h_v, dk, dv))
+        for t in range(cu[n], cu[n + 1]):
+            tok = {k_: (v_[t:t + 1] if k_ in ("x_q", "x_k", "x_v", "z", "a", "b") else v_) for k_, v_ in inp.items()}
+            r = ref.decode_step(tok, cs, st)
+            cs, st = r["conv_state"], r["state"]
+        np.testing.assert_array_equal(cache[n], cs[0])
+
+
+def test_short_sequence_prefill_then_decode():
+    """A 2-token prefill leaves a cache with one zero entry; decoding the third
+    token from it reproduces the 3-token prefill."""
+    inp = _tiny_inputs((3,), h_qk=1, h_v=2, seed=9)
+    T = 2
+    full = ref.prefill(inp, [0, T + 1])
+    head_inp = {k_: (v_[:T] if k_ in ("x_q", "x_k", "x_v", "z", "a", "b") else v_) for k_, v_ in inp.items()}
+    head = ref.prefill(head_inp, [0, T])
+    cache = ref.conv_cache_after_prefill(head_inp, [0, T])
+    assert np.all(cache[0, :, 0] == 0)
+    dec = {k_: (v_[T:T + 1] if k_ in ("x_q", "x_k", "x_v", "z", "a", "b") else v_) for k_, v_ in inp.items()}
+    r = ref.decode_step(dec, cache, head["final_state"])
+    np.testing.assert_allclose(r["y"][0], full["y"][T], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(r["state"][0], full["final_state"][0], rtol=1e-12, atol=1e-15)
