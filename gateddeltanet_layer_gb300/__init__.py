@@ -12,8 +12,9 @@ import ctypes
 import os
 import threading
 
-__all__ = ["prefill", "decode_step", "prefill_workspace_bytes", "workspace_status", "library",
-           "GdnError", "STATUS", "prefill_noalloc", "NOALLOC_SCRATCH_BYTES"]
+__all__ = ["prefill", "decode_step", "decode_step_slots", "conv_cache_from_prefill", "prefill_workspace_bytes",
+           "workspace_status", "library", "GdnError", "STATUS", "prefill_noalloc", "NOALLOC_SCRATCH_BYTES",
+           "trace_enable", "trace_read"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")

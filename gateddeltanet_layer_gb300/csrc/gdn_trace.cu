@@ -1,5 +1,7 @@
-// Kernel timing trace: CUDA events around each launch, on the launching stream.
+// Kernel timing trace: CUDA events around each launch, on the launching stream;
+// and an NVTX range (host side) around every launch, for profilers.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <mutex>
 
@@ -34,6 +36,7 @@ Trace &trace() {
 namespace gdn {
 
 void trace_begin(cudaStream_t s, int kind) {
+  nvtxRangePushA(gdn_trace_kernel_name(kind));  // host-side range around the launch (no-op without a tool)
   Trace &t = trace();
   std::lock_guard<std::mutex> lock(t.mu);
   if (!t.on || t.open >= 0 || t.n >= GDN_TRACE_MAX_LAUNCHES) return;
@@ -48,6 +51,7 @@ void trace_begin(cudaStream_t s, int kind) {
 }
 
 void trace_end(cudaStream_t s) {
+  nvtxRangePop();
   Trace &t = trace();
   std::lock_guard<std::mutex> lock(t.mu);
   if (t.open < 0) return;

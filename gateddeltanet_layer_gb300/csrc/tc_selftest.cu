@@ -79,8 +79,25 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const uint16_t *__re
   if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
+// A wait that runs out: the mbarrier expects one arrival that never comes.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(int *flag, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0, limit_ns)) atomicExch(flag, kDevTimeout);
+}
+
 }  // namespace
 }  // namespace gdn
+
+extern "C" int gdn_selftest_wait_timeout(int *flag, int limit_us, void *stream) {
+  if (!flag || limit_us < 1 || limit_us > 1000000) return GDN_ERR_INVALID_ARG;
+  gdn::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(flag, (uint64_t)limit_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
 
 extern "C" int gdn_selftest_umma(const void *A, const void *B, float *D, int *flag, int N, int K, int b_row0,
                                  int fp16, void *stream) {

@@ -30,6 +30,16 @@ extern "C" {
 GDN_API int gdn_selftest_umma(const void *A, const void *B, float *D, int *flag, int N, int K, int b_row0,
                               int fp16, void *stream);
 
+/*
+ * Failure detection without a fault: one CTA waits, with the bounded wait every
+ * kernel of the library uses, on an mbarrier that nothing ever signals.  After
+ * limit_us microseconds (1 .. 1,000,000) of %globaltimer the wait gives up, the
+ * kernel writes GDN_ERR_TIMEOUT to *flag (device int32) and returns: no trap,
+ * no hang, and the CUDA context stays usable.  Returns GDN_OK, GDN_ERR_INVALID_ARG
+ * or GDN_ERR_CUDA (launch).
+ */
+GDN_API int gdn_selftest_wait_timeout(int *flag, int limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -117,3 +117,11 @@ def test_hand_off_calls_reject_bad_arguments_without_a_gpu(lib):
     dd = ctypes.byref(D(4, 1, 2, 2, 128, 128, 0))
     assert lib.gdn_decode_step_slots(dd, *args, p, 0, p, None, None) == 1        # slots without a pool size
     assert lib.gdn_decode_step_slots(ctypes.byref(D(4, 1, 2, 3, 128, 128, 0)), *args, p, 4, p, None, None) == 1
+
+
+def test_timeout_selftest_rejects_bad_arguments_without_a_gpu(lib):
+    fn = lib.gdn_selftest_wait_timeout
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert fn(None, 1000, None) == 1
+    assert fn(ctypes.c_void_p(1 << 20), 0, None) == 1
+    assert fn(ctypes.c_void_p(1 << 20), 2000000, None) == 1
