@@ -384,10 +384,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; distributions of the workload definitions)",
-        "config": {"workload": cfg.name, "tokens": cfg.T, "seqs": cfg.N, "h_qk": cfg.h_qk, "h_v": cfg.h_v,
-                   "d_k": cfg.d_k, "d_v": cfg.d_v, "state": "fp32", "final_state": True,
-                   "l2": "flushed between steps (512 MiB write); e2e: not flushed, fresh inputs each step",
-                   "parallelism": f"replicas x{world}"},
+        "config": headline_config(cfg, world),
         "roofline": {"bound": "hbm", "achieved": top_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": top_gbs / pk["hbm_gbs"], "traffic": profiled_traffic(top),
                      "peak_source": pk["source"] + " (burst copy)", "kernel": top,
@@ -404,6 +401,14 @@ def run_ours(args):
         "extra": extra,
     }
     print(json.dumps(line), flush=True)
+
+
+def headline_config(cfg, world):
+    """The `config` of the headline line (both arms print the same one)."""
+    return {"workload": cfg.name, "tokens": cfg.T, "seqs": cfg.N, "h_qk": cfg.h_qk, "h_v": cfg.h_v,
+            "d_k": cfg.d_k, "d_v": cfg.d_v, "state": "fp32", "final_state": True,
+            "l2": "flushed between steps (512 MiB write); e2e: not flushed, fresh inputs each step",
+            "parallelism": f"replicas x{world}"}
 
 
 def profiled_traffic(kernel):
@@ -470,7 +475,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 * cfg.h_v / n_chains,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": {"workload": cfg.name, "tokens": cfg.T},
+            "data": "synthetic (seeded)", "config": headline_config(cfg, 1),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, n_chains), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
