@@ -472,7 +472,8 @@ def run_reference(args):
     dt = statistics.mean(times)
     value = cfg.T * n_chains / cfg.h_v / dt
     sample = f"{n_chains} of {cfg.h_v} (sequence, head) chains of {cfg.name} per step, all {cfg.T} tokens each"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 * cfg.h_v / n_chains,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)", "config": headline_config(cfg, 1),
