@@ -49,7 +49,7 @@ def test_tiny_fp32_config():
 
 
 @pytest.mark.parametrize("case", ["ragged_single", "varlen_edges", "long_memory", "gqa4", "gqa8", "gqa16",
-                                  "fp32_d128"])
+                                  "fp32_d128", "gqa1", "chunk_edges", "fast_decay"])
 def test_small_cases(case):
     if case == "ragged_single":      # several chunks plus a ragged tail
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(200,), h_qk=2, h_v=4)
@@ -60,6 +60,12 @@ def test_small_cases(case):
                            init_std=0.02, seed=5)
     elif case == "gqa4":             # 4 value heads per q/k head
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(97, 31), h_qk=1, h_v=4, seed=7)
+    elif case == "gqa1":             # one value head per q/k head
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(150,), h_qk=2, h_v=2, init_std=0.02, seed=10)
+    elif case == "chunk_edges":      # exactly one chunk, one chunk + 1, two chunks - 1, one token
+        cfg = synth.scaled(synth.VARLEN_32K, lengths=(64, 65, 127, 1, 128), h_qk=1, h_v=2, seed=11)
+    elif case == "fast_decay":       # gates near their strongest: A_log up to log 16 and large dt_bias
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(200,), h_qk=1, h_v=2, init_std=0.02, seed=12)
     elif case == "gqa8":             # the most value heads per q/k head the chunked path takes
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(70,), h_qk=1, h_v=8, seed=8)
     elif case == "gqa16":            # beyond it: served by the token-sequential kernel
@@ -69,6 +75,9 @@ def test_small_cases(case):
     inp = synth.make_prefill(cfg)
     if case == "long_memory":
         inp["dt_bias"][:] = -6.0
+    if case == "fast_decay":
+        inp["dt_bias"][:] = 4.0
+        inp["A_log"][:] = np.log(16.0)
     check(inp, cfg.dtype)
 
 
