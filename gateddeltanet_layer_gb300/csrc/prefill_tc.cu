@@ -727,14 +727,22 @@ struct StateCfg {
   static constexpr uint32_t kTmemCols = 3 * kBV <= 128 ? 128 : 3 * kBV <= 256 ? 256 : 512;
   static constexpr uint32_t kIdN = tc::idesc_f16(128, kBV);
   static_assert(S_NH % 1024 == 0 && S_NU % 1024 == 0 && S_KT % 1024 == 0 && S_AQ % 1024 == 0, "SW128 tiles");
-  static_assert(kBV * 256 >= 8192, "rows 64-127 of the -A_Q operand stay inside -H^T");
+  static_assert(S_AQ + 16384 <= S_MISC, "rows 64-127 of the -A_Q operand stay inside the CTA's tiles");
   static_assert(S_Z % 128 == 0 && S_Y % 128 == 0 && S_UP % 16 == 0, "TMA boxes 128-byte aligned");
   static_assert(kMinBlocks * kSmem <= 232448, "shared memory budget");
-  static_assert(kCols == 16 || kCols == 32, "TMEM access widths");
+  static_assert(kCols == 8 || kCols == 16 || kCols == 32, "TMEM access widths");
 };
 constexpr int kBarMain = 1, kBarEpi = 2;
 
-// tcgen05.ld / st of NC consecutive columns (32 lanes x 32 bit), NC = 16 or 32
+// tcgen05.ld / st of NC consecutive columns (32 lanes x 32 bit), NC = 8, 16 or 32
+[[maybe_unused]] __device__ __forceinline__ void tmem_ld_cols(uint32_t a, float (&v)[8]) { tc::tmem_ld8(a, v); }
+[[maybe_unused]] __device__ __forceinline__ void tmem_st_cols(uint32_t a, const float (&v)[8]) {
+  tc::tmem_st8_nowait(a, v);
+  tc::tmem_st_wait();
+}
+[[maybe_unused]] __device__ __forceinline__ void tmem_st_cols_nowait(uint32_t a, const float (&v)[8]) {
+  tc::tmem_st8_nowait(a, v);
+}
 [[maybe_unused]] __device__ __forceinline__ void tmem_ld_cols(uint32_t a, float (&v)[32]) { tc::tmem_ld32(a, v); }
 [[maybe_unused]] __device__ __forceinline__ void tmem_ld_cols(uint32_t a, float (&v)[16]) { tc::tmem_ld16(a, v); }
 [[maybe_unused]] __device__ __forceinline__ void tmem_st_cols(uint32_t a, const float (&v)[32]) { tc::tmem_st32(a, v); }
@@ -948,13 +956,14 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
       const int t0 = s0 + kC * c;
       const int Lc = min(kC, s1 - t0);
       if (wait_epi(bar_oready + buf, par, false)) { failed = true; break; }
+      constexpr int kEw = kBV < 32 ? kBV : 32;  // TMEM columns per epilogue load
       float ss = 0.0f;
 #pragma unroll
-      for (int c32 = 0; c32 < kBV; c32 += 32) {
-        float o[32];
-        tc::tmem_ld32(d_u + c32, o);
+      for (int c32 = 0; c32 < kBV; c32 += kEw) {
+        float o[kEw];
+        tmem_ld_cols(d_u + c32, o);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
+        for (int j = 0; j < kEw; ++j) ss = fmaf(o[j], o[j], ss);
       }
       ss *= scale * scale;
       if (m == 0) tc::mbar_arrive_expect_tx(bar_part + buf, kSlices * 64 * 4);
@@ -973,12 +982,12 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
       tc::bulk_wait_read();  // this thread's earlier y copies have left S_Y
       tc::named_barrier(kBarEpi, kEpiThreads);
 #pragma unroll
-      for (int c32 = 0; c32 < kBV; c32 += 32) {
-        float o[32];
-        tc::tmem_ld32(d_u + c32, o);
+      for (int c32 = 0; c32 < kBV; c32 += kEw) {
+        float o[kEw];
+        tmem_ld_cols(d_u + c32, o);
         const uint4 *zrow = reinterpret_cast<const uint4 *>(sm + S_Z + m * kBV * 2 + c32 * 2);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kEw / 8; ++q) {
           const uint4 zz = zrow[q];
           const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
           float y8[8];
@@ -1104,12 +1113,27 @@ size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v) { return WsLa
 
 namespace {
 
-// Slices per chain.  The pass is bound by each chain's per-chunk latency, and
-// 4 slices of 32 columns give the shortest chunk (~2 us on GB300).  Measured
-// alternatives: 2 slices of 64 columns (~2.8 us per chunk, half the CTAs per
-// chain) and one 128-column CTA per chain were no faster with many chains
-// (32768-token varlen: 0.630 and 0.732 ms against 0.618) and slower with few.
-constexpr int kStateSlices = 4;
+// Slices per chain.  The pass is bound by each chain's per-chunk latency: a
+// single thread issues the MMAs of a chunk at a fixed cost per instruction
+// whatever N is, so narrower slices only shorten the per-chunk conversions and
+// the epilogue, and they pay while every CTA of the pass is resident at once.
+// 8 slices of 16 columns when that holds at two CTAs per SM (the 4096-token
+// workload: 0.1265 against 0.1295 ms), else 4 of 32.  Measured and not taken:
+// 2 slices of 64 columns (~2.8 us per chunk, 0.630 against 0.618 ms on the
+// 32768-token varlen workload) and one 128-column CTA per chain (0.732 ms).
+int state_slices(const PrefillParams &p) {
+  static int sms[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  dev = dev < 0 || dev >= 64 ? 0 : dev;
+  std::call_once(once[dev], [dev] {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 1;
+  });
+  return 8L * p.N * p.h_v <= 2L * sms[dev] ? 8 : 4;
+}
 
 template <int NS>
 cudaError_t launch_state(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
@@ -1152,7 +1176,8 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   ws.chunk_info = reinterpret_cast<int4 *>(p.ws + L.info);
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
-  ws.up_bv_log2 = kStateSlices == 4 ? 5 : kStateSlices == 2 ? 6 : 7;
+  const int ns = state_slices(p);
+  ws.up_bv_log2 = __builtin_ctz((unsigned)(kD / ns));
 
   trace_begin(s, GDN_K_CHUNK_TABLE);
   chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
@@ -1168,7 +1193,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return launch_state<kStateSlices>(p, ws, s);
+  return ns == 8 ? launch_state<8>(p, ws, s) : launch_state<4>(p, ws, s);
 }
 
 }  // namespace gdn
