@@ -697,7 +697,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 // chunk behind (exchanging per-token partial sums of o^2 with the other CTAs
 // of the cluster through st.async into their shared memory), warp 10 issues
 // the operand copies.
-template <int NS>
+// ST = 0: one buffer per operand set, refilled as soon as each set is consumed
+// (two CTAs per SM).  ST >= 2: a ring of ST whole per-chunk operand sets
+// ([Q^; W], K~^T, -A_Q, U' slice, gamma), so the copies of the next chunks
+// stream in while one is computed (one CTA per SM).
+template <int NS, int ST>
 struct StateCfg {
   static constexpr int kSlices = NS;                    // CTAs per chain
   static constexpr int kBV = kD / NS;                   // state columns per CTA
@@ -707,29 +711,34 @@ struct StateCfg {
   static constexpr int kMainThreads = 32 * kMainWarps, kEpiThreads = 64;
   static constexpr int kEpiWarp = kMainWarps, kProdWarp = kMainWarps + 2;
   static constexpr int kThreads = 32 * (kMainWarps + 3);
-  static constexpr int kMinBlocks = 2;
-  static constexpr uint32_t S_WQ = 0;                   // [Q^; W] image (32 KB)
-  static constexpr uint32_t S_KT = 32768;               // K~^T [128 i][64 m] (16 KB)
-  static constexpr uint32_t S_AQ = 49152;               // -A_Q [64][64] (8 KB), rows 64-127 of its
-  static constexpr uint32_t S_NH = S_AQ + 8192;         //   operand read the first 8 KB here (unused)
+  static constexpr int kMinBlocks = ST == 0 ? 2 : 1;
+  // one operand set: [Q^; W] (32 KB), K~^T (16 KB), -A_Q (8 KB; rows 64-127 of its
+  // 128-row operand read the next 8 KB, unused), U' [64 m][kBV] fp16, gamma [64]
+  static constexpr uint32_t R_WQ = 0, R_KT = 32768, R_AQ = 49152, R_UP = 57344;
+  static constexpr uint32_t R_GAM = R_UP + kBV * 128;
+  static constexpr uint32_t kStage = (R_GAM + 256 + 1023) / 1024 * 1024;
+  static constexpr uint32_t kSets = ST == 0 ? 1 : ST;
+  static constexpr uint32_t S_NH = kSets * kStage;      // -H^T fp16 [kBV j][128 i]
   static constexpr uint32_t S_NU = S_NH + kBV * 256;    // U^T fp16 [kBV j][64 m]
-  static constexpr uint32_t S_UP = S_NU + kBV * 128;    // U' [64 m][kBV] fp16 (plain)
-  static constexpr uint32_t S_Z = S_UP + kBV * 128;     // z [64 t][kBV] bf16 (TMA)
+  static constexpr uint32_t S_Z = S_NU + kBV * 128;     // z [64 t][kBV] bf16 (TMA)
   static constexpr uint32_t S_Y = S_Z + kBV * 128;      // y [64 t][kBV] bf16 (TMA store)
-  static constexpr uint32_t S_GAM = S_Y + kBV * 128;    // gamma [64]
-  static constexpr uint32_t S_WN = S_GAM + 256;         // norm_w of this slice [kBV]
+  static constexpr uint32_t S_WN = S_Y + kBV * 128;     // norm_w of this slice [kBV]
   static constexpr uint32_t S_PART = S_WN + kBV * 4;    // partial sums of o^2 [2][kSlices][64]
   static constexpr uint32_t S_MISC = S_PART + 2 * kSlices * 64 * 4;
-  static constexpr size_t kSmem = S_MISC + 128 + 1024;
+  static constexpr size_t kSmem = S_MISC + 256 + 1024;
+  // barriers: chain, epilogue, then the operand-set ones of the buffering scheme
+  static constexpr int B_M1 = 0, B_M2 = 1, B_Z = 2, B_ORDY = 3, B_ODONE = 5, B_PART = 7, B_SETS = 9;
+  static constexpr int kBars = B_SETS + (ST == 0 ? 4 : 2 * ST);
   // tensor memory: H slice (fp32, lanes i), D_U in two buffers (chunk c's
   // epilogue reads one while chunk c+1's first product writes the other)
   static constexpr int COL_H = 0, COL_U = kBV;
   static constexpr uint32_t kTmemCols = 3 * kBV <= 128 ? 128 : 3 * kBV <= 256 ? 256 : 512;
   static constexpr uint32_t kIdN = tc::idesc_f16(128, kBV);
-  static_assert(S_NH % 1024 == 0 && S_NU % 1024 == 0 && S_KT % 1024 == 0 && S_AQ % 1024 == 0, "SW128 tiles");
-  static_assert(S_AQ + 16384 <= S_MISC, "rows 64-127 of the -A_Q operand stay inside the CTA's tiles");
-  static_assert(S_Z % 128 == 0 && S_Y % 128 == 0 && S_UP % 16 == 0, "TMA boxes 128-byte aligned");
-  static_assert(kMinBlocks * kSmem <= 232448, "shared memory budget");
+  static_assert(S_NH % 1024 == 0 && S_NU % 1024 == 0 && kStage % 1024 == 0, "SW128 tiles");
+  static_assert(kSets * kStage - kStage + R_AQ + 16384 <= S_MISC, "rows 64-127 of the -A_Q operand stay inside");
+  static_assert(S_Z % 128 == 0 && S_Y % 128 == 0, "TMA boxes 128-byte aligned");
+  static_assert(kMinBlocks * (kSmem + 1024) <= 233472 && kSmem <= 232448, "shared memory budget");
+  static_assert(kBars * 8 + 4 <= 256, "barrier block");
   static_assert(kCols == 8 || kCols == 16 || kCols == 32, "TMEM access widths");
 };
 constexpr int kBarMain = 1, kBarEpi = 2;
@@ -754,16 +763,17 @@ constexpr int kBarMain = 1, kBarEpi = 2;
   tc::tmem_st16_nowait(a, v);
 }
 
-template <int NS>
-__global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBlocks)
+template <int NS, int ST>
+__global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::kMinBlocks)
     state_kernel(const PrefillParams p, const Ws ws, const __grid_constant__ CUtensorMap zmap,
                  const __grid_constant__ CUtensorMap omap) {
-  using C = StateCfg<NS>;
+  using C = StateCfg<NS, ST>;
   constexpr int kSlices = C::kSlices, kBV = C::kBV, kCols = C::kCols;
   constexpr int kMainThreads = C::kMainThreads, kEpiThreads = C::kEpiThreads, kStateThreads = C::kThreads;
-  constexpr uint32_t S_WQ = C::S_WQ, S_KT = C::S_KT, S_AQ = C::S_AQ, S_NH = C::S_NH, S_NU = C::S_NU, S_UP = C::S_UP,
-                     S_Z = C::S_Z, S_Y = C::S_Y, S_GAM = C::S_GAM, S_WN = C::S_WN, S_PART = C::S_PART,
-                     S_MISC = C::S_MISC;
+  constexpr uint32_t S_NH = C::S_NH, S_NU = C::S_NU, S_Z = C::S_Z, S_Y = C::S_Y, S_WN = C::S_WN,
+                     S_PART = C::S_PART, S_MISC = C::S_MISC;
+  // operand set of the chain's chunk c (a ring slot when ST >= 2)
+  auto set_of = [](int c) -> uint32_t { return ST == 0 ? 0u : C::kStage * (uint32_t)(c % (ST == 0 ? 1 : ST)); };
   constexpr int COL_H = C::COL_H, COL_U = C::COL_U;
   constexpr uint32_t kStateTmemCols = C::kTmemCols, kIdNBV = C::kIdN;
   extern __shared__ uint8_t smem_raw[];
@@ -784,11 +794,14 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
   const int nch = valid ? g1 - g0 : 0;
 
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_MISC);
-  uint64_t *bar_s1 = bar, *bar_s2 = bar + 1, *bar_m1 = bar + 2, *bar_m2 = bar + 3, *bar_m2b = bar + 4;
-  uint64_t *bar_udone = bar + 5, *bar_z = bar + 6;
-  uint64_t *bar_oready = bar + 7, *bar_odone = bar + 9, *bar_part = bar + 11;  // [2] each
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_MISC + 112);
-  const float *sGam = reinterpret_cast<const float *>(sm + S_GAM);
+  uint64_t *bar_m1 = bar + C::B_M1, *bar_m2 = bar + C::B_M2, *bar_z = bar + C::B_Z;
+  uint64_t *bar_oready = bar + C::B_ORDY, *bar_odone = bar + C::B_ODONE, *bar_part = bar + C::B_PART;  // [2] each
+  // ST = 0: set 1 ([Q^; W], U', gamma) and set 2 (K~^T, -A_Q) full, MMA 2's second half done, U step done;
+  // ST >= 2: full[ST], empty[ST] (empty completes when both halves of MMA 2 have read the set)
+  uint64_t *bar_s1 = bar + C::B_SETS, *bar_s2 = bar + C::B_SETS + 1, *bar_m2b = bar + C::B_SETS + 2;
+  uint64_t *bar_udone = bar + C::B_SETS + 3;
+  uint64_t *bar_full = bar + C::B_SETS, *bar_empty = bar + C::B_SETS + (ST == 0 ? 0 : ST);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_MISC + 8 * C::kBars);
   float *sWn = reinterpret_cast<float *>(sm + S_WN);
   __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 
@@ -797,7 +810,7 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 13; ++i) tc::mbar_init(bar + i, 1);
+    for (int i = 0; i < C::kBars; ++i) tc::mbar_init(bar + i, (ST != 0 && i >= C::B_SETS + ST) ? 2 : 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&zmap);
     tc::prefetch_tmap(&omap);
@@ -851,9 +864,17 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
       }
       tmem_st_cols(tmem + lane_off + COL_H + jc, v);
     }
+    // gamma_C of the chain's chunk c, from its operand set
+    auto gamma_c = [&](int c) { return reinterpret_cast<const float *>(sm + set_of(c) + C::R_GAM)[kC - 1]; };
+    // wait for the operand set of chunk c (ST = 0: set 1 only; set 2 is waited before MMA 2)
+    auto wait_set = [&](int c) {
+      if constexpr (ST == 0) return wait_main(bar_s1, ph_s1);
+      uint32_t par = (uint32_t)(c / (ST == 0 ? 1 : ST)) & 1;
+      return wait_main(bar_full + c % (ST == 0 ? 1 : ST), par);
+    };
     if (nch > 0) {
-      if (wait_main(bar_s1, ph_s1)) failed = true;
-      else copy_and_scale(sGam[63]);
+      if (wait_set(0)) failed = true;
+      else copy_and_scale(gamma_c(0));
     }
     publish_main();
 
@@ -865,11 +886,12 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
         if (wait_main(bar_odone + buf, par)) { failed = true; break; }
       }
 
+      const uint32_t set = set_of(c);  // this chunk's operand set
       // ---------------- MMA 1: D_U = [Q^; W] (-H)
       if (tid == 0) {
         for (int k = 0; k < 8; ++k)
-          tc::mma16(d_u, tc::sdesc_kstep(sbase + S_WQ, 128, 0, k), tc::sdesc_kstep(sbase + S_NH, kBV, 0, k), kIdNBV,
-                    k > 0 ? 1u : 0u);
+          tc::mma16(d_u, tc::sdesc_kstep(sbase + set + C::R_WQ, 128, 0, k), tc::sdesc_kstep(sbase + S_NH, kBV, 0, k),
+                    kIdNBV, k > 0 ? 1u : 0u);
         tc::mma_commit(bar_m1);
       }
       if (wait_main(bar_m1, ph_m1)) { failed = true; break; }
@@ -877,7 +899,7 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
         const int m = i - 64;
         float u[kCols];
         tmem_ld_cols(d_u + lane_off + jc, u);
-        const uint4 *up = reinterpret_cast<const uint4 *>(sm + S_UP + m * kBV * 2 + jc * 2);
+        const uint4 *up = reinterpret_cast<const uint4 *>(sm + set + C::R_UP + m * kBV * 2 + jc * 2);
         __half *nu = reinterpret_cast<__half *>(sm + S_NU);
 #pragma unroll
         for (int q = 0; q < kCols / 8; ++q) {
@@ -894,26 +916,30 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
         for (int j = 0; j < kCols; ++j) nu[tc::sw128_offset(kBV, jc + j, m) >> 1] = __float2half_rn(u[j]);
       }
       publish_main();
-      if (tid == 0) tc::mbar_arrive(bar_udone);  // U' and [Q^; W] of this chunk are consumed
+      if constexpr (ST == 0) {
+        if (tid == 0) tc::mbar_arrive(bar_udone);  // U' and [Q^; W] of this chunk are consumed
+        if (wait_main(bar_s2, ph_s2)) { failed = true; break; }
+      }
 
       // ---------------- MMA 2: D_H += K~^T U (critical);  D_U += [-A_Q; *] U (second issuer)
-      if (wait_main(bar_s2, ph_s2)) { failed = true; break; }
       if (tid == 0) {
         for (int k = 0; k < 4; ++k)
-          tc::mma16(tmem + COL_H, tc::sdesc_kstep(sbase + S_KT, 128, 0, k), tc::sdesc_kstep(sbase + S_NU, kBV, 0, k),
-                    kIdNBV, 1u);
+          tc::mma16(tmem + COL_H, tc::sdesc_kstep(sbase + set + C::R_KT, 128, 0, k),
+                    tc::sdesc_kstep(sbase + S_NU, kBV, 0, k), kIdNBV, 1u);
         tc::mma_commit(bar_m2);
+        if constexpr (ST != 0) tc::mma_commit(bar_empty + c % (ST == 0 ? 1 : ST));
       } else if (tid == 32) {
         for (int k = 0; k < 4; ++k)
-          tc::mma16(d_u, tc::sdesc_kstep(sbase + S_AQ, 128, 0, k), tc::sdesc_kstep(sbase + S_NU, kBV, 0, k), kIdNBV,
-                    1u);
-        tc::mma_commit(bar_m2b);
+          tc::mma16(d_u, tc::sdesc_kstep(sbase + set + C::R_AQ, 128, 0, k), tc::sdesc_kstep(sbase + S_NU, kBV, 0, k),
+                    kIdNBV, 1u);
+        if constexpr (ST == 0) tc::mma_commit(bar_m2b);
+        else tc::mma_commit(bar_empty + c % (ST == 0 ? 1 : ST));
         tc::mma_commit(bar_oready + buf);
       }
       if (wait_main(bar_m2, ph_m2)) { failed = true; break; }
       if (c + 1 < nch) {
-        if (wait_main(bar_s1, ph_s1)) { failed = true; break; }
-        copy_and_scale(sGam[63]);
+        if (wait_set(c + 1)) { failed = true; break; }
+        copy_and_scale(gamma_c(c + 1));
       }
       publish_main();
     }
@@ -1026,49 +1052,72 @@ __global__ void __launch_bounds__(StateCfg<NS>::kThreads, StateCfg<NS>::kMinBloc
       if (z_pend) tc::mbar_wait(bar_z, ph_z & 1);
     }
   } else if (warp == C::kProdWarp) {
-    // ======================= operand copies (one lane), each set as soon as its buffers are free
-    uint32_t ph = 0;
-    int n1 = 0, n2 = 0;  // sets issued
-    auto issue_s1 = [&](int gg) {  // [Q^; W], U' slice, gamma
-      tc::mbar_arrive_expect_tx(bar_s1, 32768 + 64 * kBV * 2 + 256);
-      tc::bulk_g2s(sm + S_WQ, slot(gg) + kVWQ, 32768, bar_s1);
-      tc::bulk_g2s(sm + S_UP, slot(gg) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2, bar_s1);
-      tc::bulk_g2s(sm + S_GAM, slot(gg) + kVGam, 256, bar_s1);
-      ++n1;
-    };
-    auto issue_s2 = [&](int gg) {  // K~^T, -A_Q
-      tc::mbar_arrive_expect_tx(bar_s2, 16384 + 8192);
-      tc::bulk_g2s(sm + S_KT, slot(gg) + kVKt, 16384, bar_s2);
-      tc::bulk_g2s(sm + S_AQ, slot(gg) + kVAq, 8192, bar_s2);
-      ++n2;
-    };
-    if (lane == 0 && nch > 0) {
-      issue_s1(g0);
-      issue_s2(g0);
-      if (nch > 1) {
-        tc::prefetch_l2(slot(g0 + 1) + kVWQ, 32768 + 16384);
-        tc::prefetch_l2(slot(g0 + 1) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2);
-        tc::prefetch_l2(slot(g0 + 1) + kVAq, 8192 + 256);
-      }
-      for (int c = 0; c + 1 < nch; ++c) {
-        // chunk c's MMA 1 and U' are consumed (the chain signals after MMA 1 and the U step)
-        if (!tc::mbar_wait(bar_udone, ph & 1)) { failed = true; break; }
-        issue_s1(g0 + c + 1);
-        if (c + 2 < nch) {  // the chunk after: into L2 now, so its copies later come from there
-          tc::prefetch_l2(slot(g0 + c + 2) + kVWQ, 32768 + 16384);
-          tc::prefetch_l2(slot(g0 + c + 2) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2);
-          tc::prefetch_l2(slot(g0 + c + 2) + kVAq, 8192 + 256);
+    if constexpr (ST == 0) {
+      // ======================= operand copies (one lane), each set as soon as its buffers are free
+      uint32_t ph = 0;
+      int n1 = 0, n2 = 0;  // sets issued
+      auto issue_s1 = [&](int gg) {  // [Q^; W], U' slice, gamma
+        tc::mbar_arrive_expect_tx(bar_s1, 32768 + 64 * kBV * 2 + 256);
+        tc::bulk_g2s(sm + C::R_WQ, slot(gg) + kVWQ, 32768, bar_s1);
+        tc::bulk_g2s(sm + C::R_UP, slot(gg) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2, bar_s1);
+        tc::bulk_g2s(sm + C::R_GAM, slot(gg) + kVGam, 256, bar_s1);
+        ++n1;
+      };
+      auto issue_s2 = [&](int gg) {  // K~^T, -A_Q
+        tc::mbar_arrive_expect_tx(bar_s2, 16384 + 8192);
+        tc::bulk_g2s(sm + C::R_KT, slot(gg) + kVKt, 16384, bar_s2);
+        tc::bulk_g2s(sm + C::R_AQ, slot(gg) + kVAq, 8192, bar_s2);
+        ++n2;
+      };
+      if (lane == 0 && nch > 0) {
+        issue_s1(g0);
+        issue_s2(g0);
+        if (nch > 1) {
+          tc::prefetch_l2(slot(g0 + 1) + kVWQ, 32768 + 16384);
+          tc::prefetch_l2(slot(g0 + 1) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2);
+          tc::prefetch_l2(slot(g0 + 1) + kVAq, 8192 + 256);
         }
-        // chunk c's MMA 2 (both halves) has read K~^T and -A_Q
-        if (!tc::mbar_wait(bar_m2, ph & 1) || !tc::mbar_wait(bar_m2b, ph & 1)) { failed = true; break; }
-        issue_s2(g0 + c + 1);
-        ++ph;
+        for (int c = 0; c + 1 < nch; ++c) {
+          // chunk c's MMA 1 and U' are consumed (the chain signals after MMA 1 and the U step)
+          if (!tc::mbar_wait(bar_udone, ph & 1)) { failed = true; break; }
+          issue_s1(g0 + c + 1);
+          if (c + 2 < nch) {  // the chunk after: into L2 now, so its copies later come from there
+            tc::prefetch_l2(slot(g0 + c + 2) + kVWQ, 32768 + 16384);
+            tc::prefetch_l2(slot(g0 + c + 2) + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2);
+            tc::prefetch_l2(slot(g0 + c + 2) + kVAq, 8192 + 256);
+          }
+          // chunk c's MMA 2 (both halves) has read K~^T and -A_Q
+          if (!tc::mbar_wait(bar_m2, ph & 1) || !tc::mbar_wait(bar_m2b, ph & 1)) { failed = true; break; }
+          issue_s2(g0 + c + 1);
+          ++ph;
+        }
+        if (failed) set_status(p.status, kDevTimeout);
+        // copies in flight must land before the CTA's shared memory goes away
+        // (the last set of each kind; set k completes phase k of its barrier)
+        if (n1 > 0) tc::mbar_wait(bar_s1, (uint32_t)(n1 - 1) & 1);
+        if (n2 > 0) tc::mbar_wait(bar_s2, (uint32_t)(n2 - 1) & 1);
+      }
+    } else if (lane == 0 && nch > 0) {
+      // ======================= operand copies (one lane): the set of chunk c into ring slot c % ST as soon
+      // as MMA 2 of chunk c - ST has read it (a waiter here lags its signaller by at most one use)
+      constexpr int kST = ST == 0 ? 1 : ST;
+      int issued = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int r = c % kST;
+        if (c >= kST && !tc::mbar_wait(bar_empty + r, (uint32_t)(c / kST - 1) & 1)) { failed = true; break; }
+        uint8_t *dst = sm + set_of(c);
+        const uint8_t *src = slot(g0 + c);
+        tc::mbar_arrive_expect_tx(bar_full + r, 32768 + 16384 + 8192 + 64 * kBV * 2 + 256);
+        tc::bulk_g2s(dst + C::R_WQ, src + kVWQ, 32768 + 16384, bar_full + r);  // [Q^; W] and K~^T
+        tc::bulk_g2s(dst + C::R_AQ, src + kVAq, 8192, bar_full + r);
+        tc::bulk_g2s(dst + C::R_UP, src + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2, bar_full + r);
+        tc::bulk_g2s(dst + C::R_GAM, src + kVGam, 256, bar_full + r);
+        issued = c + 1;
       }
       if (failed) set_status(p.status, kDevTimeout);
       // copies in flight must land before the CTA's shared memory goes away
-      // (the last set of each kind; set k completes phase k of its barrier)
-      if (n1 > 0) tc::mbar_wait(bar_s1, (uint32_t)(n1 - 1) & 1);
-      if (n2 > 0) tc::mbar_wait(bar_s2, (uint32_t)(n2 - 1) & 1);
+      for (int c = issued - kST < 0 ? 0 : issued - kST; c < issued; ++c)
+        tc::mbar_wait(bar_full + c % kST, (uint32_t)(c / kST) & 1);
     }
   }
   tc::fence_before_sync();
@@ -1113,15 +1162,17 @@ size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v) { return WsLa
 
 namespace {
 
-// Slices per chain.  The pass is bound by each chain's per-chunk latency: a
-// single thread issues the MMAs of a chunk at a fixed cost per instruction
-// whatever N is, so narrower slices only shorten the per-chunk conversions and
-// the epilogue, and they pay while every CTA of the pass is resident at once.
-// 8 slices of 16 columns when that holds at two CTAs per SM (the 4096-token
-// workload: 0.1265 against 0.1295 ms), else 4 of 32.  Measured and not taken:
-// 2 slices of 64 columns (~2.8 us per chunk, 0.630 against 0.618 ms on the
-// 32768-token varlen workload) and one 128-column CTA per chain (0.732 ms).
-int state_slices(const PrefillParams &p) {
+// How the state pass runs.  It is bound by each chain's per-chunk latency, a
+// good part of which is the copy of the chunk's operand set (~60 KB); 4 slices
+// of 32 columns.  When every CTA fits on an SM of its own (few chains: the
+// 4096-token workload has 32 chains, 128 CTAs), a ring of 3 operand sets lets
+// the copies of the next chunks stream in while one is computed (0.114 against
+// 0.127 ms with the next best, 8 slices at two CTAs per SM); with more chains
+// one set per kind at two CTAs per SM keeps twice the chains in flight (the
+// ring, at one CTA per SM, took 0.806 against 0.624 ms on the 32768-token
+// varlen workload).  Measured and not taken: 2 slices of 64 columns and one
+// 128-column CTA per chain (no faster with many chains, slower with few).
+bool state_ring(const PrefillParams &p) {
   static int sms[64];
   static std::once_flag once[64];
   int dev = 0;
@@ -1132,19 +1183,20 @@ int state_slices(const PrefillParams &p) {
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
     sms[dev] = v > 0 ? v : 1;
   });
-  return 8L * p.N * p.h_v <= 2L * sms[dev] ? 8 : 4;
+  return 4L * p.N * p.h_v <= (long)sms[dev];
 }
+constexpr int kStateSlices = 4;
 
-template <int NS>
+template <int NS, int ST>
 cudaError_t launch_state(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
-  using C = StateCfg<NS>;
+  using C = StateCfg<NS, ST>;
   CUtensorMap zmap, omap;
   std::memset(&zmap, 0, sizeof(zmap));
   std::memset(&omap, 0, sizeof(omap));
   if (p.T > 0 && !(make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, C::kBV, kC) &&
                    make_map(&omap, p.out, (uint64_t)p.T, (uint64_t)p.h_v * kD, C::kBV, kC)))
     return cudaErrorInvalidValue;
-  auto kern = state_kernel<NS>;
+  auto kern = state_kernel<NS, ST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1176,8 +1228,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   ws.chunk_info = reinterpret_cast<int4 *>(p.ws + L.info);
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
-  const int ns = state_slices(p);
-  ws.up_bv_log2 = __builtin_ctz((unsigned)(kD / ns));
+  ws.up_bv_log2 = __builtin_ctz((unsigned)(kD / kStateSlices));
 
   trace_begin(s, GDN_K_CHUNK_TABLE);
   chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
@@ -1193,7 +1244,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return ns == 8 ? launch_state<8>(p, ws, s) : launch_state<4>(p, ws, s);
+  return state_ring(p) ? launch_state<kStateSlices, 3>(p, ws, s) : launch_state<kStateSlices, 0>(p, ws, s);
 }
 
 }  // namespace gdn

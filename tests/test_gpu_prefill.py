@@ -82,13 +82,14 @@ def test_small_cases(case):
 
 
 @pytest.mark.parametrize("lengths,h_qk,h_v", [
-    ((150, 1, 64), 2, 8),                  # 24 chains: 8 state slices per chain, all resident at once
-    ((65, 1, 128, 30, 64), 4, 8),          # 40 chains: 4 slices
-    ((65, 1, 128, 30, 64, 100, 7, 64, 129, 3), 16, 32),  # 320 chains: 4 slices, more CTAs than fit at once
+    ((150, 1, 64), 2, 8),                  # 24 chains: one CTA per SM, a ring of operand sets
+    ((65, 1, 128, 30, 64), 4, 8),          # 40 chains: two CTAs per SM, one set per kind
+    ((65, 1, 128, 30, 64, 100, 7, 64, 129, 3), 16, 32),  # 320 chains: more CTAs than fit at once
 ], ids=["chains24", "chains40", "chains320"])
 def test_state_pass_chain_counts(lengths, h_qk, h_v):
-    """Few and many (sequence, value head) chains (the state pass splits each
-    chain over 8 or 4 CTAs by their count), sampled chains against the oracle."""
+    """Few and many (sequence, value head) chains (the state pass runs a ring
+    of operand sets at one CTA per SM for few chains, two CTAs per SM
+    otherwise), sampled chains against the oracle."""
     cfg = synth.scaled(synth.VARLEN_32K, lengths=lengths, h_qk=h_qk, h_v=h_v, init_std=0.02, seed=21)
     inp = synth.make_prefill(cfg)
     chains = [(n, h) for n in range(cfg.N) for h in (0, 5, h_v - 1) if h < h_v]
