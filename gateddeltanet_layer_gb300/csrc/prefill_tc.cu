@@ -720,14 +720,14 @@ struct StateCfg {
   static constexpr uint32_t kSets = ST == 0 ? 1 : ST;
   static constexpr uint32_t S_NH = kSets * kStage;      // -H^T fp16 [kBV j][128 i]
   static constexpr uint32_t S_NU = S_NH + kBV * 256;    // U^T fp16 [kBV j][64 m]
-  static constexpr uint32_t S_Z = S_NU + kBV * 128;     // z [64 t][kBV] bf16 (TMA)
-  static constexpr uint32_t S_Y = S_Z + kBV * 128;      // y [64 t][kBV] bf16 (TMA store)
+  static constexpr uint32_t S_Z = S_NU + kBV * 128;     // z [2][64 t][kBV] bf16 (TMA), two chunks ahead
+  static constexpr uint32_t S_Y = S_Z + 2 * kBV * 128;  // y [64 t][kBV] bf16 (TMA store)
   static constexpr uint32_t S_WN = S_Y + kBV * 128;     // norm_w of this slice [kBV]
   static constexpr uint32_t S_PART = S_WN + kBV * 4;    // partial sums of o^2 [2][kSlices][64]
   static constexpr uint32_t S_MISC = S_PART + 2 * kSlices * 64 * 4;
   static constexpr size_t kSmem = S_MISC + 256 + 1024;
   // barriers: chain, epilogue, then the operand-set ones of the buffering scheme
-  static constexpr int B_M1 = 0, B_M2 = 1, B_Z = 2, B_ORDY = 3, B_ODONE = 5, B_PART = 7, B_SETS = 9;
+  static constexpr int B_M1 = 0, B_M2 = 1, B_Z = 2 /* [2] */, B_ORDY = 4, B_ODONE = 6, B_PART = 8, B_SETS = 10;
   static constexpr int kBars = B_SETS + (ST == 0 ? 4 : 2 * ST);
   // tensor memory: H slice (fp32, lanes i), D_U in two buffers (chunk c's
   // epilogue reads one while chunk c+1's first product writes the other)
@@ -957,15 +957,14 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
     // ======================= RMSNormGated epilogue (two warps; thread m owns token row m of the chunk)
     // buffer c & 1 of each two-buffer barrier completes for chunk c in phase (c >> 1) & 1
     const int m = tid - kMainThreads;
-    uint32_t ph_z = 0;
-    int z_pend = 0;
+    int z_issued = 0, z_done = 0;  // z loads issued / waited for (chunks [0, z_issued))
     const float scale = rsqrtf((float)kD);
-    auto issue_z = [&](int cc) {
+    auto issue_z = [&](int cc) {  // z of chunk cc into buffer cc & 1
       if (m == 0) {
-        tc::mbar_arrive_expect_tx(bar_z, 64 * kBV * 2);
-        tc::tma_load_2d(sm + S_Z, &zmap, h * kD + j0, s0 + kC * cc, bar_z);
+        tc::mbar_arrive_expect_tx(bar_z + (cc & 1), 64 * kBV * 2);
+        tc::tma_load_2d(sm + S_Z + (cc & 1) * kBV * 128, &zmap, h * kD + j0, s0 + kC * cc, bar_z + (cc & 1));
       }
-      z_pend = 1;
+      z_issued = cc + 1;
     };
     auto wait_epi = [&](uint64_t *b, uint32_t parity, bool cluster) {
       const bool ok = cluster ? tc::mbar_wait_cluster(b, parity) : tc::mbar_wait(b, parity);
@@ -975,6 +974,7 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
     // this thread's partial sum goes to slot [buf][sv][m] of every CTA of the cluster
     const uint32_t part_local = tc::smem_u32(sm + S_PART) + 4u * (uint32_t)(sv * 64 + m);
     if (nch > 0) issue_z(0);
+    if (nch > 1) issue_z(1);
     for (int c = 0; c < nch; ++c) {
       const int buf = c & 1;
       const uint32_t par = (c >> 1) & 1;
@@ -1002,16 +1002,15 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
 #pragma unroll
       for (int r = 0; r < kSlices; ++r) tot += part[r * 64 + m];
       const float inv = -scale * rsqrtf(tot * (1.0f / kD) + kEpsRms);  // o = -scale D_U
-      if (wait_epi(bar_z, ph_z & 1, false)) { failed = true; break; }
-      ++ph_z;
-      z_pend = 0;
+      if (wait_epi(bar_z + buf, par, false)) { failed = true; break; }
+      z_done = c + 1;
       tc::bulk_wait_read();  // this thread's earlier y copies have left S_Y
       tc::named_barrier(kBarEpi, kEpiThreads);
 #pragma unroll
       for (int c32 = 0; c32 < kBV; c32 += kEw) {
         float o[kEw];
         tmem_ld_cols(d_u + c32, o);
-        const uint4 *zrow = reinterpret_cast<const uint4 *>(sm + S_Z + m * kBV * 2 + c32 * 2);
+        const uint4 *zrow = reinterpret_cast<const uint4 *>(sm + S_Z + buf * kBV * 128 + m * kBV * 2 + c32 * 2);
 #pragma unroll
         for (int q = 0; q < kEw / 8; ++q) {
           const uint4 zz = zrow[q];
@@ -1034,8 +1033,8 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
       tc::fence_before_sync();
       tc::fence_async_smem();
       tc::named_barrier(kBarEpi, kEpiThreads);
-      if (m == 0) tc::mbar_arrive(bar_odone + buf);  // -O of this buffer is read; z is consumed
-      if (c + 1 < nch) issue_z(c + 1);
+      if (m == 0) tc::mbar_arrive(bar_odone + buf);  // -O of this buffer is read
+      if (c + 2 < nch) issue_z(c + 2);                // into the z buffer just consumed
       if (Lc == kC) {
         if (m == 0) {
           tc::tma_store_2d(&omap, h * kD + j0, t0, sm + S_Y);
@@ -1049,7 +1048,7 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
     tc::bulk_wait_all();
     if (failed) {
       if (m == 0) set_status(p.status, kDevTimeout);
-      if (z_pend) tc::mbar_wait(bar_z, ph_z & 1);
+      for (int cc = z_done; cc < z_issued; ++cc) tc::mbar_wait(bar_z + (cc & 1), (cc >> 1) & 1);
     }
   } else if (warp == C::kProdWarp) {
     if constexpr (ST == 0) {
