@@ -142,6 +142,13 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 __device__ __forceinline__ float silu_fast(float x) { return x * rcp_approx(1.0f + __expf(-x)); }
+// SiLU of a pair: x / (1 + e^-x), e^-x = 2^(-x log2 e) by the hardware 2^x (rel. error ~2^-22).
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float2 silu2(float2 x) {
+  const float2 t = tc::mul2(x, tc::splat2(-kLog2e));
+  const float2 d = tc::add2(make_float2(tc::ex2_approx(t.x), tc::ex2_approx(t.y)), tc::splat2(1.0f));
+  return tc::mul2(x, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
 
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t &phase) {
   const bool ok = tc::mbar_wait(bar, phase & 1);
@@ -217,26 +224,34 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p
 
 // ================================================================ chunk prep
 constexpr int kPrepThreads = 256;
-// shared memory (from a 1024-aligned base)
-constexpr uint32_t P_KQ = 0;                          // [K; Q] hi fp16 [128][128]; after K K^T and Q K^T:
-constexpr uint32_t P_VTT = P_KQ;                      //   V^T fp16 [128 j][64 m] (B operand of U')
-constexpr uint32_t P_TBS = P_KQ + 16384;              //   [T diag(beta gamma); T diag(beta)] fp16 [128][64]
-constexpr uint32_t P_KQL = 32768;                     // [K; Q] lo, later A and T fp32 [64][65]
-constexpr uint32_t P_AF = P_KQL;
-constexpr uint32_t P_TF = P_AF + 64 * kPad * 4;
-constexpr uint32_t P_VT = 66560;                      // K^T fp16 [128 i][64 m] (B operand of W)
-constexpr uint32_t P_XF = P_VT + 16384;               // inverse block products 32 x 32 fp32
+// Shared memory of the prep kernel (byte offsets; SW128 tiles 1024-aligned).
+//   [0, 64K): during the q/k phase the [K; Q] hi and lo fp16 tiles [128][128]
+//     (the operands of K K^T and Q K^T).  Once those products are done, for
+//     the two value heads of a pair: A, then T = (I + A)^-1 in place, fp32
+//     [64][kPad] at P_AT0 / P_AT1, each later overwritten by its
+//     [T diag(beta gamma); T diag(beta)] fp16 [128][64]; inverse scratch at
+//     P_XF; the second head's V^T fp16 [128 j][64 m] at P_VT1.
+//   [64K, 96K): K^T fp16 [128 i][64 m] at P_KT, the first head's V^T at P_VT0.
+//   So [K^T; V^T] (first head, from P_KT) and [V^T; K^T] (second head, from
+//   P_VT1) are each one 256-row B operand: one MMA gives both W and U'.
+constexpr uint32_t P_KQ = 0;
+constexpr uint32_t P_KQL = 32768;
+constexpr uint32_t P_AT0 = 0, P_AT1 = 17408;
+constexpr uint32_t P_XF = 34816;  // per head of the pair 4 KB
+constexpr uint32_t P_VT1 = 49152, P_KT = 65536, P_VT0 = 81920;
 constexpr int kMaxRep = kTcMaxRep;                    // value heads per q/k head
-constexpr uint32_t P_VEC = P_XF + 4096;               // per value head: G, gamma, beta, decay-to-end
+constexpr uint32_t P_VEC = 98304;                     // per value head: G, gamma, beta, decay-to-end
 constexpr uint32_t P_RED = P_VEC + kMaxRep * 1024;
 constexpr uint32_t P_MISC = P_RED + 64;
 constexpr size_t kPrepSmem = P_MISC + 64 + 1024;
-static_assert(P_TF + 64 * kPad * 4 <= P_VT, "A and T fit over the lo tile");
-static_assert(P_VT % 1024 == 0 && P_TBS % 1024 == 0, "SW128 tiles 1024-aligned");
-static_assert(2 * kPrepSmem <= 232448, "two prep CTAs per SM");
+static_assert(P_AT1 >= P_AT0 + 64 * kPad * 4 && P_XF >= P_AT1 + 64 * kPad * 4, "A / T tiles");
+static_assert(P_XF + 2 * 4096 <= P_VT1 && P_VT1 + 16384 == P_KT && P_KT + 16384 == P_VT0, "B operands");
+static_assert(P_AT1 % 1024 == 0 && P_VT1 % 1024 == 0, "SW128 tiles 1024-aligned");
+static_assert(P_VT0 + 16384 <= P_VEC, "regions");
+static_assert(2 * (kPrepSmem + 1024) <= 233472, "two prep CTAs per SM");
 
 constexpr uint32_t kIdN64 = tc::idesc_f16(128, 64);
-constexpr uint32_t kIdN128 = tc::idesc_f16(128, 128);
+constexpr uint32_t kIdN256 = tc::idesc_f16(128, 256);
 
 // Raw rows for conv(4) of 8 output rows r0 .. r0+7 of the chunk: input rows
 // r0-3 .. r0+7, 4 channels (x points at the first channel of token 0; bf16 row
@@ -251,47 +266,56 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16 *x, size_t stride,
     xr[rr] = (t >= s0 && row < Lc) ? *reinterpret_cast<const uint2 *>(x + (size_t)t * stride) : make_uint2(0u, 0u);
   }
 }
-// conv(4) + SiLU of the rows of load_rows, channels from conv_w row `ch`.
+// conv(4) + SiLU of the rows of load_rows, channels from conv_w row `ch`;
+// channels in pairs, one packed fp32 instruction per pair.
 __device__ __forceinline__ void conv_silu(const uint2 (&xr)[11], const float *conv_w, int ch, int Lc, int r0,
                                           float (&y)[8][4]) {
   float4 w[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const float4 *>(conv_w + (size_t)(ch + c) * 4);
-  auto val = [&](int rr, int c) {
-    const uint32_t w32 = (c < 2) ? xr[rr].x : xr[rr].y;
-    return __uint_as_float((c & 1) ? (w32 & 0xFFFF0000u) : (w32 << 16));
+  float2 wp[2][4];  // [channel pair][tap]
+#pragma unroll
+  for (int pr = 0; pr < 2; ++pr) {
+    wp[pr][0] = make_float2(w[2 * pr].x, w[2 * pr + 1].x);
+    wp[pr][1] = make_float2(w[2 * pr].y, w[2 * pr + 1].y);
+    wp[pr][2] = make_float2(w[2 * pr].z, w[2 * pr + 1].z);
+    wp[pr][3] = make_float2(w[2 * pr].w, w[2 * pr + 1].w);
+  }
+  auto pair = [&](int rr, int pr) {  // channels 2 pr, 2 pr + 1 of input row rr (bf16 -> fp32 exactly)
+    const uint32_t w32 = pr ? xr[rr].y : xr[rr].x;
+    return make_float2(__uint_as_float(w32 << 16), __uint_as_float(w32 & 0xFFFF0000u));
   };
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const bool ok = r0 + r < Lc;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float a = w[c].x * val(r, c);
-      a = fmaf(w[c].y, val(r + 1, c), a);
-      a = fmaf(w[c].z, val(r + 2, c), a);
-      a = fmaf(w[c].w, val(r + 3, c), a);
-      y[r][c] = ok ? silu_fast(a) : 0.0f;
+    for (int pr = 0; pr < 2; ++pr) {
+      float2 a = tc::mul2(wp[pr][0], pair(r, pr));
+      a = tc::fma2(wp[pr][1], pair(r + 1, pr), a);
+      a = tc::fma2(wp[pr][2], pair(r + 2, pr), a);
+      a = tc::fma2(wp[pr][3], pair(r + 3, pr), a);
+      const float2 sv = silu2(a);
+      y[r][2 * pr] = ok ? sv.x : 0.0f;
+      y[r][2 * pr + 1] = ok ? sv.y : 0.0f;
     }
   }
-}
-__device__ __forceinline__ void conv_rows(const __nv_bfloat16 *x, size_t stride, const float *conv_w, int ch,
-                                          int t0, int s0, int Lc, int r0, float (&y)[8][4]) {
-  uint2 xr[11];
-  load_rows(x, stride, t0, s0, Lc, r0, xr);
-  conv_silu(xr, conv_w, ch, Lc, r0, y);
 }
 
 // L2-normalise the 8 rows held by a warp (each lane holds 4 of the 128 channels).
 __device__ __forceinline__ void l2norm_rows(float (&y)[8][4], int lane) {
   float ss[8];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) ss[r] = y[r][0] * y[r][0] + y[r][1] * y[r][1] + y[r][2] * y[r][2] + y[r][3] * y[r][3];
+  for (int r = 0; r < 8; ++r) {
+    const float2 y01 = make_float2(y[r][0], y[r][1]), y23 = make_float2(y[r][2], y[r][3]);
+    const float2 s2 = tc::fma2(y23, y23, tc::mul2(y01, y01));
+    ss[r] = s2.x + s2.y;
+  }
   const float mine = reduce_scatter<8>(ss, lane);  // lane l: row l >> 2
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    const float inv = rsqrtf(__shfl_sync(0xffffffffu, mine, 4 * r) + kEpsL2);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) y[r][c] *= inv;
+    const float2 inv = tc::splat2(rsqrtf(__shfl_sync(0xffffffffu, mine, 4 * r) + kEpsL2));
+    const float2 y01 = tc::mul2(make_float2(y[r][0], y[r][1]), inv), y23 = tc::mul2(make_float2(y[r][2], y[r][3]), inv);
+    y[r][0] = y01.x; y[r][1] = y01.y; y[r][2] = y23.x; y[r][3] = y23.y;
   }
 }
 
@@ -306,13 +330,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const int lr = tid & 127, gh = tid >> 7;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   const int h_v = p.h_v, h_qk = p.h_qk, rep = h_v / h_qk;
+  // TMEM: the 256-column W / U' accumulator at column 0; K K^T and Q K^T (64
+  // columns) under it when the value heads come as one pair (their A is taken
+  // before the first W / U' product), else beside it
+  const uint32_t tmem_cols = rep <= 2 ? 256u : 512u;
+  const int COL_P1 = rep <= 2 ? 0 : 256;
 
   const int4 info = ws.chunk_info[g];
   const int t0 = info.y, s0 = info.z, Lc = info.w;
 
-  float *AF = reinterpret_cast<float *>(sm + P_AF);
-  float *TF = reinterpret_cast<float *>(sm + P_TF);
-  float *XF = reinterpret_cast<float *>(sm + P_XF);
   // per value head vv: G at sG[256 vv], gamma at +64, beta at +128, decay-to-end at +192
   float *sG = reinterpret_cast<float *>(sm + P_VEC);
   float *const sGall = sG;
@@ -328,7 +354,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const size_t qk_stride = (size_t)h_qk * kD, v_stride = (size_t)h_v * kD;
 
   if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, 256);
+    tc::tmem_alloc(tmem_slot, tmem_cols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -339,14 +365,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  constexpr int COL_P1 = 0, COL_W = 64;
   uint32_t phase = 0;
   bool failed = false;
 
-  const int r0 = 8 * warp, c0 = 4 * lane;  // prologue: this thread's rows and channels
+  const int r0 = 8 * warp, c0 = 4 * lane;  // conv: this thread's rows and channels
   auto v_slot_of = [&](int vv) { return ws.vs + ((size_t)g * h_v + hq * rep + vv) * kVSlot; };
 
-  // the first value head's v rows into L2 while the q/k rows are worked on
+  // the v rows of the first pair into L2 while the q/k rows are worked on
   auto prefetch_v = [&](int vv) {
     const int t = t0 - 3 + tid;
     if (tid < kC + 3 && t >= s0 && t < t0 + Lc)
@@ -388,7 +413,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     __syncthreads();
   }
 
-  // ---------------- q and k: conv + SiLU + L2 norm -> [K; Q] hi / lo tiles, K and Q images,
+  // ---------------- q and k: conv + SiLU + L2 norm -> [K; Q] hi / lo tiles, K^T tile, Q^ images,
   //                  and K~^T = (diag(e^(G_C - G)) K)^T images of every value head
   {
     float y[8][4], kreg[8][4];
@@ -397,6 +422,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       uint2 xrq[11];
       load_rows(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, xrq);
       load_rows(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, xrk);
+      if (rep > 1) prefetch_v(1);
       conv_silu(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
     }
     l2norm_rows(y, lane);
@@ -415,9 +441,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       uint8_t *dst = v_slot_of(vv) + kVWQ;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        const float gr = gam[r0 + r];
-        *reinterpret_cast<uint2 *>(dst + tc::sw128_offset(128, r0 + r, c0)) =
-            pack4_f16(gr * y[r][0], gr * y[r][1], gr * y[r][2], gr * y[r][3]);
+        const float2 gr = tc::splat2(gam[r0 + r]);
+        const float2 q01 = tc::mul2(gr, make_float2(y[r][0], y[r][1])), q23 = tc::mul2(gr, make_float2(y[r][2], y[r][3]));
+        *reinterpret_cast<uint2 *>(dst + tc::sw128_offset(128, r0 + r, c0)) = pack4_f16(q01.x, q01.y, q23.x, q23.y);
       }
     }
     conv_silu(xrk, p.conv_w, h_qk * kD + hq * kD + c0, Lc, r0, kreg);
@@ -433,11 +459,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       *reinterpret_cast<uint2 *>(sm + P_KQL + off) = lo;
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {  // K^T tile (B operand of W = T diag(beta gamma) K)
+    for (int c = 0; c < 4; ++c) {  // K^T tile (the K half of the B operand of W)
       float kt[8];
 #pragma unroll
       for (int r = 0; r < 8; ++r) kt[r] = kreg[r][c];
-      tc::st_chunk_f16(sm + P_VT + tc::sw128_chunk(128, c0 + c, warp), kt);
+      tc::st_chunk_f16(sm + P_KT + tc::sw128_chunk(128, c0 + c, warp), kt);
     }
     for (int vv = 0; vv < rep; ++vv) {
       const float *dec = sG + vv * 256 + 192;
@@ -445,7 +471,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       for (int c = 0; c < 4; ++c) {
         float kt[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) kt[r] = kreg[r][c] * dec[r0 + r];
+        for (int r = 0; r < 8; r += 2) {
+          const float2 k2 = tc::mul2(make_float2(kreg[r][c], kreg[r + 1][c]),
+                                     *reinterpret_cast<const float2 *>(dec + r0 + r));
+          kt[r] = k2.x;
+          kt[r + 1] = k2.y;
+        }
         st_chunk_f16_global(v_slot_of(vv) + kVKt + tc::sw128_chunk(128, c0 + c, warp), kt);
       }
     }
@@ -460,225 +491,263 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     tc::mma_commit(bar);
   }
 
-  for (int vv = 0; vv < rep && !failed; ++vv) {
-    const int h = hq * rep + vv;
-    uint8_t *v_slot = v_slot_of(vv);
+  // ---------------- the value heads, two at a time
+  for (int grp = 0; grp < rep && !failed; grp += 2) {
+    const int nh = min(2, rep - grp);
+    auto AT = [&](int hh) { return reinterpret_cast<float *>(sm + (hh ? P_AT1 : P_AT0)); };
+    auto XF = [&](int hh) { return reinterpret_cast<float *>(sm + P_XF + (hh ? 4096 : 0)); };
 
-    const float *sG = sGall + vv * 256, *sGam = sG + 64, *sBeta = sG + 128;
-    if (vv + 1 < rep) prefetch_v(vv + 1);
-
-    // ---------------- v: conv + SiLU -> V^T tile (over the [K; Q] tile, once K K^T and Q K^T are done)
+    // v: conv + SiLU -> V^T tiles; both heads' rows in flight at once
     {
+      uint2 xr[11];
       float y[8][4];
-      conv_rows(xv + h * kD + c0, v_stride, p.conv_w, 2 * h_qk * kD + h * kD + c0, t0, s0, Lc, r0, y);
-      if (vv == 0) {
-        if (wait_all(bar, phase)) { failed = true; break; }
-        // the [K; Q] lo tile under A and T is dead: zero the two 16 x 16 blocks of
-        // T above its diagonal blocks that the inverse never writes, once
-        {
-          const int blk = tid >> 7, r = (tid >> 3) & 15, c2 = 2 * (tid & 7);
-          *reinterpret_cast<float2 *>(TF + (32 * blk + r) * kPad + 32 * blk + 16 + c2) = make_float2(0.f, 0.f);
-        }
+      load_rows(xv + (size_t)(hq * rep + grp) * kD + c0, v_stride, t0, s0, Lc, r0, xr);
+      conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + grp) * kD + c0, Lc, r0, y);
+      // the second head's rows in flight over the first head's stores and the wait below
+      if (nh > 1) load_rows(xv + (size_t)(hq * rep + grp + 1) * kD + c0, v_stride, t0, s0, Lc, r0, xr);
+      if (grp + 2 < rep) {
+        prefetch_v(grp + 2);
+        if (grp + 3 < rep) prefetch_v(grp + 3);
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; ++c) {  // first head: its tile is not under the K K^T / Q K^T operands
         float col[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) col[r] = y[r][c];
-        tc::st_chunk_f16(sm + P_VTT + tc::sw128_chunk(128, c0 + c, warp), col);
+        tc::st_chunk_f16(sm + P_VT0 + tc::sw128_chunk(128, c0 + c, warp), col);
+      }
+      if (grp == 0 && wait_all(bar, phase)) { failed = true; break; }  // K K^T and Q K^T are done
+      if (nh > 1) {
+        conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + grp + 1) * kD + c0, Lc, r0, y);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float col[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) col[r] = y[r][c];
+          tc::st_chunk_f16(sm + P_VT1 + tc::sw128_chunk(128, c0 + c, warp), col);
+        }
       }
     }
 
-    // ---------------- A (fp32, strictly lower) and -A_Q (image)
-    {
+    // A (fp32, strictly lower, zero elsewhere) and -A_Q (image) of both heads
+#pragma unroll 1
+    for (int hh = 0; hh < nh; ++hh) {
+      const float *sGh = sGall + (grp + hh) * 256;
       float v[32];
       tc::tmem_ld32(tmem + lane_off + COL_P1 + 32 * gh, v);
-      float Gs[32];  // shared-memory reads before the stores below
+      float2 Gs[16];  // shared-memory reads before the stores below
 #pragma unroll
-      for (int q = 0; q < 32; ++q) Gs[q] = sG[32 * gh + q];
+      for (int q = 0; q < 16; ++q) Gs[q] = *reinterpret_cast<const float2 *>(sGh + 32 * gh + 2 * q);
+      const int r = lr & 63;
+      const float2 Gr = tc::splat2(sGh[r]);
       if (lr < 64) {
-        const int r = lr;
-        const float Gr = sG[r], br = sBeta[r];
+        const float2 br = tc::splat2(sGh[128 + r]);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int s = 32 * gh + q;
-          v[q] = (s < r) ? br * __expf(Gr - Gs[q]) * v[q] : 0.0f;
+        for (int q = 0; q < 16; ++q) {  // beta_r e^(G_r - G_s) (K K^T)_rs for s < r
+          const float2 d = tc::mul2(tc::sub2(Gr, Gs[q]), tc::splat2(kLog2e));
+          const float2 e = tc::mul2(tc::mul2(br, make_float2(tc::ex2_approx(d.x), tc::ex2_approx(d.y))),
+                                    make_float2(v[2 * q], v[2 * q + 1]));
+          const int s = 32 * gh + 2 * q;
+          v[2 * q] = (s < r) ? e.x : 0.0f;
+          v[2 * q + 1] = (s + 1 < r) ? e.y : 0.0f;
         }
+        float *row = AT(hh) + r * kPad + 32 * gh;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) AF[r * kPad + 32 * gh + q] = v[q];
+        for (int q = 0; q < 32; q += 2) *reinterpret_cast<float2 *>(row + q) = make_float2(v[q], v[q + 1]);
       } else {
-        const int r = lr - 64;
-        const float Gr = sG[r];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int s = 32 * gh + q;
-          v[q] = (s <= r) ? -__expf(Gr - Gs[q]) * v[q] : 0.0f;  // -A_Q
+        for (int q = 0; q < 16; ++q) {  // -A_Q = -e^(G_r - G_s) (Q K^T)_rs for s <= r
+          const float2 d = tc::mul2(tc::sub2(Gr, Gs[q]), tc::splat2(kLog2e));
+          const float2 e = tc::mul2(make_float2(-tc::ex2_approx(d.x), -tc::ex2_approx(d.y)),
+                                    make_float2(v[2 * q], v[2 * q + 1]));
+          const int s = 32 * gh + 2 * q;
+          v[2 * q] = (s <= r) ? e.x : 0.0f;
+          v[2 * q + 1] = (s + 1 <= r) ? e.y : 0.0f;
         }
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) st_chunk_f16_global(v_slot + kVAq + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
+        for (int cc = 0; cc < 4; ++cc)
+          st_chunk_f16_global(v_slot_of(grp + hh) + kVAq + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
       }
     }
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---------------- T = (I + A)^-1 by recursive doubling on the unit lower-triangular L = I + A
-    // (a) the four diagonal 16x16 blocks by forward substitution, one column per thread
-    if (tid < 64) {
-      const int bb = tid >> 4, s = tid & 15;
-      float x[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const float *arow = AF + (16 * bb + r) * kPad + 16 * bb;
-        float acc0 = (r == s) ? 1.0f : 0.0f, acc1 = 0.0f;
-#pragma unroll
-        for (int m = 0; m + 1 < r; m += 2) {
-          acc0 = fmaf(-arow[m], x[m], acc0);
-          acc1 = fmaf(-arow[m + 1], x[m + 1], acc1);
-        }
-        if (r & 1) acc0 = fmaf(-arow[r - 1], x[r - 1], acc0);
-        x[r] = acc0 + acc1;
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) TF[(16 * bb + r) * kPad + 16 * bb + s] = x[r];
-    }
-    __syncthreads();
-    // (b) T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22): two elements per thread
-    //     (the diagonal blocks of T hold zeros above their diagonal)
+    // T = (I + A)^-1 of both heads, in place, by recursive doubling on the unit lower-triangular I + A.
+    // (a) the four diagonal 16 x 16 blocks by forward substitution, one column per thread
     {
-      float xv2[2];
+      float x[16];
+      const int hh = tid >> 6, bb = (tid >> 4) & 3, s = tid & 15;
+      const bool act = hh < nh;
+      if (act) {
 #pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int e = tid + kPrepThreads * it;
-        const int blk = e >> 8, r = (e >> 4) & 15, s = e & 15, o = 32 * blk;
-        const float *arow = AF + (o + 16 + r) * kPad + o;
-        float acc0 = 0.0f, acc1 = 0.0f;
+        for (int r = 0; r < 16; ++r) {
+          const float *arow = AT(hh) + (16 * bb + r) * kPad + 16 * bb;
+          float acc0 = (r == s) ? 1.0f : 0.0f, acc1 = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          acc0 = fmaf(arow[k], TF[(o + k) * kPad + o + s], acc0);
-          acc1 = fmaf(arow[k + 1], TF[(o + k + 1) * kPad + o + s], acc1);
+          for (int m = 0; m + 1 < r; m += 2) {
+            acc0 = fmaf(-arow[m], x[m], acc0);
+            acc1 = fmaf(-arow[m + 1], x[m + 1], acc1);
+          }
+          if (r & 1) acc0 = fmaf(-arow[r - 1], x[r - 1], acc0);
+          x[r] = acc0 + acc1;
         }
-        xv2[it] = acc0 + acc1;
       }
+      __syncthreads();  // every column is solved before the blocks are overwritten
+      if (act) {
 #pragma unroll
-      for (int it = 0; it < 2; ++it) XF[tid + kPrepThreads * it] = xv2[it];
-      __syncthreads();
-#pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int e = tid + kPrepThreads * it;
-        const int blk = e >> 8, r = (e >> 4) & 15, s = e & 15, o = 32 * blk;
-        const float *trow = TF + (o + 16 + r) * kPad + o + 16;
-        float acc0 = 0.0f, acc1 = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          acc0 = fmaf(trow[k], XF[blk * 256 + k * 16 + s], acc0);
-          acc1 = fmaf(trow[k + 1], XF[blk * 256 + (k + 1) * 16 + s], acc1);
-        }
-        TF[(o + 16 + r) * kPad + o + s] = -(acc0 + acc1);
+        for (int r = 0; r < 16; ++r) AT(hh)[(16 * bb + r) * kPad + 16 * bb + s] = x[r];
       }
     }
     __syncthreads();
-    // (c) the lower-left 32x32 block T_21 = -T_2 (A_21 T_1), a 2 x 2 tile per thread
+    // (b) T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22): two elements per thread and head
+    //     (the diagonal blocks of T hold zeros above their diagonal)
+#pragma unroll 1
+    for (int hh = 0; hh < nh; ++hh) {
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int e = tid + kPrepThreads * it;
+        const int blk = e >> 8, r = (e >> 4) & 15, s = e & 15, o = 32 * blk;
+        const float *arow = AT(hh) + (o + 16 + r) * kPad + o;
+        const float *tcol = AT(hh) + o * kPad + o + s;
+        float2 acc = make_float2(0.0f, 0.0f);  // even and odd k
+#pragma unroll
+        for (int k = 0; k < 16; k += 2)
+          acc = tc::fma2(*reinterpret_cast<const float2 *>(arow + k), make_float2(tcol[k * kPad], tcol[(k + 1) * kPad]),
+                         acc);
+        XF(hh)[e] = acc.x + acc.y;
+      }
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int hh = 0; hh < nh; ++hh) {
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int e = tid + kPrepThreads * it;
+        const int blk = e >> 8, r = (e >> 4) & 15, s = e & 15, o = 32 * blk;
+        const float *trow = AT(hh) + (o + 16 + r) * kPad + o + 16;
+        const float *xf = XF(hh) + blk * 256 + s;
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < 16; k += 2)
+          acc = tc::fma2(*reinterpret_cast<const float2 *>(trow + k), make_float2(xf[k * 16], xf[(k + 1) * 16]), acc);
+        AT(hh)[(o + 16 + r) * kPad + o + s] = -(acc.x + acc.y);  // over A_10 / A_32, read above
+      }
+    }
+    __syncthreads();
+    // (c) the lower-left 32 x 32 block T_21 = -T_2 (A_21 T_1), a 2 x 2 tile per thread and head
     //     (T_1 and T_2 are whole lower-triangular blocks: zeros above the diagonal)
     {
       const int rr = 2 * (tid >> 4), ss = 2 * (tid & 15);
-      const float *a0 = AF + (32 + rr) * kPad, *a1 = a0 + kPad;
-      float y00 = 0.0f, y01 = 0.0f, y10 = 0.0f, y11 = 0.0f;
+#pragma unroll 1
+      for (int hh = 0; hh < nh; ++hh) {
+        const float *a0 = AT(hh) + (32 + rr) * kPad, *a1 = a0 + kPad;
+        float2 y0 = make_float2(0.0f, 0.0f), y1 = make_float2(0.0f, 0.0f);  // rows rr, rr + 1
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float2 t = *reinterpret_cast<const float2 *>(TF + k * kPad + ss);
-        const float av = a0[k], bv = a1[k];
-        y00 = fmaf(av, t.x, y00);
-        y01 = fmaf(av, t.y, y01);
-        y10 = fmaf(bv, t.x, y10);
-        y11 = fmaf(bv, t.y, y11);
+        for (int k = 0; k < 32; ++k) {
+          const float2 t = *reinterpret_cast<const float2 *>(AT(hh) + k * kPad + ss);
+          y0 = tc::fma2(tc::splat2(a0[k]), t, y0);
+          y1 = tc::fma2(tc::splat2(a1[k]), t, y1);
+        }
+        *reinterpret_cast<float2 *>(XF(hh) + rr * 32 + ss) = y0;
+        *reinterpret_cast<float2 *>(XF(hh) + (rr + 1) * 32 + ss) = y1;
       }
-      *reinterpret_cast<float2 *>(XF + rr * 32 + ss) = make_float2(y00, y01);
-      *reinterpret_cast<float2 *>(XF + (rr + 1) * 32 + ss) = make_float2(y10, y11);
       __syncthreads();
-      const float *t0r = TF + (32 + rr) * kPad + 32, *t1r = t0r + kPad;
-      float z00 = 0.0f, z01 = 0.0f, z10 = 0.0f, z11 = 0.0f;
+#pragma unroll 1
+      for (int hh = 0; hh < nh; ++hh) {
+        const float *t0r = AT(hh) + (32 + rr) * kPad + 32, *t1r = t0r + kPad;
+        float2 z0 = make_float2(0.0f, 0.0f), z1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float2 yk = *reinterpret_cast<const float2 *>(XF + k * 32 + ss);
-        const float p0 = t0r[k], p1 = t1r[k];
-        z00 = fmaf(p0, yk.x, z00);
-        z01 = fmaf(p0, yk.y, z01);
-        z10 = fmaf(p1, yk.x, z10);
-        z11 = fmaf(p1, yk.y, z11);
+        for (int k = 0; k < 32; ++k) {
+          const float2 yk = *reinterpret_cast<const float2 *>(XF(hh) + k * 32 + ss);
+          z0 = tc::fma2(tc::splat2(t0r[k]), yk, z0);
+          z1 = tc::fma2(tc::splat2(t1r[k]), yk, z1);
+        }
+        *reinterpret_cast<float2 *>(AT(hh) + (32 + rr) * kPad + ss) = make_float2(-z0.x, -z0.y);
+        *reinterpret_cast<float2 *>(AT(hh) + (33 + rr) * kPad + ss) = make_float2(-z1.x, -z1.y);
       }
-      *reinterpret_cast<float2 *>(TF + (32 + rr) * kPad + ss) = make_float2(-z00, -z01);
-      *reinterpret_cast<float2 *>(TF + (33 + rr) * kPad + ss) = make_float2(-z10, -z11);
     }
-    __syncthreads();
-    // [T diag(beta gamma); T diag(beta)] (one 128-row shared-memory operand)
-    {
+    // [T diag(beta gamma); T diag(beta)] of each head over its own T (read first)
+#pragma unroll 1
+    for (int hh = 0; hh < nh; ++hh) {
       const int r = tid & 63, oq = tid >> 6;  // columns [16 oq, 16 oq + 16)
-      float a16[16], b16[16];
+      const float *sGh = sGall + (grp + hh) * 256;
+      uint32_t pa[8], pb[8];  // fp16 pairs
+      __syncthreads();  // T complete (first head) / the previous head's stores done
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {  // shared-memory reads before the stores below
-        const int m = 16 * oq + e;
-        const float t = (m <= r) ? TF[r * kPad + m] : 0.0f;
-        b16[e] = t * sBeta[m];
-        a16[e] = b16[e] * sGam[m];
+      for (int e = 0; e < 16; e += 2) {
+        float b2[2], a2[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int m = 16 * oq + e + i;
+          const float t = (m <= r) ? AT(hh)[r * kPad + m] : 0.0f;
+          b2[i] = t * sGh[128 + m];
+          a2[i] = b2[i] * sGh[64 + m];
+        }
+        pa[e >> 1] = tc::pack_f16x2(a2[0], a2[1]);
+        pb[e >> 1] = tc::pack_f16x2(b2[0], b2[1]);
       }
+      __syncthreads();
+      uint8_t *tbs = reinterpret_cast<uint8_t *>(AT(hh));
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        tc::st_chunk_f16(sm + P_TBS + tc::sw128_chunk(128, r, 2 * oq + hh), a16 + 8 * hh);
-        tc::st_chunk_f16(sm + P_TBS + tc::sw128_chunk(128, 64 + r, 2 * oq + hh), b16 + 8 * hh);
+      for (int half = 0; half < 2; ++half) {
+        const int q = 4 * half;
+        *reinterpret_cast<uint4 *>(tbs + tc::sw128_chunk(128, r, 2 * oq + half)) =
+            make_uint4(pa[q], pa[q + 1], pa[q + 2], pa[q + 3]);
+        *reinterpret_cast<uint4 *>(tbs + tc::sw128_chunk(128, 64 + r, 2 * oq + half)) =
+            make_uint4(pb[q], pb[q + 1], pb[q + 2], pb[q + 3]);
       }
     }
     publish_operands();
 
-    // ---------------- W = T diag(beta gamma) K -> rows 64-127 of the [Q^; W] image
-    //                  (rows 0-63 of [T diag(beta gamma); T diag(beta)] K^T^T)
-    if (tid == 0) {
-      mma_chain(tmem + COL_W, sbase + P_TBS, 128, 0, sbase + P_VT, 128, 0, 4, kIdN128, false);
-      tc::mma_commit(bar);
-    }
-    if (wait_all(bar, phase)) { failed = true; break; }
-    if ((warp & 3) < 2) {  // TMEM lanes 0-63
-      const int r = 32 * (warp & 3) + lane, hh = warp >> 2;  // columns [64 hh, 64 hh + 64)
-#pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
-        float w[32];
-        tc::tmem_ld32(tmem + lane_off + COL_W + 64 * hh + 32 * c32, w);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          st_chunk_f16_global(v_slot + kVWQ + tc::sw128_offset(128, 64 + r, 64 * hh + 32 * c32 + 8 * cc), w + 8 * cc);
+    // ---------------- per head: [T diag(beta gamma); T diag(beta)] times the 256-row B operand
+    //   first head:  B = [K^T; V^T]: W = T diag(beta gamma) K in rows 0-63, columns 0-127,
+    //                U' = T diag(beta) V in rows 64-127, columns 128-255
+    //   second head: B = [V^T; K^T]: the same with the column halves swapped
+#pragma unroll 1
+    for (int hh = 0; hh < nh; ++hh) {
+      if (tid == 0) {
+        mma_chain(tmem, sbase + (hh ? P_AT1 : P_AT0), 128, 0, sbase + (hh ? P_VT1 : P_KT), 256, 0, 4, kIdN256,
+                  false);
+        tc::mma_commit(bar);
       }
-    }
-    tc::fence_before_sync();
-    __syncthreads();  // W is read: the accumulator takes U'
-    tc::fence_after_sync();
-
-    // ---------------- U' = T diag(beta) V -> image (rows 64-127 of [T diag(beta gamma); T diag(beta)] V)
-    if (tid == 0) {
-      mma_chain(tmem + COL_W, sbase + P_TBS, 128, 0, sbase + P_VTT, 128, 0, 4, kIdN128, false);
-      tc::mma_commit(bar);
-    }
-    if (wait_all(bar, phase)) { failed = true; break; }
-    if ((warp & 3) >= 2) {  // TMEM lanes 64-127
-      const int m = 32 * (warp & 3) - 64 + lane, hh = warp >> 2;  // columns [64 hh, 64 hh + 64)
+      if (wait_all(bar, phase)) { failed = true; break; }
+      uint8_t *v_slot = v_slot_of(grp + hh);
+      const int wcol = hh ? 128 : 0, half = warp >> 2;  // this warp's 64 columns of W or U'
+      if ((warp & 3) < 2) {  // TMEM lanes 0-63: W -> rows 64-127 of the [Q^; W] image
+        const int r = 32 * (warp & 3) + lane;
 #pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
-        float u[32];
-        tc::tmem_ld32(tmem + lane_off + COL_W + 64 * hh + 32 * c32, u);
+        for (int c32 = 0; c32 < 2; ++c32) {
+          float w[32];
+          tc::tmem_ld32(tmem + lane_off + wcol + 64 * half + 32 * c32, w);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int j = 64 * hh + 32 * c32 + 8 * cc;  // state column of this 16-byte chunk
-          const int lb = ws.up_bv_log2;
-          st_chunk_f16_global(v_slot + kVUp + ((size_t)(j >> lb) * 64 + m) * (2u << lb) + (j & ((1 << lb) - 1)) * 2,
-                              u + 8 * cc);
+          for (int cc = 0; cc < 4; ++cc)
+            st_chunk_f16_global(v_slot + kVWQ + tc::sw128_offset(128, 64 + r, 64 * half + 32 * c32 + 8 * cc),
+                                w + 8 * cc);
+        }
+      } else {  // TMEM lanes 64-127: U' -> its image
+        const int m = 32 * (warp & 3) - 64 + lane;
+        const int lb = ws.up_bv_log2;
+#pragma unroll
+        for (int c32 = 0; c32 < 2; ++c32) {
+          float u[32];
+          tc::tmem_ld32(tmem + lane_off + (128 - wcol) + 64 * half + 32 * c32, u);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int j = 64 * half + 32 * c32 + 8 * cc;  // state column of this 16-byte chunk
+            st_chunk_f16_global(v_slot + kVUp + ((size_t)(j >> lb) * 64 + m) * (2u << lb) + (j & ((1 << lb) - 1)) * 2,
+                                u + 8 * cc);
+          }
         }
       }
+      tc::fence_before_sync();
+      __syncthreads();  // the accumulator is read: the next product may overwrite it
+      tc::fence_after_sync();
     }
-    tc::fence_before_sync();
-    __syncthreads();  // A, T, V^T and the accumulator are reused by the next value head
   }
   if (failed && tid == 0) set_status(p.status, kDevTimeout);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
 }
 
 // ================================================================ state pass

@@ -401,6 +401,39 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs
+// Two fp32 lanes per instruction ({fma,mul,add,sub}.rn.f32x2, sm_100 family);
+// each lane is rounded exactly as by the scalar .rn instruction.
+#define GDN_F32X2_OP(name, op)                                                                        \
+  __device__ __forceinline__ float2 name(float2 a, float2 b) {                                       \
+    float2 d;                                                                                        \
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t" op \
+        " rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"                                              \
+        : "=f"(d.x), "=f"(d.y)                                                                       \
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                                   \
+    return d;                                                                                        \
+  }
+GDN_F32X2_OP(mul2, "mul.rn.f32x2")
+GDN_F32X2_OP(add2, "add.rn.f32x2")
+GDN_F32X2_OP(sub2, "sub.rn.f32x2")
+#undef GDN_F32X2_OP
+// a * b + c per lane, one rounding.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+// 2^x by the hardware approximation (ex2.approx.ftz.f32; relative error ~2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------ packing helpers
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);

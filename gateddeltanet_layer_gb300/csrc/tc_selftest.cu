@@ -28,12 +28,12 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const uint16_t *__re
   for (int c = 0; c < K / 8; ++c) {
     *reinterpret_cast<uint4 *>(sA + tc::sw128_chunk(128, tid, c)) =
         *reinterpret_cast<const uint4 *>(A + (size_t)tid * K + 8 * c);
-    if (tid < BR)
-      *reinterpret_cast<uint4 *>(sB + tc::sw128_chunk(BR, tid, c)) =
-          *reinterpret_cast<const uint4 *>(B + (size_t)tid * K + 8 * c);
+    for (int row = tid; row < BR; row += 128)
+      *reinterpret_cast<uint4 *>(sB + tc::sw128_chunk(BR, row, c)) =
+          *reinterpret_cast<const uint4 *>(B + (size_t)row * K + 8 * c);
   }
   if (warp == 0) {
-    tc::tmem_alloc(&tmem_base_s, 128);
+    tc::tmem_alloc(&tmem_base_s, 256);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const uint16_t *__re
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
 // A wait that runs out: the mbarrier expects one arrival that never comes.
@@ -102,8 +102,8 @@ extern "C" int gdn_selftest_wait_timeout(int *flag, int limit_us, void *stream) 
 extern "C" int gdn_selftest_umma(const void *A, const void *B, float *D, int *flag, int N, int K, int b_row0,
                                  int fp16, void *stream) {
   if (!A || !B || !D || !flag) return GDN_ERR_INVALID_ARG;
-  if ((N != 32 && N != 64 && N != 128) || (K != 64 && K != 128) || (b_row0 != 0 && b_row0 != 64) ||
-      b_row0 + N > 128)
+  if ((N != 32 && N != 64 && N != 128 && N != 256) || (K != 64 && K != 128) || (b_row0 != 0 && b_row0 != 64) ||
+      b_row0 + N > 256)
     return GDN_ERR_INVALID_ARG;
   const size_t smem = 1024 + (size_t)128 * K * 2 + (size_t)(b_row0 + N) * K * 2;
   auto kern = gdn::umma_selftest_kernel;

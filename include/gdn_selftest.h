@@ -24,7 +24,7 @@ extern "C" {
  *       memory; D[1] = the same after a tensor-memory round trip that doubles
  *       it (tcgen05.ld, x2, tcgen05.st, tcgen05.ld)
  * flag  int32 (device): set to GDN_ERR_TIMEOUT if the MMA completion wait ran out
- * Supported: N in {32, 64, 128}, K in {64, 128}, b_row0 in {0, 64}, b_row0 + N <= 128.
+ * Supported: N in {32, 64, 128, 256}, K in {64, 128}, b_row0 in {0, 64}, b_row0 + N <= 256.
  * Returns GDN_OK, GDN_ERR_INVALID_ARG or GDN_ERR_CUDA.
  */
 GDN_API int gdn_selftest_umma(const void *A, const void *B, float *D, int *flag, int N, int K, int b_row0,

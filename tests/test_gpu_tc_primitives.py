@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("fp16", [0, 1], ids=["bf16", "fp16"])
 @pytest.mark.parametrize("N,K,b_row0", [(64, 64, 0), (64, 128, 0), (128, 128, 0), (128, 64, 0), (64, 128, 64),
-                                        (32, 64, 0), (32, 128, 0)])
+                                        (32, 64, 0), (32, 128, 0), (256, 64, 0), (256, 128, 0), (128, 64, 64)])
 def test_umma_gemm(N, K, b_row0, fp16):
     import gateddeltanet_layer_gb300 as gdn
     lib = gdn.library()
