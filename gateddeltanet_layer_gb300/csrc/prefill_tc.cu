@@ -133,16 +133,15 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
   return v[0];
 }
 
-// SiLU x sigmoid(x) from the fast exponential and the hardware reciprocal
-// (rcp.approx: a few ulp of fp32, far below the fp16 rounding of the result;
-// 1 / inf = 0 gives the right limit for very negative x).
+// The hardware reciprocal (rcp.approx: a few ulp of fp32, far below the fp16
+// rounding of the results it feeds; 1 / inf = 0).
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float silu_fast(float x) { return x * rcp_approx(1.0f + __expf(-x)); }
-// SiLU of a pair: x / (1 + e^-x), e^-x = 2^(-x log2 e) by the hardware 2^x (rel. error ~2^-22).
+// SiLU of a pair: x / (1 + e^-x), e^-x = 2^(-x log2 e) by the hardware 2^x
+// (rel. error ~2^-22); 1 / inf = 0 gives the right limit for very negative x.
 constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ float2 silu2(float2 x) {
   const float2 t = tc::mul2(x, tc::splat2(-kLog2e));
@@ -634,36 +633,55 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       }
     }
     __syncthreads();
-    // (c) the lower-left 32 x 32 block T_21 = -T_2 (A_21 T_1), a 2 x 2 tile per thread and head
-    //     (T_1 and T_2 are whole lower-triangular blocks: zeros above the diagonal)
+    // (c) the lower-left 32 x 32 block T_21 = -T_2 (A_21 T_1); threads 128 hh .. 128 hh + 127 take
+    //     head hh, a 2 x 4 tile each (T_1 and T_2 are whole lower-triangular blocks: zeros above the diagonal)
     {
-      const int rr = 2 * (tid >> 4), ss = 2 * (tid & 15);
-#pragma unroll 1
-      for (int hh = 0; hh < nh; ++hh) {
-        const float *a0 = AT(hh) + (32 + rr) * kPad, *a1 = a0 + kPad;
-        float2 y0 = make_float2(0.0f, 0.0f), y1 = make_float2(0.0f, 0.0f);  // rows rr, rr + 1
+      const int hh = tid >> 7, t = tid & 127, rr = 2 * (t >> 3), cc = 4 * (t & 7);
+      const bool act = hh < nh;
+      if (act) {
+        const float *At = AT(hh);
+        const float *a0 = At + (32 + rr) * kPad, *a1 = a0 + kPad;
+        float2 y0a = make_float2(0.0f, 0.0f), y0b = y0a, y1a = y0a, y1b = y0a;  // rows rr, rr + 1
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float2 t = *reinterpret_cast<const float2 *>(AT(hh) + k * kPad + ss);
-          y0 = tc::fma2(tc::splat2(a0[k]), t, y0);
-          y1 = tc::fma2(tc::splat2(a1[k]), t, y1);
+        for (int k = 0; k < 32; k += 2) {
+          const float2 av = *reinterpret_cast<const float2 *>(a0 + k), bv = *reinterpret_cast<const float2 *>(a1 + k);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const float *trow = At + (k + kk) * kPad + cc;
+            const float2 t01 = *reinterpret_cast<const float2 *>(trow), t23 = *reinterpret_cast<const float2 *>(trow + 2);
+            const float2 x = tc::splat2(kk ? av.y : av.x), z = tc::splat2(kk ? bv.y : bv.x);
+            y0a = tc::fma2(x, t01, y0a);
+            y0b = tc::fma2(x, t23, y0b);
+            y1a = tc::fma2(z, t01, y1a);
+            y1b = tc::fma2(z, t23, y1b);
+          }
         }
-        *reinterpret_cast<float2 *>(XF(hh) + rr * 32 + ss) = y0;
-        *reinterpret_cast<float2 *>(XF(hh) + (rr + 1) * 32 + ss) = y1;
+        *reinterpret_cast<float4 *>(XF(hh) + rr * 32 + cc) = make_float4(y0a.x, y0a.y, y0b.x, y0b.y);
+        *reinterpret_cast<float4 *>(XF(hh) + (rr + 1) * 32 + cc) = make_float4(y1a.x, y1a.y, y1b.x, y1b.y);
       }
       __syncthreads();
-#pragma unroll 1
-      for (int hh = 0; hh < nh; ++hh) {
-        const float *t0r = AT(hh) + (32 + rr) * kPad + 32, *t1r = t0r + kPad;
-        float2 z0 = make_float2(0.0f, 0.0f), z1 = make_float2(0.0f, 0.0f);
+      if (act) {
+        float *At = AT(hh);
+        const float *t0r = At + (32 + rr) * kPad + 32, *t1r = t0r + kPad;
+        float2 z0a = make_float2(0.0f, 0.0f), z0b = z0a, z1a = z0a, z1b = z0a;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float2 yk = *reinterpret_cast<const float2 *>(XF(hh) + k * 32 + ss);
-          z0 = tc::fma2(tc::splat2(t0r[k]), yk, z0);
-          z1 = tc::fma2(tc::splat2(t1r[k]), yk, z1);
+        for (int k = 0; k < 32; k += 2) {
+          const float2 pv = *reinterpret_cast<const float2 *>(t0r + k), qv = *reinterpret_cast<const float2 *>(t1r + k);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const float4 yk = *reinterpret_cast<const float4 *>(XF(hh) + (k + kk) * 32 + cc);
+            const float2 x = tc::splat2(kk ? pv.y : pv.x), z = tc::splat2(kk ? qv.y : qv.x);
+            z0a = tc::fma2(x, make_float2(yk.x, yk.y), z0a);
+            z0b = tc::fma2(x, make_float2(yk.z, yk.w), z0b);
+            z1a = tc::fma2(z, make_float2(yk.x, yk.y), z1a);
+            z1b = tc::fma2(z, make_float2(yk.z, yk.w), z1b);
+          }
         }
-        *reinterpret_cast<float2 *>(AT(hh) + (32 + rr) * kPad + ss) = make_float2(-z0.x, -z0.y);
-        *reinterpret_cast<float2 *>(AT(hh) + (33 + rr) * kPad + ss) = make_float2(-z1.x, -z1.y);
+        float *o0 = At + (32 + rr) * kPad + cc, *o1 = o0 + kPad;
+        *reinterpret_cast<float2 *>(o0) = make_float2(-z0a.x, -z0a.y);
+        *reinterpret_cast<float2 *>(o0 + 2) = make_float2(-z0b.x, -z0b.y);
+        *reinterpret_cast<float2 *>(o1) = make_float2(-z1a.x, -z1a.y);
+        *reinterpret_cast<float2 *>(o1 + 2) = make_float2(-z1b.x, -z1b.y);
       }
     }
     // [T diag(beta gamma); T diag(beta)] of each head over its own T (read first)
