@@ -140,7 +140,9 @@ def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False, trace=False):
     between steps) of one gdn_prefill call; optionally the end-to-end time with
     pinned-host inputs copied in and outputs copied out every step, and the
     library's per-kernel trace (CUDA events around each of its launches, on the
-    same stream) over the timed steps."""
+    same stream) over as many steps again, run right after the timed ones: the
+    trace's events between launches hold back the early start of the next
+    kernel (programmatic dependent launch), so they stay out of the timed steps."""
     import torch
 
     import gateddeltanet_layer_gb300 as gdn
@@ -163,20 +165,23 @@ def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False, trace=False):
         call()
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    if trace:
-        gdn.trace_enable(True)
-        gdn.trace_read()
     for s, e in ev:
         flush.zero_()
         s.record(stream)
         call()
         e.record(stream)
     torch.cuda.synchronize(dev)
+    ms = [s.elapsed_time(e) for s, e in ev]
     kernels = None
     if trace:
+        gdn.trace_enable(True)
+        gdn.trace_read()
+        for _ in range(steps):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize(dev)
         kernels = gdn.trace_read()
         gdn.trace_enable(False)
-    ms = [s.elapsed_time(e) for s, e in ev]
     status = gdn.workspace_status(ws, stream)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed prefill")

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p
   __shared__ int scan[1024];
   __shared__ int bad;
   const int N = p.N, tid = threadIdx.x;
+  tc::launch_dependents();  // the prep CTAs may take their places; they wait for this table
   if (tid == 0) bad = 0;
   const int per = (N + 1023) / 1024;
   const int n0 = min(N, tid * per), n1 = min(N, n0 + per);
@@ -320,6 +321,8 @@ __device__ __forceinline__ void l2norm_rows(float (&y)[8][4], int lane) {
 
 __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const PrefillParams p, const Ws ws) {
   const int g = blockIdx.x, hq = blockIdx.y;
+  tc::grid_dependency_wait();  // the chunk table
+  tc::launch_dependents();     // the state pass may be scheduled once every prep CTA has started
   const int total = ws.chunk_base[p.N];
   if (g >= total) return;
   extern __shared__ uint8_t smem_raw[];
@@ -875,10 +878,6 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
   const int j0 = kBV * sv;  // first state column of this CTA
 
   const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
-  bool valid = s0 >= 0 && s1 >= s0 && s1 <= p.T;  // else reported by the chunk table
-  const int g0 = valid ? ws.chunk_base[n] : 0, g1 = valid ? ws.chunk_base[n + 1] : 0;
-  if (valid && g1 - g0 != (s1 - s0 + kC - 1) / kC) valid = false;  // table overflow, reported
-  const int nch = valid ? g1 - g0 : 0;
 
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_MISC);
   uint64_t *bar_m1 = bar + C::B_M1, *bar_m2 = bar + C::B_M2, *bar_z = bar + C::B_Z;
@@ -908,6 +907,12 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
+
+  tc::grid_dependency_wait();  // the chunk table and the operand images
+  bool valid = s0 >= 0 && s1 >= s0 && s1 <= p.T;  // else reported by the chunk table
+  const int g0 = valid ? ws.chunk_base[n] : 0, g1 = valid ? ws.chunk_base[n + 1] : 0;
+  if (valid && g1 - g0 != (s1 - s0 + kC - 1) / kC) valid = false;  // table overflow, reported
+  const int nch = valid ? g1 - g0 : 0;
   auto slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
 
   if (warp < C::kMainWarps) {
@@ -1290,13 +1295,17 @@ cudaError_t launch_state(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = NS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // many chains: the prologue runs beside the prep's last CTAs.  Few chains (one
+  // CTA per SM): clusters placed while the prep still holds SMs ran slower.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = ST == 0 ? 2 : 1;
   trace_begin(s, GDN_K_STATE);
   e = cudaLaunchKernelEx(&cfg, kern, p, ws, zmap, omap);
   trace_end(s);
@@ -1324,10 +1333,19 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   if (p.T > 0) {
     e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)L.max_chunks, (unsigned)p.h_qk);
+    cfg.blockDim = dim3(kPrepThreads);
+    cfg.dynamicSmemBytes = kPrepSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // launched while the table runs
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     trace_begin(s, GDN_K_CHUNK_PREP);
-    chunk_prep_kernel<<<dim3((unsigned)L.max_chunks, (unsigned)p.h_qk), kPrepThreads, kPrepSmem, s>>>(p, ws);
+    e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel, p, ws);
     trace_end(s);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return state_ring(p) ? launch_state<kStateSlices, 3>(p, ws, s) : launch_state<kStateSlices, 0>(p, ws, s);
