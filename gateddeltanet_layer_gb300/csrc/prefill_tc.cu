@@ -964,6 +964,15 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
       uint32_t par = (uint32_t)(c / (ST == 0 ? 1 : ST)) & 1;
       return wait_main(bar_full + c % (ST == 0 ? 1 : ST), par);
     };
+    // the same wait, this thread only (the caller joins the chain's barrier)
+    auto set_arrived = [&](int c) -> bool {
+      if constexpr (ST == 0) {
+        const bool ok = tc::mbar_wait(bar_s1, ph_s1 & 1);
+        ++ph_s1;
+        return ok;
+      }
+      return tc::mbar_wait(bar_full + c % (ST == 0 ? 1 : ST), (uint32_t)(c / (ST == 0 ? 1 : ST)) & 1);
+    };
     if (nch > 0) {
       if (wait_set(0)) failed = true;
       else copy_and_scale(gamma_c(0));
@@ -972,11 +981,7 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
 
     for (int c = 0; c < nch && !failed; ++c) {
       const int buf = c & 1;
-      const uint32_t d_u = tmem + COL_U + kBV * buf;
-      if (c >= 2) {  // the epilogue has read chunk c-2's -O from this buffer
-        uint32_t par = ((c - 2) >> 1) & 1;
-        if (wait_main(bar_odone + buf, par)) { failed = true; break; }
-      }
+      const uint32_t d_u = tmem + COL_U + kBV * buf;  // chunk c-2's -O read from it: waited below
 
       const uint32_t set = set_of(c);  // this chunk's operand set
       // ---------------- MMA 1: D_U = [Q^; W] (-H)
@@ -1028,12 +1033,23 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
         else tc::mma_commit(bar_empty + c % (ST == 0 ? 1 : ST));
         tc::mma_commit(bar_oready + buf);
       }
-      if (wait_main(bar_m2, ph_m2)) { failed = true; break; }
-      if (c + 1 < nch) {
-        if (wait_set(c + 1)) { failed = true; break; }
-        copy_and_scale(gamma_c(c + 1));
+      {  // MMA 2 done and chunk c+1's operand set in: one barrier for both
+        bool ok = tc::mbar_wait(bar_m2, ph_m2 & 1);
+        ++ph_m2;
+        if (c + 1 < nch) ok = set_arrived(c + 1) && ok;
+        tc::fence_after_sync();
+        if (tc::named_barrier_or(kBarMain, kMainThreads, !ok)) { failed = true; break; }
       }
-      publish_main();
+      if (c + 1 < nch) copy_and_scale(gamma_c(c + 1));
+      {  // publish chunk c+1's -H^T; the epilogue has read chunk c-1's -O (chunk c+1 reuses its buffer)
+        bool ok = true;
+        if (c >= 1 && c + 1 < nch) ok = tc::mbar_wait(bar_odone + ((c + 1) & 1), ((c - 1) >> 1) & 1);
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        const bool bad = tc::named_barrier_or(kBarMain, kMainThreads, !ok);
+        tc::fence_after_sync();
+        if (bad) { failed = true; break; }
+      }
     }
 
     if (failed) {
