@@ -818,7 +818,9 @@ struct StateCfg {
   static constexpr size_t kSmem = S_MISC + 256 + 1024;
   // barriers: chain, epilogue, then the operand-set ones of the buffering scheme
   static constexpr int B_M1 = 0, B_M2 = 1, B_Z = 2 /* [2] */, B_ORDY = 4, B_ODONE = 6, B_PART = 8, B_SETS = 10;
-  static constexpr int kBars = B_SETS + (ST == 0 ? 4 : 2 * ST);
+  // ST >= 2: after full[ST] and empty[ST], "U published" (chain -> copy warp) and "-A_Q U done"
+  static constexpr int B_UPUB = B_SETS + 2 * ST, B_AQ = B_UPUB + 1;
+  static constexpr int kBars = B_SETS + (ST == 0 ? 4 : 2 * ST + 2);
   // tensor memory: H slice (fp32, lanes i), D_U in two buffers (chunk c's
   // epilogue reads one while chunk c+1's first product writes the other)
   static constexpr int COL_H = 0, COL_U = kBV;
@@ -887,6 +889,7 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
   uint64_t *bar_s1 = bar + C::B_SETS, *bar_s2 = bar + C::B_SETS + 1, *bar_m2b = bar + C::B_SETS + 2;
   uint64_t *bar_udone = bar + C::B_SETS + 3;
   uint64_t *bar_full = bar + C::B_SETS, *bar_empty = bar + C::B_SETS + (ST == 0 ? 0 : ST);
+  uint64_t *bar_upub = bar + (ST == 0 ? 0 : C::B_UPUB), *bar_aq = bar + (ST == 0 ? 0 : C::B_AQ);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_MISC + 8 * C::kBars);
   float *sWn = reinterpret_cast<float *>(sm + S_WN);
   __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
@@ -896,7 +899,8 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < C::kBars; ++i) tc::mbar_init(bar + i, (ST != 0 && i >= C::B_SETS + ST) ? 2 : 1);
+    for (int i = 0; i < C::kBars; ++i)
+      tc::mbar_init(bar + i, (ST != 0 && i >= C::B_SETS + ST && i < C::B_SETS + 2 * ST) ? 2 : 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&zmap);
     tc::prefetch_tmap(&omap);
@@ -991,7 +995,14 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
                     kIdNBV, k > 0 ? 1u : 0u);
         tc::mma_commit(bar_m1);
       }
-      if (wait_main(bar_m1, ph_m1)) { failed = true; break; }
+      {  // MMA 1 done; ring form: the previous chunk's -A_Q U (copy warp) has read U^T, rewritten below
+        bool ok = tc::mbar_wait(bar_m1, ph_m1 & 1);
+        ++ph_m1;
+        if constexpr (ST != 0)
+          if (c >= 1) ok = tc::mbar_wait(bar_aq, (uint32_t)(c - 1) & 1) && ok;
+        tc::fence_after_sync();
+        if (tc::named_barrier_or(kBarMain, kMainThreads, !ok)) { failed = true; break; }
+      }
       if (warp & 2) {  // U = U' + D_U rows 64-127 -> U^T fp16 operand
         const int m = i - 64;
         float u[kCols];
@@ -1018,19 +1029,22 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
         if (wait_main(bar_s2, ph_s2)) { failed = true; break; }
       }
 
-      // ---------------- MMA 2: D_H += K~^T U (critical);  D_U += [-A_Q; *] U (second issuer)
+      // ---------------- MMA 2: D_H += K~^T U (critical);  D_U += [-A_Q; *] U (second issuer: with the
+      //                  ring, the copy warp, once these four are in, so they run first on the tensor core)
       if (tid == 0) {
         for (int k = 0; k < 4; ++k)
           tc::mma16(tmem + COL_H, tc::sdesc_kstep(sbase + set + C::R_KT, 128, 0, k),
                     tc::sdesc_kstep(sbase + S_NU, kBV, 0, k), kIdNBV, 1u);
         tc::mma_commit(bar_m2);
-        if constexpr (ST != 0) tc::mma_commit(bar_empty + c % (ST == 0 ? 1 : ST));
-      } else if (tid == 32) {
+        if constexpr (ST != 0) {
+          tc::mma_commit(bar_empty + c % (ST == 0 ? 1 : ST));
+          tc::mbar_arrive(bar_upub);
+        }
+      } else if (ST == 0 && tid == 32) {
         for (int k = 0; k < 4; ++k)
           tc::mma16(d_u, tc::sdesc_kstep(sbase + set + C::R_AQ, 128, 0, k), tc::sdesc_kstep(sbase + S_NU, kBV, 0, k),
                     kIdNBV, 1u);
-        if constexpr (ST == 0) tc::mma_commit(bar_m2b);
-        else tc::mma_commit(bar_empty + c % (ST == 0 ? 1 : ST));
+        tc::mma_commit(bar_m2b);
         tc::mma_commit(bar_oready + buf);
       }
       {  // MMA 2 done and chunk c+1's operand set in: one barrier for both
@@ -1206,12 +1220,13 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
       }
     } else if (lane == 0 && nch > 0) {
       // ======================= operand copies (one lane): the set of chunk c into ring slot c % ST as soon
-      // as MMA 2 of chunk c - ST has read it (a waiter here lags its signaller by at most one use)
+      // as MMA 2 of chunk c - ST has read it; and MMA 2's -A_Q U of every chunk, issued once the chain's
+      // K~^T U is in (a waiter here lags its signaller by at most one use: the chain waits for chunk c's
+      // -A_Q U before it publishes chunk c + 1's U)
       constexpr int kST = ST == 0 ? 1 : ST;
       int issued = 0;
-      for (int c = 0; c < nch; ++c) {
+      auto issue_set = [&](int c) {
         const int r = c % kST;
-        if (c >= kST && !tc::mbar_wait(bar_empty + r, (uint32_t)(c / kST - 1) & 1)) { failed = true; break; }
         uint8_t *dst = sm + set_of(c);
         const uint8_t *src = slot(g0 + c);
         tc::mbar_arrive_expect_tx(bar_full + r, 32768 + 16384 + 8192 + 64 * kBV * 2 + 256);
@@ -1220,6 +1235,22 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
         tc::bulk_g2s(dst + C::R_UP, src + kVUp + (size_t)sv * 64 * kBV * 2, 64 * kBV * 2, bar_full + r);
         tc::bulk_g2s(dst + C::R_GAM, src + kVGam, 256, bar_full + r);
         issued = c + 1;
+      };
+      for (int c = 0; c < kST && c < nch; ++c) issue_set(c);
+      for (int c = 0; c < nch; ++c) {
+        if (!tc::mbar_wait(bar_upub, (uint32_t)c & 1)) { failed = true; break; }
+        tc::fence_after_sync();
+        const uint32_t d_u = tmem + COL_U + kBV * (c & 1), set = set_of(c);
+        for (int k = 0; k < 4; ++k)
+          tc::mma16(d_u, tc::sdesc_kstep(sbase + set + C::R_AQ, 128, 0, k), tc::sdesc_kstep(sbase + S_NU, kBV, 0, k),
+                    kIdNBV, 1u);
+        tc::mma_commit(bar_empty + c % kST);
+        tc::mma_commit(bar_oready + (c & 1));
+        tc::mma_commit(bar_aq);
+        if (c + kST < nch) {
+          if (!tc::mbar_wait(bar_empty + c % kST, (uint32_t)(c / kST) & 1)) { failed = true; break; }
+          issue_set(c + kST);
+        }
       }
       if (failed) set_status(p.status, kDevTimeout);
       // copies in flight must land before the CTA's shared memory goes away

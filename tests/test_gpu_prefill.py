@@ -49,7 +49,7 @@ def test_tiny_fp32_config():
 
 
 @pytest.mark.parametrize("case", ["ragged_single", "varlen_edges", "long_memory", "gqa4", "gqa8", "gqa16",
-                                  "fp32_d128", "gqa1", "chunk_edges", "fast_decay"])
+                                  "fp32_d128", "gqa1", "gqa3", "chunk_edges", "fast_decay"])
 def test_small_cases(case):
     if case == "ragged_single":      # several chunks plus a ragged tail
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(200,), h_qk=2, h_v=4)
@@ -60,6 +60,8 @@ def test_small_cases(case):
                            init_std=0.02, seed=5)
     elif case == "gqa4":             # 4 value heads per q/k head
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(97, 31), h_qk=1, h_v=4, seed=7)
+    elif case == "gqa3":             # value heads in a pair and a single one after it
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(130, 45), h_qk=2, h_v=6, init_std=0.02, seed=11)
     elif case == "gqa1":             # one value head per q/k head
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(150,), h_qk=2, h_v=2, init_std=0.02, seed=10)
     elif case == "chunk_edges":      # exactly one chunk, one chunk + 1, two chunks - 1, one token
