@@ -72,8 +72,8 @@ constexpr int kPad = 66;  // fp32 64 x 64 matrices: padded rows (even: 8-byte al
 //   [Q^; W]  [128 rows][128 cols]: rows 0-63 Q^ = diag(gamma) Q, rows 64-127
 //            W = T diag(beta gamma) K (one 128-row MMA operand)
 //   K~^T     [128 i][64 m] = (diag(e^(G_C - G)) K)^T
-//   U'       T diag(beta) V, plain row-major per state slice: [128 / bv][64 m][bv]
-//            (bv = the state pass's slice width)
+//   U'       T diag(beta) V, plain row-major per state slice: [4][64 m][32]
+//            (32 = the state pass's slice width)
 //   -A_Q     [64 r][64 s], A_Q = D o (Q K^T), lower triangle with the diagonal
 //   gamma    [64] fp32
 constexpr uint32_t kVWQ = 0, kVKt = 32768, kVUp = 49152, kVAq = 65536, kVGam = 73728;
@@ -84,7 +84,6 @@ struct Ws {
   int4 *chunk_info;  // [max_chunks]: (sequence, first token, sequence start, tokens in the chunk)
   uint8_t *vs;       // [max_chunks][h_v] x kVSlot
   int max_chunks;
-  int up_bv_log2;    // log2 of the column width of the U' image slices (the state pass's slice width)
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -165,14 +164,6 @@ __device__ __forceinline__ void publish_operands() {
 
 __device__ __forceinline__ uint2 pack4_f16(float a, float b, float c, float d) {
   return make_uint2(tc::pack_f16x2(a, b), tc::pack_f16x2(c, d));
-}
-__device__ __forceinline__ void st_chunk_f16_global(uint8_t *dst, const float *x) {
-  uint4 u;
-  u.x = tc::pack_f16x2(x[0], x[1]);
-  u.y = tc::pack_f16x2(x[2], x[3]);
-  u.z = tc::pack_f16x2(x[4], x[5]);
-  u.w = tc::pack_f16x2(x[6], x[7]);
-  *reinterpret_cast<uint4 *>(dst) = u;
 }
 
 // ================================================================ chunk table
@@ -415,8 +406,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     __syncthreads();
   }
 
-  // ---------------- q and k: conv + SiLU + L2 norm -> [K; Q] hi / lo tiles, K^T tile, Q^ images,
-  //                  and K~^T = (diag(e^(G_C - G)) K)^T images of every value head
+  // ---------------- q and k: conv + SiLU + L2 norm -> [K; Q] hi / lo tiles, K^T tile, Q^ images
   {
     float y[8][4], kreg[8][4];
     uint2 xrk[11];
@@ -467,21 +457,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       for (int r = 0; r < 8; ++r) kt[r] = kreg[r][c];
       tc::st_chunk_f16(sm + P_KT + tc::sw128_chunk(128, c0 + c, warp), kt);
     }
-    for (int vv = 0; vv < rep; ++vv) {
-      const float *dec = sG + vv * 256 + 192;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float kt[8];
-#pragma unroll
-        for (int r = 0; r < 8; r += 2) {
-          const float2 k2 = tc::mul2(make_float2(kreg[r][c], kreg[r + 1][c]),
-                                     *reinterpret_cast<const float2 *>(dec + r0 + r));
-          kt[r] = k2.x;
-          kt[r + 1] = k2.y;
-        }
-        st_chunk_f16_global(v_slot_of(vv) + kVKt + tc::sw128_chunk(128, c0 + c, warp), kt);
-      }
-    }
   }
   publish_operands();
 
@@ -491,6 +466,28 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     mma_chain(tmem + COL_P1, sbase + P_KQ, 128, 0, sbase + P_KQL, 128, 0, 8, kIdN64, true);
     mma_chain(tmem + COL_P1, sbase + P_KQL, 128, 0, sbase + P_KQ, 128, 0, 8, kIdN64, true);
     tc::mma_commit(bar);
+  }
+
+  // ---------------- K~^T = (diag(e^(G_C - G)) K)^T images of every value head, from the K^T tile (the
+  //                  image has its SW128 layout): the tile's 16-byte chunks in order, so a warp stores
+  //                  512 contiguous bytes
+  for (int vv = 0; vv < rep; ++vv) {
+    const float *dec = sGall + vv * 256 + 192;
+    uint8_t *dst = v_slot_of(vv) + kVKt;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = tid + kPrepThreads * k;          // chunk q: row i = q / 8, physical position q % 8
+      const int mc = (q & 7) ^ ((q >> 3) & 7);       // its columns m = 8 mc .. 8 mc + 7
+      const uint4 raw = *reinterpret_cast<const uint4 *>(sm + P_KT + 16 * q);
+      const float4 d0 = *reinterpret_cast<const float4 *>(dec + 8 * mc);
+      const float4 d1 = *reinterpret_cast<const float4 *>(dec + 8 * mc + 4);
+      const float2 k0 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.x)), make_float2(d0.x, d0.y));
+      const float2 k1 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.y)), make_float2(d0.z, d0.w));
+      const float2 k2 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.z)), make_float2(d1.x, d1.y));
+      const float2 k3 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.w)), make_float2(d1.z, d1.w));
+      *reinterpret_cast<uint4 *>(dst + 16 * q) = make_uint4(tc::pack_f16x2(k0.x, k0.y), tc::pack_f16x2(k1.x, k1.y),
+                                                          tc::pack_f16x2(k2.x, k2.y), tc::pack_f16x2(k3.x, k3.y));
+    }
   }
 
   // ---------------- the value heads, two at a time
@@ -567,9 +564,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
           v[2 * q + 1] = (s + 1 <= r) ? e.y : 0.0f;
         }
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          st_chunk_f16_global(v_slot_of(grp + hh) + kVAq + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
+        for (int cc = 0; cc < 4; ++cc)  // staged in the image's layout (the inverse's scratch is free)
+          tc::st_chunk_f16(sm + P_XF + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
       }
+      __syncthreads();
+      uint8_t *dst = v_slot_of(grp + hh) + kVAq;  // the 8 KB image in order: 512 contiguous bytes per warp store
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int q = tid + kPrepThreads * k;
+        *reinterpret_cast<uint4 *>(dst + 16 * q) = *reinterpret_cast<const uint4 *>(sm + P_XF + 16 * q);
+      }
+      if (hh + 1 < nh) __syncthreads();  // read before the next head's staging
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -724,17 +729,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     //   first head:  B = [K^T; V^T]: W = T diag(beta gamma) K in rows 0-63, columns 0-127,
     //                U' = T diag(beta) V in rows 64-127, columns 128-255
     //   second head: B = [V^T; K^T]: the same with the column halves swapped
-#pragma unroll 1
-    for (int hh = 0; hh < nh; ++hh) {
+    // Each head's W and U' are staged in shared memory (over its own operands, which the product has
+    // read) and stored to their images in order, while the next head's product runs.
+    auto issue_wu = [&](int hh) {
       if (tid == 0) {
         mma_chain(tmem, sbase + (hh ? P_AT1 : P_AT0), 128, 0, sbase + (hh ? P_VT1 : P_KT), 256, 0, 4, kIdN256,
                   false);
         tc::mma_commit(bar);
       }
+    };
+    issue_wu(0);
+#pragma unroll 1
+    for (int hh = 0; hh < nh; ++hh) {
       if (wait_all(bar, phase)) { failed = true; break; }
-      uint8_t *v_slot = v_slot_of(grp + hh);
+      uint8_t *stw = sm + (hh ? P_AT1 : P_AT0);  // W staging: the image's two 8 KB slab halves (rows 64-127)
+      uint8_t *stu = sm + (hh ? P_VT1 : P_VT0);  // U' staging: [4 slices][64 m][32 j], chunks permuted per row
       const int wcol = hh ? 128 : 0, half = warp >> 2;  // this warp's 64 columns of W or U'
-      if ((warp & 3) < 2) {  // TMEM lanes 0-63: W -> rows 64-127 of the [Q^; W] image
+      if ((warp & 3) < 2) {  // TMEM lanes 0-63: W
         const int r = 32 * (warp & 3) + lane;
 #pragma unroll
         for (int c32 = 0; c32 < 2; ++c32) {
@@ -742,28 +753,37 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
           tc::tmem_ld32(tmem + lane_off + wcol + 64 * half + 32 * c32, w);
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
-            st_chunk_f16_global(v_slot + kVWQ + tc::sw128_offset(128, 64 + r, 64 * half + 32 * c32 + 8 * cc),
-                                w + 8 * cc);
+            tc::st_chunk_f16(stw + half * 8192 + tc::sw128_chunk(64, r, 4 * c32 + cc), w + 8 * cc);
         }
-      } else {  // TMEM lanes 64-127: U' -> its image
+      } else {  // TMEM lanes 64-127: U'
         const int m = 32 * (warp & 3) - 64 + lane;
-        const int lb = ws.up_bv_log2;
 #pragma unroll
         for (int c32 = 0; c32 < 2; ++c32) {
           float u[32];
           tc::tmem_ld32(tmem + lane_off + (128 - wcol) + 64 * half + 32 * c32, u);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int j = 64 * half + 32 * c32 + 8 * cc;  // state column of this 16-byte chunk
-            st_chunk_f16_global(v_slot + kVUp + ((size_t)(j >> lb) * 64 + m) * (2u << lb) + (j & ((1 << lb) - 1)) * 2,
-                                u + 8 * cc);
-          }
+          for (int cc = 0; cc < 4; ++cc)  // state columns 64 half + 32 c32 + 8 cc .. + 7: slice 2 half + c32
+            tc::st_chunk_f16(stu + (2 * half + c32) * 4096 + m * 64 + ((cc ^ ((m >> 1) & 3)) << 4), u + 8 * cc);
         }
       }
       tc::fence_before_sync();
-      __syncthreads();  // the accumulator is read: the next product may overwrite it
+      __syncthreads();  // staged, and the accumulator is read: the next product may overwrite it
       tc::fence_after_sync();
+      if (hh + 1 < nh) issue_wu(hh + 1);
+      uint8_t *v_slot = v_slot_of(grp + hh);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int q = tid + kPrepThreads * k;  // 16-byte chunk q of 1024
+        // W: staged bytes [0, 8K) -> image slab 0 rows 64-127, [8K, 16K) -> slab 1 rows 64-127
+        *reinterpret_cast<uint4 *>(v_slot + kVWQ + 8192 + 16 * q + (q >= 512 ? 8192 : 0)) =
+            *reinterpret_cast<const uint4 *>(stw + 16 * q);
+        // U': image chunk q = (slice q / 256, row m, chunk q % 4)
+        const int m = (q >> 2) & 63;
+        *reinterpret_cast<uint4 *>(v_slot + kVUp + 16 * q) =
+            *reinterpret_cast<const uint4 *>(stu + (q >> 8) * 4096 + m * 64 + (((q & 3) ^ ((m >> 1) & 3)) << 4));
+      }
     }
+    if (grp + 2 < rep) __syncthreads();  // the stagings are read before the next pair's tiles go there
   }
   if (failed && tid == 0) set_status(p.status, kDevTimeout);
   tc::fence_before_sync();
@@ -1324,6 +1344,7 @@ bool state_ring(const PrefillParams &p) {
   return 4L * p.N * p.h_v <= (long)sms[dev];
 }
 constexpr int kStateSlices = 4;
+static_assert(kD / kStateSlices == 32, "the prep writes U' in slices of 32 state columns");
 
 template <int NS, int ST>
 cudaError_t launch_state(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
@@ -1370,7 +1391,6 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   ws.chunk_info = reinterpret_cast<int4 *>(p.ws + L.info);
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
-  ws.up_bv_log2 = __builtin_ctz((unsigned)(kD / kStateSlices));
 
   trace_begin(s, GDN_K_CHUNK_TABLE);
   chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
