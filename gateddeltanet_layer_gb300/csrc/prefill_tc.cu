@@ -468,28 +468,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     tc::mma_commit(bar);
   }
 
-  // ---------------- K~^T = (diag(e^(G_C - G)) K)^T images of every value head, from the K^T tile (the
-  //                  image has its SW128 layout): the tile's 16-byte chunks in order, so a warp stores
-  //                  512 contiguous bytes
-  for (int vv = 0; vv < rep; ++vv) {
-    const float *dec = sGall + vv * 256 + 192;
-    uint8_t *dst = v_slot_of(vv) + kVKt;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int q = tid + kPrepThreads * k;          // chunk q: row i = q / 8, physical position q % 8
-      const int mc = (q & 7) ^ ((q >> 3) & 7);       // its columns m = 8 mc .. 8 mc + 7
-      const uint4 raw = *reinterpret_cast<const uint4 *>(sm + P_KT + 16 * q);
-      const float4 d0 = *reinterpret_cast<const float4 *>(dec + 8 * mc);
-      const float4 d1 = *reinterpret_cast<const float4 *>(dec + 8 * mc + 4);
-      const float2 k0 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.x)), make_float2(d0.x, d0.y));
-      const float2 k1 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.y)), make_float2(d0.z, d0.w));
-      const float2 k2 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.z)), make_float2(d1.x, d1.y));
-      const float2 k3 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.w)), make_float2(d1.z, d1.w));
-      *reinterpret_cast<uint4 *>(dst + 16 * q) = make_uint4(tc::pack_f16x2(k0.x, k0.y), tc::pack_f16x2(k1.x, k1.y),
-                                                          tc::pack_f16x2(k2.x, k2.y), tc::pack_f16x2(k3.x, k3.y));
-    }
-  }
-
   // ---------------- the value heads, two at a time
   for (int grp = 0; grp < rep && !failed; grp += 2) {
     const int nh = min(2, rep - grp);
@@ -585,6 +563,27 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       float x[16];
       const int hh = tid >> 6, bb = (tid >> 4) & 3, s = tid & 15;
       const bool act = hh < nh;
+      if (tid >= 128) {  // meanwhile: the K~^T = (diag(e^(G_C - G)) K)^T images of the pair, from the K^T
+                         // tile (the image has its SW128 layout), 16-byte chunks in order
+        for (int h2 = 0; h2 < nh; ++h2) {
+          const float *dec = sGall + (grp + h2) * 256 + 192;
+          uint8_t *dst = v_slot_of(grp + h2) + kVKt;
+#pragma unroll 4
+          for (int k = 0; k < 8; ++k) {
+            const int q = tid - 128 + 128 * k;              // chunk q: row i = q / 8, physical position q % 8
+            const int mc = (q & 7) ^ ((q >> 3) & 7);        // its columns m = 8 mc .. 8 mc + 7
+            const uint4 raw = *reinterpret_cast<const uint4 *>(sm + P_KT + 16 * q);
+            const float4 d0 = *reinterpret_cast<const float4 *>(dec + 8 * mc);
+            const float4 d1 = *reinterpret_cast<const float4 *>(dec + 8 * mc + 4);
+            const float2 k0 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.x)), make_float2(d0.x, d0.y));
+            const float2 k1 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.y)), make_float2(d0.z, d0.w));
+            const float2 k2 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.z)), make_float2(d1.x, d1.y));
+            const float2 k3 = tc::mul2(__half22float2(*reinterpret_cast<const __half2 *>(&raw.w)), make_float2(d1.z, d1.w));
+            *reinterpret_cast<uint4 *>(dst + 16 * q) = make_uint4(tc::pack_f16x2(k0.x, k0.y), tc::pack_f16x2(k1.x, k1.y),
+                                                                tc::pack_f16x2(k2.x, k2.y), tc::pack_f16x2(k3.x, k3.y));
+          }
+        }
+      }
       if (act) {
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
