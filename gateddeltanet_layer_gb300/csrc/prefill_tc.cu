@@ -544,15 +544,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)  // staged in the image's layout (the inverse's scratch is free)
           tc::st_chunk_f16(sm + P_XF + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
-      }
-      __syncthreads();
-      uint8_t *dst = v_slot_of(grp + hh) + kVAq;  // the 8 KB image in order: 512 contiguous bytes per warp store
+        // warps 2 and 6 hold rows 0-31 of -A_Q, warps 3 and 7 rows 32-63: each pair stores its 4 KB of the
+        // image in order (512 contiguous bytes per warp store), synchronised among its own 64 threads
+        const int pr = warp & 1, t = 32 * (warp >> 2) + lane;
+        tc::named_barrier(1 + pr, 64);
+        uint8_t *dst = v_slot_of(grp + hh) + kVAq;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int q = tid + kPrepThreads * k;
-        *reinterpret_cast<uint4 *>(dst + 16 * q) = *reinterpret_cast<const uint4 *>(sm + P_XF + 16 * q);
+        for (int k = 0; k < 4; ++k) {
+          const int q = 256 * pr + t + 64 * k;
+          *reinterpret_cast<uint4 *>(dst + 16 * q) = *reinterpret_cast<const uint4 *>(sm + P_XF + 16 * q);
+        }
+        if (hh + 1 < nh) tc::named_barrier(1 + pr, 64);  // read before the next head's staging
       }
-      if (hh + 1 < nh) __syncthreads();  // read before the next head's staging
     }
     tc::fence_before_sync();
     __syncthreads();
