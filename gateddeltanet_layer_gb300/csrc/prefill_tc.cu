@@ -801,14 +801,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 //           U    = U' + D_U[64:128]         (fp32, then the fp16 operand U^T)
 //   MMA 2:  D_H += K~^T U                   (D_H scaled by gamma_C before)
 //           D_U += [-A_Q; *] U              (rows 0-63 become -O; rows 64-127 unused)
-// Every product has M = 128 rows and N = kBV columns.  A single thread issues
-// tcgen05.mma at a fixed cost per instruction, so the critical path per chunk
-// is kept to MMA 1 (8 instructions) and the K~^T U half of MMA 2 (4); the
-// A_Q U half is issued by a second thread.  Warps 0-7 run the chain (each TMEM
-// lane by two warps, one per half of the columns), warps 8-9 the epilogue one
-// chunk behind (exchanging per-token partial sums of o^2 with the other CTAs
-// of the cluster through st.async into their shared memory), warp 10 issues
-// the operand copies.
+// Every product has M = 128 rows and N = kBV columns.  tcgen05.mma issues at
+// a fixed cost per instruction, so the critical path per chunk is kept to
+// MMA 1 (8 instructions) and the K~^T U half of MMA 2 (4); the A_Q U half is
+// issued by a second thread (ST >= 2: the copy warp, once the K~^T U half is
+// in, so that half runs first on the tensor core).  Warps 0-7 run the chain
+// (each TMEM lane by two warps, one per half of the columns), warps 8-9 the
+// epilogue one chunk behind (exchanging per-token partial sums of o^2 with the
+// other CTAs of the cluster through st.async into their shared memory), warp
+// 10 issues the operand copies.
 // ST = 0: one buffer per operand set, refilled as soon as each set is consumed
 // (two CTAs per SM).  ST >= 2: a ring of ST whole per-chunk operand sets
 // ([Q^; W], K~^T, -A_Q, U' slice, gamma), so the copies of the next chunks
