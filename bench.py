@@ -62,6 +62,18 @@ def prefill_work(cfg) -> tuple[int, float]:
     return nbytes, float(cfg.T) * FLOPS_PER_TOKEN
 
 
+def max_over_ranks(values, device):
+    """Elementwise maximum of `values` over the ranks of the default process
+    group (the values themselves without one, or with a single rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 # ---------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi SM clock / throttle reasons sampled every 200 ms during a timed region."""
@@ -339,23 +351,14 @@ def run_ours(args):
         res = time_prefill(cfg, args.steps, args.warmup, dev, flush, with_e2e=True, trace=True)
         barrier()
         wall = time.perf_counter() - t0
-    ms = statistics.mean(res["ms"])
-    e2e_ms = res["e2e"]["ms"]
-    if world > 1:
-        tt = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(tt[0]), float(tt[1])
+    ms, e2e_ms = max_over_ranks([statistics.mean(res["ms"]), res["e2e"]["ms"]], dev)
     nbytes, flops = prefill_work(cfg)
     rf = roofline_of(nbytes, flops, ms, pk)
     # the dominant kernel: most device time over the timed steps (library trace)
     kernels = res["kernels"]
     top = max(kernels, key=lambda k: kernels[k][1])
     top_n, top_ms_total = kernels[top]
-    top_ms = top_ms_total / top_n
-    if world > 1:
-        tt = torch.tensor([top_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        top_ms = float(tt[0])
+    top_ms, = max_over_ranks([top_ms_total / top_n], dev)
     top_gbs = nbytes / (top_ms * 1e-3) / 1e9
     launches = sum(n for n, _ in kernels.values())
 

@@ -1,0 +1,53 @@
+"""The bench's multi-rank path on the CPU: two `gloo` processes reduce their
+timings with `bench.max_over_ranks` (each rank's step time is the slowest
+rank's), and the whole-job throughput counts every rank's tokens."""
+import os
+import socket
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r measured (1 + r) ms per step and (10 - r) ms end to end
+        ms, e2e = bench.max_over_ranks([1.0 + rank, 10.0 - rank], torch.device("cpu"))
+        out[rank] = (ms, e2e, bench.headline_config(bench.synth.SINGLE_4K, world)["parallelism"])
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_processes():
+    world = 2
+    with mp.Manager() as manager:
+        out = manager.dict()
+        mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
+        got = dict(out)
+    assert set(got) == {0, 1}
+    for rank in range(world):
+        ms, e2e, par = got[rank]
+        assert ms == 2.0 and e2e == 10.0  # the slowest rank's time, on every rank
+        assert par == "replicas x2"
+
+
+def test_max_over_ranks_single_process():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks([3.5, 1.25], torch.device("cpu")) == [3.5, 1.25]
