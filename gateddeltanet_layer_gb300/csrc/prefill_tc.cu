@@ -81,6 +81,7 @@ constexpr uint32_t kVSlot = 73984;
 
 struct Ws {
   int *chunk_base;   // [N + 1]: first chunk of each sequence; [N] = number of chunks
+  int *seq_order;    // [N]: the sequences, longest first (by powers of two of their chunk counts); N > 1
   int4 *chunk_info;  // [max_chunks]: (sequence, first token, sequence start, tokens in the chunk)
   uint8_t *vs;       // [max_chunks][h_v] x kVSlot
   int max_chunks;
@@ -89,13 +90,14 @@ struct Ws {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t base, info, vs, total;
+  size_t base, order, info, vs, total;
   int max_chunks;
   WsLayout(int T, int N, int h_qk, int h_v) {
     (void)h_qk;
     max_chunks = (T + kC - 1) / kC + N;
     base = 0;
-    info = align_up(sizeof(int) * (size_t)(N + 1), 1024);
+    order = align_up(sizeof(int) * (size_t)(N + 1), 256);
+    info = align_up(order + sizeof(int) * (size_t)N, 1024);
     vs = align_up(info + sizeof(int4) * (size_t)max_chunks, 1024);
     total = vs + (size_t)max_chunks * h_v * kVSlot;
   }
@@ -167,9 +169,13 @@ __device__ __forceinline__ uint2 pack4_f16(float a, float b, float c, float d) {
 }
 
 // ================================================================ chunk table
+// Chunk-count class of a sequence for the state pass's order: 1 + floor(log2(chunks)), 0 when empty.
+__device__ __forceinline__ int length_class(int chunks) { return chunks > 0 ? 32 - __clz(chunks) : 0; }
+
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p, Ws ws) {
   __shared__ int scan[1024];
   __shared__ int bad;
+  __shared__ int cls_next[33];  // sequences per length class, then the next free place of each
   const int N = p.N, tid = threadIdx.x;
   tc::launch_dependents();  // the prep CTAs may take their places; they wait for this table
   if (tid == 0) bad = 0;
@@ -179,6 +185,29 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p
   for (int n = n0; n < n1; ++n) {
     const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
     if (s0 >= 0 && s1 >= s0 && s1 <= p.T) cnt += (s1 - s0 + kC - 1) / kC;
+  }
+  if (N > 1) {  // the state pass's order: length classes longest first, so long chains start first
+    if (tid < 33) cls_next[tid] = 0;
+    __syncthreads();
+    for (int n = n0; n < n1; ++n) {
+      const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+      atomicAdd(&cls_next[length_class((s0 >= 0 && s1 >= s0 && s1 <= p.T) ? (s1 - s0 + kC - 1) / kC : 0)], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int at = 0;
+      for (int k = 32; k >= 0; --k) {
+        const int c = cls_next[k];
+        cls_next[k] = at;
+        at += c;
+      }
+    }
+    __syncthreads();
+    for (int n = n0; n < n1; ++n) {  // the order inside a class does not matter for the results
+      const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+      const int c = (s0 >= 0 && s1 >= s0 && s1 <= p.T) ? (s1 - s0 + kC - 1) / kC : 0;
+      ws.seq_order[atomicAdd(&cls_next[length_class(c)], 1)] = n;
+    }
   }
   scan[tid] = cnt;
   __syncthreads();
@@ -895,14 +924,13 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = tc::smem_u32(sm);
   const int h_v = p.h_v;
-  const int chain = blockIdx.x / kSlices;
+  const int chain = blockIdx.x / kSlices;  // chains go sequence by sequence, longest sequences first
   const int sv = (int)tc::cluster_ctarank();
-  const int n = chain / h_v, h = chain % h_v;
+  const int h = chain % h_v;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   const int j0 = kBV * sv;  // first state column of this CTA
-
-  const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+  int s0 = p.cu_seqlens[chain / h_v], s1 = p.cu_seqlens[chain / h_v + 1];  // one sequence: it is n = 0
 
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_MISC);
   uint64_t *bar_m1 = bar + C::B_M1, *bar_m2 = bar + C::B_M2, *bar_z = bar + C::B_Z;
@@ -936,6 +964,11 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
   bool failed = false;
 
   tc::grid_dependency_wait();  // the chunk table and the operand images
+  const int n = p.N > 1 ? ws.seq_order[chain / h_v] : chain / h_v;
+  if (n != chain / h_v) {
+    s0 = p.cu_seqlens[n];
+    s1 = p.cu_seqlens[n + 1];
+  }
   bool valid = s0 >= 0 && s1 >= s0 && s1 <= p.T;  // else reported by the chunk table
   const int g0 = valid ? ws.chunk_base[n] : 0, g1 = valid ? ws.chunk_base[n + 1] : 0;
   if (valid && g1 - g0 != (s1 - s0 + kC - 1) / kC) valid = false;  // table overflow, reported
@@ -1391,6 +1424,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   if (p.ws_bytes < L.total) return cudaErrorInvalidValue;
   Ws ws;
   ws.chunk_base = reinterpret_cast<int *>(p.ws + L.base);
+  ws.seq_order = reinterpret_cast<int *>(p.ws + L.order);
   ws.chunk_info = reinterpret_cast<int4 *>(p.ws + L.info);
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
