@@ -51,3 +51,21 @@ def test_max_over_ranks_single_process():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks([3.5, 1.25], torch.device("cpu")) == [3.5, 1.25]
+
+
+def test_reference_arm_prints_one_line():
+    """`bench.py --impl reference` runs the oracle on the host cores (no GPU)
+    and prints one JSON line with the keys the bench's contract names."""
+    import json
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["config"]["workload"] == "prefill_T4096"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
