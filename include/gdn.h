@@ -92,10 +92,13 @@ typedef struct {
 
 /*
  * Bytes of device workspace gdn_prefill needs for `dims` (0 if dims is NULL or
- * invalid).  The workspace holds the device status word and the schedule of
- * (sequence, head) chains.  It is scratch: its contents need not be preserved
- * between calls, but a call's status word stays readable until the next call
- * that uses the same workspace.
+ * invalid).  The workspace holds the device status word, the chunk schedule
+ * (per sequence its first chunk, the order in which the state pass takes the
+ * sequences, per chunk its tokens) and, on the chunked path, the operand
+ * images the chunk preparation hands to the state pass (72.25 KiB per chunk
+ * of 64 tokens and value head).  It is scratch: its contents need not be
+ * preserved between calls, but a call's status word stays readable until the
+ * next call that uses the same workspace.
  */
 GDN_API size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
 
