@@ -484,7 +484,7 @@ def run_reference(args):
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 * cfg.h_v / n_chains,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": headline_config(cfg, 1),
+            "data": "synthetic (seeded)", "config": headline_config(cfg, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, n_chains), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
