@@ -1,11 +1,12 @@
 """Benchmark of the GatedDeltaNet layer on GB300.
 
-One step = one ``gdn_prefill`` call over the single-sequence workload
-(T = 4096 tokens, H_qk = 16, H_v = 32, d_k = d_v = 128, bf16 streams, fp32
-state, final state returned), inputs resident in HBM, L2 flushed between
-steps.  Prints one JSON line.  Also measured, in ``extra``: the 32768-token
-varlen prefill, the 131072-token long prefill and the 256-sequence decode
-step, each with its roofline fraction.
+One step = one ``gdn_prefill`` call over the long packed prefill (131072
+tokens = 16 sequences x 8192, H_qk = 16, H_v = 32, d_k = d_v = 128, bf16
+streams, fp32 state, final state returned), the largest single-GPU workload,
+inputs resident in HBM, L2 flushed between steps.  Prints one JSON line.  Also
+measured, in ``extra``: the 4096-token single-sequence prefill, the
+32768-token varlen prefill and the 256-sequence decode step, each with its
+roofline fraction and per-kernel split.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
 
@@ -13,7 +14,7 @@ Under torchrun (N > 1) every rank runs its own copy of the workload on its
 own GPU (sequences are independent: no data-path collective), the per-step
 time is the max over ranks and ``value`` counts the tokens of all ranks.
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead
-(rank 0 only), on a bounded sample of the same workload.
+(rank 0 only), each step a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -134,6 +135,16 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
+_INPUTS = {}
+
+
+def inputs_of(cfg):
+    """The seeded inputs of a prefill workload, drawn once per run."""
+    if cfg.name not in _INPUTS:
+        _INPUTS[cfg.name] = synth.make_prefill(cfg)
+    return _INPUTS[cfg.name]
+
+
 # ---------------------------------------------------------------------- GPU arm
 def _device_inputs(inp, dev):
     import torch
@@ -158,7 +169,7 @@ def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False, trace=False):
     import torch
 
     import gateddeltanet_layer_gb300 as gdn
-    inp = synth.make_prefill(cfg)
+    inp = inputs_of(cfg)
     t = _device_inputs(inp, dev)
     T, N = cfg.T, cfg.N
     out = torch.empty((T, cfg.h_v, cfg.d_v), dtype=torch.bfloat16, device=dev)
@@ -322,6 +333,52 @@ def roofline_of(nbytes, flops, ms, pk, peak_key="hbm_gbs"):
             "hbm_frac": gbs / pk["hbm_gbs"]}
 
 
+HEADLINE = synth.LONG_128K
+# A smaller copy of the headline workload (2 of its 16 sequences) for ncu
+# captures; per sequence it does the same work, so its DRAM traffic scales to
+# the headline call by the number of sequences.
+LONG_2X8192 = synth.scaled(synth.LONG_128K, name="prefill_long_T16384", lengths=(8192,) * 2)
+PROFILE_CASES = {LONG_2X8192.name: LONG_2X8192}
+
+
+def prefill_line(cfg, res, steps, pk, dev):
+    """Roofline of one prefill workload: the whole call against the slower of
+    its byte and flop bounds, and the per-kernel split of the call."""
+    ms, = max_over_ranks([statistics.mean(res["ms"])], dev)
+    nbytes, flops = prefill_work(cfg)
+    rf = roofline_of(nbytes, flops, ms, pk)
+    bound = "hbm" if nbytes / pk["hbm_gbs"] >= flops / (pk["bf16_tflops"] * 1e3) else "tensor"
+    per_kernel = {}
+    traffic = profiled_traffic(cfg)
+    kernels = res["kernels"] or {}
+    for name, (n, total) in kernels.items():
+        k_ms = total / steps
+        entry = {"ms_per_call": k_ms, "share_of_traced_call": None, "launches_per_call": n / steps}
+        kt = (traffic or {}).get("kernels", {}).get(name)
+        if kt is not None:
+            entry["dram_bytes_per_call"] = kt
+            entry["dram_gbs"] = kt / (k_ms * 1e-3) / 1e9
+            entry["dram_frac_of_peak"] = entry["dram_gbs"] / pk["hbm_gbs"]
+        per_kernel[name] = entry
+    traced = sum(e["ms_per_call"] for e in per_kernel.values())
+    for e in per_kernel.values():
+        e["share_of_traced_call"] = e["ms_per_call"] / traced if traced > 0 else None
+    if bound == "hbm":
+        achieved, peak, unit = rf["achieved_gbs"], pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = rf["achieved_tflops"], pk["bf16_tflops"], "TFLOP/s"
+    return ms, {
+        "bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": rf["roofline_frac"],
+        "traffic": None if traffic is None else traffic["call"],
+        "scope": "whole gdn_prefill call (every kernel it launches)",
+        "peak_source": pk["source"] + (" (burst copy)" if bound == "hbm" else " (burst cuBLAS bf16)"),
+        "algorithmic_bytes_per_call": nbytes, "algorithmic_flops_per_call": flops,
+        "flop_bound_frac": flops / (pk["bf16_tflops"] * 1e12) / (ms * 1e-3),
+        "byte_bound_frac": nbytes / (pk["hbm_gbs"] * 1e9) / (ms * 1e-3),
+        "per_kernel": per_kernel,
+    }
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -337,48 +394,42 @@ def run_ours(args):
     gdn.library()
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    cfg = synth.SINGLE_4K
+    cfg = HEADLINE
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # ---- the headline: T=4096 prefill
+    # ---- the headline: the 131072-token long prefill
     barrier()
     with ClockSampler(torch.cuda.current_device()) as clk:
         t0 = time.perf_counter()
         res = time_prefill(cfg, args.steps, args.warmup, dev, flush, with_e2e=True, trace=True)
         barrier()
         wall = time.perf_counter() - t0
-    ms, e2e_ms = max_over_ranks([statistics.mean(res["ms"]), res["e2e"]["ms"]], dev)
-    nbytes, flops = prefill_work(cfg)
-    rf = roofline_of(nbytes, flops, ms, pk)
-    # the dominant kernel: most device time over the timed steps (library trace)
-    kernels = res["kernels"]
-    top = max(kernels, key=lambda k: kernels[k][1])
-    top_n, top_ms_total = kernels[top]
-    top_ms, = max_over_ranks([top_ms_total / top_n], dev)
-    top_gbs = nbytes / (top_ms * 1e-3) / 1e9
-    launches = sum(n for n, _ in kernels.values())
+    ms, roof = prefill_line(cfg, res, args.steps, pk, dev)
+    e2e_ms, = max_over_ranks([res["e2e"]["ms"]], dev)
+    launches = int(round(sum(e["launches_per_call"] for e in roof["per_kernel"].values()) * args.steps))
 
     extra = {}
     if not args.quick:
-        for c in (synth.VARLEN_32K, synth.LONG_128K):
-            n_steps = max(3, args.steps // 4)
+        for c in (synth.SINGLE_4K, synth.VARLEN_32K):
+            n_steps = args.steps
             r = time_prefill(c, n_steps, args.warmup, dev, flush, trace=True)
-            m = statistics.mean(r["ms"])
-            b_, f_ = prefill_work(c)
-            extra[c.name] = {"tokens_per_s": c.T / (m * 1e-3), "ms": m, **roofline_of(b_, f_, m, pk),
-                             "kernels_ms_per_step": {k: v[1] / n_steps for k, v in r["kernels"].items()}}
+            m, rl = prefill_line(c, r, n_steps, pk, dev)
+            extra[c.name] = {"tokens_per_s": c.T / (m * 1e-3), "ms": m, "roofline_frac": rl["frac"],
+                             "achieved_gbs": rl["achieved"] if rl["unit"] == "GB/s" else None,
+                             "flop_bound_frac": rl["flop_bound_frac"], "byte_bound_frac": rl["byte_bound_frac"],
+                             "per_kernel": rl["per_kernel"], "traffic": rl["traffic"]}
         dc = synth.DECODE_256
         r = time_decode(dc, args.steps, args.warmup, dev, flush)
-        m = statistics.mean(r["ms"])
+        m, = max_over_ranks([statistics.mean(r["ms"])], dev)
         extra[dc.name] = {"seqs_per_s": dc.batch / (m * 1e-3), "ms": m,
                           **roofline_of(dc.batch * DECODE_BYTES_PER_SEQ, dc.batch * DECODE_FLOPS_PER_SEQ, m, pk)}
     if rank != 0:
         return
-    cpu = cpu_baseline(cfg, args)
+    cpu = cpu_baseline(cfg)
     line = {
         "metric": METRIC,
         "value": world * cfg.T / (ms * 1e-3),
@@ -393,12 +444,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded; distributions of the workload definitions)",
         "config": headline_config(cfg, world),
-        "roofline": {"bound": "hbm", "achieved": top_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": top_gbs / pk["hbm_gbs"], "traffic": profiled_traffic(top),
-                     "peak_source": pk["source"] + " (burst copy)", "kernel": top,
-                     "kernel_ms": top_ms, "algorithmic_bytes_per_launch": nbytes,
-                     "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kernels.items()},
-                     "whole_call": {"achieved": rf["achieved_gbs"], "frac": rf["roofline_frac"]}},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": world * cfg.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"],
@@ -413,79 +459,110 @@ def run_ours(args):
 
 def headline_config(cfg, world):
     """The `config` of the headline line (both arms print the same one)."""
-    return {"workload": cfg.name, "tokens": cfg.T, "seqs": cfg.N, "h_qk": cfg.h_qk, "h_v": cfg.h_v,
-            "d_k": cfg.d_k, "d_v": cfg.d_v, "state": "fp32", "final_state": True,
+    return {"workload": cfg.name, "tokens": cfg.T, "seqs": cfg.N, "seq_len": max(cfg.lengths), "h_qk": cfg.h_qk,
+            "h_v": cfg.h_v, "d_k": cfg.d_k, "d_v": cfg.d_v, "state": "fp32", "init_state": cfg.init_std > 0,
+            "final_state": True,
             "l2": "flushed between steps (512 MiB write); e2e: not flushed, fresh inputs each step",
             "parallelism": f"replicas x{world}"}
 
 
-def profiled_traffic(kernel):
-    """DRAM bytes (read + write) per launch of `kernel` on the headline workload,
-    from the committed ncu summary, or None when that summary is missing or was
-    taken on another version of the kernel's source file."""
+def _source_digest():
+    """sha256 over the library's CUDA sources (csrc/*.cu, *.cuh, *.h), in name order."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"{kernel}_prefill_T4096.md")
+    csrc = os.path.join(ROOT, "gateddeltanet_layer_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()
+
+
+def profiled_traffic(cfg):
+    """DRAM bytes (read + write) of one call on workload `cfg`, whole call and
+    per kernel, from the committed ncu summary ``profiles/dram_<workload>.md``,
+    or None when that summary is missing or was taken on other library sources.
+    The summary holds lines ``traffic_bytes_per_call: N`` and
+    ``traffic_<kernel>: N`` (already scaled to the named workload)."""
+    path = os.path.join(ROOT, "profiles", f"dram_{cfg.name}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_bytes", "source_")))
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith(("traffic_", "sources_sha256")) and ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
     try:
-        src = fields["source_file"].strip()
-        digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()
-        if digest != fields["source_sha256"].strip():
+        if fields["sources_sha256"] != _source_digest():
             return None
-        return int(fields["traffic_bytes_per_launch"].strip())
-    except (KeyError, OSError, ValueError):
+        call = int(fields.pop("traffic_bytes_per_call"))
+    except (KeyError, ValueError):
         return None
+    kernels = {k[len("traffic_"):]: int(v) for k, v in fields.items() if k.startswith("traffic_")}
+    return {"call": call, "kernels": kernels}
 
 
 # ---------------------------------------------------------------------- CPU oracle
-def cpu_baseline(cfg, args, budget_chains=None):
+def _oracle_sample(cfg, n_chains):
+    """(sequence, head) chains of the first sequences of `cfg`, all heads of each."""
+    return [(n, h) for n in range(cfg.N) for h in range(cfg.h_v)][:n_chains]
+
+
+def _sample_tokens(cfg, chains):
+    """Tokens of the whole layer (all heads) the chains amount to."""
+    return float(sum(int(cfg.lengths[n]) for n, _ in chains)) / cfg.h_v
+
+
+def cpu_baseline(cfg, n_chains=64):
     """The fp64 oracle, as it is, on the host cores: a bounded sample of the
-    workload's (sequence, head) chains, scaled to tokens/s of the whole layer."""
+    workload's (sequence, head) chains, as tokens/s of the whole layer."""
     from oracle import oracle as ref
     cores = os.cpu_count() or 1
-    inp = synth.make_prefill(cfg)
-    n_chains = budget_chains or min(cfg.h_v * cfg.N, max(cores, 8))
-    chains = [(0, h) for h in range(n_chains)]
+    inp = inputs_of(cfg)
+    chains = _oracle_sample(cfg, n_chains)
     t0 = time.perf_counter()
     ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], chains=chains, threads=cores)
     dt = time.perf_counter() - t0
-    tokens_equiv = cfg.T * n_chains / cfg.h_v
-    return {"value": tokens_equiv / dt, "unit": "tokens/s", "cores": min(cores, n_chains), "kind": "oracle",
-            "sample": f"{n_chains} of {cfg.h_v * cfg.N} (sequence, head) chains of {cfg.name}, all {cfg.T} tokens "
-                      f"each, {dt:.2f} s wall"}
+    return {"value": _sample_tokens(cfg, chains) / dt, "unit": "tokens/s", "cores": min(cores, len(chains)),
+            "kind": "oracle",
+            "sample": f"{len(chains)} of {cfg.h_v * cfg.N} (sequence, head) chains of {cfg.name} (all tokens of "
+                      f"each), {dt:.2f} s wall on {min(cores, len(chains))} threads; tokens/s of the whole layer = "
+                      f"the chains' tokens / {cfg.h_v} heads / wall time"}
 
 
 def run_reference(args):
-    """The reference arm: the fp64 CPU oracle, timed on the host cores."""
+    """The reference arm: the fp64 CPU oracle, timed on the host cores.  Each
+    step runs one chain per host core of the headline workload (a bounded
+    sample of it); ms_per_step is that step's measured wall time and value the
+    tokens/s of the whole layer the sample amounts to."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    cfg = synth.SINGLE_4K
+    cfg = HEADLINE
     from oracle import oracle as ref
     ref.build()
     cores = os.cpu_count() or 1
     inp = synth.make_prefill(cfg)
-    n_chains = min(cfg.h_v, cores)
-    chains = [(0, h) for h in range(n_chains)]
-    for _ in range(min(args.warmup, 1)):
-        ref.prefill(inp, inp["cu_seqlens"], chains=chains[:1], threads=1)
+    chains = _oracle_sample(cfg, min(cores, cfg.h_v * cfg.N))
+    for _ in range(args.warmup):
+        ref.prefill(inp, inp["cu_seqlens"], chains=chains, threads=cores)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
         ref.prefill(inp, inp["cu_seqlens"], chains=chains, threads=cores)
         times.append(time.perf_counter() - t0)
     dt = statistics.mean(times)
-    value = cfg.T * n_chains / cfg.h_v / dt
-    sample = f"{n_chains} of {cfg.h_v} (sequence, head) chains of {cfg.name} per step, all {cfg.T} tokens each"
+    value = _sample_tokens(cfg, chains) / dt
+    sample = (f"{len(chains)} of {cfg.h_v * cfg.N} (sequence, head) chains of {cfg.name} per step, all tokens of "
+              f"each; tokens/s of the whole layer = the chains' tokens / {cfg.h_v} heads / step time")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 * cfg.h_v / n_chains,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)", "config": headline_config(cfg, int(os.environ.get("WORLD_SIZE", "1"))),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, n_chains), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, len(chains)), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -499,7 +576,7 @@ def run_case(args):
     gdn.library()
     dev = torch.device("cuda", 0)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    cfg = synth.CONFIGS[args.case]
+    cfg = {**synth.CONFIGS, **PROFILE_CASES}[args.case]
     if isinstance(cfg, synth.DecodeConfig):
         r = time_decode(cfg, args.steps, args.warmup, dev, flush)
     else:
@@ -514,7 +591,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
-    ap.add_argument("--case", choices=sorted(synth.CONFIGS), help="run only this workload's GPU call")
+    ap.add_argument("--case", choices=sorted({**synth.CONFIGS, **PROFILE_CASES}),
+                    help="run only this workload's GPU call")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -15,7 +15,10 @@
 // cannot use the array's name as a device address: it names a host-side
 // stand-in.  The device address is looked up once per device with
 // cudaGetSymbolAddress, with that device current, on the first call made on
-// it; that first call should therefore come before any stream capture.
+// it; that first call should therefore come before any stream capture.  The
+// address is kept for the life of the process: after a cudaDeviceReset() of a
+// device the kept address is stale, so a process that resets a device must not
+// call this entry point on that device again.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -66,6 +66,7 @@ def test_reference_arm_prints_one_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
-    assert d["config"]["workload"] == "prefill_T4096"
+    assert d["config"]["workload"] == "prefill_long_T131072"
+    assert d["ms_per_step"] > 0 and "chains" in d["cpu_baseline"]["sample"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0

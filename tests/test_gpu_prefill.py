@@ -1,16 +1,18 @@
 """GPU parity of gdn_prefill against the fp64 oracle.
 
-Small cases run the oracle on every chain; the full-size workloads run the
-whole GPU call exactly as the benchmark launches it and compare the chains the
-oracle computes (sampled (sequence, head) pairs, every token and the final
-state of each).
+Every case compares every (sequence, value head) chain: all of `out` and all
+of `final_state`.  The full-size workloads run the whole GPU call exactly as
+the benchmark launches it and run the oracle sequence by sequence on every
+host core.
 """
+import os
+
 import numpy as np
 import pytest
 
 from gateddeltanet_layer_gb300 import synth
 from oracle import oracle as ref
-from tests.helpers import parity, to_torch
+from tests.helpers import Parity, parity, to_torch
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -34,10 +36,10 @@ def run_gpu(inp, bf16, *, workspace=None, in_place=False):
     return out.float().cpu().numpy(), fs.cpu().numpy()
 
 
-def check(inp, cfg_dtype, chains=None, **kw):
+def check(inp, cfg_dtype, **kw):
     bf16 = cfg_dtype == "bf16"
     y, fs = run_gpu(inp, bf16, **kw)
-    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], chains=chains)
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"])
     parity(y, r["y"], cfg_dtype, "out")
     parity(fs, r["final_state"], cfg_dtype, "final_state")
     return y, fs, r
@@ -91,43 +93,55 @@ def test_small_cases(case):
 def test_state_pass_chain_counts(lengths, h_qk, h_v):
     """Few and many (sequence, value head) chains (the state pass runs a ring
     of operand sets at one CTA per SM for few chains, two CTAs per SM
-    otherwise), sampled chains against the oracle."""
+    otherwise), every chain against the oracle."""
     cfg = synth.scaled(synth.VARLEN_32K, lengths=lengths, h_qk=h_qk, h_v=h_v, init_std=0.02, seed=21)
+    check(synth.make_prefill(cfg), "bf16")
+
+
+def _sequence(inp, cu, n):
+    """The inputs of sequence n alone (tokens [cu[n], cu[n+1])), as a one-sequence workload."""
+    s0, s1 = int(cu[n]), int(cu[n + 1])
+    one = dict(inp)
+    for key in ("x_q", "x_k", "x_v", "z", "a", "b"):
+        one[key] = inp[key][s0:s1]
+    one["cu_seqlens"] = np.array([0, s1 - s0], dtype=np.int32)
+    one["init_state"] = None if inp["init_state"] is None else inp["init_state"][n:n + 1]
+    return one
+
+
+def check_every_chain(cfg):
+    """The whole GPU call, exactly as the benchmark launches it, against the
+    oracle on every (sequence, value head) chain: all of `out` and all of
+    `final_state`, element by element, one sequence at a time on every host core."""
     inp = synth.make_prefill(cfg)
-    chains = [(n, h) for n in range(cfg.N) for h in (0, 5, h_v - 1) if h < h_v]
     y, fs = run_gpu(inp, True)
-    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], chains=chains)
     cu = inp["cu_seqlens"]
-    for n, h in chains:
-        sl = slice(cu[n], cu[n + 1])
-        if cu[n + 1] > cu[n]:
-            parity(y[sl, h], r["y"][sl, h], "bf16", f"out chain {(n, h)}")
-        parity(fs[n, h], r["final_state"][n, h], "bf16", f"final_state chain {(n, h)}")
-
-
-def _sample_chains(cfg, picks):
-    return [(n, h) for n, h in picks if n < cfg.N and h < cfg.h_v]
+    py, pf = Parity("bf16", f"{cfg.name} out"), Parity("bf16", f"{cfg.name} final_state")
+    for n in range(cfg.N):
+        one = _sequence(inp, cu, n)
+        r = ref.prefill(one, one["cu_seqlens"], one["init_state"], threads=os.cpu_count())
+        py.add(y[cu[n]:cu[n + 1]], r["y"])
+        pf.add(fs[n:n + 1], r["final_state"])
+    assert py.count == y.size and pf.count == fs.size
+    print(py.summary())
+    print(pf.summary())
+    py.check()
+    pf.check()
 
 
 @pytest.mark.slow
 def test_full_single_4k():
-    cfg = synth.SINGLE_4K
-    check(synth.make_prefill(cfg), "bf16", chains=_sample_chains(cfg, [(0, 0), (0, 1), (0, 17), (0, 31)]))
+    check_every_chain(synth.SINGLE_4K)
 
 
 @pytest.mark.slow
 def test_full_varlen_32k():
-    cfg = synth.VARLEN_32K
-    lengths = np.array(cfg.lengths)
-    longest, shortest = int(lengths.argmax()), int(lengths.argmin())
-    picks = [(longest, 0), (longest, 31), (shortest, 5), (shortest, 6), (cfg.N - 1, 30), (3, 14)]
-    check(synth.make_prefill(cfg), "bf16", chains=_sample_chains(cfg, picks))
+    check_every_chain(synth.VARLEN_32K)
 
 
 @pytest.mark.slow
 def test_full_long_128k():
-    cfg = synth.LONG_128K
-    check(synth.make_prefill(cfg), "bf16", chains=_sample_chains(cfg, [(0, 0), (7, 13), (15, 31)]))
+    check_every_chain(synth.LONG_128K)
 
 
 def test_deterministic_and_workspace_equivalent():

@@ -9,6 +9,8 @@ against gdn_prefill (which uses a caller workspace) on the same inputs, within
 the parity tolerances of the other tests.  This file is collected last so that
 a failure here stops a `-x` run only after every other test has run.
 """
+import ctypes
+
 import pytest
 
 from gateddeltanet_layer_gb300 import synth
@@ -24,6 +26,28 @@ def _inputs(cfg):
             t["norm_w"], t["cu_seqlens"], t.get("init_state"))
 
 
+# Driver attribute of a memory pool: the most memory of the pool in use at once
+# since the watermark was last reset to zero (CU_MEMPOOL_ATTR_USED_MEM_HIGH).
+_USED_MEM_HIGH = 8
+
+
+def _default_pool():
+    """The device's default stream-ordered memory pool (where cudaMallocAsync
+    takes memory), through the driver library, which every GPU process has."""
+    cu = ctypes.CDLL("libcuda.so.1")
+    dev = ctypes.c_int(0)
+    assert cu.cuDeviceGet(ctypes.byref(dev), torch.cuda.current_device()) == 0
+    pool = ctypes.c_void_p()
+    assert cu.cuDeviceGetDefaultMemPool(ctypes.byref(pool), dev) == 0
+    return cu, pool
+
+
+def _pool_used_high(cu, pool) -> int:
+    v = ctypes.c_uint64(0)
+    assert cu.cuMemPoolGetAttribute(pool, _USED_MEM_HIGH, ctypes.byref(v)) == 0
+    return v.value
+
+
 def test_noalloc_matches_prefill_on_two_calls_in_a_row():
     import gateddeltanet_layer_gb300 as gdn
     gdn.library()
@@ -32,12 +56,24 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row():
     args = [_inputs(cfg) for cfg in cases]
     refs = [gdn.prefill(*a) for a in args]          # the existing entry point, caller workspace
     torch.cuda.synchronize()
+    outs = [(torch.empty_like(ro), torch.empty_like(rf)) for ro, rf in refs]
+    # gdn_prefill takes its own workspace from the default pool; with every such
+    # call complete, no pool memory is in use: reset the watermark to zero, so
+    # any pool allocation made by the calls below would raise it again
+    cu, pool = _default_pool()
+    torch.cuda.synchronize()
+    assert cu.cuMemPoolSetAttribute(pool, _USED_MEM_HIGH, ctypes.byref(ctypes.c_uint64(0))) == 0
+    assert _pool_used_high(cu, pool) == 0
     got = []
-    for a, (ro, rf) in zip(args, refs):             # two gdn_prefill_noalloc calls back to back
-        out, fs = torch.empty_like(ro), torch.empty_like(rf)
+    for a, (out, fs) in zip(args, outs):            # two gdn_prefill_noalloc calls back to back
         gdn.prefill_noalloc(*a, out=out, final_state=fs)
         got.append((out, fs))
     torch.cuda.synchronize()
+    assert _pool_used_high(cu, pool) == 0, "gdn_prefill_noalloc took memory from the stream-ordered pool"
+    # the control: gdn_prefill without a workspace does take pool memory, so the watermark sees it
+    gdn.prefill(*args[0])
+    torch.cuda.synchronize()
+    assert _pool_used_high(cu, pool) > 0
     for cfg, (ro, rf), (out, fs) in zip(cases, refs, got):
         parity(out.float().cpu().numpy(), ro.float().cpu().numpy(), cfg.dtype, f"noalloc out {cfg.lengths}")
         parity(fs.cpu().numpy(), rf.cpu().numpy(), cfg.dtype, f"noalloc final_state {cfg.lengths}")
