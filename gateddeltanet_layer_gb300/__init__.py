@@ -12,7 +12,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["prefill", "decode_step", "decode_step_slots", "conv_cache_from_prefill", "prefill_workspace_bytes",
+__all__ = ["prefill", "prefill_carry", "decode_step", "decode_step_slots", "conv_cache_from_prefill", "prefill_workspace_bytes",
            "workspace_status", "library", "GdnError", "STATUS", "prefill_noalloc", "NOALLOC_SCRATCH_BYTES",
            "trace_enable", "trace_read"]
 
@@ -55,6 +55,8 @@ def library() -> ctypes.CDLL:
             lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
             lib.gdn_prefill.argtypes = [dp] + [_vp] * 15 + [ctypes.c_size_t, _vp]
             lib.gdn_prefill.restype = ctypes.c_int
+            lib.gdn_prefill_carry.argtypes = [dp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
+            lib.gdn_prefill_carry.restype = ctypes.c_int
             lib.gdn_decode_step.argtypes = [dp] + [_vp] * 14
             lib.gdn_decode_step.restype = ctypes.c_int
             lib.gdn_workspace_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
@@ -169,6 +171,54 @@ def prefill(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_s
                          _stream_handle(stream, q.device))
     _check(st, "gdn_prefill")
     return out, final_state
+
+
+def prefill_carry(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state=None, init_conv=None,
+                  *, out=None, final_state=None, final_conv=None, workspace=None, stream=None):
+    """``gdn_prefill_carry``: ``prefill`` that continues each sequence from a
+    carried conv history ``init_conv`` ([N, Cc, 3], stream dtype, the raw inputs
+    of the three tokens before the sequence, oldest first; None = zeros) as well
+    as ``init_state``, and returns the conv history it leaves.  Consecutive
+    segments of a sequence, each started from the previous one's final state
+    and final conv history, give the result of one call over the whole
+    sequence.  Returns (out, final_state, final_conv)."""
+    torch = _torch()
+    lib = library()
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("z", z)):
+        _req(t, name, dt)
+    for name, t in (("conv_w", conv_w), ("A_log", A_log), ("dt_bias", dt_bias), ("norm_w", norm_w)):
+        _req(t, name, torch.float32)
+    _req(cu_seqlens, "cu_seqlens", torch.int32)
+    N = cu_seqlens.numel() - 1
+    d = dims_of(q, v, N)
+    T, h_v, d_v = v.shape
+    Cc = 2 * d.h_qk * d.d_k + h_v * d_v
+    if init_state is not None:
+        _req(init_state, "init_state", torch.float32)
+    if init_conv is not None:
+        _req(init_conv, "init_conv", dt)
+        if tuple(init_conv.shape) != (N, Cc, 3):
+            raise ValueError(f"init_conv must be [{N}, {Cc}, 3]")
+    if out is None:
+        out = torch.empty((T, h_v, d_v), dtype=dt, device=q.device)
+    _req(out, "out", dt)
+    if final_state is None:
+        final_state = torch.empty((N, h_v, d.d_k, d_v), dtype=torch.float32, device=q.device)
+    _req(final_state, "final_state", torch.float32)
+    if final_conv is None:
+        final_conv = torch.empty((N, Cc, 3), dtype=dt, device=q.device)
+    _req(final_conv, "final_conv", dt)
+    ws_bytes = 0
+    if workspace is not None:
+        _req(workspace, "workspace", torch.uint8)
+        ws_bytes = workspace.numel()
+    st = lib.gdn_prefill_carry(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z),
+                               _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(cu_seqlens),
+                               _ptr(init_state), _ptr(init_conv), _ptr(out), _ptr(final_state), _ptr(final_conv),
+                               _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    _check(st, "gdn_prefill_carry")
+    return out, final_state, final_conv
 
 
 def decode_step(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, conv_state, state, *, out=None,

@@ -193,9 +193,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
 }
 
 // Conv cache after a prefill: for sequence n and conv channel c, the raw
-// inputs of its last three tokens, oldest first, zero where the sequence is
-// shorter (the prefill's conv sees zeros before a sequence start).  One thread
-// per (sequence, channel); an invalid cu_seqlens range gives zeros.
+// inputs of its last three tokens, oldest first; where the sequence is shorter
+// than three tokens, the carried history before its start (init_conv) or
+// zeros.  One thread per (sequence, channel), which reads everything it needs
+// before it writes (so the cache may overwrite the history in place); an
+// invalid cu_seqlens range gives zeros.
 template <typename IO>
 __global__ void __launch_bounds__(256) conv_cache_kernel(ConvCacheParams p) {
   const int n = blockIdx.y;
@@ -213,12 +215,16 @@ __global__ void __launch_bounds__(256) conv_cache_kernel(ConvCacheParams p) {
   } else {
     src = static_cast<const IO *>(p.v); stride = (size_t)p.h_v * p.d_v; col = ch - 2 * cq;
   }
-  IO *dst = static_cast<IO *>(p.conv_cache) + ((size_t)n * Cc + ch) * 3;
+  const IO *hist = p.init_conv ? static_cast<const IO *>(p.init_conv) + ((size_t)n * Cc + ch) * 3 : nullptr;
+  IO val[3];
 #pragma unroll
   for (int j = 0; j < 3; ++j) {
-    const int t = s1 - 3 + j;
-    dst[j] = (ok && t >= s0) ? src[(size_t)t * stride + col] : from_f<IO>(0.0f);
+    const int t = s1 - 3 + j;  // >= s0 - 3: history entry t - s0 + 3 when t < s0
+    val[j] = !ok ? from_f<IO>(0.0f) : t >= s0 ? src[(size_t)t * stride + col] : hist ? hist[t - s0 + 3] : from_f<IO>(0.0f);
   }
+  IO *dst = static_cast<IO *>(p.conv_cache) + ((size_t)n * Cc + ch) * 3;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) dst[j] = val[j];
 }
 
 }  // namespace

@@ -42,11 +42,17 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *d) {
   return bytes;
 }
 
-int gdn_prefill(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
-                const void *b, const void *z, const float *conv_w, const float *A_log,
-                const float *dt_bias, const float *norm_w, const int32_t *cu_seqlens,
-                const float *init_state, void *out, float *final_state, void *workspace,
-                size_t ws_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// gdn_prefill and gdn_prefill_carry: validation, workspace, the kernels, and
+// (when final_conv is given) the conv cache the call leaves.
+int prefill_impl(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a, const void *b,
+                 const void *z, const float *conv_w, const float *A_log, const float *dt_bias,
+                 const float *norm_w, const int32_t *cu_seqlens, const float *init_state, const void *init_conv,
+                 void *out, float *final_state, void *final_conv, void *workspace, size_t ws_bytes,
+                 void *stream) {
   int st = check_dims(d);
   if (st != GDN_OK) return st;
   if (d->num_seqs <= 0) return GDN_ERR_INVALID_ARG;
@@ -66,14 +72,18 @@ int gdn_prefill(const gdn_dims *d, const void *q, const void *k, const void *v, 
     if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return GDN_ERR_CUDA;
     owned = true;
   }
-  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) {
+    if (owned) cudaFreeAsync(ws, s);
+    return GDN_ERR_CUDA;
+  }
 
   gdn::PrefillParams p{};
   p.T = d->num_tokens; p.N = d->num_seqs; p.h_qk = d->h_qk; p.h_v = d->h_v;
   p.d_k = d->d_k; p.d_v = d->d_v;
   p.q = q; p.k = k; p.v = v; p.a = a; p.b = b; p.z = z;
   p.conv_w = conv_w; p.A_log = A_log; p.dt_bias = dt_bias; p.norm_w = norm_w;
-  p.cu_seqlens = cu_seqlens; p.init_state = init_state; p.out = out; p.final_state = final_state;
+  p.cu_seqlens = cu_seqlens; p.init_state = init_state; p.init_conv = init_conv;
+  p.out = out; p.final_state = final_state;
   p.status = static_cast<int *>(ws);
   p.ws = static_cast<uint8_t *>(ws) + kStatusBytes;
   p.ws_bytes = need - kStatusBytes;
@@ -83,8 +93,36 @@ int gdn_prefill(const gdn_dims *d, const void *q, const void *k, const void *v, 
     e = gdn::launch_prefill_tc(p, s);
   else
     e = gdn::launch_prefill_simt(p, d->io_dtype == GDN_BF16, s);
+  if (e == cudaSuccess && final_conv) {  // after every kernel that reads init_conv (stream order)
+    gdn::ConvCacheParams c{};
+    c.T = d->num_tokens; c.N = d->num_seqs; c.h_qk = d->h_qk; c.h_v = d->h_v; c.d_k = d->d_k; c.d_v = d->d_v;
+    c.q = q; c.k = k; c.v = v; c.cu_seqlens = cu_seqlens; c.init_conv = init_conv; c.conv_cache = final_conv;
+    e = gdn::launch_conv_cache(c, d->io_dtype == GDN_BF16, s);
+  }
   if (owned) cudaFreeAsync(ws, s);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_prefill(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
+                const void *b, const void *z, const float *conv_w, const float *A_log,
+                const float *dt_bias, const float *norm_w, const int32_t *cu_seqlens,
+                const float *init_state, void *out, float *final_state, void *workspace,
+                size_t ws_bytes, void *stream) {
+  return prefill_impl(d, q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state, nullptr, out,
+                      final_state, nullptr, workspace, ws_bytes, stream);
+}
+
+int gdn_prefill_carry(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
+                      const void *b, const void *z, const float *conv_w, const float *A_log,
+                      const float *dt_bias, const float *norm_w, const int32_t *cu_seqlens,
+                      const float *init_state, const void *init_conv, void *out, float *final_state,
+                      void *final_conv, void *workspace, size_t ws_bytes, void *stream) {
+  return prefill_impl(d, q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state, init_conv, out,
+                      final_state, final_conv, workspace, ws_bytes, stream);
 }
 
 int gdn_decode_step(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,

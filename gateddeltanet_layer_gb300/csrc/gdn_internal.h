@@ -12,6 +12,7 @@ struct PrefillParams {
   const float *conv_w, *A_log, *dt_bias, *norm_w;
   const int32_t *cu_seqlens;
   const float *init_state;
+  const void *init_conv;  // [N, Cc, 3] io dtype: raw inputs before each sequence start, oldest first; may be null
   void *out;
   float *final_state;
   int *status;       // device status word (workspace), may be null
@@ -35,6 +36,7 @@ struct ConvCacheParams {
   int T, N, h_qk, h_v, d_k, d_v;
   const void *q, *k, *v;
   const int32_t *cu_seqlens;
+  const void *init_conv; // [N, Cc, 3] history before each sequence start, or null (zeros); may equal conv_cache
   void *conv_cache;      // [N, Cc, 3]
 };
 

@@ -66,11 +66,13 @@ __global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
   const float dtb = p.dt_bias[h];
   const float scale = rsqrtf((float)dk);
   const int nch = 2 * dk + dv;
+  const int Cc = 2 * h_qk * dk + h_v * dv;
+  const IO *__restrict__ hist = static_cast<const IO *>(p.init_conv);  // conv history, or null (zeros)
 
   for (int t0 = s0; t0 < s1; t0 += kTB) {
     const int nt = min(kTB, s1 - t0);
     __syncthreads();  // the previous batch's buffers are consumed
-    // conv (width 4, zero history before s0) + SiLU
+    // conv (width 4; before s0 the carried history, or zeros) + SiLU
     for (int idx = threadIdx.x; idx < nt * nch; idx += blockDim.x) {
       const int tt = idx / nch, c = idx % nch;
       const int t = t0 + tt;
@@ -93,7 +95,10 @@ __global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int tau = t - 3 + j;
-        if (tau >= s0) pre = fmaf(p.conv_w[ch * 4 + j], to_f(src[(size_t)tau * stride]), pre);
+        if (tau >= s0)
+          pre = fmaf(p.conv_w[ch * 4 + j], to_f(src[(size_t)tau * stride]), pre);
+        else if (hist)  // the carried input of token tau = s0 - 3 + m sits at m (oldest first)
+          pre = fmaf(p.conv_w[ch * 4 + j], to_f(hist[((size_t)n * Cc + ch) * 3 + (tau - s0 + 3)]), pre);
       }
       *dst = silu_f(pre);
     }

@@ -275,15 +275,24 @@ constexpr uint32_t kIdN256 = tc::idesc_f16(128, 256);
 
 // Raw rows for conv(4) of 8 output rows r0 .. r0+7 of the chunk: input rows
 // r0-3 .. r0+7, 4 channels (x points at the first channel of token 0; bf16 row
-// pitch `stride` elements) as packed bf16; rows before the sequence start or
-// past the chunk's end are 0.
+// pitch `stride` elements) as packed bf16; rows past the chunk's end are 0, and
+// so are the (at most three) rows before the sequence start unless `hist`
+// points at the carried conv history of the 4 channels ([channel][3] bf16,
+// oldest first: token s0 - 3 + m at m).
 __device__ __forceinline__ void load_rows(const __nv_bfloat16 *x, size_t stride, int t0, int s0, int Lc, int r0,
-                                          uint2 (&xr)[11]) {
+                                          const __nv_bfloat16 *hist, uint2 (&xr)[11]) {
 #pragma unroll
   for (int rr = 0; rr < 11; ++rr) {
     const int row = r0 - 3 + rr;
     const int t = t0 + row;
-    xr[rr] = (t >= s0 && row < Lc) ? *reinterpret_cast<const uint2 *>(x + (size_t)t * stride) : make_uint2(0u, 0u);
+    if (t >= s0) {
+      xr[rr] = row < Lc ? *reinterpret_cast<const uint2 *>(x + (size_t)t * stride) : make_uint2(0u, 0u);
+    } else if (hist) {  // t >= t0 - 3 >= s0 - 3
+      const uint16_t *h = reinterpret_cast<const uint16_t *>(hist) + (t - s0 + 3);
+      xr[rr] = make_uint2((uint32_t)h[0] | ((uint32_t)h[3] << 16), (uint32_t)h[6] | ((uint32_t)h[9] << 16));
+    } else {
+      xr[rr] = make_uint2(0u, 0u);
+    }
   }
 }
 // conv(4) + SiLU of the rows of load_rows, channels from conv_w row `ch`;
@@ -360,6 +369,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 
   const int4 info = ws.chunk_info[g];
   const int t0 = info.y, s0 = info.z, Lc = info.w;
+  // conv history of channel ch for this thread's 4 channels (only the first chunk of a sequence reads it)
+  const size_t conv_ch = 2 * (size_t)h_qk * kD + (size_t)h_v * kD;
+  const __nv_bfloat16 *hist0 =
+      (p.init_conv && t0 == s0) ? static_cast<const __nv_bfloat16 *>(p.init_conv) + (size_t)info.x * conv_ch * 3 : nullptr;
+  auto hist = [&](int ch) { return hist0 ? hist0 + (size_t)ch * 3 : nullptr; };
 
   // per value head vv: G at sG[256 vv], gamma at +64, beta at +128, decay-to-end at +192
   float *sG = reinterpret_cast<float *>(sm + P_VEC);
@@ -441,8 +455,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     uint2 xrk[11];
     {  // both heads' rows in flight at once
       uint2 xrq[11];
-      load_rows(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, xrq);
-      load_rows(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, xrk);
+      load_rows(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(hq * kD + c0), xrq);
+      load_rows(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(h_qk * kD + hq * kD + c0), xrk);
       if (rep > 1) prefetch_v(1);
       conv_silu(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
     }
@@ -507,10 +521,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     {
       uint2 xr[11];
       float y[8][4];
-      load_rows(xv + (size_t)(hq * rep + grp) * kD + c0, v_stride, t0, s0, Lc, r0, xr);
+      load_rows(xv + (size_t)(hq * rep + grp) * kD + c0, v_stride, t0, s0, Lc, r0,
+                hist(2 * h_qk * kD + (hq * rep + grp) * kD + c0), xr);
       conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + grp) * kD + c0, Lc, r0, y);
       // the second head's rows in flight over the first head's stores and the wait below
-      if (nh > 1) load_rows(xv + (size_t)(hq * rep + grp + 1) * kD + c0, v_stride, t0, s0, Lc, r0, xr);
+      if (nh > 1)
+        load_rows(xv + (size_t)(hq * rep + grp + 1) * kD + c0, v_stride, t0, s0, Lc, r0,
+                  hist(2 * h_qk * kD + (hq * rep + grp + 1) * kD + c0), xr);
       if (grp + 2 < rep) {
         prefetch_v(grp + 2);
         if (grp + 3 < rep) prefetch_v(grp + 3);

@@ -127,6 +127,43 @@ GDN_API int gdn_prefill(const gdn_dims *dims, const void *q, const void *k, cons
                 size_t ws_bytes, void *stream);
 
 /*
+ * Prefill that carries the conv history across calls: gdn_prefill plus an
+ * initial conv history in and the conv history the call leaves out.
+ *
+ * The pages run the layer under context parallelism ("[Qwen3.5 MoE] Add
+ * hybrid decoder model (GatedDeltaNet + full attention + MoE)", Summary:
+ * parallelize.py bullet, TP/FSDP/CP/EP with a DTensor-safe depthwise conv1d;
+ * "feat(models): dense Qwen3.5 custom attention", Summary: ring / Ulysses CP
+ * substitution, and its E2E notes: CP hooks at cp = 2), where one sequence is
+ * split into consecutive segments on different ranks.  The recurrence carries
+ * across a split through init_state / final_state; the width-4 causal conv
+ * also reads the three raw inputs before a segment's first token, which a
+ * plain gdn_prefill takes as zeros.  With this entry point, running a sequence
+ * as segments [t_0, t_1), [t_1, t_2), ... -- each call's init_state and
+ * init_conv the previous call's final_state and final_conv -- gives the same
+ * result as one call over the whole sequence (and the same for long prompts
+ * prefilled piece by piece).
+ *
+ * init_conv   io_dtype [N, Cc, 3] or NULL (= zeros, a plain gdn_prefill): per
+ *             sequence and conv channel (order [q | k | v], as conv_w) the raw
+ *             inputs of the three tokens before the sequence's first token,
+ *             oldest first -- the layout of the decode conv cache.
+ * final_conv  io_dtype [N, Cc, 3] or NULL (= not returned): the same for the
+ *             three tokens after the call (for a sequence shorter than three
+ *             tokens, partly taken from init_conv).  It may equal init_conv
+ *             (written after every read of it); it is also exactly the
+ *             conv_state gdn_decode_step continues from.
+ * Every other argument, the workspace and the errors are those of
+ * gdn_prefill.  Returns a gdn_status.
+ */
+GDN_API int gdn_prefill_carry(const gdn_dims *dims, const void *q, const void *k, const void *v,
+                              const void *a, const void *b, const void *z, const float *conv_w,
+                              const float *A_log, const float *dt_bias, const float *norm_w,
+                              const int32_t *cu_seqlens, const float *init_state, const void *init_conv,
+                              void *out, float *final_state, void *final_conv, void *workspace,
+                              size_t ws_bytes, void *stream);
+
+/*
  * Decode step: one new token for each of B = dims->num_tokens independent
  * sequences, against a carried state; the state and the conv cache are
  * updated in place.
@@ -206,7 +243,10 @@ GDN_API int gdn_workspace_status(void *workspace, void *stream, int *device_stat
  *  - The array is a device global of the library: every GPU that loads the
  *    library holds it until the process exits.  The first call on a device
  *    looks up its device address (cudaGetSymbolAddress, on the current
- *    device); make that first call before any stream capture.
+ *    device) and keeps it for later calls; make that first call before any
+ *    stream capture.  A cudaDeviceReset() of that device invalidates the kept
+ *    address (the reset context reloads the library's module elsewhere): a
+ *    process that resets a device must not call this entry point on it again.
  *  - Every call on a device shares the one array and leaves its contents
  *    behind; each call clears the part that must start at zero.  Calls whose
  *    kernels overlap on the GPU (different streams, or different host threads

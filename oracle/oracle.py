@@ -192,10 +192,21 @@ def _pool_map(fn, items, threads):
         return list(ex.map(fn, items))
 
 
-def prefill(inp: dict, cu_seqlens, init_state=None, chains=None, threads=None, **kw):
+def _hist_of(conv, h_qk, h_v, dk, dv, hv):
+    """The conv history of value head hv from a [Cc, 3] conv cache (raw inputs
+    of the three tokens before, oldest first): dict of q, k [3, dk] and v [3, dv]."""
+    hq = hv // (h_v // h_qk)
+    qc, kc, vc = _channels(h_qk, h_v, dk, dv, hq, hv)
+    c = _f64(conv)
+    return {"q": c[qc].T, "k": c[kc].T, "v": c[vc].T}
+
+
+def prefill(inp: dict, cu_seqlens, init_state=None, chains=None, threads=None, init_conv=None, **kw):
     """Prefill over packed sequences.
 
-    cu_seqlens [N+1] (int); init_state [N, h_v, dk, dv] or None.
+    cu_seqlens [N+1] (int); init_state [N, h_v, dk, dv] or None; init_conv
+    [N, Cc, 3] (the raw inputs of the three tokens before each sequence, oldest
+    first, channels as conv_w) or None (= zeros: a sequence start).
     chains: list of (n, hv) to compute (None = all).  Returns dict with
     y [T, h_v, dv] and o [T, h_v, dv] (NaN outside the computed chains) and
     final_state [N, h_v, dk, dv] (NaN for chains not computed).
@@ -210,10 +221,13 @@ def prefill(inp: dict, cu_seqlens, init_state=None, chains=None, threads=None, *
     o = np.full((T, h_v, dv), np.nan)
     fs = np.full((N, h_v, dk, dv), np.nan)
 
+    h_qk = inp["x_q"].shape[1]
+
     def run(nh):
         n, h = nh
         H0 = None if init_state is None else init_state[n, h]
-        return nh, chain(inp, int(cu[n]), int(cu[n + 1]), h, H0, **kw)
+        hist = None if init_conv is None else _hist_of(init_conv[n], h_qk, h_v, dk, dv, h)
+        return nh, chain(inp, int(cu[n]), int(cu[n + 1]), h, H0, hist, **kw)
 
     for (n, h), r in _pool_map(run, list(chains), threads):
         y[cu[n]:cu[n + 1], h] = r["y"]
@@ -251,10 +265,11 @@ def decode_step(inp: dict, conv_state, state, threads=None, **kw):
     return dict(y=y, state=new_state, conv_state=new_cs)
 
 
-def conv_cache_after_prefill(inp: dict, cu_seqlens):
+def conv_cache_after_prefill(inp: dict, cu_seqlens, init_conv=None):
     """The decode conv cache [N, Cc, 3] a prefill leaves: per sequence and conv
     channel ([q | k | v], as conv_w) the raw inputs of its last three tokens,
-    oldest first, zero before the sequence start (the zero conv history of the
+    oldest first; before the sequence start the carried history ``init_conv``
+    ([N, Cc, 3], token s0 - 3 + m at m) or zero (the zero conv history of a
     prefill, reading of the depthwise-conv bullet of "[Qwen3.5 MoE] Add hybrid
     decoder model ...", Summary).  Plain slicing, written from that definition."""
     cu = np.asarray(cu_seqlens, dtype=np.int64)
@@ -269,4 +284,6 @@ def conv_cache_after_prefill(inp: dict, cu_seqlens):
             t = cu[n + 1] - 3 + j
             if t >= cu[n]:
                 cache[n, :, j] = x_all[t]
+            elif init_conv is not None:
+                cache[n, :, j] = np.asarray(init_conv[n], np.float64)[:, t - cu[n] + 3]
     return cache

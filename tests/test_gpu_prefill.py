@@ -207,3 +207,66 @@ def test_kernel_trace_counts_each_launch():
         assert n == 2 and ms > 0, (name, n, ms)
     run_gpu(inp, True)
     assert gdn.trace_read() == {}
+
+
+def _segment(inp, cu, bounds):
+    """Tokens [bounds[n][0], bounds[n][1]) of every sequence n, as one packed workload."""
+    idx = np.concatenate([np.arange(cu[n] + b0, cu[n] + b1) for n, (b0, b1) in enumerate(bounds)]).astype(np.int64)
+    seg = {k_: (v_[idx] if k_ in ("x_q", "x_k", "x_v", "z", "a", "b") else v_) for k_, v_ in inp.items()}
+    seg["cu_seqlens"] = np.concatenate([[0], np.cumsum([b1 - b0 for b0, b1 in bounds])]).astype(np.int32)
+    return seg, idx
+
+
+def _run_segments(inp, cuts, dtype, in_place=False):
+    """gdn_prefill_carry over consecutive segments of every sequence, each call
+    started from the previous call's final state and final conv history.
+    Returns the outputs of the token indices, the last final state and conv."""
+    gdn = _gdn()
+    bf16 = dtype == "bf16"
+    cu = inp["cu_seqlens"].astype(np.int64)
+    state = None if inp["init_state"] is None else to_torch({"init_state": inp["init_state"]}, bf16)["init_state"]
+    conv = None
+    ys, idxs = [], []
+    for s in range(len(cuts[0]) - 1):
+        seg, idx = _segment(inp, cu, [(c[s], c[s + 1]) for c in cuts])
+        t = to_torch(seg, bf16)
+        kw = {"final_conv": conv} if (in_place and conv is not None) else {}
+        out, state, conv = gdn.prefill_carry(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"],
+                                             t["A_log"], t["dt_bias"], t["norm_w"], t["cu_seqlens"], state, conv,
+                                             **kw)
+        ys.append(out.float().cpu().numpy())
+        idxs.append(idx)
+    torch.cuda.synchronize()
+    return np.concatenate(ys), np.concatenate(idxs), state.cpu().numpy(), conv.float().cpu().numpy()
+
+
+def test_split_4096_token_sequence_into_two_calls():
+    """One 4096-token sequence (16/32 heads, d = 128) as two gdn_prefill_carry
+    calls, split inside a chunk; the second call starts from the first one's
+    final state and conv history.  Every chain against the oracle's single run."""
+    cfg = synth.SINGLE_4K
+    inp = synth.make_prefill(cfg)
+    y, idx, fs, conv = _run_segments(inp, [(0, 1500, 4096)], "bf16")
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"])
+    parity(y, r["y"][idx], "bf16", "out")
+    parity(fs, r["final_state"], "bf16", "final_state")
+    np.testing.assert_array_equal(conv, ref.conv_cache_after_prefill(inp, inp["cu_seqlens"]))
+
+
+@pytest.mark.parametrize("dtype,d,in_place", [("bf16", 128, False), ("bf16", 128, True), ("fp32", 32, False)],
+                         ids=["tensor_core", "tensor_core_in_place", "fp32"])
+def test_split_packed_sequences_into_short_segments(dtype, d, in_place):
+    """Three packed sequences, each cut into four consecutive segments of its
+    own lengths (empty, 1- and 2-token segments among them: the conv history of
+    a token then reaches back over several calls).  The concatenated outputs,
+    the last final state and the last conv history equal the oracle's single
+    run (the conv history exactly: it is a byte move)."""
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=(150, 64, 9), h_qk=2, h_v=4, d_k=d, d_v=d, dtype=dtype,
+                       init_std=0.02, seed=41)
+    inp = synth.make_prefill(cfg)
+    cuts = [(0, 70, 71, 73, 150), (0, 0, 64, 64, 64), (0, 1, 2, 4, 9)]
+    y, idx, fs, conv = _run_segments(inp, cuts, dtype, in_place=in_place)
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"])
+    parity(y, r["y"][idx], dtype, "out")
+    parity(fs, r["final_state"], dtype, "final_state")
+    np.testing.assert_array_equal(conv, ref.conv_cache_after_prefill(inp, inp["cu_seqlens"]))

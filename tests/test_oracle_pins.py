@@ -404,3 +404,51 @@ def test_short_sequence_prefill_then_decode():
     r = ref.decode_step(dec, cache, head["final_state"])
     np.testing.assert_allclose(r["y"][0], full["y"][T], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(r["state"][0], full["final_state"][0], rtol=1e-12, atol=1e-15)
+
+
+def _segment(inp, cu, bounds):
+    """Tokens [bounds[n][0], bounds[n][1]) of every sequence n, as one packed workload."""
+    idx = np.concatenate([np.arange(cu[n] + b0, cu[n] + b1) for n, (b0, b1) in enumerate(bounds)]).astype(np.int64)
+    seg = {k_: (v_[idx] if k_ in ("x_q", "x_k", "x_v", "z", "a", "b") else v_) for k_, v_ in inp.items()}
+    seg["cu_seqlens"] = np.concatenate([[0], np.cumsum([b1 - b0 for b0, b1 in bounds])]).astype(np.int64)
+    return seg, idx
+
+
+def test_split_prefill_with_carried_state_and_conv_equals_one_run():
+    """Running every sequence as consecutive segments, each started from the
+    previous segment's final state and conv history (the last three raw inputs,
+    carried through conv_cache_after_prefill), equals one run over the whole
+    sequence, bitwise -- including segments of 1 and 2 tokens, whose conv
+    history reaches back through more than one segment, and empty ones."""
+    lengths = (37, 64, 9)
+    inp = _tiny_inputs(lengths, h_qk=1, h_v=2, seed=10, init_std=0.02)
+    cu = inp["cu_seqlens"].astype(np.int64)
+    full = ref.prefill(inp, cu, inp["init_state"])
+    cuts = [(0, 20, 21, 23, 37), (0, 0, 64, 64, 64), (0, 1, 2, 4, 9)]   # segment boundaries per sequence
+    state, conv = inp["init_state"], None
+    for s in range(4):
+        bounds = [(c[s], c[s + 1]) for c in cuts]
+        seg, idx = _segment(inp, cu, bounds)
+        r = ref.prefill(seg, seg["cu_seqlens"], state, init_conv=conv)
+        np.testing.assert_array_equal(r["y"], full["y"][idx])
+        conv = ref.conv_cache_after_prefill(seg, seg["cu_seqlens"], init_conv=conv)
+        state = r["final_state"]
+    np.testing.assert_array_equal(state, full["final_state"])
+    np.testing.assert_array_equal(conv, ref.conv_cache_after_prefill(inp, cu))
+
+
+def test_split_prefill_without_conv_history_differs():
+    """The control: the same split with the state carried but the conv history
+    dropped (zeros, as a plain prefill takes) changes the first three tokens
+    after the split and none before it."""
+    inp = _tiny_inputs((30,), h_qk=1, h_v=2, seed=11)
+    full = ref.prefill(inp, [0, 30])
+    head, _ = _segment(inp, np.array([0, 30]), [(0, 12)])
+    tail, _ = _segment(inp, np.array([0, 30]), [(12, 30)])
+    rh = ref.prefill(head, head["cu_seqlens"])
+    rt = ref.prefill(tail, tail["cu_seqlens"], rh["final_state"])
+    np.testing.assert_array_equal(rh["y"], full["y"][:12])
+    assert not np.allclose(rt["y"][:3], full["y"][12:15])
+    rc = ref.prefill(tail, tail["cu_seqlens"], rh["final_state"],
+                     init_conv=ref.conv_cache_after_prefill(head, head["cu_seqlens"]))
+    np.testing.assert_array_equal(rc["y"], full["y"][12:])
