@@ -265,3 +265,219 @@ void gdn_ref_rmsnorm_gated(int L, int dv, double eps, const double *o, const dou
     }
   }
 }
+
+/* ======================================================================
+ * Backward pass (reverse mode) of each stage, for a scalar loss whose
+ * gradient with respect to the layer output y is given (dy).  Each function
+ * takes the stage's forward inputs again and the gradient of its outputs, and
+ * returns (accumulates where noted) the gradient of its inputs.  They are the
+ * chain rule applied to the definitions above, step by step in reverse order;
+ * the tests pin them to central finite differences of the forward functions.
+ * ====================================================================== */
+
+/* RMSNormGated: y = o r w silu(z), r = 1 / sqrt(mean(o^2) + eps).
+ *   dz  = dy o r w silu'(z),   silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *   dw += dy o r silu(z)       (accumulated over rows)
+ *   do  = r c dy - o r^3 (sum_j dy_j o_j c_j) / dv,   c = w silu(z)       */
+void gdn_ref_rmsnorm_gated_backward(int L, int dv, double eps, const double *o, const double *z,
+                                    const double *w, const double *dy, double *d_o, double *dz,
+                                    double *dw_acc) {
+  for (int t = 0; t < L; ++t) {
+    const double *ot = o + (size_t)t * dv, *zt = z + (size_t)t * dv, *gt = dy + (size_t)t * dv;
+    double ss = 0.0;
+    for (int j = 0; j < dv; ++j) ss += ot[j] * ot[j];
+    double r = 1.0 / sqrt(ss / dv + eps);
+    double dot = 0.0;
+    for (int j = 0; j < dv; ++j) {
+      double s = sigmoid(zt[j]);
+      double c = w[j] * zt[j] * s;
+      dot += gt[j] * ot[j] * c;
+    }
+    for (int j = 0; j < dv; ++j) {
+      double s = sigmoid(zt[j]);
+      double silu = zt[j] * s;
+      double c = w[j] * silu;
+      d_o[(size_t)t * dv + j] = r * c * gt[j] - ot[j] * r * r * r * dot / dv;
+      dz[(size_t)t * dv + j] = gt[j] * ot[j] * r * w[j] * s * (1.0 + zt[j] * (1.0 - s));
+      dw_acc[j] += gt[j] * ot[j] * r * silu;
+    }
+  }
+}
+
+/*
+ * The gated delta rule in reverse, for one chain.  Forward (per token t, H
+ * entering as H_{t-1}): p = H^T k, u = beta (v - alpha p), H_t = alpha H +
+ * k u^T, o_t = scale H_t^T q, alpha = exp(g).  Given do [L][dv] (gradient of
+ * o) and dHf [dk][dv] (gradient of the final state, NULL = 0), returns dq,
+ * dk [L][dk], dv [L][dv], dg, dbeta [L] and dH0 [dk][dv] (gradient of the
+ * entering state).  The states H_t are recomputed forward first (kept for all
+ * t: L (dk dv) doubles of scratch).  Reverse step t, with G the gradient of H_t:
+ *   G   += scale q_t do_t^T ;          dq_t = scale H_t do_t
+ *   dalpha = <G, H_{t-1}> ;            du = G^T k ;       dk_t = G u
+ *   dbeta = du . (v - alpha p) ;       dv_t = beta du ;   dalpha -= beta du . p
+ *   dp = -alpha beta du ;              dk_t += H_{t-1} dp
+ *   G <- alpha G + k dp^T   (the gradient of H_{t-1}) ;  dg_t = alpha dalpha
+ */
+void gdn_ref_recurrence_backward(int L, int dk, int dv, double scale, const double *q, const double *k,
+                                 const double *v, const double *g, const double *beta, const double *H0,
+                                 const double *d_o, const double *dHf, double *dq, double *dkk, double *dvv,
+                                 double *dg, double *dbeta, double *dH0) {
+  size_t S = (size_t)dk * dv;
+  double *Hs = (double *)malloc(sizeof(double) * S * (size_t)(L + 1)); /* Hs[t] = state before token t */
+  double *G = (double *)malloc(sizeof(double) * S);
+  double *p = (double *)malloc(sizeof(double) * (size_t)dv);
+  double *u = (double *)malloc(sizeof(double) * (size_t)dv);
+  double *du = (double *)malloc(sizeof(double) * (size_t)dv);
+  double *dp = (double *)malloc(sizeof(double) * (size_t)dv);
+  if (H0)
+    memcpy(Hs, H0, sizeof(double) * S);
+  else
+    memset(Hs, 0, sizeof(double) * S);
+  for (int t = 0; t < L; ++t) { /* forward, keeping every state */
+    const double *H = Hs + S * t;
+    double *Hn = Hs + S * (t + 1);
+    const double *kt = k + (size_t)t * dk, *vt = v + (size_t)t * dv;
+    double alpha = exp(g[t]);
+    for (int j = 0; j < dv; ++j) {
+      double s = 0.0;
+      for (int i = 0; i < dk; ++i) s += H[(size_t)i * dv + j] * kt[i];
+      u[j] = beta[t] * (vt[j] - alpha * s);
+    }
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) Hn[(size_t)i * dv + j] = alpha * H[(size_t)i * dv + j] + kt[i] * u[j];
+  }
+  if (dHf)
+    memcpy(G, dHf, sizeof(double) * S);
+  else
+    memset(G, 0, sizeof(double) * S);
+  for (int t = L - 1; t >= 0; --t) {
+    const double *Hp = Hs + S * t, *Ht = Hs + S * (t + 1);
+    const double *qt = q + (size_t)t * dk, *kt = k + (size_t)t * dk, *vt = v + (size_t)t * dv;
+    const double *ot = d_o + (size_t)t * dv;
+    double alpha = exp(g[t]);
+    /* output: o_t = scale H_t^T q_t */
+    for (int i = 0; i < dk; ++i) {
+      double s = 0.0;
+      for (int j = 0; j < dv; ++j) {
+        G[(size_t)i * dv + j] += scale * qt[i] * ot[j];
+        s += Ht[(size_t)i * dv + j] * ot[j];
+      }
+      dq[(size_t)t * dk + i] = scale * s;
+    }
+    /* recompute p and u of token t */
+    for (int j = 0; j < dv; ++j) {
+      double s = 0.0;
+      for (int i = 0; i < dk; ++i) s += Hp[(size_t)i * dv + j] * kt[i];
+      p[j] = s;
+      u[j] = beta[t] * (vt[j] - alpha * s);
+    }
+    /* H_t = alpha H_{t-1} + k u^T */
+    double dalpha = 0.0;
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) dalpha += G[(size_t)i * dv + j] * Hp[(size_t)i * dv + j];
+    for (int j = 0; j < dv; ++j) {
+      double s = 0.0;
+      for (int i = 0; i < dk; ++i) s += G[(size_t)i * dv + j] * kt[i];
+      du[j] = s;
+    }
+    for (int i = 0; i < dk; ++i) {
+      double s = 0.0;
+      for (int j = 0; j < dv; ++j) s += G[(size_t)i * dv + j] * u[j];
+      dkk[(size_t)t * dk + i] = s;
+    }
+    /* u = beta (v - alpha p) */
+    double db = 0.0, dup = 0.0;
+    for (int j = 0; j < dv; ++j) {
+      db += du[j] * (vt[j] - alpha * p[j]);
+      dup += du[j] * p[j];
+      dvv[(size_t)t * dv + j] = beta[t] * du[j];
+      dp[j] = -alpha * beta[t] * du[j];
+    }
+    dalpha -= beta[t] * dup;
+    dbeta[t] = db;
+    /* p = H_{t-1}^T k */
+    for (int i = 0; i < dk; ++i) {
+      double s = 0.0;
+      for (int j = 0; j < dv; ++j) s += Hp[(size_t)i * dv + j] * dp[j];
+      dkk[(size_t)t * dk + i] += s;
+    }
+    /* the gradient of H_{t-1} */
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) G[(size_t)i * dv + j] = alpha * G[(size_t)i * dv + j] + kt[i] * dp[j];
+    dg[t] = alpha * dalpha;
+  }
+  memcpy(dH0, G, sizeof(double) * S);
+  free(Hs);
+  free(G);
+  free(p);
+  free(u);
+  free(du);
+  free(dp);
+}
+
+/* L2 normalisation x / sqrt(sum x^2 + eps), row-wise, in reverse: with
+ * n = sqrt(sum x^2 + eps) and y = x / n,  dx = (dy - y (y . dy)) / n.
+ * x [L][D] is the forward input; dy in, dx out. */
+void gdn_ref_l2norm_backward(int L, int D, double eps, const double *x, const double *dy, double *dx) {
+  for (int t = 0; t < L; ++t) {
+    const double *xt = x + (size_t)t * D, *gt = dy + (size_t)t * D;
+    double ss = 0.0;
+    for (int i = 0; i < D; ++i) ss += xt[i] * xt[i];
+    double n = sqrt(ss + eps);
+    double yg = 0.0;
+    for (int i = 0; i < D; ++i) yg += (xt[i] / n) * gt[i];
+    for (int i = 0; i < D; ++i) dx[(size_t)t * D + i] = (gt[i] - (xt[i] / n) * yg) / n;
+  }
+}
+
+/* conv(4) + SiLU in reverse (see gdn_ref_conv_silu for the forward).  dy is
+ * the gradient of silu(pre); with dpre = dy silu'(pre):
+ *   dx[tau][c]   += dpre[t][c] w[c][j]     (tau = t - 3 + j >= 0)
+ *   dhist[m][c]  += dpre[t][c] w[c][j]     (tau = m - 3 < 0; dhist may be NULL)
+ *   dw[c][j]     += dpre[t][c] x_tau[c]    (x_tau from hist before the start)
+ * dx, dhist and dw are accumulated. */
+void gdn_ref_conv_silu_backward(int L, int C, const double *x, const double *w, const double *hist,
+                                const double *dy, double *dx, double *dhist, double *dw) {
+  for (int t = 0; t < L; ++t) {
+    for (int c = 0; c < C; ++c) {
+      double pre = 0.0;
+      for (int j = 0; j < 4; ++j) {
+        int tau = t - 3 + j;
+        double xv = tau >= 0 ? x[(size_t)tau * C + c] : (hist ? hist[(size_t)(tau + 3) * C + c] : 0.0);
+        pre += w[(size_t)c * 4 + j] * xv;
+      }
+      double s = sigmoid(pre);
+      double dpre = dy[(size_t)t * C + c] * s * (1.0 + pre * (1.0 - s));
+      for (int j = 0; j < 4; ++j) {
+        int tau = t - 3 + j;
+        double xv;
+        if (tau >= 0) {
+          xv = x[(size_t)tau * C + c];
+          dx[(size_t)tau * C + c] += dpre * w[(size_t)c * 4 + j];
+        } else {
+          xv = hist ? hist[(size_t)(tau + 3) * C + c] : 0.0;
+          if (dhist) dhist[(size_t)(tau + 3) * C + c] += dpre * w[(size_t)c * 4 + j];
+        }
+        dw[(size_t)c * 4 + j] += dpre * xv;
+      }
+    }
+  }
+}
+
+/* Gates in reverse: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b).
+ *   da_t = dg_t (-exp(A_log)) sigmoid(a_t + dt_bias) ;  ddt_bias += da_t
+ *   dA_log += dg_t g_t ;  db_t = dbeta_t beta_t (1 - beta_t)
+ * da, db [L] out; dA_log, ddt_bias accumulated (one value head). */
+void gdn_ref_gates_backward(int L, const double *a, const double *b, double A_log, double dt_bias,
+                            const double *dg, const double *dbeta, double *da, double *db,
+                            double *dA_log_acc, double *ddt_bias_acc) {
+  for (int t = 0; t < L; ++t) {
+    double x = a[t] + dt_bias;
+    double g = -exp(A_log) * softplus(x);
+    da[t] = dg[t] * (-exp(A_log)) * sigmoid(x);
+    *ddt_bias_acc += da[t];
+    *dA_log_acc += dg[t] * g;
+    double be = sigmoid(b[t]);
+    db[t] = dbeta[t] * be * (1.0 - be);
+  }
+}

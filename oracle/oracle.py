@@ -70,8 +70,15 @@ def _load():
             lib.gdn_ref_recurrence.argtypes = [i, i, i, d, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
             lib.gdn_ref_recurrence_chunked.argtypes = [i, i, i, i, d, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
             lib.gdn_ref_rmsnorm_gated.argtypes = [i, i, d, _dp, _dp, _dp, _dp]
+            lib.gdn_ref_rmsnorm_gated_backward.argtypes = [i, i, d, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
+            lib.gdn_ref_recurrence_backward.argtypes = [i, i, i, d] + [_dp] * 14
+            lib.gdn_ref_l2norm_backward.argtypes = [i, i, d, _dp, _dp, _dp]
+            lib.gdn_ref_conv_silu_backward.argtypes = [i, i, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
+            lib.gdn_ref_gates_backward.argtypes = [i, _dp, _dp, d, d, _dp, _dp, _dp, _dp, _dp, _dp]
             for f in ("gdn_ref_conv_silu", "gdn_ref_l2norm", "gdn_ref_gates", "gdn_ref_recurrence",
-                      "gdn_ref_recurrence_chunked", "gdn_ref_rmsnorm_gated"):
+                      "gdn_ref_recurrence_chunked", "gdn_ref_rmsnorm_gated", "gdn_ref_rmsnorm_gated_backward",
+                      "gdn_ref_recurrence_backward", "gdn_ref_l2norm_backward", "gdn_ref_conv_silu_backward",
+                      "gdn_ref_gates_backward"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -287,3 +294,117 @@ def conv_cache_after_prefill(inp: dict, cu_seqlens, init_conv=None):
             elif init_conv is not None:
                 cache[n, :, j] = np.asarray(init_conv[n], np.float64)[:, t - cu[n] + 3]
     return cache
+
+
+# ---------------------------------------------------------------- backward (reverse mode)
+# The gradient of a scalar loss  sum(dy * y) + sum(dfinal * final_state)  with
+# respect to every input of the layer, by the stages' reverse-mode functions
+# of gdn_oracle.c applied in the reverse of the forward order.  Training
+# frameworks run this layer ("[Qwen3.5 MoE] Add hybrid decoder model ...",
+# "Support Qwen35 SFT", "feat(models): dense Qwen3.5 custom attention": all
+# train it); the pages state no backward, so this is the chain rule of the
+# forward definitions, pinned to finite differences of the forward oracle.
+def chain_backward(inp: dict, s0: int, s1: int, hv: int, dy, H0=None, hist=None, dHf=None, *,
+                   eps_l2=EPS_L2, eps_rms=EPS_RMS, scale=None):
+    """Gradients for tokens [s0, s1) of one sequence and value head hv.
+    dy [L, dv] (gradient of y), dHf [dk, dv] or None (gradient of the final state).
+    Returns dict: x_q, x_k [L, dk] and x_v, z [L, dv] (raw stream gradients of
+    this chain's heads), a, b [L], conv_w_q, conv_w_k [dk, 4], conv_w_v [dv, 4],
+    A_log, dt_bias (scalars), norm_w [dv], H0 [dk, dv], hist (dict q, k [3, dk],
+    v [3, dv]: gradient of the carried conv history)."""
+    lib = _load()
+    h_qk, dk = inp["x_q"].shape[1:]
+    h_v, dv = inp["x_v"].shape[1:]
+    hq = hv // (h_v // h_qk)
+    qc, kc, vc = _channels(h_qk, h_v, dk, dv, hq, hv)
+    w = _f64(inp["conv_w"])
+    L = s1 - s0
+    if scale is None:
+        scale = dk ** -0.5
+    hq_, hk_, hv_ = (None, None, None) if hist is None else (_f64(hist["q"]), _f64(hist["k"]), _f64(hist["v"]))
+    xq, xk, xv = _f64(inp["x_q"][s0:s1, hq, :]), _f64(inp["x_k"][s0:s1, hq, :]), _f64(inp["x_v"][s0:s1, hv, :])
+    zz, aa, bb = _f64(inp["z"][s0:s1, hv, :]), _f64(inp["a"][s0:s1, hv]), _f64(inp["b"][s0:s1, hv])
+    A_log, dt_bias = float(inp["A_log"][hv]), float(inp["dt_bias"][hv])
+    nw = _f64(inp["norm_w"])
+    # forward, keeping what the reverse steps read
+    qr, kr, v = conv_silu(xq, w[qc], hq_), conv_silu(xk, w[kc], hk_), conv_silu(xv, w[vc], hv_)
+    q, k = l2norm(qr, eps_l2), l2norm(kr, eps_l2)
+    g, beta = gates(aa, bb, A_log, dt_bias)
+    H0 = None if H0 is None else _f64(H0)
+    o, _ = recurrence(q, k, v, g, beta, H0, scale=scale)
+    # reverse
+    dyy = _f64(dy)
+    d_o, dz, dnw = np.empty((L, dv)), np.empty((L, dv)), np.zeros(dv)
+    lib.gdn_ref_rmsnorm_gated_backward(L, dv, eps_rms, _ptr(o), _ptr(zz), _ptr(nw), _ptr(dyy), _ptr(d_o), _ptr(dz),
+                                       _ptr(dnw))
+    dq, dkk, dvv = np.empty((L, dk)), np.empty((L, dk)), np.empty((L, dv))
+    dg, dbeta, dH0 = np.empty(L), np.empty(L), np.empty((dk, dv))
+    dHf_ = None if dHf is None else _f64(dHf)
+    lib.gdn_ref_recurrence_backward(L, dk, dv, float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                    _ptr(H0), _ptr(d_o), _ptr(dHf_), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg),
+                                    _ptr(dbeta), _ptr(dH0))
+    dqr, dkr = np.empty((L, dk)), np.empty((L, dk))
+    lib.gdn_ref_l2norm_backward(L, dk, eps_l2, _ptr(qr), _ptr(dq), _ptr(dqr))
+    lib.gdn_ref_l2norm_backward(L, dk, eps_l2, _ptr(kr), _ptr(dkk), _ptr(dkr))
+    res = {}
+    for name, x, wc, hh, dyx in (("q", xq, w[qc], hq_, dqr), ("k", xk, w[kc], hk_, dkr), ("v", xv, w[vc], hv_, dvv)):
+        C = x.shape[1]
+        dx, dw, dh = np.zeros((L, C)), np.zeros((C, 4)), np.zeros((3, C))
+        wc = _f64(wc)
+        lib.gdn_ref_conv_silu_backward(L, C, _ptr(x), _ptr(wc), _ptr(hh), _ptr(_f64(dyx)), _ptr(dx), _ptr(dh),
+                                       _ptr(dw))
+        res["x_" + name], res["conv_w_" + name], res["hist_" + name] = dx, dw, dh
+    da, db = np.empty(L), np.empty(L)
+    dA, ddt = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    lib.gdn_ref_gates_backward(L, _ptr(aa), _ptr(bb), A_log, dt_bias, _ptr(dg), _ptr(dbeta), _ptr(da), _ptr(db),
+                               ctypes.byref(dA), ctypes.byref(ddt))
+    res.update(z=dz, a=da, b=db, A_log=dA.value, dt_bias=ddt.value, norm_w=dnw, H0=dH0,
+               hist={"q": res.pop("hist_q"), "k": res.pop("hist_k"), "v": res.pop("hist_v")})
+    return res
+
+
+def prefill_backward(inp: dict, cu_seqlens, dy, init_state=None, dfinal_state=None, threads=None, init_conv=None,
+                     **kw):
+    """Gradients of  sum(dy * y) + sum(dfinal_state * final_state)  of a prefill
+    with respect to every input: dict with x_q, x_k [T, h_qk, dk]; x_v, z
+    [T, h_v, dv]; a, b [T, h_v]; conv_w [Cc, 4]; A_log, dt_bias [h_v];
+    norm_w [dv]; init_state [N, h_v, dk, dv]; init_conv [N, Cc, 3]."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    N = len(cu) - 1
+    T, h_v, dv = inp["x_v"].shape
+    h_qk, dk = inp["x_q"].shape[1:]
+    Cc = 2 * h_qk * dk + h_v * dv
+    dy = _f64(dy)
+    gr = {"x_q": np.zeros((T, h_qk, dk)), "x_k": np.zeros((T, h_qk, dk)), "x_v": np.zeros((T, h_v, dv)),
+          "z": np.zeros((T, h_v, dv)), "a": np.zeros((T, h_v)), "b": np.zeros((T, h_v)),
+          "conv_w": np.zeros((Cc, 4)), "A_log": np.zeros(h_v), "dt_bias": np.zeros(h_v), "norm_w": np.zeros(dv),
+          "init_state": np.zeros((N, h_v, dk, dv)), "init_conv": np.zeros((N, Cc, 3))}
+
+    def run(nh):
+        n, h = nh
+        H0 = None if init_state is None else init_state[n, h]
+        hist = None if init_conv is None else _hist_of(init_conv[n], h_qk, h_v, dk, dv, h)
+        dHf = None if dfinal_state is None else dfinal_state[n, h]
+        return nh, chain_backward(inp, int(cu[n]), int(cu[n + 1]), h, dy[cu[n]:cu[n + 1], h], H0, hist, dHf, **kw)
+
+    for (n, h), r in _pool_map(run, [(n, h) for n in range(N) for h in range(h_v)], threads):
+        s0, s1 = cu[n], cu[n + 1]
+        hq = h // (h_v // h_qk)
+        qc, kc, vc = _channels(h_qk, h_v, dk, dv, hq, h)
+        gr["x_q"][s0:s1, hq] += r["x_q"]
+        gr["x_k"][s0:s1, hq] += r["x_k"]
+        gr["x_v"][s0:s1, h] += r["x_v"]
+        gr["z"][s0:s1, h] = r["z"]
+        gr["a"][s0:s1, h] = r["a"]
+        gr["b"][s0:s1, h] = r["b"]
+        gr["conv_w"][qc] += r["conv_w_q"]
+        gr["conv_w"][kc] += r["conv_w_k"]
+        gr["conv_w"][vc] += r["conv_w_v"]
+        gr["A_log"][h] += r["A_log"]
+        gr["dt_bias"][h] += r["dt_bias"]
+        gr["norm_w"] += r["norm_w"]
+        gr["init_state"][n, h] = r["H0"]
+        gr["init_conv"][n][qc] += r["hist"]["q"].T
+        gr["init_conv"][n][kc] += r["hist"]["k"].T
+        gr["init_conv"][n][vc] += r["hist"]["v"].T
+    return gr
