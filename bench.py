@@ -292,6 +292,45 @@ def _prefill_e2e(t, cfg, steps, warmup, dev, flush, out, fs, ws, stream):
     return {"ms": start.elapsed_time(end) / steps, "h2d": h2d, "d2h": d2h, "pipelined": "2 buffer sets, 3 streams"}
 
 
+def time_backward(cfg, steps, warmup, dev, flush):
+    """Per-step device time of one gdn_prefill_backward call (all gradients,
+    dy of the output, no final-state gradient), L2 flushed between steps."""
+    import torch
+
+    import gateddeltanet_layer_gb300 as gdn
+    inp = inputs_of(cfg)
+    t = _device_inputs(inp, dev)
+    dy = torch.randn((cfg.T, cfg.h_v, cfg.d_v), generator=torch.Generator().manual_seed(1)).to(dev, torch.bfloat16)
+    ws = torch.empty(gdn.prefill_backward_workspace_bytes(cfg.T, cfg.N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        gdn.prefill_backward(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                             t["dt_bias"], t["norm_w"], t["cu_seqlens"], dy, t["init_state"], workspace=ws,
+                             stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        ms.append(s.elapsed_time(e))
+    gdn.trace_enable(True)
+    gdn.trace_read()
+    call()
+    torch.cuda.synchronize(dev)
+    kernels = {k: v[1] for k, v in gdn.trace_read().items()}
+    gdn.trace_enable(False)
+    return {"ms": ms, "kernels": kernels}
+
+
 def time_decode(cfg, steps, warmup, dev, flush):
     import torch
 
@@ -422,6 +461,11 @@ def run_ours(args):
                              "achieved_gbs": rl["achieved"] if rl["unit"] == "GB/s" else None,
                              "flop_bound_frac": rl["flop_bound_frac"], "byte_bound_frac": rl["byte_bound_frac"],
                              "per_kernel": rl["per_kernel"], "traffic": rl["traffic"]}
+        r = time_backward(synth.SINGLE_4K, max(3, args.steps // 4), args.warmup, dev, flush)
+        m, = max_over_ranks([statistics.mean(r["ms"])], dev)
+        extra["prefill_backward_T4096"] = {"tokens_per_s": synth.SINGLE_4K.T / (m * 1e-3), "ms": m,
+                                           "kernels": "bwd_chain_kernel, bwd_prologue_kernel, bwd_gate_kernel",
+                                           "kernels_ms_per_step": r["kernels"]}
         dc = synth.DECODE_256
         r = time_decode(dc, args.steps, args.warmup, dev, flush)
         m, = max_over_ranks([statistics.mean(r["ms"])], dev)

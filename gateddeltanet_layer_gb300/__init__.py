@@ -12,7 +12,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["prefill", "prefill_carry", "decode_step", "decode_step_slots", "conv_cache_from_prefill", "prefill_workspace_bytes",
+__all__ = ["prefill", "prefill_carry", "prefill_backward", "prefill_backward_workspace_bytes", "decode_step", "decode_step_slots", "conv_cache_from_prefill", "prefill_workspace_bytes",
            "workspace_status", "library", "GdnError", "STATUS", "prefill_noalloc", "NOALLOC_SCRATCH_BYTES",
            "trace_enable", "trace_read"]
 
@@ -57,6 +57,10 @@ def library() -> ctypes.CDLL:
             lib.gdn_prefill.restype = ctypes.c_int
             lib.gdn_prefill_carry.argtypes = [dp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
             lib.gdn_prefill_carry.restype = ctypes.c_int
+            lib.gdn_prefill_backward_workspace_bytes.argtypes = [dp]
+            lib.gdn_prefill_backward_workspace_bytes.restype = ctypes.c_size_t
+            lib.gdn_prefill_backward.argtypes = [dp] + [_vp] * 26 + [ctypes.c_size_t, _vp]
+            lib.gdn_prefill_backward.restype = ctypes.c_int
             lib.gdn_decode_step.argtypes = [dp] + [_vp] * 14
             lib.gdn_decode_step.restype = ctypes.c_int
             lib.gdn_workspace_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
@@ -221,6 +225,51 @@ def prefill_carry(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, 
     return out, final_state, final_conv
 
 
+def prefill_backward_workspace_bytes(T: int, N: int, h_qk: int, h_v: int, d_k: int, d_v: int,
+                                     bf16: bool = True) -> int:
+    d = Dims(T, N, h_qk, h_v, d_k, d_v, GDN_BF16 if bf16 else GDN_FP32)
+    return int(library().gdn_prefill_backward_workspace_bytes(ctypes.byref(d)))
+
+
+def prefill_backward(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, dy, init_state=None,
+                     dfinal_state=None, *, want_dinit_state=True, workspace=None, stream=None):
+    """``gdn_prefill_backward``: gradients of sum(dy * y) + sum(dfinal_state *
+    final_state) of the prefill with these inputs.  Returns a dict of fp32
+    tensors named after the inputs: q, k, v, a, b, z, conv_w, A_log, dt_bias,
+    norm_w and init_state (None unless want_dinit_state)."""
+    torch = _torch()
+    lib = library()
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("z", z), ("dy", dy)):
+        _req(t, name, dt)
+    for name, t in (("conv_w", conv_w), ("A_log", A_log), ("dt_bias", dt_bias), ("norm_w", norm_w)):
+        _req(t, name, torch.float32)
+    _req(cu_seqlens, "cu_seqlens", torch.int32)
+    for name, t in (("init_state", init_state), ("dfinal_state", dfinal_state)):
+        if t is not None:
+            _req(t, name, torch.float32)
+    N = cu_seqlens.numel() - 1
+    d = dims_of(q, v, N)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = {"q": torch.empty(q.shape, **f32), "k": torch.empty(k.shape, **f32), "v": torch.empty(v.shape, **f32),
+         "a": torch.empty(a.shape, **f32), "b": torch.empty(b.shape, **f32), "z": torch.empty(z.shape, **f32),
+         "conv_w": torch.empty(conv_w.shape, **f32), "A_log": torch.empty(A_log.shape, **f32),
+         "dt_bias": torch.empty(dt_bias.shape, **f32), "norm_w": torch.empty(norm_w.shape, **f32),
+         "init_state": torch.empty((N, d.h_v, d.d_k, d.d_v), **f32) if want_dinit_state else None}
+    ws_bytes = 0
+    if workspace is not None:
+        _req(workspace, "workspace", torch.uint8)
+        ws_bytes = workspace.numel()
+    st = lib.gdn_prefill_backward(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z),
+                                  _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(cu_seqlens),
+                                  _ptr(init_state), _ptr(dy), _ptr(dfinal_state), _ptr(g["q"]), _ptr(g["k"]),
+                                  _ptr(g["v"]), _ptr(g["a"]), _ptr(g["b"]), _ptr(g["z"]), _ptr(g["conv_w"]),
+                                  _ptr(g["A_log"]), _ptr(g["dt_bias"]), _ptr(g["norm_w"]), _ptr(g["init_state"]),
+                                  _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    _check(st, "gdn_prefill_backward")
+    return g
+
+
 def decode_step(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, conv_state, state, *, out=None,
                 stream=None):
     """``gdn_decode_step``: one token per sequence; updates ``state`` (fp32
@@ -312,7 +361,7 @@ def workspace_status(workspace, stream=None) -> int:
 
 
 # Number of kernel kinds the trace distinguishes (GDN_K_COUNT in include/gdn_trace.h).
-TRACE_KINDS = 5
+TRACE_KINDS = 7
 
 
 def trace_enable(on: bool = True) -> None:

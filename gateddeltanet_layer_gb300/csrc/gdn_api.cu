@@ -125,6 +125,59 @@ int gdn_prefill_carry(const gdn_dims *d, const void *q, const void *k, const voi
                       final_state, final_conv, workspace, ws_bytes, stream);
 }
 
+size_t gdn_prefill_backward_workspace_bytes(const gdn_dims *d) {
+  if (check_dims(d) != GDN_OK || d->num_seqs <= 0) return 0;
+  return kStatusBytes +
+         gdn::prefill_backward_workspace_bytes(d->num_tokens, d->num_seqs, d->h_qk, d->h_v, d->d_k, d->d_v);
+}
+
+int gdn_prefill_backward(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
+                         const void *b, const void *z, const float *conv_w, const float *A_log,
+                         const float *dt_bias, const float *norm_w, const int32_t *cu_seqlens,
+                         const float *init_state, const void *dy, const float *dfinal_state, float *dq, float *dk,
+                         float *dv, float *da, float *db, float *dz, float *dconv_w, float *dA_log,
+                         float *ddt_bias, float *dnorm_w, float *dinit_state, void *workspace, size_t ws_bytes,
+                         void *stream) {
+  int st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (d->num_seqs <= 0) return GDN_ERR_INVALID_ARG;
+  if (!conv_w || !A_log || !dt_bias || !norm_w || !cu_seqlens || !dconv_w || !dA_log || !ddt_bias || !dnorm_w)
+    return GDN_ERR_INVALID_ARG;
+  if (d->num_tokens > 0 &&
+      (!q || !k || !v || !a || !b || !z || !dy || !dq || !dk || !dv || !da || !db || !dz))
+    return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, a, b, z, dy, init_state, dfinal_state, dq, dk, dv, dz, dinit_state, conv_w};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_prefill_backward_workspace_bytes(d);
+  if (workspace && (ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GDN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void *ws = workspace;
+  bool owned = false;
+  if (!ws) {
+    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return GDN_ERR_CUDA;
+    owned = true;
+  }
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) {
+    if (owned) cudaFreeAsync(ws, s);
+    return GDN_ERR_CUDA;
+  }
+  gdn::BwdParams p{};
+  p.T = d->num_tokens; p.N = d->num_seqs; p.h_qk = d->h_qk; p.h_v = d->h_v; p.d_k = d->d_k; p.d_v = d->d_v;
+  p.q = q; p.k = k; p.v = v; p.a = a; p.b = b; p.z = z; p.dy = dy;
+  p.conv_w = conv_w; p.A_log = A_log; p.dt_bias = dt_bias; p.norm_w = norm_w;
+  p.cu_seqlens = cu_seqlens; p.init_state = init_state; p.dfinal_state = dfinal_state;
+  p.dq = dq; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.dz = dz;
+  p.dconv_w = dconv_w; p.dA_log = dA_log; p.ddt_bias = ddt_bias; p.dnorm_w = dnorm_w; p.dinit_state = dinit_state;
+  p.status = static_cast<int *>(ws);
+  p.ws = static_cast<uint8_t *>(ws) + kStatusBytes;
+  p.ws_bytes = need - kStatusBytes;
+  cudaError_t e = gdn::launch_prefill_backward(p, d->io_dtype == GDN_BF16, s);
+  if (owned) cudaFreeAsync(ws, s);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 int gdn_decode_step(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
                     const void *b, const void *z, const float *conv_w, const float *A_log,
                     const float *dt_bias, const float *norm_w, void *conv_state, float *state,

@@ -40,6 +40,25 @@ struct ConvCacheParams {
   void *conv_cache;      // [N, Cc, 3]
 };
 
+// Backward pass of a prefill: the gradient of sum(dy * y) (+ sum(dfinal * final_state)).
+struct BwdParams {
+  int T, N, h_qk, h_v, d_k, d_v;
+  const void *q, *k, *v, *a, *b, *z;
+  const void *dy;              // [T, h_v, d_v] io dtype
+  const float *conv_w, *A_log, *dt_bias, *norm_w;
+  const int32_t *cu_seqlens;
+  const float *init_state;     // may be null
+  const float *dfinal_state;   // may be null
+  float *dq, *dk, *dv, *da, *db, *dz;               // stream gradients (fp32, the streams' layouts)
+  float *dconv_w, *dA_log, *ddt_bias, *dnorm_w;     // parameter gradients (fp32)
+  float *dinit_state;          // may be null
+  int *status;
+  uint8_t *ws;
+  size_t ws_bytes;
+};
+cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t s);
+size_t prefill_backward_workspace_bytes(int T, int N, int h_qk, int h_v, int d_k, int d_v);
+
 // Token-sequential fp32 prefill (any supported shape, bf16 or fp32 streams).
 cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t s);
 // Chunked tensor-core prefill (bf16 streams, d_k = d_v = 128, at most

@@ -164,6 +164,41 @@ GDN_API int gdn_prefill_carry(const gdn_dims *dims, const void *q, const void *k
                               size_t ws_bytes, void *stream);
 
 /*
+ * Backward pass of gdn_prefill: the gradient, with respect to every input, of
+ * the scalar loss  sum(dy * y) + sum(dfinal_state * final_state).
+ *
+ * The pages run the layer in training frameworks ("[Qwen3.5 MoE] Add hybrid
+ * decoder model (GatedDeltaNet + full attention + MoE)", Summary; "Support
+ * Qwen35 SFT"; "feat(models): dense Qwen3.5 custom attention", its E2E
+ * training-throughput table) but state no backward; this is the chain rule of
+ * the forward definitions above, in fp32 on the CUDA cores (the state's
+ * gradient is carried token by token in reverse, the states recomputed from a
+ * checkpoint every 32 tokens).
+ *
+ * Inputs: dims, the forward's q, k, v, a, b, z, conv_w, A_log, dt_bias,
+ *   norm_w, cu_seqlens and init_state (NULL = zeros), exactly as given to
+ *   gdn_prefill; dy io_dtype [T, h_v, d_v]; dfinal_state fp32
+ *   [N, h_v, d_k, d_v] or NULL (= 0).
+ * Outputs (fp32, overwritten): dq, dk [T, h_qk, d_k]; dv, dz [T, h_v, d_v];
+ *   da, db [T, h_v]; dconv_w [Cc, 4]; dA_log, ddt_bias [h_v]; dnorm_w [d_v];
+ *   dinit_state [N, h_v, d_k, d_v] or NULL (= not returned).  The parameter
+ *   gradients are sums over tokens and heads taken with atomic adds, so their
+ *   last bits may differ from run to run.
+ * workspace: gdn_prefill_backward_workspace_bytes(dims) bytes, 256-byte
+ *   aligned, or NULL (stream-ordered allocation, as gdn_prefill).
+ * Supported shapes and error behaviour as gdn_prefill (every supported shape
+ * and both stream dtypes run this one kernel set).  Returns a gdn_status.
+ */
+GDN_API size_t gdn_prefill_backward_workspace_bytes(const gdn_dims *dims);
+GDN_API int gdn_prefill_backward(const gdn_dims *dims, const void *q, const void *k, const void *v,
+                                 const void *a, const void *b, const void *z, const float *conv_w,
+                                 const float *A_log, const float *dt_bias, const float *norm_w,
+                                 const int32_t *cu_seqlens, const float *init_state, const void *dy,
+                                 const float *dfinal_state, float *dq, float *dk, float *dv, float *da, float *db,
+                                 float *dz, float *dconv_w, float *dA_log, float *ddt_bias, float *dnorm_w,
+                                 float *dinit_state, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Decode step: one new token for each of B = dims->num_tokens independent
  * sequences, against a carried state; the state and the conv cache are
  * updated in place.

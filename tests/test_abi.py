@@ -100,7 +100,7 @@ def test_trace_read_without_launches(lib):
     assert gdn.trace_read() == {}
     names = [lib.gdn_trace_kernel_name(k).decode() for k in range(gdn.TRACE_KINDS)]
     assert names == ["chunk_table_kernel", "chunk_prep_kernel", "state_kernel", "prefill_simt_kernel",
-                     "decode_kernel"]
+                     "decode_kernel", "bwd_chain_kernel", "bwd_prologue_kernel"]
     assert lib.gdn_trace_kernel_name(gdn.TRACE_KINDS) == b""
     assert lib.gdn_trace_read(0, None, None) == 1
 
@@ -125,3 +125,19 @@ def test_timeout_selftest_rejects_bad_arguments_without_a_gpu(lib):
     assert fn(None, 1000, None) == 1
     assert fn(ctypes.c_void_p(1 << 20), 0, None) == 1
     assert fn(ctypes.c_void_p(1 << 20), 2000000, None) == 1
+
+
+def test_backward_and_carry_reject_bad_arguments_without_a_gpu(lib):
+    """Host-side validation of gdn_prefill_backward and gdn_prefill_carry (and
+    the binding's argument lists) without a launch."""
+    D = gdn.Dims
+    d = D(64, 1, 2, 2, 16, 16, gdn.GDN_FP32)
+    null = [None] * 26
+    assert lib.gdn_prefill_backward(ctypes.byref(d), *null, 0, None) == 1       # required pointers missing
+    bad = D(64, 1, 2, 3, 16, 16, gdn.GDN_FP32)                                  # h_v % h_qk != 0
+    assert lib.gdn_prefill_backward(ctypes.byref(bad), *null, 0, None) == 1
+    assert lib.gdn_prefill_backward_workspace_bytes(ctypes.byref(d)) > 256
+    assert lib.gdn_prefill_backward_workspace_bytes(ctypes.byref(bad)) == 0
+    assert lib.gdn_prefill_carry(ctypes.byref(d), *([None] * 17), 0, None) == 1
+    unsup = D(64, 1, 2, 2, 24, 16, gdn.GDN_FP32)                                # head dim not a multiple of 16
+    assert lib.gdn_prefill_carry(ctypes.byref(unsup), *([None] * 17), 0, None) == 2
