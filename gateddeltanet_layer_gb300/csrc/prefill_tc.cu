@@ -1337,6 +1337,337 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
   tc::cluster_sync();  // no CTA leaves while a peer may still store into its shared memory
 }
 
+// ================================================================ state pass, transposed
+// One CTA per (sequence, value head) chain, owning the whole state.  The state
+// is kept transposed, S = H^T (lanes j over d_v, columns i over d_k, fp32 in
+// tensor memory), so both products of a chunk take their A operand straight
+// from tensor memory (an fp16 copy written there by the chain warps) and run at
+// N = 128:
+//   MMA 1:  D1 = (-S) [Q^; W]^T        columns 0-63: -(Q^ H)^T, 64-127: -(W H)^T
+//           U^T = U'^T + D1[:, 64:128]  (fp32, then its fp16 copy in tensor memory)
+//   MMA 2:  S  += U^T K~               (S scaled by gamma_C before)
+//           D1[:, 0:64] += U^T (-A_Q)^T  (-O^T, for the epilogue)
+// 16 tcgen05.mma per chunk (8 + 4 + 4) against 64 when the columns of H are
+// split over four CTAs, and no shared-memory round trip for the operands the
+// chain computes.  Warps 0-7 run the chain (warp w: TMEM lanes 32 (w & 3), half
+// w >> 2 of the columns), warps 8-15 the RMSNormGated epilogue one chunk behind
+// (thread = state column j, warp half = 32 of the chunk's tokens; the
+// per-token sums of o^2 reduced across lanes and warps).  The MMA-issuing
+// thread also streams the operand sets in by TMA, a ring of two: set c + 2
+// goes into the slot of chunk c right after MMA 1 of chunk c + 1 is issued
+// (MMAs complete in issue order, so chunk c's products have then read it).
+namespace ts {
+constexpr int kChainWarps = 8, kEpiWarps = 8;
+constexpr int kChainThreads = 32 * kChainWarps, kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 32 * (kChainWarps + kEpiWarps);
+constexpr int kSets = 2;
+// one operand set: [Q^; W] (32 KB), K~^T (16 KB), -A_Q (8 KB), U' of every column (16 KB), gamma
+constexpr uint32_t R_WQ = 0, R_KT = 32768, R_AQ = 49152, R_UP = 57344, R_GAM = 73728;
+constexpr uint32_t kStage = 74752;                     // 73 KB, 1024-aligned
+constexpr uint32_t S_Z = kSets * kStage;                // z [2][64 t][128] bf16 (TMA)
+constexpr uint32_t S_Y = S_Z + 2 * 16384;               // y [64 t][128] bf16 (TMA store)
+constexpr uint32_t S_WN = S_Y + 16384;                  // norm_w [128]
+constexpr uint32_t S_PART = S_WN + 512;                 // sums of o^2 [4 lane quarters][64 tokens]
+constexpr uint32_t S_INV = S_PART + 1024;               // 1 / rms per token [64]
+constexpr uint32_t S_MISC = S_INV + 256;
+constexpr size_t kSmem = S_MISC + 256 + 1024;
+// barriers: full[2], empty[2], m1, m2, oready[2], odone[2], z[2]
+constexpr int B_FULL = 0, B_EMPTY = 2, B_M1 = 4, B_M2 = 5, B_ORDY = 6, B_ODONE = 8, B_Z = 10, kBars = 12;
+// tensor memory: S, two D1 buffers, the fp16 -S (64 columns) and U^T (32 columns)
+constexpr uint32_t COL_S = 0, COL_D = 128, COL_AS = 384, COL_AU = 448, kTmemCols = 512;
+constexpr uint32_t kId128 = tc::idesc_f16(128, 128), kId64 = tc::idesc_f16(128, 64);
+static_assert(R_GAM + 256 <= kStage && kStage % 1024 == 0, "operand set");
+static_assert(kSmem <= 232448, "shared memory budget (one CTA per SM)");
+static_assert(kBars * 8 + 4 <= 256, "barrier block");
+constexpr int kBarChain = 3, kBarEpiTs = 4;
+}  // namespace ts
+
+__global__ void __launch_bounds__(ts::kThreads, 1)
+    state_ts_kernel(const PrefillParams p, const Ws ws, const __grid_constant__ CUtensorMap zmap,
+                    const __grid_constant__ CUtensorMap omap) {
+  using namespace ts;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = tc::smem_u32(sm);
+  const int h_v = p.h_v;
+  const int chain = blockIdx.x, h = chain % h_v;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_MISC);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_MISC + 8 * kBars);
+  float *sWn = reinterpret_cast<float *>(sm + S_WN);
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kBars; ++i) tc::mbar_init(bar + i, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&zmap);
+    tc::prefetch_tmap(&omap);
+  }
+  for (int j = tid; j < kD; j += kThreads) sWn[j] = p.norm_w[j];
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  bool failed = false;
+
+  tc::grid_dependency_wait();  // the chunk table and the operand images
+  const int n = p.N > 1 ? ws.seq_order[chain / h_v] : chain / h_v;
+  const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+  bool valid = s0 >= 0 && s1 >= s0 && s1 <= p.T;  // else reported by the chunk table
+  const int g0 = valid ? ws.chunk_base[n] : 0, g1 = valid ? ws.chunk_base[n + 1] : 0;
+  if (valid && g1 - g0 != (s1 - s0 + kC - 1) / kC) valid = false;  // table overflow, reported
+  const int nch = valid ? g1 - g0 : 0;
+  auto slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
+  auto set_at = [](int c) -> uint32_t { return kStage * (uint32_t)(c % kSets); };
+
+  int issued = 0;  // operand sets issued (thread 0)
+  auto issue_set = [&](int c) {
+    uint8_t *dst = sm + set_at(c);
+    const uint8_t *src = slot(g0 + c);
+    uint64_t *full = bar + B_FULL + c % kSets;
+    tc::mbar_arrive_expect_tx(full, 32768 + 16384 + 8192 + 16384 + 256);
+    tc::bulk_g2s(dst + R_WQ, src + kVWQ, 32768 + 16384, full);  // [Q^; W] and K~^T
+    tc::bulk_g2s(dst + R_AQ, src + kVAq, 8192, full);
+    tc::bulk_g2s(dst + R_UP, src + kVUp, 16384, full);
+    tc::bulk_g2s(dst + R_GAM, src + kVGam, 256, full);
+    if (c + 1 < nch) {  // the set after: into L2 now
+      const uint8_t *nx = slot(g0 + c + 1);
+      tc::prefetch_l2(nx, kVSlot / 2);
+      tc::prefetch_l2(nx + kVSlot / 2, kVSlot / 2);
+    }
+    issued = c + 1;
+  };
+  if (tid == 0)
+    for (int c = 0; c < kSets && c < nch; ++c) issue_set(c);
+
+  if (warp < kChainWarps) {
+    // ======================= the chain: lane j = 32 (warp & 3) + lane, columns half hf
+    const int hf = warp >> 2, j = 32 * (warp & 3) + lane;
+    const size_t st_base = ((size_t)n * h_v + h) * kD * kD + j;  // element (i, j) at + i * kD
+    // every chain thread waits on the mbarriers itself; a wait that runs out is
+    // ORed into the next barrier the chain passes anyway (its publish)
+    bool ok = true;
+    auto publish_chain = [&]() {  // tensor-memory stores of every chain thread are done; true: a wait failed
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      const bool bad = tc::named_barrier_or(kBarChain, kChainThreads, !ok);
+      tc::fence_after_sync();
+      return bad;
+    };
+    // shared-memory descriptors of each ring slot's operands at K step 0; step k adds
+    // (k >> 2) R 128 + (k & 3) 32 bytes, i.e. (k >> 2) R 8 + 2 (k & 3) in the 16-byte address field
+    static_assert(kSets == 2, "two ring slots");
+    const uint64_t desc_wq0 = tc::sdesc_sw128(sbase + R_WQ), desc_wq1 = tc::sdesc_sw128(sbase + kStage + R_WQ);
+    const uint64_t desc_kt0 = tc::sdesc_sw128(sbase + R_KT), desc_kt1 = tc::sdesc_sw128(sbase + kStage + R_KT);
+    {  // initial state slice: S[j][i] = H[i][j], columns [64 hf, 64 hf + 64)
+      float v[32];
+#pragma unroll 1
+      for (int c32 = 0; c32 < 2; ++c32) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int i = 64 * hf + 32 * c32 + e;
+          v[e] = p.init_state ? p.init_state[st_base + (size_t)i * kD] : 0.0f;
+        }
+        tc::tmem_st32_nowait(tmem + lane_off + COL_S + 64 * hf + 32 * c32, v);
+      }
+    }
+    if (publish_chain()) failed = true;
+    for (int c = 0; c < nch && !failed; ++c) {
+      const int b = c & 1, rs = c % kSets;
+      const uint32_t set = set_at(c);
+      const uint32_t d1 = COL_D + 128 * b;
+      ok = tc::mbar_wait(bar + B_FULL + rs, (uint32_t)(c / kSets) & 1) && ok;
+      // ---- S -> gamma_C S in place, and its fp16 negative as the A operand of MMA 1
+      {
+        const float gC = reinterpret_cast<const float *>(sm + set + R_GAM)[kC - 1];
+        uint32_t r0[32], r1[32];  // both loads in flight before the wait
+        tc::tmem_ld32_issue(tmem + lane_off + COL_S + 64 * hf, r0);
+        tc::tmem_ld32_issue(tmem + lane_off + COL_S + 64 * hf + 32, r1);
+        tc::tmem_ld_wait_regs(r0);
+        tc::tmem_ld_wait_regs(r1);
+        auto convert = [&](uint32_t (&r)[32], uint32_t col) {
+          float pk[16], w[32];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = __uint_as_float(tc::pack_f16x2(-__uint_as_float(r[2 * e]), -__uint_as_float(r[2 * e + 1])));
+          tc::tmem_st16_nowait(tmem + lane_off + COL_AS + col / 2, pk);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = __uint_as_float(r[e]) * gC;
+          tc::tmem_st32_nowait(tmem + lane_off + COL_S + col, w);
+        };
+        convert(r0, 64 * hf);
+        convert(r1, 64 * hf + 32);
+      }
+      if (publish_chain()) { failed = true; break; }
+      // ---- MMA 1 (D1 of chunk c - 2 has been read by the epilogue)
+      if (tid == 0) {
+        bool ok0 = true;
+        if (c >= 2) ok0 = tc::mbar_wait(bar + B_ODONE + b, (uint32_t)((c - 2) >> 1) & 1);
+        if (!ok0) set_status(p.status, kDevTimeout);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          tc::mma16_ts(tmem + d1, tmem + COL_AS + 8 * k,
+                       (rs ? desc_wq1 : desc_wq0) + (uint64_t)((k >> 2) * 128 * 8 + 2 * (k & 3)), kId128,
+                       k > 0 ? 1u : 0u);
+        tc::mma_commit(bar + B_M1);
+        // the slot of chunk c - 1 is free once its products are done (before this MMA 1 completes): refill it
+        if (c >= 1 && c + 1 < nch) {
+          if (tc::mbar_wait(bar + B_EMPTY + (c - 1) % kSets, (uint32_t)((c - 1) / kSets) & 1))
+            issue_set(c + 1);
+          else
+            set_status(p.status, kDevTimeout);
+        }
+      }
+      // ---- U^T = U'^T + D1[:, 64:128] -> fp16 A operand; tokens [32 hf, 32 hf + 32).  U' (image: [4 slices of
+      //      32 columns][64 m][32] fp16, row-major) is read while MMA 1 runs
+      {
+        float u[32], upv[32];
+        const __half *up = reinterpret_cast<const __half *>(sm + set + R_UP + (j >> 5) * 4096) + (j & 31);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) upv[e] = __half2float(up[(32 * hf + e) * 32]);
+        ok = tc::mbar_wait(bar + B_M1, (uint32_t)c & 1) && ok;
+        tc::fence_after_sync();
+        tc::tmem_ld32(tmem + lane_off + d1 + 64 + 32 * hf, u);
+        float pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(tc::pack_f16x2(u[2 * e] + upv[2 * e], u[2 * e + 1] + upv[2 * e + 1]));
+        tc::tmem_st16_nowait(tmem + lane_off + COL_AU + 16 * hf, pk);
+      }
+      if (publish_chain()) { failed = true; break; }
+      // ---- MMA 2: S += U^T K~ (the chain's next step waits for it), then -O^T += U^T (-A_Q)^T
+      //      (K~^T and -A_Q are adjacent in the set: the -A_Q descriptor is the K~^T one + 16 KB)
+      if (tid == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma16_ts(tmem + COL_S, tmem + COL_AU + 8 * k, (rs ? desc_kt1 : desc_kt0) + (uint64_t)(2 * k), kId128, 1u);
+        tc::mma_commit(bar + B_M2);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma16_ts(tmem + d1, tmem + COL_AU + 8 * k,
+                       (rs ? desc_kt1 : desc_kt0) + (uint64_t)((R_AQ - R_KT) / 16 + 2 * k), kId64, 1u);
+        tc::mma_commit(bar + B_ORDY + b);
+        tc::mma_commit(bar + B_EMPTY + rs);
+      }
+      ok = tc::mbar_wait(bar + B_M2, (uint32_t)c & 1) && ok;
+      tc::fence_after_sync();
+    }
+    if (!ok) failed = true;
+    if (failed) {
+      if (tid == 0) set_status(p.status, kDevTimeout);
+    } else if (valid && p.final_state) {
+      float v[32];
+#pragma unroll 1
+      for (int c32 = 0; c32 < 2; ++c32) {
+        tc::tmem_ld32(tmem + lane_off + COL_S + 64 * hf + 32 * c32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) p.final_state[st_base + (size_t)(64 * hf + 32 * c32 + e) * kD] = v[e];
+      }
+    }
+  } else if (warp < kChainWarps + kEpiWarps) {
+    // ======================= RMSNormGated epilogue: thread = state column j, tokens [32 th, 32 th + 32)
+    const int ew = warp - kChainWarps, q = ew & 3, th = ew >> 2, j = 32 * q + lane, et = tid - kChainThreads;
+    const float scale = rsqrtf((float)kD);
+    float *part = reinterpret_cast<float *>(sm + S_PART);
+    float *inv = reinterpret_cast<float *>(sm + S_INV);
+    int z_issued = 0, z_done = 0;
+    auto issue_z = [&](int cc) {
+      if (et == 0) {
+        tc::mbar_arrive_expect_tx(bar + B_Z + (cc & 1), 64 * kD * 2);
+        tc::tma_load_2d(sm + S_Z + (cc & 1) * 16384, &zmap, h * kD, s0 + kC * cc, bar + B_Z + (cc & 1));
+      }
+      z_issued = cc + 1;
+    };
+    auto wait_epi = [&](uint64_t *b, uint32_t parity) {
+      const bool ok = tc::mbar_wait(b, parity);
+      tc::fence_after_sync();
+      return tc::named_barrier_or(kBarEpiTs, kEpiThreads, !ok);
+    };
+    if (nch > 0) issue_z(0);
+    if (nch > 1) issue_z(1);
+    for (int c = 0; c < nch; ++c) {
+      const int b = c & 1;
+      const uint32_t par = (c >> 1) & 1;
+      const int t0 = s0 + kC * c, Lc = min(kC, s1 - t0);
+      if (wait_epi(bar + B_ORDY + b, par)) { failed = true; break; }
+      float o[32];
+      tc::tmem_ld32(tmem + lane_off + COL_D + 128 * b + 32 * th, o);
+      tc::fence_before_sync();
+      tc::named_barrier(kBarEpiTs, kEpiThreads);
+      if (et == 0) tc::mbar_arrive(bar + B_ODONE + b);  // this chunk's D1 is read: MMA 1 of chunk c + 2 may write it
+      {  // per token: the sum over j of D1[j][r]^2 (o = -scale D1), across lanes and then lane quarters
+        float sq[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
+        part[q * 64 + 32 * th + lane] = reduce_scatter<32>(sq, lane);  // token 32 th + lane
+      }
+      tc::named_barrier(kBarEpiTs, kEpiThreads);
+      if (et < kC) {
+        const float tot = part[et] + part[64 + et] + part[128 + et] + part[192 + et];
+        inv[et] = -scale * rsqrtf(tot * (scale * scale / kD) + kEpsRms);  // o = -scale D1
+      }
+      if (wait_epi(bar + B_Z + b, par)) { failed = true; break; }  // also publishes inv[]
+      z_done = c + 1;
+      tc::bulk_wait_read();  // the previous chunk's y copies have left S_Y
+      tc::named_barrier(kBarEpiTs, kEpiThreads);
+      const __nv_bfloat16 *zt = reinterpret_cast<const __nv_bfloat16 *>(sm + S_Z + b * 16384) + 32 * th * kD + j;
+      __nv_bfloat16 *yt = reinterpret_cast<__nv_bfloat16 *>(sm + S_Y) + 32 * th * kD + j;
+      const float hw = 0.5f * sWn[j];
+      {
+        float z[32];  // every load before any store: the y tile and the z tile are not known apart
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = __bfloat162float(zt[e * kD]);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {  // o / rms(o) for four tokens
+          const float4 iv = *reinterpret_cast<const float4 *>(inv + 32 * th + e);
+          o[e] *= iv.x; o[e + 1] *= iv.y; o[e + 2] *= iv.z; o[e + 3] *= iv.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {  // token pairs: packed fp32 arithmetic
+          // silu(z) w = (w / 2) z (1 + tanh(z / 2)), the hardware tanh (as the epilogue of the split pass)
+          const float2 zz = make_float2(z[e], z[e + 1]);
+          const float2 hz = tc::mul2(zz, tc::splat2(0.5f));
+          const float2 g = tc::fma2(zz, make_float2(tc::tanh_approx(hz.x), tc::tanh_approx(hz.y)), zz);
+          const float2 y = tc::mul2(make_float2(o[e], o[e + 1]), tc::mul2(g, tc::splat2(hw)));
+          z[e] = y.x;
+          z[e + 1] = y.y;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) yt[e * kD] = __float2bfloat16_rn(z[e]);
+      }
+      tc::fence_before_sync();
+      tc::fence_async_smem();
+      tc::named_barrier(kBarEpiTs, kEpiThreads);
+      if (c + 2 < nch) issue_z(c + 2);  // into the z buffer just consumed
+      if (Lc == kC) {
+        if (et == 0) {
+          tc::tma_store_2d(&omap, h * kD, t0, sm + S_Y);
+          tc::bulk_commit();
+        }
+      } else if (et < Lc) {  // a sequence's last, short chunk: only its own rows
+        tc::bulk_s2g(out + ((size_t)(t0 + et) * h_v + h) * kD, sm + S_Y + et * kD * 2, kD * 2);
+        tc::bulk_commit();
+      }
+    }
+    tc::bulk_wait_all();
+    if (failed) {
+      if (et == 0) set_status(p.status, kDevTimeout);
+      for (int cc = z_done; cc < z_issued; ++cc) tc::mbar_wait(bar + B_Z + (cc & 1), (cc >> 1) & 1);
+    }
+  }
+  if (tid == 0)  // copies in flight must land before the CTA's shared memory goes away
+    for (int c = issued - kSets < 0 ? 0 : issued - kSets; c < issued; ++c)
+      tc::mbar_wait(bar + B_FULL + c % kSets, (uint32_t)(c / kSets) & 1);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
 // ================================================================ host side
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1433,6 +1764,22 @@ cudaError_t launch_state(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
   return e;
 }
 
+cudaError_t launch_state_ts(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
+  CUtensorMap zmap, omap;
+  std::memset(&zmap, 0, sizeof(zmap));
+  std::memset(&omap, 0, sizeof(omap));
+  if (p.T > 0 && !(make_map(&zmap, p.z, (uint64_t)p.T, (uint64_t)p.h_v * kD, kD, kC) &&
+                   make_map(&omap, p.out, (uint64_t)p.T, (uint64_t)p.h_v * kD, kD, kC)))
+    return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(state_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ts::kSmem);
+  if (e != cudaSuccess) return e;
+  trace_begin(s, GDN_K_STATE);
+  state_ts_kernel<<<(unsigned)p.N * (unsigned)p.h_v, ts::kThreads, ts::kSmem, s>>>(p, ws, zmap, omap);
+  trace_end(s);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
@@ -1469,7 +1816,10 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
     trace_end(s);
     if (e != cudaSuccess) return e;
   }
-  return state_ring(p) ? launch_state<kStateSlices, 3>(p, ws, s) : launch_state<kStateSlices, 0>(p, ws, s);
+  // Few chains (every split-column cluster on SMs of its own): the split state
+  // pass with a ring of operand sets has the shorter chain (1.6 against 2.0 us
+  // per chunk on the 4096-token workload); otherwise one CTA per chain.
+  return state_ring(p) ? launch_state<kStateSlices, 3>(p, ws, s) : launch_state_ts(p, ws, s);
 }
 
 }  // namespace gdn

@@ -31,6 +31,16 @@ GDN_API int gdn_selftest_umma(const void *A, const void *B, float *D, int *flag,
                               int fp16, void *stream);
 
 /*
+ * The same product with the A operand read from tensor memory instead of shared
+ * memory (tcgen05.mma with A in TMEM: row m in lane m, 16-bit elements packed
+ * two per 32-bit column), as the transposed state pass uses it.
+ * A [128, K], B [N, K] row-major (device), bf16 or (fp16 != 0) fp16;
+ * D fp32 [128, N].  Supported: N in {64, 128, 256}, K in {32, 64, 128}.
+ */
+GDN_API int gdn_selftest_umma_ts(const void *A, const void *B, float *D, int *flag, int N, int K, int fp16,
+                                 void *stream);
+
+/*
  * Failure detection without a fault: one CTA waits, with the bounded wait every
  * kernel of the library uses, on an mbarrier that nothing ever signals.  After
  * limit_us microseconds (1 .. 1,000,000) of %globaltimer the wait gives up, the
