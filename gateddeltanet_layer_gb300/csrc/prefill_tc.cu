@@ -78,13 +78,28 @@ constexpr int kPad = 66;  // fp32 64 x 64 matrices: padded rows (even: 8-byte al
 //   gamma    [64] fp32
 constexpr uint32_t kVWQ = 0, kVKt = 32768, kVUp = 49152, kVAq = 65536, kVGam = 73728;
 constexpr uint32_t kVSlot = 73984;
+// The compact images of the one-CTA-per-chain state pass: nothing per value
+// head that depends only on the q/k head.  Per (chunk, value head):
+//   W        2 slabs x [64 rows][64 cols] (SW128), 16 KB
+//   U'       as above, [4][64 m][32]
+//   -A_Q     as above
+//   gamma    [64] fp32;  decay-to-end e^(G_C - G_m) [64] fp32
+// and per (chunk, q/k head): Q (2 slabs x [64][64], SW128, unscaled) and the
+// K^T tile [128 i][64 m] (SW128) -- the state pass applies gamma to Q H and
+// the decay to U itself.
+constexpr uint32_t kCW = 0, kCUp = 16384, kCAq = 32768, kCGam = 40960, kCDec = 41216;
+constexpr uint32_t kCSlot = 41472;
+constexpr uint32_t kQQ = 0, kQKt = 16384, kQSlot = 32768;
+static_assert(kCSlot % 256 == 0 && kCDec + 256 == kCSlot, "compact value-head slot");
 
 struct Ws {
   int *chunk_base;   // [N + 1]: first chunk of each sequence; [N] = number of chunks
   int *seq_order;    // [N]: the sequences, longest first (by powers of two of their chunk counts); N > 1
   int4 *chunk_info;  // [max_chunks]: (sequence, first token, sequence start, tokens in the chunk)
-  uint8_t *vs;       // [max_chunks][h_v] x kVSlot
+  uint8_t *vs;       // [max_chunks][h_v] x kVSlot, or (compact) x kCSlot
+  uint8_t *qs;       // compact: [max_chunks][h_qk] x kQSlot (after the value-head slots)
   int max_chunks;
+  int compact;       // the images are the compact ones (one-CTA-per-chain state pass)
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -93,13 +108,15 @@ struct WsLayout {
   size_t base, order, info, vs, total;
   int max_chunks;
   WsLayout(int T, int N, int h_qk, int h_v) {
-    (void)h_qk;
     max_chunks = (T + kC - 1) / kC + N;
     base = 0;
     order = align_up(sizeof(int) * (size_t)(N + 1), 256);
     info = align_up(order + sizeof(int) * (size_t)N, 1024);
     vs = align_up(info + sizeof(int4) * (size_t)max_chunks, 1024);
-    total = vs + (size_t)max_chunks * h_v * kVSlot;
+    // the larger of the two image layouts (split pass: kVSlot per value head; compact: kCSlot per
+    // value head and kQSlot per q/k head)
+    const size_t split = (size_t)h_v * kVSlot, compact = (size_t)h_v * kCSlot + (size_t)h_qk * kQSlot;
+    total = vs + (size_t)max_chunks * (split > compact ? split : compact);
   }
 };
 
@@ -405,7 +422,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   bool failed = false;
 
   const int r0 = 8 * warp, c0 = 4 * lane;  // conv: this thread's rows and channels
-  auto v_slot_of = [&](int vv) { return ws.vs + ((size_t)g * h_v + hq * rep + vv) * kVSlot; };
+  const bool compact = ws.compact != 0;
+  auto v_slot_of = [&](int vv) {
+    return ws.vs + ((size_t)g * h_v + hq * rep + vv) * (compact ? kCSlot : kVSlot);
+  };
+  uint8_t *const q_slot = ws.qs + ((size_t)g * h_qk + hq) * kQSlot;  // compact only
 
   // the v rows of the first pair into L2 while the q/k rows are worked on
   auto prefetch_v = [&](int vv) {
@@ -442,10 +463,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       sG[vv * 256 + r] = gsum;
       const float gm = expf(gsum);
       sG[vv * 256 + 64 + r] = gm;
-      *reinterpret_cast<float *>(v_slot_of(vv) + kVGam + 4 * r) = gm;
+      *reinterpret_cast<float *>(v_slot_of(vv) + (compact ? kCGam : kVGam) + 4 * r) = gm;
     }
     __syncthreads();
-    if (vv < rep) sG[vv * 256 + 192 + r] = expf(sG[vv * 256 + 63] - sG[vv * 256 + r]);
+    if (vv < rep) {
+      const float dec = expf(sG[vv * 256 + 63] - sG[vv * 256 + r]);
+      sG[vv * 256 + 192 + r] = dec;
+      if (compact) *reinterpret_cast<float *>(v_slot_of(vv) + kCDec + 4 * r) = dec;
+    }
     __syncthreads();
   }
 
@@ -471,14 +496,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       *reinterpret_cast<uint2 *>(sm + P_KQ + off) = hi;
       *reinterpret_cast<uint2 *>(sm + P_KQL + off) = lo;
     }
-    for (int vv = 0; vv < rep; ++vv) {  // Q^ = diag(gamma) Q: rows 0-63 of the [Q^; W] image
-      const float *gam = sG + vv * 256 + 64;
-      uint8_t *dst = v_slot_of(vv) + kVWQ;
+    if (compact) {  // Q, once per q/k head: [64 rows] SW128 slabs
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const float2 gr = tc::splat2(gam[r0 + r]);
-        const float2 q01 = tc::mul2(gr, make_float2(y[r][0], y[r][1])), q23 = tc::mul2(gr, make_float2(y[r][2], y[r][3]));
-        *reinterpret_cast<uint2 *>(dst + tc::sw128_offset(128, r0 + r, c0)) = pack4_f16(q01.x, q01.y, q23.x, q23.y);
+      for (int r = 0; r < 8; ++r)
+        *reinterpret_cast<uint2 *>(q_slot + kQQ + tc::sw128_offset(64, r0 + r, c0)) =
+            pack4_f16(y[r][0], y[r][1], y[r][2], y[r][3]);
+    } else {
+      for (int vv = 0; vv < rep; ++vv) {  // Q^ = diag(gamma) Q: rows 0-63 of the [Q^; W] image
+        const float *gam = sG + vv * 256 + 64;
+        uint8_t *dst = v_slot_of(vv) + kVWQ;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float2 gr = tc::splat2(gam[r0 + r]);
+          const float2 q01 = tc::mul2(gr, make_float2(y[r][0], y[r][1])),
+                       q23 = tc::mul2(gr, make_float2(y[r][2], y[r][3]));
+          *reinterpret_cast<uint2 *>(dst + tc::sw128_offset(128, r0 + r, c0)) = pack4_f16(q01.x, q01.y, q23.x, q23.y);
+        }
       }
     }
     conv_silu(xrk, p.conv_w, h_qk * kD + hq * kD + c0, Lc, r0, kreg);
@@ -594,7 +627,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         // image in order (512 contiguous bytes per warp store), synchronised among its own 64 threads
         const int pr = warp & 1, t = 32 * (warp >> 2) + lane;
         tc::named_barrier(1 + pr, 64);
-        uint8_t *dst = v_slot_of(grp + hh) + kVAq;
+        uint8_t *dst = v_slot_of(grp + hh) + (compact ? kCAq : kVAq);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int q = 256 * pr + t + 64 * k;
@@ -612,8 +645,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       float x[16];
       const int hh = tid >> 6, bb = (tid >> 4) & 3, s = tid & 15;
       const bool act = hh < nh;
-      if (tid >= 128) {  // meanwhile: the K~^T = (diag(e^(G_C - G)) K)^T images of the pair, from the K^T
-                         // tile (the image has its SW128 layout), 16-byte chunks in order
+      if (tid >= 128 && compact) {  // meanwhile: the K^T tile to its image, once per q/k head
+        if (grp == 0) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int q = tid - 128 + 128 * k;
+            *reinterpret_cast<uint4 *>(q_slot + kQKt + 16 * q) = *reinterpret_cast<const uint4 *>(sm + P_KT + 16 * q);
+          }
+        }
+      } else if (tid >= 128) {  // meanwhile: the K~^T = (diag(e^(G_C - G)) K)^T images of the pair, from the
+                                // K^T tile (the image has its SW128 layout), 16-byte chunks in order
         for (int h2 = 0; h2 < nh; ++h2) {
           const float *dec = sGall + (grp + h2) * 256 + 192;
           uint8_t *dst = v_slot_of(grp + h2) + kVKt;
@@ -822,12 +863,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int q = tid + kPrepThreads * k;  // 16-byte chunk q of 1024
-        // W: staged bytes [0, 8K) -> image slab 0 rows 64-127, [8K, 16K) -> slab 1 rows 64-127
-        *reinterpret_cast<uint4 *>(v_slot + kVWQ + 8192 + 16 * q + (q >= 512 ? 8192 : 0)) =
+        // W: staged bytes [0, 8K) -> image slab 0 rows 64-127, [8K, 16K) -> slab 1 rows 64-127 (compact: the
+        // two 64-row slabs of the W image, the same bytes in order)
+        *reinterpret_cast<uint4 *>(v_slot + (compact ? kCW + 16 * q : kVWQ + 8192 + 16 * q + (q >= 512 ? 8192 : 0))) =
             *reinterpret_cast<const uint4 *>(stw + 16 * q);
         // U': image chunk q = (slice q / 256, row m, chunk q % 4)
         const int m = (q >> 2) & 63;
-        *reinterpret_cast<uint4 *>(v_slot + kVUp + 16 * q) =
+        *reinterpret_cast<uint4 *>(v_slot + (compact ? kCUp : kVUp) + 16 * q) =
             *reinterpret_cast<const uint4 *>(stu + (q >> 8) * 4096 + m * 64 + (((q & 3) ^ ((m >> 1) & 3)) << 4));
       }
     }
@@ -1338,15 +1380,19 @@ __global__ void __launch_bounds__(StateCfg<NS, ST>::kThreads, StateCfg<NS, ST>::
 }
 
 // ================================================================ state pass, transposed
-// One CTA per (sequence, value head) chain, owning the whole state.  The state
-// is kept transposed, S = H^T (lanes j over d_v, columns i over d_k, fp32 in
-// tensor memory), so both products of a chunk take their A operand straight
-// from tensor memory (an fp16 copy written there by the chain warps) and run at
-// N = 128:
-//   MMA 1:  D1 = (-S) [Q^; W]^T        columns 0-63: -(Q^ H)^T, 64-127: -(W H)^T
-//           U^T = U'^T + D1[:, 64:128]  (fp32, then its fp16 copy in tensor memory)
-//   MMA 2:  S  += U^T K~               (S scaled by gamma_C before)
-//           D1[:, 0:64] += U^T (-A_Q)^T  (-O^T, for the epilogue)
+// One CTA per (sequence, value head) chain, owning the whole state, on the
+// compact images.  The state is kept transposed, S = H^T (lanes j over d_v,
+// columns i over d_k, fp32 in tensor memory), so both products of a chunk
+// take their A operand straight from tensor memory (fp16 copies written there
+// by the chain warps) and run at N = 128:
+//   MMA 1:  D1 = (-S) [Q; W]^T          columns 0-63: -(Q H)^T, 64-127: -(W H)^T
+//           U^T = U'^T + D1[:, 64:128]   (fp32), then two fp16 copies in tensor
+//           memory: U^T diag(d) (d_m = e^(G_C - G_m), the decay to the chunk's
+//           end) and U^T itself
+//   MMA 2:  S  += (U^T diag(d)) K        (S scaled by gamma_C before; K from the
+//                                          unscaled K^T image: this is K~^T U)
+//           O2  = U^T (-A_Q)^T           (-(A_Q U)^T)
+//   y:      o_r = -scale (gamma_r D1[:, r] + O2[:, r]),  y = o / rms(o) w silu(z)
 // 16 tcgen05.mma per chunk (8 + 4 + 4) against 64 when the columns of H are
 // split over four CTAs, and no shared-memory round trip for the operands the
 // chain computes.  Warps 0-7 run the chain (warp w: TMEM lanes 32 (w & 3), half
@@ -1361,9 +1407,11 @@ constexpr int kChainWarps = 8, kEpiWarps = 8;
 constexpr int kChainThreads = 32 * kChainWarps, kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 32 * (kChainWarps + kEpiWarps);
 constexpr int kSets = 2;
-// one operand set: [Q^; W] (32 KB), K~^T (16 KB), -A_Q (8 KB), U' of every column (16 KB), gamma
-constexpr uint32_t R_WQ = 0, R_KT = 32768, R_AQ = 49152, R_UP = 57344, R_GAM = 73728;
-constexpr uint32_t kStage = 74752;                     // 73 KB, 1024-aligned
+// one operand set: [Q; W] (two slabs of [64 Q rows; 64 W rows], 32 KB), K^T (16 KB), -A_Q (8 KB),
+// U' of every column (16 KB), gamma and the decays to the chunk's end (256 B each)
+constexpr uint32_t R_WQ = 0, R_KT = 32768, R_AQ = 49152, R_UP = 57344, R_GAM = 73728, R_DEC = 73984;
+constexpr uint32_t kSetBytes = 32768 + 16384 + 8192 + 16384 + 512;
+constexpr uint32_t kStage = 75776;                      // 74 KB, 1024-aligned
 constexpr uint32_t S_Z = kSets * kStage;                // z [2][64 t][128] bf16 (TMA)
 constexpr uint32_t S_Y = S_Z + 2 * 16384;               // y [64 t][128] bf16 (TMA store)
 constexpr uint32_t S_WN = S_Y + 16384;                  // norm_w [128]
@@ -1371,14 +1419,16 @@ constexpr uint32_t S_PART = S_WN + 512;                 // sums of o^2 [4 lane q
 constexpr uint32_t S_INV = S_PART + 1024;               // 1 / rms per token [64]
 constexpr uint32_t S_MISC = S_INV + 256;
 constexpr size_t kSmem = S_MISC + 256 + 1024;
-// barriers: full[2], empty[2], m1, m2, oready[2], odone[2], z[2]
-constexpr int B_FULL = 0, B_EMPTY = 2, B_M1 = 4, B_M2 = 5, B_ORDY = 6, B_ODONE = 8, B_Z = 10, kBars = 12;
-// tensor memory: S, two D1 buffers, the fp16 -S (64 columns) and U^T (32 columns)
-constexpr uint32_t COL_S = 0, COL_D = 128, COL_AS = 384, COL_AU = 448, kTmemCols = 512;
+// barriers: full[2], empty[2], m1, m2, oready, odone, z[2]
+constexpr int B_FULL = 0, B_EMPTY = 2, B_M1 = 4, B_M2 = 5, B_ORDY = 6, B_ODONE = 7, B_Z = 8, kBars = 10;
+// tensor memory: S, D1, O2, the fp16 -S (64 columns), U^T diag(d) and U^T (32 columns each)
+constexpr uint32_t COL_S = 0, COL_D = 128, COL_O2 = 256, COL_AS = 320, COL_AU = 384, COL_AU2 = 416;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kId128 = tc::idesc_f16(128, 128), kId64 = tc::idesc_f16(128, 64);
-static_assert(R_GAM + 256 <= kStage && kStage % 1024 == 0, "operand set");
+static_assert(R_DEC + 256 <= kStage && kStage % 1024 == 0 && R_WQ + kSetBytes == R_DEC + 256, "operand set");
 static_assert(kSmem <= 232448, "shared memory budget (one CTA per SM)");
 static_assert(kBars * 8 + 4 <= 256, "barrier block");
+static_assert(COL_AU2 + 32 <= kTmemCols, "tensor memory");
 constexpr int kBarChain = 3, kBarEpiTs = 4;
 }  // namespace ts
 
@@ -1389,7 +1439,7 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = tc::smem_u32(sm);
-  const int h_v = p.h_v;
+  const int h_v = p.h_v, h_qk = p.h_qk, hq = (blockIdx.x % h_v) / (h_v / h_qk);
   const int chain = blockIdx.x, h = chain % h_v;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -1422,23 +1472,27 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
   const int g0 = valid ? ws.chunk_base[n] : 0, g1 = valid ? ws.chunk_base[n + 1] : 0;
   if (valid && g1 - g0 != (s1 - s0 + kC - 1) / kC) valid = false;  // table overflow, reported
   const int nch = valid ? g1 - g0 : 0;
-  auto slot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kVSlot; };
+  auto vslot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kCSlot; };
+  auto qslot = [&](int gg) { return ws.qs + ((size_t)gg * h_qk + hq) * kQSlot; };
   auto set_at = [](int c) -> uint32_t { return kStage * (uint32_t)(c % kSets); };
 
   int issued = 0;  // operand sets issued (thread 0)
   auto issue_set = [&](int c) {
     uint8_t *dst = sm + set_at(c);
-    const uint8_t *src = slot(g0 + c);
+    const uint8_t *v = vslot(g0 + c), *q = qslot(g0 + c);
     uint64_t *full = bar + B_FULL + c % kSets;
-    tc::mbar_arrive_expect_tx(full, 32768 + 16384 + 8192 + 16384 + 256);
-    tc::bulk_g2s(dst + R_WQ, src + kVWQ, 32768 + 16384, full);  // [Q^; W] and K~^T
-    tc::bulk_g2s(dst + R_AQ, src + kVAq, 8192, full);
-    tc::bulk_g2s(dst + R_UP, src + kVUp, 16384, full);
-    tc::bulk_g2s(dst + R_GAM, src + kVGam, 256, full);
+    tc::mbar_arrive_expect_tx(full, kSetBytes);
+    tc::bulk_g2s(dst + R_WQ, q + kQQ, 8192, full);                   // slab 0: Q rows 0-63
+    tc::bulk_g2s(dst + R_WQ + 8192, v + kCW, 8192, full);            //         W rows 64-127
+    tc::bulk_g2s(dst + R_WQ + 16384, q + kQQ + 8192, 8192, full);    // slab 1: Q
+    tc::bulk_g2s(dst + R_WQ + 24576, v + kCW + 8192, 8192, full);    //         W
+    tc::bulk_g2s(dst + R_KT, q + kQKt, 16384, full);
+    tc::bulk_g2s(dst + R_AQ, v + kCAq, 8192, full);
+    tc::bulk_g2s(dst + R_UP, v + kCUp, 16384, full);
+    tc::bulk_g2s(dst + R_GAM, v + kCGam, 512, full);                  // gamma and the decays
     if (c + 1 < nch) {  // the set after: into L2 now
-      const uint8_t *nx = slot(g0 + c + 1);
-      tc::prefetch_l2(nx, kVSlot / 2);
-      tc::prefetch_l2(nx + kVSlot / 2, kVSlot / 2);
+      tc::prefetch_l2(vslot(g0 + c + 1), kCSlot);
+      tc::prefetch_l2(qslot(g0 + c + 1), kQSlot);
     }
     issued = c + 1;
   };
@@ -1478,9 +1532,8 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
     }
     if (publish_chain()) failed = true;
     for (int c = 0; c < nch && !failed; ++c) {
-      const int b = c & 1, rs = c % kSets;
+      const int rs = c % kSets;
       const uint32_t set = set_at(c);
-      const uint32_t d1 = COL_D + 128 * b;
       ok = tc::mbar_wait(bar + B_FULL + rs, (uint32_t)(c / kSets) & 1) && ok;
       // ---- S -> gamma_C S in place, and its fp16 negative as the A operand of MMA 1
       {
@@ -1504,15 +1557,15 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
         convert(r1, 64 * hf + 32);
       }
       if (publish_chain()) { failed = true; break; }
-      // ---- MMA 1 (D1 of chunk c - 2 has been read by the epilogue)
+      // ---- MMA 1 (D1 and O2 of chunk c - 1 have been read by the epilogue)
       if (tid == 0) {
         bool ok0 = true;
-        if (c >= 2) ok0 = tc::mbar_wait(bar + B_ODONE + b, (uint32_t)((c - 2) >> 1) & 1);
+        if (c >= 1) ok0 = tc::mbar_wait(bar + B_ODONE, (uint32_t)(c - 1) & 1);
         if (!ok0) set_status(p.status, kDevTimeout);
         tc::fence_after_sync();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          tc::mma16_ts(tmem + d1, tmem + COL_AS + 8 * k,
+          tc::mma16_ts(tmem + COL_D, tmem + COL_AS + 8 * k,
                        (rs ? desc_wq1 : desc_wq0) + (uint64_t)((k >> 2) * 128 * 8 + 2 * (k & 3)), kId128,
                        k > 0 ? 1u : 0u);
         tc::mma_commit(bar + B_M1);
@@ -1524,24 +1577,34 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
             set_status(p.status, kDevTimeout);
         }
       }
-      // ---- U^T = U'^T + D1[:, 64:128] -> fp16 A operand; tokens [32 hf, 32 hf + 32).  U' (image: [4 slices of
-      //      32 columns][64 m][32] fp16, row-major) is read while MMA 1 runs
+      // ---- U^T = U'^T + D1[:, 64:128] -> fp16 A operands; tokens [32 hf, 32 hf + 32).  U' (image: [4 slices
+      //      of 32 columns][64 m][32] fp16, row-major) and the decays are read while MMA 1 runs
       {
-        float u[32], upv[32];
+        float u[32], upv[32], dm[32];
         const __half *up = reinterpret_cast<const __half *>(sm + set + R_UP + (j >> 5) * 4096) + (j & 31);
 #pragma unroll
         for (int e = 0; e < 32; ++e) upv[e] = __half2float(up[(32 * hf + e) * 32]);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = *reinterpret_cast<const float4 *>(sm + set + R_DEC + 4 * (32 * hf + e));
+          dm[e] = d4.x; dm[e + 1] = d4.y; dm[e + 2] = d4.z; dm[e + 3] = d4.w;
+        }
         ok = tc::mbar_wait(bar + B_M1, (uint32_t)c & 1) && ok;
         tc::fence_after_sync();
-        tc::tmem_ld32(tmem + lane_off + d1 + 64 + 32 * hf, u);
-        float pk[16];
+        tc::tmem_ld32(tmem + lane_off + COL_D + 64 + 32 * hf, u);
+        float pk[16], pd[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(tc::pack_f16x2(u[2 * e] + upv[2 * e], u[2 * e + 1] + upv[2 * e + 1]));
-        tc::tmem_st16_nowait(tmem + lane_off + COL_AU + 16 * hf, pk);
+        for (int e = 0; e < 16; ++e) {
+          const float u0 = u[2 * e] + upv[2 * e], u1 = u[2 * e + 1] + upv[2 * e + 1];
+          pk[e] = __uint_as_float(tc::pack_f16x2(u0, u1));
+          pd[e] = __uint_as_float(tc::pack_f16x2(u0 * dm[2 * e], u1 * dm[2 * e + 1]));
+        }
+        tc::tmem_st16_nowait(tmem + lane_off + COL_AU + 16 * hf, pd);
+        tc::tmem_st16_nowait(tmem + lane_off + COL_AU2 + 16 * hf, pk);
       }
       if (publish_chain()) { failed = true; break; }
-      // ---- MMA 2: S += U^T K~ (the chain's next step waits for it), then -O^T += U^T (-A_Q)^T
-      //      (K~^T and -A_Q are adjacent in the set: the -A_Q descriptor is the K~^T one + 16 KB)
+      // ---- MMA 2: S += (U^T diag(d)) K (the chain's next step waits for it), then O2 = U^T (-A_Q)^T
+      //      (K^T and -A_Q are adjacent in the set: the -A_Q descriptor is the K^T one + 16 KB)
       if (tid == 0) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -1549,9 +1612,9 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
         tc::mma_commit(bar + B_M2);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc::mma16_ts(tmem + d1, tmem + COL_AU + 8 * k,
-                       (rs ? desc_kt1 : desc_kt0) + (uint64_t)((R_AQ - R_KT) / 16 + 2 * k), kId64, 1u);
-        tc::mma_commit(bar + B_ORDY + b);
+          tc::mma16_ts(tmem + COL_O2, tmem + COL_AU2 + 8 * k,
+                       (rs ? desc_kt1 : desc_kt0) + (uint64_t)((R_AQ - R_KT) / 16 + 2 * k), kId64, k > 0 ? 1u : 0u);
+        tc::mma_commit(bar + B_ORDY);
         tc::mma_commit(bar + B_EMPTY + rs);
       }
       ok = tc::mbar_wait(bar + B_M2, (uint32_t)c & 1) && ok;
@@ -1569,7 +1632,7 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
         for (int e = 0; e < 32; ++e) p.final_state[st_base + (size_t)(64 * hf + 32 * c32 + e) * kD] = v[e];
       }
     }
-  } else if (warp < kChainWarps + kEpiWarps) {
+  } else {
     // ======================= RMSNormGated epilogue: thread = state column j, tokens [32 th, 32 th + 32)
     const int ew = warp - kChainWarps, q = ew & 3, th = ew >> 2, j = 32 * q + lane, et = tid - kChainThreads;
     const float scale = rsqrtf((float)kD);
@@ -1594,13 +1657,30 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
       const int b = c & 1;
       const uint32_t par = (c >> 1) & 1;
       const int t0 = s0 + kC * c, Lc = min(kC, s1 - t0);
-      if (wait_epi(bar + B_ORDY + b, par)) { failed = true; break; }
+      float gam[32];  // gamma of this thread's tokens, from the chunk's image (its ring slot may be refilled)
+      {
+        const float4 *gp = reinterpret_cast<const float4 *>(vslot(g0 + c) + kCGam) + 8 * th;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 g4 = gp[e];
+          gam[4 * e] = g4.x; gam[4 * e + 1] = g4.y; gam[4 * e + 2] = g4.z; gam[4 * e + 3] = g4.w;
+        }
+      }
+      if (wait_epi(bar + B_ORDY, (uint32_t)c & 1)) { failed = true; break; }
       float o[32];
-      tc::tmem_ld32(tmem + lane_off + COL_D + 128 * b + 32 * th, o);
+      {
+        uint32_t r1[32], r2[32];
+        tc::tmem_ld32_issue(tmem + lane_off + COL_D + 32 * th, r1);
+        tc::tmem_ld32_issue(tmem + lane_off + COL_O2 + 32 * th, r2);
+        tc::tmem_ld_wait_regs(r1);
+        tc::tmem_ld_wait_regs(r2);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = fmaf(gam[e], __uint_as_float(r1[e]), __uint_as_float(r2[e]));
+      }
       tc::fence_before_sync();
       tc::named_barrier(kBarEpiTs, kEpiThreads);
-      if (et == 0) tc::mbar_arrive(bar + B_ODONE + b);  // this chunk's D1 is read: MMA 1 of chunk c + 2 may write it
-      {  // per token: the sum over j of D1[j][r]^2 (o = -scale D1), across lanes and then lane quarters
+      if (et == 0) tc::mbar_arrive(bar + B_ODONE);  // D1 and O2 are read: the next chunk's products may write them
+      {  // per token: the sum over j of o^2 (o = -scale (gamma D1 + O2)), across lanes and then lane quarters
         float sq[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
@@ -1609,7 +1689,7 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
       tc::named_barrier(kBarEpiTs, kEpiThreads);
       if (et < kC) {
         const float tot = part[et] + part[64 + et] + part[128 + et] + part[192 + et];
-        inv[et] = -scale * rsqrtf(tot * (scale * scale / kD) + kEpsRms);  // o = -scale D1
+        inv[et] = -scale * rsqrtf(tot * (scale * scale / kD) + kEpsRms);
       }
       if (wait_epi(bar + B_Z + b, par)) { failed = true; break; }  // also publishes inv[]
       z_done = c + 1;
@@ -1792,6 +1872,9 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   ws.chunk_info = reinterpret_cast<int4 *>(p.ws + L.info);
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
+  const bool split_pass = state_ring(p);
+  ws.compact = split_pass ? 0 : 1;
+  ws.qs = ws.vs + (size_t)L.max_chunks * p.h_v * kCSlot;
 
   trace_begin(s, GDN_K_CHUNK_TABLE);
   chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
@@ -1819,7 +1902,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   // Few chains (every split-column cluster on SMs of its own): the split state
   // pass with a ring of operand sets has the shorter chain (1.6 against 2.0 us
   // per chunk on the 4096-token workload); otherwise one CTA per chain.
-  return state_ring(p) ? launch_state<kStateSlices, 3>(p, ws, s) : launch_state_ts(p, ws, s);
+  return split_pass ? launch_state<kStateSlices, 3>(p, ws, s) : launch_state_ts(p, ws, s);
 }
 
 }  // namespace gdn
