@@ -1,25 +1,34 @@
 // Backward pass of the layer (reverse mode), fp32 on the CUDA cores.
 //
 // The gradient of a scalar loss with respect to every input, given the
-// gradient dy of the output y (and optionally of the final state).  Three
-// launches on the caller's stream:
+// gradient dy of the output y (and optionally of the final state).  The
+// columns j of the state H = S^T (d_v) evolve independently under the rule,
+// and so do the columns of its gradient G, so every chain (sequence, value
+// head) is split over ceil(d_v / 32) CTAs of 32 columns each; what a token
+// step sums over columns (the gradients of q, k, alpha, beta) is added up
+// across them with atomic adds.  Five launches on the caller's stream:
 //
-//   bwd_chain_kernel     one CTA per (sequence, value head) chain.  Forward
-//                        over the sequence in blocks of kB tokens, writing the
-//                        state H = S^T at each block start to the workspace;
-//                        then the blocks in reverse: the block's q, k, v, gates
-//                        and states recomputed from its checkpoint (every
-//                        state kept in the workspace), RMSNormGated in reverse
-//                        (dz, dnorm_w, do), and the rule in reverse token by
-//                        token with the gradient G of the state in registers:
+//   bwd_fwd_kernel       per (chain, column slice): forward over the sequence
+//                        in blocks of kB tokens, writing the slice of the
+//                        state at each block start and o of every token to
+//                        the workspace.
+//   bwd_norm_kernel      per (token, value head) row: RMSNormGated in reverse
+//                        (it needs whole rows): do to the workspace, dz, and
+//                        the sums into dnorm_w.
+//   bwd_rev_kernel       per (chain, column slice): the blocks in reverse: the
+//                        block's q, k, v and gates, and its states from the
+//                        checkpoint (every state kept in the workspace), then
+//                        the rule in reverse token by token with the slice of
+//                        the state's gradient G in registers:
 //                          G += scale q do^T,        dq = scale H_t do
 //                          dalpha = <G, H_{t-1}>,    du = G^T k,  dk = G u
 //                          dbeta = du.(v - alpha p), dv = beta du
 //                          dalpha -= beta du.p,      dp = -alpha beta du
 //                          dk += H_{t-1} dp,         G <- alpha G + k dp^T
-//                        Writes dz, the gradients of the normalised q, k, of
-//                        the conv'd v and of the gates per (token, value head)
-//                        to the workspace, and the initial state's gradient.
+//                        adding the gradients of the normalised q, k and of
+//                        the gates per (token, value head) into the workspace,
+//                        writing those of silu(conv(v)) and of the initial
+//                        state for its columns.
 //   bwd_prologue_kernel  per (token tile, conv head): the q / k gradients of
 //                        the value heads of a q/k head summed, L2 norm and
 //                        SiLU in reverse (the conv recomputed), then the
@@ -27,10 +36,12 @@
 //   bwd_gate_kernel      per (token, value head): da, db, and the sums into
 //                        dA_log and ddt_bias.
 //
-// The state layout follows the forward fp32 kernel: warp w owns columns
-// [8w, 8w+8) of H, lane l rows l, l+32, l+64, l+96.  Sums over tokens or
-// heads into one parameter (conv_w, A_log, dt_bias, norm_w) are fp32 atomic
-// adds, so their rounding order is not fixed from run to run.
+// The slice layout follows the forward fp32 kernel: warp w owns columns
+// [8w, 8w+8) of the slice, lane l rows l, l+32, l+64, l+96.  Sums into one
+// value from several CTAs are atomic adds, so their rounding order is not
+// fixed from run to run: fp32 for the per-token q, k and gate gradients (a
+// few terms each), fp64 for the parameter gradients (conv_w, A_log, dt_bias,
+// norm_w: sums over every token and head, converted to fp32 at the end).
 #include "gdn_common.cuh"
 #include "../../include/gdn_trace.h"
 #include "gdn_internal.h"
@@ -38,49 +49,56 @@
 namespace gdn {
 namespace {
 
-constexpr int kB = 32;     // tokens per block (checkpoint interval, prologue batch)
-constexpr int kCW = 8;     // state columns per warp
-constexpr int kRows = 4;   // rows per lane (d_k <= 128)
+constexpr int kB = 32;        // tokens per block (checkpoint interval, prologue batch)
+constexpr int kCW = 8;        // state columns per warp
+constexpr int kRows = 4;      // rows per lane (d_k <= 128)
 constexpr int kSlot = kRows * kCW;  // state values per thread
+constexpr int kSliceWarps = 4, kSliceCols = kCW * kSliceWarps, kSliceThreads = 32 * kSliceWarps;
 
 struct BwdWs {
-  float *ckpt;   // [slots][h_v][threads][kSlot]: the state at each block start
-  float *hs;     // [N][h_v][kB + 1][threads][kSlot]: the states of the block in reverse
-  float *dqn;    // [T][h_v][d_k]: gradient of the normalised q (per value head)
+  float *ckpt;   // [slots][h_v][slices][kSliceThreads][kSlot]: the state slice at each block start
+  float *hs;     // [N][h_v][slices][kB + 1][kSliceThreads][kSlot]: the block's states, in reverse
+  float *wo;     // [T][h_v][d_v]: o (scaled) of every token
+  float *wdo;    // [T][h_v][d_v]: its gradient
+  float *dqn;    // [T][h_v][d_k]: gradient of the normalised q (per value head; summed over slices)
   float *dkn;    // [T][h_v][d_k]
   float *dvs;    // [T][h_v][d_v]: gradient of silu(conv(v))
   float *dg;     // [T][h_v]
   float *dbeta;  // [T][h_v]
-  int slots;     // ceil(T / kB) + N
+  double *acc;   // fp64 sums: conv_w [Cc][4], A_log [h_v], dt_bias [h_v], norm_w [d_v]
+  int slices;    // ceil(d_v / kSliceCols)
 };
 
 struct BwdLayout {
-  size_t ckpt, hs, dqn, dkn, dvs, dg, dbeta, total;
-  int slots;
-  BwdLayout(int T, int N, int h_v, int d_k, int d_v) {
-    const size_t threads = 32 * (size_t)((d_v + kCW - 1) / kCW);
-    const size_t st = threads * kSlot * sizeof(float);
+  size_t ckpt, hs, wo, wdo, dqn, dkn, dvs, dg, dbeta, acc, total;
+  int slots, slices;
+  BwdLayout(int T, int N, int h_qk, int h_v, int d_k, int d_v) {
+    slices = (d_v + kSliceCols - 1) / kSliceCols;
+    const size_t st = (size_t)kSliceThreads * kSlot * sizeof(float);  // one state slice
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     slots = (T + kB - 1) / kB + N;
     ckpt = 0;
-    hs = up(ckpt + (size_t)slots * h_v * st);
-    dqn = up(hs + (size_t)N * h_v * (kB + 1) * st);
+    hs = up(ckpt + (size_t)slots * h_v * slices * st);
+    wo = up(hs + (size_t)N * h_v * slices * (kB + 1) * st);
+    wdo = up(wo + (size_t)T * h_v * d_v * sizeof(float));
+    dqn = up(wdo + (size_t)T * h_v * d_v * sizeof(float));
     dkn = up(dqn + (size_t)T * h_v * d_k * sizeof(float));
     dvs = up(dkn + (size_t)T * h_v * d_k * sizeof(float));
     dg = up(dvs + (size_t)T * h_v * d_v * sizeof(float));
     dbeta = up(dg + (size_t)T * h_v * sizeof(float));
-    total = up(dbeta + (size_t)T * h_v * sizeof(float));
+    acc = up(dbeta + (size_t)T * h_v * sizeof(float));
+    total = up(acc + sizeof(double) * ((size_t)(2 * h_qk * d_k + h_v * d_v) * 4 + 2 * h_v + d_v));
   }
 };
 
-// The block's prologue (as the forward fp32 kernel): conv(4) + SiLU of q, k,
-// v, L2 norm of q, k, and the gates, for tokens [t0, t0 + nt) of sequence
-// [s0, s1) into shared memory.
+// The block's prologue (as the forward fp32 kernel): conv(4) + SiLU of q, k
+// and of the slice's columns [j0, j0 + kSliceCols) of v, L2 norm of q, k, and
+// the gates, for tokens [t0, t0 + nt) of sequence [s0, s1) into shared memory.
 template <typename IO>
-__device__ void block_prologue(const BwdParams &p, int h, int hq, int s0, int t0, int nt, float *sq, float *sk,
-                               float *sv, float *salpha, float *sbeta, float A_exp, float dtb) {
+__device__ void block_prologue(const BwdParams &p, int h, int hq, int s0, int t0, int nt, int j0, float *sq,
+                               float *sk, float *sv, float *salpha, float *sbeta, float A_exp, float dtb) {
   const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
-  const int nch = 2 * dk + dv;
+  const int nch = 2 * dk + kSliceCols;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const IO *xq = static_cast<const IO *>(p.q), *xk = static_cast<const IO *>(p.k), *xv = static_cast<const IO *>(p.v);
   const IO *xa = static_cast<const IO *>(p.a), *xb = static_cast<const IO *>(p.b);
@@ -97,8 +115,10 @@ __device__ void block_prologue(const BwdParams &p, int h, int hq, int s0, int t0
       const int cc = c - dk;
       src = xk + hq * dk + cc; stride = (size_t)h_qk * dk; ch = h_qk * dk + hq * dk + cc; dst = sk + tt * dk + cc;
     } else {
-      const int cc = c - 2 * dk;
-      src = xv + h * dv + cc; stride = (size_t)h_v * dv; ch = 2 * h_qk * dk + h * dv + cc; dst = sv + tt * dv + cc;
+      const int cc = c - 2 * dk, jj = j0 + cc;
+      dst = sv + tt * kSliceCols + cc;
+      if (jj >= dv) { *dst = 0.0f; continue; }
+      src = xv + h * dv + jj; stride = (size_t)h_v * dv; ch = 2 * h_qk * dk + h * dv + jj;
     }
     float pre = 0.0f;
 #pragma unroll
@@ -124,165 +144,204 @@ __device__ void block_prologue(const BwdParams &p, int h, int hq, int s0, int t0
   __syncthreads();
 }
 
-template <typename IO>
-__global__ void __launch_bounds__(512) bwd_chain_kernel(const BwdParams p, const BwdWs ws) {
-  const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
-  const int n = blockIdx.x / h_v, h = blockIdx.x % h_v, hq = h / (h_v / h_qk);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
-  const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
-  if (s0 < 0 || s1 < s0 || s1 > p.T) {
-    if (tid == 0) set_status(p.status, kDevBadSeqlens);
-    return;
+// What a (chain, column slice) CTA works with: its chain, sequence and slice.
+struct SliceCtx {
+  int n, h, hq, sl, j0, s0, s1, nblk, slot0;
+  bool ok;
+};
+__device__ __forceinline__ SliceCtx slice_ctx(const BwdParams &p, int slices) {
+  SliceCtx c;
+  const int chain = blockIdx.x / slices;
+  c.sl = blockIdx.x % slices;
+  c.n = chain / p.h_v;
+  c.h = chain % p.h_v;
+  c.hq = c.h / (p.h_v / p.h_qk);
+  c.j0 = kSliceCols * c.sl;
+  c.s0 = p.cu_seqlens[c.n];
+  c.s1 = p.cu_seqlens[c.n + 1];
+  c.ok = c.s0 >= 0 && c.s1 >= c.s0 && c.s1 <= p.T;
+  c.nblk = c.ok ? (c.s1 - c.s0 + kB - 1) / kB : 0;
+  c.slot0 = c.s0 / kB + c.n;  // the sequence's first checkpoint slot (sequences never overlap)
+  return c;
+}
+
+// This thread's kSlot state values of slice `slot` in a [..][kSliceThreads][kSlot] array, contiguous.
+__device__ __forceinline__ float *slice_ptr(float *base, size_t slot) {
+  return base + (slot * kSliceThreads + threadIdx.x) * kSlot;
+}
+__device__ __forceinline__ void store_state(float *dst, const float (&H)[kRows][kCW]) {
+#pragma unroll
+  for (int r = 0; r < kRows; ++r)
+#pragma unroll
+    for (int c = 0; c < kCW; c += 4)
+      *reinterpret_cast<float4 *>(dst + r * kCW + c) = make_float4(H[r][c], H[r][c + 1], H[r][c + 2], H[r][c + 3]);
+}
+__device__ __forceinline__ void load_state(const float *src, float (&H)[kRows][kCW]) {
+#pragma unroll
+  for (int r = 0; r < kRows; ++r)
+#pragma unroll
+    for (int c = 0; c < kCW; c += 4) {
+      const float4 f = *reinterpret_cast<const float4 *>(src + r * kCW + c);
+      H[r][c] = f.x; H[r][c + 1] = f.y; H[r][c + 2] = f.z; H[r][c + 3] = f.w;
+    }
+}
+// One forward step of the rule on this warp's columns (jw = its first column in the slice); o of the
+// token (scaled) to wo_row (the token's row of o, at the slice's first column) if given.
+__device__ __forceinline__ void fwd_step(float (&H)[kRows][kCW], int tt, int dk, int jw, int jmax, const float *sq,
+                                         const float *sk, const float *sv, const float *salpha, const float *sbeta,
+                                         float scale, float *wo_row) {
+  const int lane = threadIdx.x & 31;
+  float kr[kRows], qr[kRows];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int i = lane + 32 * r;
+    kr[r] = i < dk ? sk[tt * dk + i] : 0.0f;
+    qr[r] = i < dk ? sq[tt * dk + i] : 0.0f;
   }
-  const int L = s1 - s0, nblk = (L + kB - 1) / kB;
-  const int slot0 = s0 / kB + n;  // the sequence's first checkpoint slot (sequences never overlap)
-
-  extern __shared__ float smem[];
-  float *sq = smem;                 // [kB][dk]
-  float *sk = sq + kB * dk;         // [kB][dk]
-  float *sv = sk + kB * dk;         // [kB][dv]
-  float *so = sv + kB * dv;         // [kB][dv]  o of the block's tokens
-  float *sdo = so + kB * dv;        // [kB][dv]  their do
-  float *red_q = sdo + kB * dv;     // [nwarps][128]
-  float *red_k = red_q + nwarps * 128;
-  float *red_s = red_k + nwarps * 128;  // [nwarps][4]
-  float *snw = red_s + nwarps * 4;      // [dv] partial dnorm_w
-  float *salpha = snw + dv;             // [kB]
-  float *sbeta = salpha + kB;           // [kB]
-
-  const IO *xz = static_cast<const IO *>(p.z);
-  const IO *gy = static_cast<const IO *>(p.dy);
-  const int j0 = warp * kCW;
-  const float A_exp = expf(p.A_log[h]), dtb = p.dt_bias[h];
-  const float scale = rsqrtf((float)dk);
-  for (int j = tid; j < dv; j += blockDim.x) snw[j] = 0.0f;
-
-  auto elem_ok = [&](int r, int c) { return lane + 32 * r < dk && j0 + c < dv; };
-  auto slot_ptr = [&](float *base, size_t slot) {
-    return base + (slot * blockDim.x + tid) * kSlot;  // this thread's kSlot values, contiguous
-  };
-  auto store_state = [&](float *dst, const float (&H)[kRows][kCW]) {
+  const float al = salpha[tt], be = sbeta[tt];
 #pragma unroll
-    for (int r = 0; r < kRows; ++r)
+  for (int c = 0; c < kCW; ++c) {
+    float s = 0.0f;
 #pragma unroll
-      for (int c = 0; c < kCW; c += 4)
-        *reinterpret_cast<float4 *>(dst + r * kCW + c) = make_float4(H[r][c], H[r][c + 1], H[r][c + 2], H[r][c + 3]);
-  };
-  auto load_state = [&](const float *src, float (&H)[kRows][kCW]) {
-#pragma unroll
-    for (int r = 0; r < kRows; ++r)
-#pragma unroll
-      for (int c = 0; c < kCW; c += 4) {
-        const float4 f = *reinterpret_cast<const float4 *>(src + r * kCW + c);
-        H[r][c] = f.x; H[r][c + 1] = f.y; H[r][c + 2] = f.z; H[r][c + 3] = f.w;
-      }
-  };
-  // one forward step of the rule on this warp's columns; o of the token (scaled) to so[tt] if wanted
-  auto step = [&](float (&H)[kRows][kCW], int tt, bool want_o) {
-    float kr[kRows], qr[kRows];
+    for (int r = 0; r < kRows; ++r) s = fmaf(H[r][c], kr[r], s);
+    const float pc = warp_sum(s);
+    const float u = be * (sv[tt * kSliceCols + jw + c] - al * pc);
+    float o = 0.0f;
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
-      const int i = lane + 32 * r;
-      kr[r] = i < dk ? sk[tt * dk + i] : 0.0f;
-      qr[r] = i < dk ? sq[tt * dk + i] : 0.0f;
+      H[r][c] = fmaf(kr[r], u, al * H[r][c]);
+      o = fmaf(H[r][c], qr[r], o);
     }
-    const float al = salpha[tt], be = sbeta[tt];
-    float pc[kCW];
-#pragma unroll
-    for (int c = 0; c < kCW; ++c) {
-      float s = 0.0f;
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) s = fmaf(H[r][c], kr[r], s);
-      pc[c] = warp_sum(s);
+    if (wo_row) {
+      o = warp_sum(o);
+      if (lane == c && jw + c < jmax) wo_row[jw + c] = o * scale;
     }
-    float oc[kCW];
-#pragma unroll
-    for (int c = 0; c < kCW; ++c) {
-      const int j = j0 + c;
-      const float u = be * ((j < dv ? sv[tt * dv + j] : 0.0f) - al * pc[c]);
-      float s = 0.0f;
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        H[r][c] = fmaf(kr[r], u, al * H[r][c]);
-        s = fmaf(H[r][c], qr[r], s);
-      }
-      oc[c] = s;
-    }
-    if (want_o) {
-#pragma unroll
-      for (int c = 0; c < kCW; ++c) {
-        const float o = warp_sum(oc[c]);
-        if (lane == c && j0 + c < dv) so[tt * dv + j0 + c] = o * scale;
-      }
-    }
-  };
+  }
+}
 
-  // ---------------- forward: checkpoints at block starts
-  const size_t chain_off = ((size_t)n * h_v + h) * dk * dv;
+constexpr size_t slice_smem_floats(int dk) {
+  return (size_t)kB * (2 * dk + 2 * kSliceCols) + (size_t)kSliceWarps * (2 * 128 + 4) + 2 * kB;
+}
+
+// Forward with checkpoints: the slice of the state at each block start, and o of every token.
+template <typename IO>
+__global__ void __launch_bounds__(kSliceThreads) bwd_fwd_kernel(const BwdParams p, const BwdWs ws) {
+  const int h_v = p.h_v, dk = p.d_k, dv = p.d_v;
+  const SliceCtx cx = slice_ctx(p, ws.slices);
+  if (!cx.ok) {
+    if (threadIdx.x == 0) set_status(p.status, kDevBadSeqlens);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, jw = kCW * warp;
+  extern __shared__ float smem[];
+  float *sq = smem, *sk = sq + kB * dk, *sv = sk + kB * dk, *salpha = sv + 2 * kB * kSliceCols;
+  float *sbeta = salpha + kB;
+  const float A_exp = expf(p.A_log[cx.h]), dtb = p.dt_bias[cx.h], scale = rsqrtf((float)dk);
+  const size_t chain_off = ((size_t)cx.n * h_v + cx.h) * dk * dv;
   float H[kRows][kCW];
 #pragma unroll
   for (int r = 0; r < kRows; ++r)
 #pragma unroll
-    for (int c = 0; c < kCW; ++c)
-      H[r][c] = (p.init_state && elem_ok(r, c)) ? p.init_state[chain_off + (size_t)(lane + 32 * r) * dv + j0 + c]
-                                                : 0.0f;
-  for (int b = 0; b < nblk; ++b) {
-    const int t0 = s0 + kB * b, nt = min(kB, s1 - t0);
-    store_state(slot_ptr(ws.ckpt, (size_t)(slot0 + b) * h_v + h), H);
-    if (b + 1 == nblk) break;  // the last block's tokens are only needed in reverse
-    __syncthreads();
-    block_prologue<IO>(p, h, hq, s0, t0, nt, sq, sk, sv, salpha, sbeta, A_exp, dtb);
-    if (j0 < dv)
-      for (int tt = 0; tt < nt; ++tt) step(H, tt, false);
+    for (int c = 0; c < kCW; ++c) {
+      const int i = lane + 32 * r, j = cx.j0 + jw + c;
+      H[r][c] = (p.init_state && i < dk && j < dv) ? p.init_state[chain_off + (size_t)i * dv + j] : 0.0f;
+    }
+  for (int b = 0; b < cx.nblk; ++b) {
+    const int t0 = cx.s0 + kB * b, nt = min(kB, cx.s1 - t0);
+    store_state(slice_ptr(ws.ckpt, ((size_t)(cx.slot0 + b) * h_v + cx.h) * ws.slices + cx.sl), H);
+    __syncthreads();  // the previous block's shared memory is consumed
+    block_prologue<IO>(p, cx.h, cx.hq, cx.s0, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta, A_exp, dtb);
+    for (int tt = 0; tt < nt; ++tt)
+      fwd_step(H, tt, dk, jw, dv - cx.j0, sq, sk, sv, salpha, sbeta, scale,
+               ws.wo + ((size_t)(t0 + tt) * h_v + cx.h) * dv + cx.j0);
   }
+}
 
-  // ---------------- reverse, block by block
-  float G[kRows][kCW];
+// RMSNormGated in reverse, one warp per (token, value head) row; dnorm_w summed per CTA, then atomically.
+template <typename IO>
+__global__ void __launch_bounds__(256) bwd_norm_kernel(const BwdParams p, const BwdWs ws) {
+  const int dv = p.d_v, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ double snw[128];
+  for (int j = threadIdx.x; j < dv; j += blockDim.x) snw[j] = 0.0;
+  __syncthreads();
+  const size_t rows = (size_t)p.T * p.h_v;
+  const size_t rw = (size_t)blockIdx.x * 8 + warp;
+  if (rw < rows) {
+    const IO *xz = static_cast<const IO *>(p.z) + rw * dv;
+    const IO *gy = static_cast<const IO *>(p.dy) + rw * dv;
+    const float *o = ws.wo + rw * dv;
+    float ss = 0.0f, dot = 0.0f;
+    for (int j = lane; j < dv; j += 32) {
+      const float z = to_f(xz[j]);
+      ss = fmaf(o[j], o[j], ss);
+      dot = fmaf(to_f(gy[j]) * o[j], p.norm_w[j] * silu_f(z), dot);
+    }
+    ss = warp_sum(ss);
+    dot = warp_sum(dot);
+    const float r = rsqrtf(ss / (float)dv + kEpsRms);
+    for (int j = lane; j < dv; j += 32) {
+      const float z = to_f(xz[j]), g = to_f(gy[j]);
+      const float s = sigmoid_f(z), silu = z * s, w = p.norm_w[j];
+      ws.wdo[rw * dv + j] = r * w * silu * g - o[j] * r * r * r * dot / (float)dv;
+      p.dz[rw * dv + j] = g * o[j] * r * w * s * (1.0f + z * (1.0f - s));
+      atomicAdd(&snw[j], (double)(g * o[j] * r * silu));
+    }
+  }
+  __syncthreads();
+  double *acc_nw = ws.acc + (size_t)(2 * p.h_qk * p.d_k + p.h_v * dv) * 4 + 2 * p.h_v;
+  for (int j = threadIdx.x; j < dv; j += blockDim.x) atomicAdd(&acc_nw[j], snw[j]);
+}
+
+// The rule in reverse, per (chain, column slice).
+template <typename IO>
+__global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams p, const BwdWs ws) {
+  const int h_v = p.h_v, dk = p.d_k, dv = p.d_v;
+  const SliceCtx cx = slice_ctx(p, ws.slices);
+  if (!cx.ok) return;  // reported by the forward kernel
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, jw = kCW * warp;
+  extern __shared__ float smem[];
+  float *sq = smem, *sk = sq + kB * dk, *sv = sk + kB * dk, *sdo = sv + kB * kSliceCols;
+  float *red_q = sdo + kB * kSliceCols;         // [kSliceWarps][128]
+  float *red_k = red_q + kSliceWarps * 128;
+  float *red_s = red_k + kSliceWarps * 128;     // [kSliceWarps][4]
+  float *salpha = red_s + kSliceWarps * 4, *sbeta = salpha + kB;
+  const float A_exp = expf(p.A_log[cx.h]), dtb = p.dt_bias[cx.h], scale = rsqrtf((float)dk);
+  const size_t chain_off = ((size_t)cx.n * h_v + cx.h) * dk * dv;
+  auto elem_ok = [&](int r, int c) { return lane + 32 * r < dk && cx.j0 + jw + c < dv; };
+  float G[kRows][kCW], H[kRows][kCW];
 #pragma unroll
   for (int r = 0; r < kRows; ++r)
 #pragma unroll
     for (int c = 0; c < kCW; ++c)
       G[r][c] = (p.dfinal_state && elem_ok(r, c))
-                    ? p.dfinal_state[chain_off + (size_t)(lane + 32 * r) * dv + j0 + c] : 0.0f;
-  float *hs = ws.hs + ((size_t)n * h_v + h) * (kB + 1) * blockDim.x * kSlot;
-  for (int b = nblk - 1; b >= 0; --b) {
-    const int t0 = s0 + kB * b, nt = min(kB, s1 - t0);
+                    ? p.dfinal_state[chain_off + (size_t)(lane + 32 * r) * dv + cx.j0 + jw + c] : 0.0f;
+  float *hs = ws.hs + (((size_t)cx.n * h_v + cx.h) * ws.slices + cx.sl) * (kB + 1) * kSliceThreads * kSlot;
+  for (int b = cx.nblk - 1; b >= 0; --b) {
+    const int t0 = cx.s0 + kB * b, nt = min(kB, cx.s1 - t0);
     __syncthreads();
-    block_prologue<IO>(p, h, hq, s0, t0, nt, sq, sk, sv, salpha, sbeta, A_exp, dtb);
-    load_state(slot_ptr(ws.ckpt, (size_t)(slot0 + b) * h_v + h), H);
-    for (int tt = 0; tt < nt; ++tt) {  // the block's states and outputs again
-      store_state(slot_ptr(hs, tt), H);
-      if (j0 < dv) step(H, tt, true);
+    block_prologue<IO>(p, cx.h, cx.hq, cx.s0, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta, A_exp, dtb);
+    for (int e = tid; e < nt * kSliceCols; e += kSliceThreads) {  // do of the slice's columns
+      const int tt = e / kSliceCols, jj = e % kSliceCols;
+      sdo[e] = cx.j0 + jj < dv ? ws.wdo[((size_t)(t0 + tt) * h_v + cx.h) * dv + cx.j0 + jj] : 0.0f;
     }
-    store_state(slot_ptr(hs, nt), H);
-    __syncthreads();
-    // RMSNormGated in reverse, one warp per token
-    for (int tt = warp; tt < nt; tt += nwarps) {
-      const size_t row = ((size_t)(t0 + tt) * h_v + h) * dv;
-      float ss = 0.0f, dot = 0.0f;
-      for (int j = lane; j < dv; j += 32) {
-        const float o = so[tt * dv + j], z = to_f(xz[row + j]);
-        ss = fmaf(o, o, ss);
-        dot = fmaf(to_f(gy[row + j]) * o, p.norm_w[j] * silu_f(z), dot);
-      }
-      ss = warp_sum(ss);
-      dot = warp_sum(dot);
-      const float r = rsqrtf(ss / (float)dv + kEpsRms);
-      for (int j = lane; j < dv; j += 32) {
-        const float o = so[tt * dv + j], z = to_f(xz[row + j]), g = to_f(gy[row + j]);
-        const float s = sigmoid_f(z), silu = z * s, w = p.norm_w[j];
-        sdo[tt * dv + j] = r * w * silu * g - o * r * r * r * dot / (float)dv;
-        p.dz[row + j] = g * o * r * w * s * (1.0f + z * (1.0f - s));
-        atomicAdd(&snw[j], g * o * r * silu);
-      }
+    load_state(slice_ptr(ws.ckpt, ((size_t)(cx.slot0 + b) * h_v + cx.h) * ws.slices + cx.sl), H);
+    for (int tt = 0; tt < nt; ++tt) {  // the block's states again (before each token)
+      store_state(slice_ptr(hs, tt), H);
+      fwd_step(H, tt, dk, jw, dv - cx.j0, sq, sk, sv, salpha, sbeta, scale, nullptr);
     }
     __syncthreads();
-    const float *hs_c = hs;
+    // H holds the state after the block; the state before token tt is loaded one token ahead (each
+    // thread reads back only values it wrote itself)
+    float Ht[kRows][kCW], Hp[kRows][kCW];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+      for (int c = 0; c < kCW; ++c) Ht[r][c] = H[r][c];
+    load_state(slice_ptr(hs, nt - 1), Hp);
     for (int tt = nt - 1; tt >= 0; --tt) {
-      const size_t tok = (size_t)(t0 + tt) * h_v + h;
-      float Hp[kRows][kCW], Ht[kRows][kCW];
-      load_state(slot_ptr(const_cast<float *>(hs_c), tt), Hp);
-      load_state(slot_ptr(const_cast<float *>(hs_c), tt + 1), Ht);
+      const size_t tok = (size_t)(t0 + tt) * h_v + cx.h;
+      float Hn[kRows][kCW];  // the state before token tt - 1, in flight over this step
+      load_state(slice_ptr(hs, tt > 0 ? tt - 1 : 0), Hn);
       float kr[kRows], qr[kRows];
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
@@ -294,9 +353,8 @@ __global__ void __launch_bounds__(512) bwd_chain_kernel(const BwdParams p, const
       float doc[kCW], vc[kCW];
 #pragma unroll
       for (int c = 0; c < kCW; ++c) {
-        const int j = j0 + c;
-        doc[c] = j < dv ? sdo[tt * dv + j] : 0.0f;
-        vc[c] = j < dv ? sv[tt * dv + j] : 0.0f;
+        doc[c] = sdo[tt * kSliceCols + jw + c];
+        vc[c] = sv[tt * kSliceCols + jw + c];
       }
       float dqp[kRows], dkp[kRows];
       float s_dal = 0.0f;
@@ -310,6 +368,7 @@ __global__ void __launch_bounds__(512) bwd_chain_kernel(const BwdParams p, const
           s_dal = fmaf(G[r][c], Hp[r][c], s_dal);
         }
         dqp[r] = scale * sq_;
+        dkp[r] = 0.0f;
       }
       float pc[kCW], du[kCW];
 #pragma unroll
@@ -331,10 +390,7 @@ __global__ void __launch_bounds__(512) bwd_chain_kernel(const BwdParams p, const
         s_dup = fmaf(du[c], pc[c], s_dup);
         dp[c] = -al * be * du[c];
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          if (c == 0) dkp[r] = 0.0f;
-          dkp[r] = fmaf(G[r][c], u, dkp[r]);
-        }
+        for (int r = 0; r < kRows; ++r) dkp[r] = fmaf(G[r][c], u, dkp[r]);
       }
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
@@ -344,11 +400,9 @@ __global__ void __launch_bounds__(512) bwd_chain_kernel(const BwdParams p, const
           G[r][c] = fmaf(kr[r], dp[c], al * G[r][c]);
         }
       }
-      if (j0 < dv) {
 #pragma unroll
-        for (int c = 0; c < kCW; ++c)
-          if (lane == c && j0 + c < dv) ws.dvs[tok * dv + j0 + c] = be * du[c];
-      }
+      for (int c = 0; c < kCW; ++c)
+        if (lane == c && cx.j0 + jw + c < dv) ws.dvs[tok * dv + cx.j0 + jw + c] = be * du[c];
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
         red_q[warp * 128 + lane + 32 * r] = dqp[r];
@@ -361,26 +415,35 @@ __global__ void __launch_bounds__(512) bwd_chain_kernel(const BwdParams p, const
         red_s[warp * 4 + 2] = s_dup;
       }
       __syncthreads();
-      for (int i = tid; i < dk; i += blockDim.x) {
+      for (int i = tid; i < dk; i += kSliceThreads) {  // this slice's part of the sums over columns
         float a = 0.0f, c2 = 0.0f;
-        for (int w = 0; w < nwarps; ++w) {
+#pragma unroll
+        for (int w = 0; w < kSliceWarps; ++w) {
           a += red_q[w * 128 + i];
           c2 += red_k[w * 128 + i];
         }
-        ws.dqn[tok * dk + i] = a;
-        ws.dkn[tok * dk + i] = c2;
+        atomicAdd(&ws.dqn[tok * dk + i], a);
+        atomicAdd(&ws.dkn[tok * dk + i], c2);
       }
-      if (tid == 32 * (nwarps - 1)) {  // a lane of the last warp: the scalar sums
+      if (tid == kSliceThreads - 32) {  // a lane of the last warp: the scalar sums
         float dal = 0.0f, db = 0.0f, dup = 0.0f;
-        for (int w = 0; w < nwarps; ++w) {
+#pragma unroll
+        for (int w = 0; w < kSliceWarps; ++w) {
           dal += red_s[w * 4 + 0];
           db += red_s[w * 4 + 1];
           dup += red_s[w * 4 + 2];
         }
-        ws.dg[tok] = al * (dal - be * dup);
-        ws.dbeta[tok] = db;
+        atomicAdd(&ws.dg[tok], al * (dal - be * dup));  // linear in the slice's parts
+        atomicAdd(&ws.dbeta[tok], db);
       }
       __syncthreads();
+#pragma unroll
+      for (int r = 0; r < kRows; ++r)
+#pragma unroll
+        for (int c = 0; c < kCW; ++c) {
+          Ht[r][c] = Hp[r][c];
+          Hp[r][c] = Hn[r][c];
+        }
     }
   }
   if (p.dinit_state) {
@@ -388,10 +451,8 @@ __global__ void __launch_bounds__(512) bwd_chain_kernel(const BwdParams p, const
     for (int r = 0; r < kRows; ++r)
 #pragma unroll
       for (int c = 0; c < kCW; ++c)
-        if (elem_ok(r, c)) p.dinit_state[chain_off + (size_t)(lane + 32 * r) * dv + j0 + c] = G[r][c];
+        if (elem_ok(r, c)) p.dinit_state[chain_off + (size_t)(lane + 32 * r) * dv + cx.j0 + jw + c] = G[r][c];
   }
-  __syncthreads();
-  for (int j = tid; j < dv; j += blockDim.x) atomicAdd(&p.dnorm_w[j], snw[j]);
 }
 
 // Sequence [s0, s1) of token t (binary search over cu_seqlens).
@@ -492,7 +553,7 @@ __global__ void __launch_bounds__(128) bwd_prologue_kernel(const BwdParams p, co
     dx[(size_t)t * stride + c] = acc;
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) atomicAdd(&p.dconv_w[(size_t)(cb + c) * 4 + j], dw[j]);
+  for (int j = 0; j < 4; ++j) atomicAdd(&ws.acc[(size_t)(cb + c) * 4 + j], (double)dw[j]);
 }
 
 template <typename IO>
@@ -507,50 +568,66 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(const BwdParams p, const 
   const float be = sigmoid_f(b);
   p.da[idx] = da;
   p.db[idx] = ws.dbeta[idx] * be * (1.0f - be);
-  atomicAdd(&p.ddt_bias[h], da);
-  atomicAdd(&p.dA_log[h], dg * gate_g(a, A_exp, p.dt_bias[h]));
+  double *acc_g = ws.acc + (size_t)(2 * p.h_qk * p.d_k + p.h_v * p.d_v) * 4;  // A_log [h_v], dt_bias [h_v]
+  atomicAdd(&acc_g[h], (double)(dg * gate_g(a, A_exp, p.dt_bias[h])));
+  atomicAdd(&acc_g[p.h_v + h], (double)da);
+}
+
+// The parameter gradients, from their fp64 sums.
+__global__ void __launch_bounds__(256) bwd_param_kernel(const BwdParams p, const BwdWs ws) {
+  const int Cc = 2 * p.h_qk * p.d_k + p.h_v * p.d_v;
+  const int n = Cc * 4 + 2 * p.h_v + p.d_v;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const float v = (float)ws.acc[i];
+    if (i < Cc * 4) p.dconv_w[i] = v;
+    else if (i < Cc * 4 + p.h_v) p.dA_log[i - Cc * 4] = v;
+    else if (i < Cc * 4 + 2 * p.h_v) p.ddt_bias[i - Cc * 4 - p.h_v] = v;
+    else p.dnorm_w[i - Cc * 4 - 2 * p.h_v] = v;
+  }
 }
 
 }  // namespace
 
 size_t prefill_backward_workspace_bytes(int T, int N, int h_qk, int h_v, int d_k, int d_v) {
-  (void)h_qk;
-  return BwdLayout(T, N, h_v, d_k, d_v).total;
+  return BwdLayout(T, N, h_qk, h_v, d_k, d_v).total;
 }
 
 cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t s) {
-  const BwdLayout L(p.T, p.N, p.h_v, p.d_k, p.d_v);
+  const BwdLayout L(p.T, p.N, p.h_qk, p.h_v, p.d_k, p.d_v);
   if (p.ws_bytes < L.total) return cudaErrorInvalidValue;
   BwdWs ws;
   ws.ckpt = reinterpret_cast<float *>(p.ws + L.ckpt);
   ws.hs = reinterpret_cast<float *>(p.ws + L.hs);
+  ws.wo = reinterpret_cast<float *>(p.ws + L.wo);
+  ws.wdo = reinterpret_cast<float *>(p.ws + L.wdo);
   ws.dqn = reinterpret_cast<float *>(p.ws + L.dqn);
   ws.dkn = reinterpret_cast<float *>(p.ws + L.dkn);
   ws.dvs = reinterpret_cast<float *>(p.ws + L.dvs);
   ws.dg = reinterpret_cast<float *>(p.ws + L.dg);
   ws.dbeta = reinterpret_cast<float *>(p.ws + L.dbeta);
-  ws.slots = L.slots;
-  const int Cc = 2 * p.h_qk * p.d_k + p.h_v * p.d_v;
+  ws.acc = reinterpret_cast<double *>(p.ws + L.acc);
+  ws.slices = L.slices;
   cudaError_t e;
-  // the parameter gradients are sums (atomic adds) over tokens and heads
-  if ((e = cudaMemsetAsync(p.dconv_w, 0, sizeof(float) * (size_t)Cc * 4, s)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(p.dA_log, 0, sizeof(float) * (size_t)p.h_v, s)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(p.ddt_bias, 0, sizeof(float) * (size_t)p.h_v, s)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(p.dnorm_w, 0, sizeof(float) * (size_t)p.d_v, s)) != cudaSuccess) return e;
-  const int warps = (p.d_v + kCW - 1) / kCW;
-  const int threads = 32 * warps;
-  const size_t smem = sizeof(float) * ((size_t)kB * (2 * p.d_k + 3 * p.d_v) + (size_t)warps * (2 * 128 + 4) +
-                                       p.d_v + 2 * kB);
-  const unsigned chains = (unsigned)p.N * (unsigned)p.h_v;
+  // the per-token q, k and gate gradients and the parameter gradients' fp64 sums are atomic adds
+  if ((e = cudaMemsetAsync(p.ws + L.dqn, 0, L.total - L.dqn, s)) != cudaSuccess) return e;
+  const size_t smem = sizeof(float) * slice_smem_floats(p.d_k);
+  const unsigned ctas = (unsigned)p.N * (unsigned)p.h_v * (unsigned)L.slices;
+  const unsigned rows = (unsigned)(((size_t)p.T * p.h_v + 7) / 8);
   const dim3 pgrid((unsigned)((p.T + kTile - 1) / kTile), (unsigned)(2 * p.h_qk + p.h_v));
   const unsigned ggrid = (unsigned)(((size_t)p.T * p.h_v + 255) / 256);
-  auto run = [&](auto chain_k, auto pro_k, auto gate_k) -> cudaError_t {
-    cudaError_t err = cudaFuncSetAttribute(chain_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto run = [&](auto fwd_k, auto norm_k, auto rev_k, auto pro_k, auto gate_k) -> cudaError_t {
+    cudaError_t err = cudaFuncSetAttribute(fwd_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    trace_begin(s, GDN_K_BWD_CHAIN);
-    if (chains) chain_k<<<chains, threads, smem, s>>>(p, ws);
-    trace_end(s);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = cudaFuncSetAttribute(rev_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return err;
+    if (ctas) {
+      trace_begin(s, GDN_K_BWD_CHAIN);
+      fwd_k<<<ctas, kSliceThreads, smem, s>>>(p, ws);
+      if (p.T > 0) norm_k<<<rows, 256, 0, s>>>(p, ws);
+      rev_k<<<ctas, kSliceThreads, smem, s>>>(p, ws);
+      trace_end(s);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
     if (p.T > 0) {
       trace_begin(s, GDN_K_BWD_PROLOGUE);
       pro_k<<<pgrid, 128, 0, s>>>(p, ws);
@@ -558,11 +635,14 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
       if ((err = cudaGetLastError()) != cudaSuccess) return err;
       gate_k<<<ggrid, 256, 0, s>>>(p, ws);
     }
+    bwd_param_kernel<<<64, 256, 0, s>>>(p, ws);
     return cudaGetLastError();
   };
   if (bf16)
-    return run(bwd_chain_kernel<__nv_bfloat16>, bwd_prologue_kernel<__nv_bfloat16>, bwd_gate_kernel<__nv_bfloat16>);
-  return run(bwd_chain_kernel<float>, bwd_prologue_kernel<float>, bwd_gate_kernel<float>);
+    return run(bwd_fwd_kernel<__nv_bfloat16>, bwd_norm_kernel<__nv_bfloat16>, bwd_rev_kernel<__nv_bfloat16>,
+               bwd_prologue_kernel<__nv_bfloat16>, bwd_gate_kernel<__nv_bfloat16>);
+  return run(bwd_fwd_kernel<float>, bwd_norm_kernel<float>, bwd_rev_kernel<float>, bwd_prologue_kernel<float>,
+             bwd_gate_kernel<float>);
 }
 
 }  // namespace gdn

@@ -119,7 +119,7 @@ const char *gdn_trace_kernel_name(int kind) {
     case GDN_K_STATE: return "state_kernel";
     case GDN_K_PREFILL_SIMT: return "prefill_simt_kernel";
     case GDN_K_DECODE: return "decode_kernel";
-    case GDN_K_BWD_CHAIN: return "bwd_chain_kernel";
+    case GDN_K_BWD_CHAIN: return "bwd_state_kernels";
     case GDN_K_BWD_PROLOGUE: return "bwd_prologue_kernel";
     default: return "";
   }

@@ -172,8 +172,9 @@ GDN_API int gdn_prefill_carry(const gdn_dims *dims, const void *q, const void *k
  * Qwen35 SFT"; "feat(models): dense Qwen3.5 custom attention", its E2E
  * training-throughput table) but state no backward; this is the chain rule of
  * the forward definitions above, in fp32 on the CUDA cores (the state's
- * gradient is carried token by token in reverse, the states recomputed from a
- * checkpoint every 32 tokens).
+ * gradient is carried token by token in reverse, each chain's state columns
+ * split over CTAs of 32, the states recomputed from a checkpoint every 32
+ * tokens).
  *
  * Inputs: dims, the forward's q, k, v, a, b, z, conv_w, A_log, dt_bias,
  *   norm_w, cu_seqlens and init_state (NULL = zeros), exactly as given to

@@ -100,7 +100,7 @@ def test_trace_read_without_launches(lib):
     assert gdn.trace_read() == {}
     names = [lib.gdn_trace_kernel_name(k).decode() for k in range(gdn.TRACE_KINDS)]
     assert names == ["chunk_table_kernel", "chunk_prep_kernel", "state_kernel", "prefill_simt_kernel",
-                     "decode_kernel", "bwd_chain_kernel", "bwd_prologue_kernel"]
+                     "decode_kernel", "bwd_state_kernels", "bwd_prologue_kernel"]
     assert lib.gdn_trace_kernel_name(gdn.TRACE_KINDS) == b""
     assert lib.gdn_trace_read(0, None, None) == 1
 
