@@ -158,14 +158,15 @@ def _device_inputs(inp, dev):
     return t
 
 
-def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False, trace=False):
+def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False, trace=False, seg_chunks=0):
     """Per-step device time (CUDA events on the launching stream, L2 flushed
     between steps) of one gdn_prefill call; optionally the end-to-end time with
     pinned-host inputs copied in and outputs copied out every step, and the
     library's per-kernel trace (CUDA events around each of its launches, on the
     same stream) over as many steps again, run right after the timed ones: the
     trace's events between launches hold back the early start of the next
-    kernel (programmatic dependent launch), so they stay out of the timed steps."""
+    kernel (programmatic dependent launch), so they stay out of the timed steps.
+    seg_chunks > 0 times gdn_prefill_segmented with segments of that many chunks."""
     import torch
 
     import gateddeltanet_layer_gb300 as gdn
@@ -174,14 +175,21 @@ def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False, trace=False):
     T, N = cfg.T, cfg.N
     out = torch.empty((T, cfg.h_v, cfg.d_v), dtype=torch.bfloat16, device=dev)
     fs = torch.empty((N, cfg.h_v, cfg.d_k, cfg.d_v), dtype=torch.float32, device=dev)
-    ws = torch.zeros(gdn.prefill_workspace_bytes(T, N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v, True),
-                     dtype=torch.uint8, device=dev)
+    if seg_chunks:
+        ws_bytes = gdn.prefill_segmented_workspace_bytes(T, N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v, seg_chunks)
+    else:
+        ws_bytes = gdn.prefill_workspace_bytes(T, N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v, True)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def call():
-        gdn.prefill(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
-                    t["dt_bias"], t["norm_w"], t["cu_seqlens"], t["init_state"], out=out, final_state=fs,
-                    workspace=ws, stream=stream)
+        args = (t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"], t["dt_bias"],
+                t["norm_w"], t["cu_seqlens"], t["init_state"])
+        if seg_chunks:
+            gdn.prefill_segmented(*args, seg_chunks=seg_chunks, out=out, final_state=fs, workspace=ws,
+                                  stream=stream)
+        else:
+            gdn.prefill(*args, out=out, final_state=fs, workspace=ws, stream=stream)
 
     for _ in range(warmup):
         flush.zero_()
@@ -377,7 +385,7 @@ HEADLINE = synth.LONG_128K
 # captures; per sequence it does the same work, so its DRAM traffic scales to
 # the headline call by the number of sequences.
 LONG_2X8192 = synth.scaled(synth.LONG_128K, name="prefill_long_T16384", lengths=(8192,) * 2)
-PROFILE_CASES = {LONG_2X8192.name: LONG_2X8192}
+PROFILE_CASES = {LONG_2X8192.name: LONG_2X8192, synth.FEW_CHAINS_16K.name: synth.FEW_CHAINS_16K}
 
 
 def prefill_line(cfg, res, steps, pk, dev):
@@ -461,6 +469,19 @@ def run_ours(args):
                              "achieved_gbs": rl["achieved"] if rl["unit"] == "GB/s" else None,
                              "flop_bound_frac": rl["flop_bound_frac"], "byte_bound_frac": rl["byte_bound_frac"],
                              "per_kernel": rl["per_kernel"], "traffic": rl["traffic"]}
+        # the segment-parallel prefill, next to the plain one on the same input: the few-chain
+        # workload it is for, and the 4096-token one (32 chains, where the plain pass already
+        # keeps 128 SMs busy)
+        for c, seg in ((synth.FEW_CHAINS_16K, 16), (synth.SINGLE_4K, 22)):
+            ent = {}
+            for label, sc in (("plain", 0), ("segmented", seg)):
+                r = time_prefill(c, args.steps, args.warmup, dev, flush, trace=True, seg_chunks=sc)
+                m, rl = prefill_line(c, r, args.steps, pk, dev)
+                ent[label] = {"tokens_per_s": c.T / (m * 1e-3), "ms": m, "roofline_frac": rl["frac"],
+                              "per_kernel": rl["per_kernel"]}
+            ent["segmented"]["seg_chunks"] = seg
+            ent["speedup"] = ent["plain"]["ms"] / ent["segmented"]["ms"]
+            extra[f"{c.name}_segmented"] = ent
         r = time_backward(synth.SINGLE_4K, max(3, args.steps // 4), args.warmup, dev, flush)
         m, = max_over_ranks([statistics.mean(r["ms"])], dev)
         extra["prefill_backward_T4096"] = {"tokens_per_s": synth.SINGLE_4K.T / (m * 1e-3), "ms": m,
@@ -624,8 +645,8 @@ def run_case(args):
     if isinstance(cfg, synth.DecodeConfig):
         r = time_decode(cfg, args.steps, args.warmup, dev, flush)
     else:
-        r = time_prefill(cfg, args.steps, args.warmup, dev, flush)
-    print(json.dumps({"case": args.case, "ms": r["ms"]}), flush=True)
+        r = time_prefill(cfg, args.steps, args.warmup, dev, flush, seg_chunks=args.seg_chunks)
+    print(json.dumps({"case": args.case, "seg_chunks": args.seg_chunks, "ms": r["ms"]}), flush=True)
 
 
 def main():
@@ -637,6 +658,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--case", choices=sorted({**synth.CONFIGS, **PROFILE_CASES}),
                     help="run only this workload's GPU call")
+    ap.add_argument("--seg-chunks", type=int, default=0,
+                    help="with --case: time the segment-parallel prefill with segments of this many chunks")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -12,8 +12,9 @@ import ctypes
 import os
 import threading
 
-__all__ = ["prefill", "prefill_carry", "prefill_backward", "prefill_backward_workspace_bytes", "decode_step", "decode_step_slots", "conv_cache_from_prefill", "prefill_workspace_bytes",
-           "workspace_status", "library", "GdnError", "STATUS", "prefill_noalloc", "NOALLOC_SCRATCH_BYTES",
+__all__ = ["prefill", "prefill_carry", "prefill_segmented", "prefill_segmented_workspace_bytes", "prefill_backward",
+           "prefill_backward_workspace_bytes", "decode_step", "decode_step_slots", "conv_cache_from_prefill",
+           "prefill_workspace_bytes", "workspace_status", "library", "GdnError", "STATUS", "prefill_noalloc", "NOALLOC_SCRATCH_BYTES",
            "trace_enable", "trace_read"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -57,6 +58,10 @@ def library() -> ctypes.CDLL:
             lib.gdn_prefill.restype = ctypes.c_int
             lib.gdn_prefill_carry.argtypes = [dp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
             lib.gdn_prefill_carry.restype = ctypes.c_int
+            lib.gdn_prefill_segmented_workspace_bytes.argtypes = [dp, ctypes.c_int]
+            lib.gdn_prefill_segmented_workspace_bytes.restype = ctypes.c_size_t
+            lib.gdn_prefill_segmented.argtypes = [dp] + [_vp] * 14 + [ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+            lib.gdn_prefill_segmented.restype = ctypes.c_int
             lib.gdn_prefill_backward_workspace_bytes.argtypes = [dp]
             lib.gdn_prefill_backward_workspace_bytes.restype = ctypes.c_size_t
             lib.gdn_prefill_backward.argtypes = [dp] + [_vp] * 26 + [ctypes.c_size_t, _vp]
@@ -145,6 +150,30 @@ def prefill(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_s
     cu_seqlens int32 [N+1]; init_state fp32 [N, h_v, d_k, d_v] or None.
     Returns (out [T, h_v, d_v], final_state or None).
     """
+    return _prefill(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state, 0, out,
+                    final_state, return_final_state, workspace, stream)
+
+
+def prefill_segmented_workspace_bytes(T: int, N: int, h_qk: int, h_v: int, d_k: int, d_v: int,
+                                      seg_chunks: int) -> int:
+    d = Dims(T, N, h_qk, h_v, d_k, d_v, GDN_BF16)
+    return int(library().gdn_prefill_segmented_workspace_bytes(ctypes.byref(d), int(seg_chunks)))
+
+
+def prefill_segmented(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state=None, *,
+                      seg_chunks: int, out=None, final_state=None, return_final_state=True, workspace=None,
+                      stream=None):
+    """``gdn_prefill_segmented``: ``prefill``'s results with every sequence cut
+    into segments of ``seg_chunks`` chunks of 64 tokens, run in parallel and
+    joined by a scan over the segments' affine state maps (more chains in
+    flight for few long sequences).  bf16 streams with d_k = d_v = 128 only.
+    Returns (out, final_state or None)."""
+    return _prefill(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state, int(seg_chunks), out,
+                    final_state, return_final_state, workspace, stream)
+
+
+def _prefill(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state, seg, out, final_state,
+             return_final_state, workspace, stream):
     torch = _torch()
     lib = library()
     dt = q.dtype
@@ -169,11 +198,13 @@ def prefill(q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_s
     if workspace is not None:
         _req(workspace, "workspace", torch.uint8)
         ws_bytes = workspace.numel()
-    st = lib.gdn_prefill(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(conv_w),
-                         _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(cu_seqlens), _ptr(init_state),
-                         _ptr(out), _ptr(final_state), _ptr(workspace), ws_bytes,
-                         _stream_handle(stream, q.device))
-    _check(st, "gdn_prefill")
+    args = (ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(conv_w), _ptr(A_log),
+            _ptr(dt_bias), _ptr(norm_w), _ptr(cu_seqlens), _ptr(init_state), _ptr(out), _ptr(final_state))
+    tail = (_ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    if seg:
+        _check(lib.gdn_prefill_segmented(*args, seg, *tail), "gdn_prefill_segmented")
+    else:
+        _check(lib.gdn_prefill(*args, *tail), "gdn_prefill")
     return out, final_state
 
 
@@ -361,7 +392,7 @@ def workspace_status(workspace, stream=None) -> int:
 
 
 # Number of kernel kinds the trace distinguishes (GDN_K_COUNT in include/gdn_trace.h).
-TRACE_KINDS = 7
+TRACE_KINDS = 8
 
 
 def trace_enable(on: bool = True) -> None:

@@ -42,26 +42,34 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *d) {
   return bytes;
 }
 
+size_t gdn_prefill_segmented_workspace_bytes(const gdn_dims *d, int seg_chunks) {
+  if (check_dims(d) != GDN_OK || d->num_seqs <= 0 || seg_chunks < 1 || !use_tensor_core_prefill(d)) return 0;
+  return kStatusBytes +
+         gdn::prefill_segmented_workspace_bytes(d->num_tokens, d->num_seqs, d->h_qk, d->h_v, seg_chunks);
+}
+
 }  // extern "C"
 
 namespace {
 
-// gdn_prefill and gdn_prefill_carry: validation, workspace, the kernels, and
-// (when final_conv is given) the conv cache the call leaves.
+// gdn_prefill, gdn_prefill_carry and gdn_prefill_segmented (seg > 0):
+// validation, workspace, the kernels, and (when final_conv is given) the conv
+// cache the call leaves.
 int prefill_impl(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a, const void *b,
                  const void *z, const float *conv_w, const float *A_log, const float *dt_bias,
                  const float *norm_w, const int32_t *cu_seqlens, const float *init_state, const void *init_conv,
                  void *out, float *final_state, void *final_conv, void *workspace, size_t ws_bytes,
-                 void *stream) {
+                 void *stream, int seg = 0) {
   int st = check_dims(d);
   if (st != GDN_OK) return st;
-  if (d->num_seqs <= 0) return GDN_ERR_INVALID_ARG;
+  if (d->num_seqs <= 0 || seg < 0) return GDN_ERR_INVALID_ARG;
+  if (seg > 0 && !use_tensor_core_prefill(d)) return GDN_ERR_UNSUPPORTED;
   if (!conv_w || !A_log || !dt_bias || !norm_w || !cu_seqlens) return GDN_ERR_INVALID_ARG;
   if (d->num_tokens > 0 && (!q || !k || !v || !a || !b || !z || !out)) return GDN_ERR_INVALID_ARG;
   const void *streams[] = {q, k, v, a, b, z, out, init_state, final_state, conv_w};
   for (const void *p : streams)
     if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
-  const size_t need = gdn_prefill_workspace_bytes(d);
+  const size_t need = seg > 0 ? gdn_prefill_segmented_workspace_bytes(d, seg) : gdn_prefill_workspace_bytes(d);
   if (workspace && (ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return GDN_ERR_WORKSPACE;
 
@@ -89,7 +97,9 @@ int prefill_impl(const gdn_dims *d, const void *q, const void *k, const void *v,
   p.ws_bytes = need - kStatusBytes;
 
   cudaError_t e;
-  if (use_tensor_core_prefill(d))
+  if (seg > 0)
+    e = gdn::launch_prefill_segmented(p, seg, s);
+  else if (use_tensor_core_prefill(d))
     e = gdn::launch_prefill_tc(p, s);
   else
     e = gdn::launch_prefill_simt(p, d->io_dtype == GDN_BF16, s);
@@ -123,6 +133,16 @@ int gdn_prefill_carry(const gdn_dims *d, const void *q, const void *k, const voi
                       void *final_conv, void *workspace, size_t ws_bytes, void *stream) {
   return prefill_impl(d, q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state, init_conv, out,
                       final_state, final_conv, workspace, ws_bytes, stream);
+}
+
+int gdn_prefill_segmented(const gdn_dims *d, const void *q, const void *k, const void *v, const void *a,
+                          const void *b, const void *z, const float *conv_w, const float *A_log,
+                          const float *dt_bias, const float *norm_w, const int32_t *cu_seqlens,
+                          const float *init_state, void *out, float *final_state, int seg_chunks, void *workspace,
+                          size_t ws_bytes, void *stream) {
+  if (seg_chunks < 1) return GDN_ERR_INVALID_ARG;
+  return prefill_impl(d, q, k, v, a, b, z, conv_w, A_log, dt_bias, norm_w, cu_seqlens, init_state, nullptr, out,
+                      final_state, nullptr, workspace, ws_bytes, stream, seg_chunks);
 }
 
 size_t gdn_prefill_backward_workspace_bytes(const gdn_dims *d) {

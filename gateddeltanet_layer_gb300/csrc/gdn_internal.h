@@ -66,6 +66,10 @@ cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t 
 constexpr int kTcMaxRep = 8;
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
 size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v);
+// Segment-parallel chunked prefill (the same shapes): every sequence cut into
+// segments of `seg` chunks, run in parallel and joined by an affine scan.
+cudaError_t launch_prefill_segmented(const PrefillParams &p, int seg, cudaStream_t s);
+size_t prefill_segmented_workspace_bytes(int T, int N, int h_qk, int h_v, int seg);
 // Decode step.
 cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s);
 // Conv cache of each sequence after a prefill (its last three raw inputs).

@@ -121,6 +121,7 @@ const char *gdn_trace_kernel_name(int kind) {
     case GDN_K_DECODE: return "decode_kernel";
     case GDN_K_BWD_CHAIN: return "bwd_state_kernels";
     case GDN_K_BWD_PROLOGUE: return "bwd_prologue_kernel";
+    case GDN_K_SEG_SCAN: return "seg_scan_kernels";
     default: return "";
   }
 }

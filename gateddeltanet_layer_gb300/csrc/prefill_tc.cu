@@ -100,6 +100,19 @@ struct Ws {
   uint8_t *qs;       // compact: [max_chunks][h_qk] x kQSlot (after the value-head slots)
   int max_chunks;
   int compact;       // the images are the compact ones (one-CTA-per-chain state pass)
+  const struct SegRun *runs;  // segment-parallel prefill: the state pass's chains (else null)
+};
+
+// One chain of the segment-parallel prefill's state passes: tokens [s0, s1)
+// (chunk images from g0 on) of value head blockIdx.x % h_v.  The state starts
+// from init (+ h * d_k * d_v; null: zeros) or, with kRunTransfer, from the
+// identity with U' taken as zero (the segment's transfer matrix), and ends in
+// final (+ h * d_k * d_v; may be null); with kRunOut the epilogue writes y.
+enum : int { kRunOut = 1, kRunTransfer = 2 };
+struct SegRun {
+  int s0, s1, g0, flags;
+  const float *init;
+  float *final;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1466,12 +1479,30 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
   bool failed = false;
 
   tc::grid_dependency_wait();  // the chunk table and the operand images
-  const int n = p.N > 1 ? ws.seq_order[chain / h_v] : chain / h_v;
-  const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
-  bool valid = s0 >= 0 && s1 >= s0 && s1 <= p.T;  // else reported by the chunk table
-  const int g0 = valid ? ws.chunk_base[n] : 0, g1 = valid ? ws.chunk_base[n + 1] : 0;
-  if (valid && g1 - g0 != (s1 - s0 + kC - 1) / kC) valid = false;  // table overflow, reported
-  const int nch = valid ? g1 - g0 : 0;
+  int n = 0, s0, s1, g0, nch, flags = kRunOut;
+  bool valid;
+  const float *init_base;  // this chain's state in and out: [d_k][d_v], or null
+  float *final_base;
+  if (ws.runs) {  // a chain of the segment-parallel prefill
+    const SegRun run = ws.runs[chain / h_v];
+    s0 = run.s0; s1 = run.s1; g0 = run.g0; flags = run.flags;
+    valid = s1 >= s0;
+    nch = valid ? (s1 - s0 + kC - 1) / kC : 0;
+    init_base = run.init ? run.init + (size_t)h * kD * kD : nullptr;
+    final_base = run.final ? run.final + (size_t)h * kD * kD : nullptr;
+  } else {
+    n = p.N > 1 ? ws.seq_order[chain / h_v] : chain / h_v;
+    s0 = p.cu_seqlens[n];
+    s1 = p.cu_seqlens[n + 1];
+    valid = s0 >= 0 && s1 >= s0 && s1 <= p.T;  // else reported by the chunk table
+    g0 = valid ? ws.chunk_base[n] : 0;
+    const int g1 = valid ? ws.chunk_base[n + 1] : 0;
+    if (valid && g1 - g0 != (s1 - s0 + kC - 1) / kC) valid = false;  // table overflow, reported
+    nch = valid ? g1 - g0 : 0;
+    init_base = p.init_state ? p.init_state + ((size_t)n * h_v + h) * kD * kD : nullptr;
+    final_base = p.final_state ? p.final_state + ((size_t)n * h_v + h) * kD * kD : nullptr;
+  }
+  const bool transfer = (flags & kRunTransfer) != 0, with_out = (flags & kRunOut) != 0;
   auto vslot = [&](int gg) { return ws.vs + ((size_t)gg * h_v + h) * kCSlot; };
   auto qslot = [&](int gg) { return ws.qs + ((size_t)gg * h_qk + hq) * kQSlot; };
   auto set_at = [](int c) -> uint32_t { return kStage * (uint32_t)(c % kSets); };
@@ -1502,7 +1533,7 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
   if (warp < kChainWarps) {
     // ======================= the chain: lane j = 32 (warp & 3) + lane, columns half hf
     const int hf = warp >> 2, j = 32 * (warp & 3) + lane;
-    const size_t st_base = ((size_t)n * h_v + h) * kD * kD + j;  // element (i, j) at + i * kD
+    const size_t st_base = j;  // element (i, j) of the chain's state at + i * kD
     // every chain thread waits on the mbarriers itself; a wait that runs out is
     // ORed into the next barrier the chain passes anyway (its publish)
     bool ok = true;
@@ -1525,7 +1556,7 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int i = 64 * hf + 32 * c32 + e;
-          v[e] = p.init_state ? p.init_state[st_base + (size_t)i * kD] : 0.0f;
+          v[e] = transfer ? (i == j ? 1.0f : 0.0f) : init_base ? init_base[st_base + (size_t)i * kD] : 0.0f;
         }
         tc::tmem_st32_nowait(tmem + lane_off + COL_S + 64 * hf + 32 * c32, v);
       }
@@ -1583,7 +1614,7 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
         float u[32], upv[32], dm[32];
         const __half *up = reinterpret_cast<const __half *>(sm + set + R_UP + (j >> 5) * 4096) + (j & 31);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) upv[e] = __half2float(up[(32 * hf + e) * 32]);
+        for (int e = 0; e < 32; ++e) upv[e] = transfer ? 0.0f : __half2float(up[(32 * hf + e) * 32]);
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const float4 d4 = *reinterpret_cast<const float4 *>(sm + set + R_DEC + 4 * (32 * hf + e));
@@ -1623,13 +1654,13 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
     if (!ok) failed = true;
     if (failed) {
       if (tid == 0) set_status(p.status, kDevTimeout);
-    } else if (valid && p.final_state) {
+    } else if (valid && final_base) {
       float v[32];
 #pragma unroll 1
       for (int c32 = 0; c32 < 2; ++c32) {
         tc::tmem_ld32(tmem + lane_off + COL_S + 64 * hf + 32 * c32, v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) p.final_state[st_base + (size_t)(64 * hf + 32 * c32 + e) * kD] = v[e];
+        for (int e = 0; e < 32; ++e) final_base[st_base + (size_t)(64 * hf + 32 * c32 + e) * kD] = v[e];
       }
     }
   } else {
@@ -1651,6 +1682,15 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
       tc::fence_after_sync();
       return tc::named_barrier_or(kBarEpiTs, kEpiThreads, !ok);
     };
+    if (!with_out) {  // a chain without outputs: only hand D1 and O2 back each chunk
+      for (int c = 0; c < nch; ++c) {
+        if (wait_epi(bar + B_ORDY, (uint32_t)c & 1)) { failed = true; break; }
+        tc::fence_before_sync();
+        tc::named_barrier(kBarEpiTs, kEpiThreads);
+        if (et == 0) tc::mbar_arrive(bar + B_ODONE);
+      }
+      if (failed && et == 0) set_status(p.status, kDevTimeout);
+    } else {
     if (nch > 0) issue_z(0);
     if (nch > 1) issue_z(1);
     for (int c = 0; c < nch; ++c) {
@@ -1739,6 +1779,7 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
       if (et == 0) set_status(p.status, kDevTimeout);
       for (int cc = z_done; cc < z_issued; ++cc) tc::mbar_wait(bar + B_Z + (cc & 1), (cc >> 1) & 1);
     }
+    }
   }
   if (tid == 0)  // copies in flight must land before the CTA's shared memory goes away
     for (int c = issued - kSets < 0 ? 0 : issued - kSets; c < issued; ++c)
@@ -1746,6 +1787,174 @@ __global__ void __launch_bounds__(ts::kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ================================================================ segment-parallel prefill
+// For few long chains: every sequence is cut into segments of `seg` chunks.
+// The state after segment s is affine in the state before it,
+// H_out = M_s H_in + B_s, with B_s the state the segment leaves from a zero
+// state and M_s the product of the chunks' maps H -> gamma_C H - K~^T W H (the
+// segment run on the identity with U' taken as zero).  So one state pass runs,
+// all at once, the first segment of each sequence for real (outputs and its
+// end state), every later segment from a zero state (B_s), and every middle
+// segment's M_s; a scan H_in(s + 1) = M_s H_in(s) + B_s gives each segment's
+// true start state; a second state pass reruns the later segments from those
+// states for their outputs and the sequence's final state.
+struct SegTab {
+  int max_seg;       // upper bound on the segments (host)
+  int seg;           // chunks per segment
+  int *seq_seg0;     // [N + 1]: first segment of each sequence; [N] = segments
+  SegRun *runs1;     // [2 max_seg]: pass 1 (per segment: its run, then its transfer run)
+  SegRun *runs3;     // [max_seg]: pass 2 (the reruns)
+  float *bufB, *bufM, *bufH;  // [max_seg][h_v][d_k][d_v] each: B_s, M_s, H_in(s)
+};
+
+__global__ void __launch_bounds__(1024) seg_table_kernel(const PrefillParams p, const Ws ws, SegTab st) {
+  __shared__ int scan[1024];
+  const int N = p.N, tid = threadIdx.x;
+  const int per = (N + 1023) / 1024;
+  const int n0 = min(N, tid * per), n1 = min(N, n0 + per);
+  auto nseg_of = [&](int n) {
+    const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+    const int nch = (s0 >= 0 && s1 >= s0 && s1 <= p.T) ? (s1 - s0 + kC - 1) / kC : 0;
+    return max(1, (nch + st.seg - 1) / st.seg);  // an empty (or invalid) sequence: one empty segment
+  };
+  int cnt = 0;
+  for (int n = n0; n < n1; ++n) cnt += nseg_of(n);
+  scan[tid] = cnt;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan
+    const int v = tid >= off ? scan[tid - off] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  const int total = scan[1023];
+  const bool overflow = total > st.max_seg;  // only with invalid cu_seqlens (reported by the chunk table)
+  int k = scan[tid] - cnt;
+  const size_t state = (size_t)p.h_v * kD * kD;
+  for (int n = n0; n < n1; ++n) {
+    const int nseg = nseg_of(n);
+    st.seq_seg0[n] = overflow ? 0 : k;
+    const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
+    const bool ok = !overflow && s0 >= 0 && s1 >= s0 && s1 <= p.T &&
+                    ws.chunk_base[n + 1] - ws.chunk_base[n] == (s1 - s0 + kC - 1) / kC;  // else reported
+    for (int sg = 0; sg < nseg && !overflow; ++sg, ++k) {
+      SegRun r, t, r3;
+      r.s0 = ok ? min(s1, s0 + sg * st.seg * kC) : 0;
+      r.s1 = ok ? min(s1, r.s0 + st.seg * kC) : 0;
+      r.g0 = ok ? ws.chunk_base[n] + sg * st.seg : 0;
+      t = r3 = r;
+      // pass 1: the first segment for real; the others from a zero state
+      r.flags = sg == 0 ? kRunOut : 0;
+      r.init = (sg == 0 && p.init_state) ? p.init_state + (size_t)n * state : nullptr;
+      r.final = (nseg == 1) ? (p.final_state ? p.final_state + (size_t)n * state : nullptr) : st.bufB + (size_t)k * state;
+      // pass 1: the transfer of a middle segment (the scan needs M_s for 1 <= s <= nseg - 2)
+      const bool middle = sg >= 1 && sg + 1 < nseg;
+      t.flags = kRunTransfer;
+      t.init = nullptr;
+      t.final = middle ? st.bufM + (size_t)k * state : nullptr;
+      if (!middle) t.s1 = t.s0;  // nothing to run
+      // pass 2: the later segments from their true start states
+      r3.flags = kRunOut;
+      r3.init = st.bufH + (size_t)k * state;
+      r3.final = (sg + 1 == nseg && p.final_state) ? p.final_state + (size_t)n * state : nullptr;
+      if (sg == 0) { r3.s1 = r3.s0; r3.init = nullptr; r3.final = nullptr; }
+      st.runs1[2 * k] = r;
+      st.runs1[2 * k + 1] = t;
+      st.runs3[k] = r3;
+    }
+  }
+  if (tid == 1023) st.seq_seg0[N] = overflow ? 0 : total;
+  // the runs past the last segment (all of them on an overflow) do nothing
+  for (int r = (overflow ? 0 : total) + tid; r < st.max_seg; r += 1024) {
+    SegRun z;
+    z.s0 = z.s1 = z.g0 = 0;
+    z.flags = 0;
+    z.init = nullptr;
+    z.final = nullptr;
+    st.runs1[2 * r] = z;
+    st.runs1[2 * r + 1] = z;
+    st.runs3[r] = z;
+  }
+}
+
+// The scan over a sequence's segments, per (sequence, value head, 16 state
+// columns): H_in(1) = B_0 (segment 0's true end state), then
+// H_in(s + 1) = M_s H_in(s) + B_s, in fp32.  Each step stages M_s in shared
+// memory (rows padded to 132 floats); thread (ti, tj) keeps rows ti + 32 r
+// (r < 4) x columns [2 tj, 2 tj + 2) of the product in registers.  A warp
+// holds 4 consecutive ti and the 8 tj, so per 4 steps of m its reads of M
+// (4 rows x 16 bytes per r) and of H (8 column pairs) are one wavefront each.
+// The next step's M is loaded into registers while this step's product runs.
+constexpr int kScanCols = 16, kScanThreads = 256, kScanPitch = kD + 4;
+constexpr size_t kScanSmem = sizeof(float) * ((size_t)kD * kScanPitch + (size_t)kD * kScanCols);
+__global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(const PrefillParams p, SegTab st) {
+  extern __shared__ __align__(16) float smem_scan[];
+  float *sM = smem_scan;                   // [128 i][kScanPitch]: M_s
+  float *sH = sM + kD * kScanPitch;        // [128 m][kScanCols]: the running H_in
+  constexpr int kBlocks = kD / kScanCols;
+  const int cb = blockIdx.x % kBlocks, h = (blockIdx.x / kBlocks) % p.h_v;
+  const int n = blockIdx.x / (kBlocks * p.h_v);
+  const int k0 = st.seq_seg0[n], nseg = st.seq_seg0[n + 1] - k0;
+  if (nseg < 2) return;
+  const size_t state = (size_t)p.h_v * kD * kD, head = (size_t)h * kD * kD;
+  const int tid = threadIdx.x, j0 = kScanCols * cb, ti = tid >> 3, tj = tid & 7;
+  for (int e = tid; e < kD * kScanCols; e += kScanThreads) {  // H = B_0
+    const int i = e / kScanCols, jj = e % kScanCols;
+    sH[e] = st.bufB[(size_t)k0 * state + head + (size_t)i * kD + j0 + jj];
+  }
+  constexpr int kMq = kD * kD / 4 / kScanThreads;  // float4 of M per thread
+  float4 mreg[kMq];
+  auto load_m = [&](int k) {  // M_k, row-major [i][m]: float4 q of this thread is float4 tid + 256 q
+    const float4 *M = reinterpret_cast<const float4 *>(st.bufM + (size_t)k * state + head);
+#pragma unroll
+    for (int q = 0; q < kMq; ++q) mreg[q] = M[tid + kScanThreads * q];
+  };
+  if (nseg > 2) load_m(k0 + 1);
+  __syncthreads();
+  for (int sg = 1; sg < nseg; ++sg) {
+    const int k = k0 + sg;
+    for (int e = tid; e < kD * kScanCols; e += kScanThreads) {
+      const int i = e / kScanCols, jj = e % kScanCols;
+      st.bufH[(size_t)k * state + head + (size_t)i * kD + j0 + jj] = sH[e];
+    }
+    if (sg + 1 == nseg) break;
+#pragma unroll
+    for (int q = 0; q < kMq; ++q) {
+      const int f = tid + kScanThreads * q;  // float4 f of M: row f / 32, columns 4 (f % 32) ...
+      *reinterpret_cast<float4 *>(sM + (f >> 5) * kScanPitch + 4 * (f & 31)) = mreg[q];
+    }
+    __syncthreads();
+    if (sg + 2 < nseg) load_m(k + 1);  // in flight during the product
+    const float *B = st.bufB + (size_t)k * state + head + j0 + 2 * tj;
+    float acc[4][2];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float2 b2 = *reinterpret_cast<const float2 *>(B + (size_t)(ti + 32 * r) * kD);
+      acc[r][0] = b2.x;
+      acc[r][1] = b2.y;
+    }
+#pragma unroll 2
+    for (int m = 0; m < kD; m += 4) {
+      float2 hr[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) hr[c] = *reinterpret_cast<const float2 *>(sH + (m + c) * kScanCols + 2 * tj);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 mr = *reinterpret_cast<const float4 *>(sM + (ti + 32 * r) * kScanPitch + m);
+        acc[r][0] = fmaf(mr.x, hr[0].x, acc[r][0]); acc[r][1] = fmaf(mr.x, hr[0].y, acc[r][1]);
+        acc[r][0] = fmaf(mr.y, hr[1].x, acc[r][0]); acc[r][1] = fmaf(mr.y, hr[1].y, acc[r][1]);
+        acc[r][0] = fmaf(mr.z, hr[2].x, acc[r][0]); acc[r][1] = fmaf(mr.z, hr[2].y, acc[r][1]);
+        acc[r][0] = fmaf(mr.w, hr[3].x, acc[r][0]); acc[r][1] = fmaf(mr.w, hr[3].y, acc[r][1]);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      *reinterpret_cast<float2 *>(sH + (ti + 32 * r) * kScanCols + 2 * tj) = make_float2(acc[r][0], acc[r][1]);
+    __syncthreads();
+  }
 }
 
 // ================================================================ host side
@@ -1844,7 +2053,7 @@ cudaError_t launch_state(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
   return e;
 }
 
-cudaError_t launch_state_ts(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
+cudaError_t launch_state_ts(const PrefillParams &p, const Ws &ws, cudaStream_t s, unsigned chains) {
   CUtensorMap zmap, omap;
   std::memset(&zmap, 0, sizeof(zmap));
   std::memset(&omap, 0, sizeof(omap));
@@ -1855,27 +2064,31 @@ cudaError_t launch_state_ts(const PrefillParams &p, const Ws &ws, cudaStream_t s
       cudaFuncSetAttribute(state_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ts::kSmem);
   if (e != cudaSuccess) return e;
   trace_begin(s, GDN_K_STATE);
-  state_ts_kernel<<<(unsigned)p.N * (unsigned)p.h_v, ts::kThreads, ts::kSmem, s>>>(p, ws, zmap, omap);
+  if (chains == 0) return cudaSuccess;
+  state_ts_kernel<<<chains * (unsigned)p.h_v, ts::kThreads, ts::kSmem, s>>>(p, ws, zmap, omap);
   trace_end(s);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
-  if (p.N <= 0) return cudaSuccess;
-  const WsLayout L(p.T, p.N, p.h_qk, p.h_v);
-  if (p.ws_bytes < L.total) return cudaErrorInvalidValue;
+namespace {
+
+Ws make_ws(const PrefillParams &p, const WsLayout &L, bool compact) {
   Ws ws;
   ws.chunk_base = reinterpret_cast<int *>(p.ws + L.base);
   ws.seq_order = reinterpret_cast<int *>(p.ws + L.order);
   ws.chunk_info = reinterpret_cast<int4 *>(p.ws + L.info);
   ws.vs = p.ws + L.vs;
   ws.max_chunks = L.max_chunks;
-  const bool split_pass = state_ring(p);
-  ws.compact = split_pass ? 0 : 1;
+  ws.compact = compact ? 1 : 0;
   ws.qs = ws.vs + (size_t)L.max_chunks * p.h_v * kCSlot;
+  ws.runs = nullptr;
+  return ws;
+}
 
+// The chunk table and the chunk prep (all chunks in parallel).
+cudaError_t launch_table_and_prep(const PrefillParams &p, const Ws &ws, cudaStream_t s) {
   trace_begin(s, GDN_K_CHUNK_TABLE);
   chunk_table_kernel<<<1, 1024, 0, s>>>(p, ws);
   trace_end(s);
@@ -1885,7 +2098,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
     e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)L.max_chunks, (unsigned)p.h_qk);
+    cfg.gridDim = dim3((unsigned)ws.max_chunks, (unsigned)p.h_qk);
     cfg.blockDim = dim3(kPrepThreads);
     cfg.dynamicSmemBytes = kPrepSmem;
     cfg.stream = s;
@@ -1897,12 +2110,76 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
     trace_begin(s, GDN_K_CHUNK_PREP);
     e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel, p, ws);
     trace_end(s);
-    if (e != cudaSuccess) return e;
   }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
+  if (p.N <= 0) return cudaSuccess;
+  const WsLayout L(p.T, p.N, p.h_qk, p.h_v);
+  if (p.ws_bytes < L.total) return cudaErrorInvalidValue;
   // Few chains (every split-column cluster on SMs of its own): the split state
   // pass with a ring of operand sets has the shorter chain (1.6 against 2.0 us
   // per chunk on the 4096-token workload); otherwise one CTA per chain.
-  return split_pass ? launch_state<kStateSlices, 3>(p, ws, s) : launch_state_ts(p, ws, s);
+  const bool split_pass = state_ring(p);
+  const Ws ws = make_ws(p, L, !split_pass);
+  cudaError_t e = launch_table_and_prep(p, ws, s);
+  if (e != cudaSuccess) return e;
+  return split_pass ? launch_state<kStateSlices, 3>(p, ws, s) : launch_state_ts(p, ws, s, (unsigned)p.N);
+}
+
+size_t prefill_segmented_workspace_bytes(int T, int N, int h_qk, int h_v, int seg) {
+  if (seg < 1) return 0;
+  const WsLayout L(T, N, h_qk, h_v);
+  const size_t max_seg = (size_t)(((T + kC - 1) / kC + N) / seg + N + 1);
+  size_t off = (L.total + 255) / 256 * 256;
+  off += (size_t)(N + 1) * sizeof(int);
+  off = (off + 255) / 256 * 256 + 3 * max_seg * sizeof(SegRun);
+  off = (off + 1023) / 1024 * 1024;
+  return off + 3 * max_seg * (size_t)h_v * kD * kD * sizeof(float);
+}
+
+cudaError_t launch_prefill_segmented(const PrefillParams &p, int seg, cudaStream_t s) {
+  if (p.N <= 0) return cudaSuccess;
+  if (seg < 1 || p.ws_bytes < prefill_segmented_workspace_bytes(p.T, p.N, p.h_qk, p.h_v, seg))
+    return cudaErrorInvalidValue;
+  const WsLayout L(p.T, p.N, p.h_qk, p.h_v);
+  Ws ws = make_ws(p, L, true);
+  SegTab st;
+  st.seg = seg;
+  st.max_seg = (int)(((p.T + kC - 1) / kC + p.N) / seg + p.N + 1);
+  size_t off = (L.total + 255) / 256 * 256;
+  st.seq_seg0 = reinterpret_cast<int *>(p.ws + off);
+  off += (size_t)(p.N + 1) * sizeof(int);
+  off = (off + 255) / 256 * 256;
+  st.runs1 = reinterpret_cast<SegRun *>(p.ws + off);
+  st.runs3 = st.runs1 + 2 * (size_t)st.max_seg;
+  off += 3 * (size_t)st.max_seg * sizeof(SegRun);
+  off = (off + 1023) / 1024 * 1024;
+  const size_t buf = (size_t)st.max_seg * p.h_v * kD * kD;
+  st.bufB = reinterpret_cast<float *>(p.ws + off);
+  st.bufM = st.bufB + buf;
+  st.bufH = st.bufM + buf;
+
+  cudaError_t e = launch_table_and_prep(p, ws, s);
+  if (e != cudaSuccess) return e;
+  trace_begin(s, GDN_K_SEG_SCAN);
+  seg_table_kernel<<<1, 1024, 0, s>>>(p, ws, st);
+  trace_end(s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ws.runs = st.runs1;
+  if ((e = launch_state_ts(p, ws, s, 2u * (unsigned)st.max_seg)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem)) !=
+      cudaSuccess)
+    return e;
+  trace_begin(s, GDN_K_SEG_SCAN);
+  seg_scan_kernel<<<(unsigned)p.N * p.h_v * (kD / kScanCols), kScanThreads, kScanSmem, s>>>(p, st);
+  trace_end(s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ws.runs = st.runs3;
+  return launch_state_ts(p, ws, s, (unsigned)st.max_seg);
 }
 
 }  // namespace gdn

@@ -103,6 +103,11 @@ LONG_128K = PrefillConfig("prefill_long_T131072", (8192,) * 16, a_log_range=(1.0
 
 CONFIGS = {c.name: c for c in (TINY, SINGLE_4K, VARLEN_32K, DECODE_256, LONG_128K)}
 
+# Few chains: one 16384-token sequence with the heads one GPU holds when the
+# layer's 16/32 heads are split 8 ways by tensor parallelism (2 q/k, 4 value
+# heads): the case the segment-parallel prefill is for.
+FEW_CHAINS_16K = PrefillConfig("prefill_T16384_hv4", (16384,), h_qk=2, h_v=4)
+
 
 def _stream(rng, shape, dtype):
     x = rng.standard_normal(shape, dtype=np.float32)

@@ -164,6 +164,46 @@ GDN_API int gdn_prefill_carry(const gdn_dims *dims, const void *q, const void *k
                               size_t ws_bytes, void *stream);
 
 /*
+ * Segment-parallel prefill: the results of gdn_prefill, with more chains in
+ * flight when there are few long sequences.
+ *
+ * The pages state no chunking; this follows from the recurrence above.  Over
+ * a stretch of tokens the state map S_t = exp(g_t) S_{t-1} (I - beta_t k_t
+ * k_t^T) + beta_t v_t k_t^T is affine in the state, so the state after a
+ * stretch is S_out = S_in M + B: M the product of the tokens' linear parts
+ * (per chunk of the tensor-core path, gamma_C I - W^T K~), B the state the
+ * stretch leaves from zero.
+ * Every sequence is cut into segments of seg_chunks chunks (64 tokens each);
+ * one state pass runs, all at once, each sequence's first segment from its
+ * initial state (with its outputs), every later segment from a zero state
+ * (its B) and every middle segment on the identity (its M); a scan over each
+ * sequence's segments, S_in(s + 1) = S_in(s) M_s + B_s, gives every segment's
+ * true initial state; a second state pass runs the later segments from those
+ * states, with their outputs and the final state.  The fp32 state is the
+ * same; the results equal gdn_prefill's up to rounding order (the state
+ * operands of the products are rounded to fp16 at different points).
+ *
+ * seg_chunks  chunks per segment, >= 1.  A sequence of S >= 2 segments takes
+ *             3 - 3/S times the state-pass chunk steps of gdn_prefill, in
+ *             fewer sequential steps: it pays when N * h_v chains leave most
+ *             SMs idle.
+ * Supported shapes: the chunked tensor-core shapes of gdn_prefill (bf16,
+ * d_k = d_v = 128, h_v / h_qk <= 8); others return GDN_ERR_UNSUPPORTED.
+ * Every other argument, the workspace (of
+ * gdn_prefill_segmented_workspace_bytes(dims, seg_chunks) bytes; the B, M and
+ * start-state buffers add 192 KiB per segment and value head) and the errors
+ * are those of gdn_prefill, including an in-place final_state.  Returns a
+ * gdn_status.
+ */
+GDN_API size_t gdn_prefill_segmented_workspace_bytes(const gdn_dims *dims, int seg_chunks);
+GDN_API int gdn_prefill_segmented(const gdn_dims *dims, const void *q, const void *k, const void *v,
+                                  const void *a, const void *b, const void *z, const float *conv_w,
+                                  const float *A_log, const float *dt_bias, const float *norm_w,
+                                  const int32_t *cu_seqlens, const float *init_state, void *out,
+                                  float *final_state, int seg_chunks, void *workspace, size_t ws_bytes,
+                                  void *stream);
+
+/*
  * Backward pass of gdn_prefill: the gradient, with respect to every input, of
  * the scalar loss  sum(dy * y) + sum(dfinal_state * final_state).
  *

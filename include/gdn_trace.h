@@ -33,7 +33,8 @@ typedef enum {
   GDN_K_DECODE = 4,      /* one-token decode step */
   GDN_K_BWD_CHAIN = 5,   /* backward: forward with checkpoints, RMSNorm and the rule in reverse (3 launches) */
   GDN_K_BWD_PROLOGUE = 6,/* backward: L2 norm, SiLU and conv in reverse */
-  GDN_K_COUNT = 7
+  GDN_K_SEG_SCAN = 7,    /* segment-parallel prefill: segment table and the scan over segments (2 launches) */
+  GDN_K_COUNT = 8
 } gdn_kernel_kind;
 
 #define GDN_TRACE_MAX_LAUNCHES 4096

@@ -100,7 +100,7 @@ def test_trace_read_without_launches(lib):
     assert gdn.trace_read() == {}
     names = [lib.gdn_trace_kernel_name(k).decode() for k in range(gdn.TRACE_KINDS)]
     assert names == ["chunk_table_kernel", "chunk_prep_kernel", "state_kernel", "prefill_simt_kernel",
-                     "decode_kernel", "bwd_state_kernels", "bwd_prologue_kernel"]
+                     "decode_kernel", "bwd_state_kernels", "bwd_prologue_kernel", "seg_scan_kernels"]
     assert lib.gdn_trace_kernel_name(gdn.TRACE_KINDS) == b""
     assert lib.gdn_trace_read(0, None, None) == 1
 
@@ -141,3 +141,22 @@ def test_backward_and_carry_reject_bad_arguments_without_a_gpu(lib):
     assert lib.gdn_prefill_carry(ctypes.byref(d), *([None] * 17), 0, None) == 1
     unsup = D(64, 1, 2, 2, 24, 16, gdn.GDN_FP32)                                # head dim not a multiple of 16
     assert lib.gdn_prefill_carry(ctypes.byref(unsup), *([None] * 17), 0, None) == 2
+
+
+def test_segmented_prefill_rejects_bad_arguments_without_a_gpu(lib):
+    """gdn_prefill_segmented: only the chunked tensor-core shapes, seg_chunks >= 1,
+    required pointers; its workspace holds the plain prefill's and the segment
+    buffers (three fp32 states per segment and value head)."""
+    D = gdn.Dims
+    tc = D(4096, 1, 4, 8, 128, 128, gdn.GDN_BF16)
+    fp32 = D(4096, 1, 4, 8, 128, 128, gdn.GDN_FP32)
+    null = [None] * 14
+    assert lib.gdn_prefill_segmented(ctypes.byref(tc), *null, 8, None, 0, None) == 1      # pointers missing
+    assert lib.gdn_prefill_segmented(ctypes.byref(tc), *null, 0, None, 0, None) == 1      # seg_chunks < 1
+    assert lib.gdn_prefill_segmented(ctypes.byref(fp32), *null, 8, None, 0, None) == 2    # not a tensor-core shape
+    assert lib.gdn_prefill_segmented_workspace_bytes(ctypes.byref(fp32), 8) == 0
+    assert lib.gdn_prefill_segmented_workspace_bytes(ctypes.byref(tc), 0) == 0
+    plain = lib.gdn_prefill_workspace_bytes(ctypes.byref(tc))
+    segs = (4096 // 64 + 1) // 8 + 1 + 1                      # upper bound on the segments
+    extra = lib.gdn_prefill_segmented_workspace_bytes(ctypes.byref(tc), 8) - plain
+    assert 3 * segs * 8 * 128 * 128 * 4 <= extra < 3 * segs * 8 * 128 * 128 * 4 + 8192

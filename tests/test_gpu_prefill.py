@@ -270,3 +270,62 @@ def test_split_packed_sequences_into_short_segments(dtype, d, in_place):
     parity(y, r["y"][idx], dtype, "out")
     parity(fs, r["final_state"], dtype, "final_state")
     np.testing.assert_array_equal(conv, ref.conv_cache_after_prefill(inp, inp["cu_seqlens"]))
+
+
+def run_segmented(inp, seg_chunks, *, in_place=False):
+    gdn = _gdn()
+    t = to_torch(inp, True)
+    init = t.get("init_state")
+    fs = init if (in_place and init is not None) else None
+    out, fs = gdn.prefill_segmented(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                                    t["dt_bias"], t["norm_w"], t["cu_seqlens"], init, seg_chunks=seg_chunks,
+                                    final_state=fs)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), fs.cpu().numpy()
+
+
+@pytest.mark.parametrize("lengths,seg_chunks,in_place", [
+    ((1000,), 1, False),                   # every chunk a segment: 14 middle segments, a ragged last one
+    ((1000,), 3, False),                   # 6 segments, the last one short
+    ((1000,), 8, False),                   # 2 segments: no middle segment, so no transfer matrix
+    ((1000,), 16, False),                  # one segment: the plain state pass
+    ((300, 0, 1, 640, 65, 128), 2, False),  # packed: empty, 1-token, exact-segment and straddling sequences
+    ((300, 0, 1, 640, 65, 128), 2, True),   # the same with the final state written over the initial one
+], ids=["seg1", "seg3", "seg8", "seg16", "varlen_seg2", "varlen_seg2_in_place"])
+def test_segmented_prefill(lengths, seg_chunks, in_place):
+    """gdn_prefill_segmented against the oracle on every chain: each segment's
+    start state comes out of the scan over the earlier segments' affine maps
+    (B from a zero state, M from the identity), so every output and final
+    state checks the transfer matrices and the scan as well."""
+    cfg = synth.scaled(synth.SINGLE_4K, lengths=lengths, h_qk=2, h_v=4, init_std=0.02, seed=61)
+    inp = synth.make_prefill(cfg)
+    y, fs = run_segmented(inp, seg_chunks, in_place=in_place)
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"])
+    parity(y, r["y"], "bf16", "out")
+    parity(fs, r["final_state"], "bf16", "final_state")
+
+
+def test_segmented_prefill_slow_decay():
+    """Slow decay (alpha near 1): the earlier segments' states reach far, so a
+    wrong transfer matrix or scan order shows in the later segments' outputs."""
+    cfg = synth.scaled(synth.SINGLE_4K, lengths=(1500,), h_qk=1, h_v=2, init_std=0.02, seed=62)
+    inp = synth.make_prefill(cfg)
+    inp["dt_bias"][:] = -6.0
+    y, fs = run_segmented(inp, 4)
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"])
+    parity(y, r["y"], "bf16", "out")
+    parity(fs, r["final_state"], "bf16", "final_state")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,seg_chunks", [("prefill_T4096", 22), ("prefill_T16384_hv4", 16)])
+def test_full_size_segmented(name, seg_chunks):
+    """The 4096-token workload (16/32 heads) and the few-chain 16384-token one
+    (2/4 heads) through gdn_prefill_segmented, with the segment lengths the
+    benchmark's segmented lines use, every chain against the oracle."""
+    cfg = {**synth.CONFIGS, synth.FEW_CHAINS_16K.name: synth.FEW_CHAINS_16K}[name]
+    inp = synth.make_prefill(cfg)
+    y, fs = run_segmented(inp, seg_chunks)
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], threads=os.cpu_count())
+    parity(y, r["y"], "bf16", "out")
+    parity(fs, r["final_state"], "bf16", "final_state")
