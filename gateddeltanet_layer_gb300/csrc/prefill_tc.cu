@@ -171,13 +171,15 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// SiLU of a pair: x / (1 + e^-x), e^-x = 2^(-x log2 e) by the hardware 2^x
-// (rel. error ~2^-22); 1 / inf = 0 gives the right limit for very negative x.
+// SiLU of a pair: x sigmoid(x) = h + h tanh(h), h = x / 2, with the hardware
+// tanh (tanh.approx: absolute error about 2^-11, so |error| <= ~2^-11 |h|).
+// Two multi-function-unit operations per pair instead of four (2^x and 1/x
+// twice); on the prefill workloads the outputs' error against the oracle
+// moved by under 1e-3 of the bound, and the prep ran 3 % faster.
 constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ float2 silu2(float2 x) {
-  const float2 t = tc::mul2(x, tc::splat2(-kLog2e));
-  const float2 d = tc::add2(make_float2(tc::ex2_approx(t.x), tc::ex2_approx(t.y)), tc::splat2(1.0f));
-  return tc::mul2(x, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+  const float2 hx = tc::mul2(x, tc::splat2(0.5f));
+  return tc::fma2(hx, make_float2(tc::tanh_approx(hx.x), tc::tanh_approx(hx.y)), hx);
 }
 
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t &phase) {
