@@ -56,11 +56,18 @@ def peaks():
 
 
 def prefill_work(cfg) -> tuple[int, float]:
-    """Algorithmic bytes and flops of one prefill call (streams, states, no intermediates)."""
-    nbytes = cfg.T * BYTES_PER_TOKEN + cfg.N * STATE_BYTES  # final state written
+    """Algorithmic bytes and flops of one prefill call (streams, states, no intermediates):
+    per token q, k [h_qk, d_k], v, z and out [h_v, d_v], a, b [h_v] in the stream dtype; per
+    sequence the fp32 state [h_v, d_k, d_v] written (and read when there is an initial one).
+    32,896 B and FLOPS_PER_TOKEN per token at 16/32 heads, d = 128, bf16."""
+    es = 4 if cfg.dtype == "fp32" else 2
+    per_token = es * (2 * cfg.h_qk * cfg.d_k + 3 * cfg.h_v * cfg.d_v + 2 * cfg.h_v)
+    state = 4 * cfg.h_v * cfg.d_k * cfg.d_v
+    nbytes = cfg.T * per_token + cfg.N * state               # final state written
     if cfg.init_std > 0:
-        nbytes += cfg.N * STATE_BYTES                        # initial state read
-    return nbytes, float(cfg.T) * FLOPS_PER_TOKEN
+        nbytes += cfg.N * state                              # initial state read
+    flops = float(cfg.T) * cfg.h_v * (10 * 64 * cfg.d_v + 6 * cfg.d_k * cfg.d_v)
+    return nbytes, flops
 
 
 def max_over_ranks(values, device):
@@ -146,11 +153,12 @@ def inputs_of(cfg):
 
 
 # ---------------------------------------------------------------------- GPU arm
-def _device_inputs(inp, dev):
+def _device_inputs(inp, dev, fp32=False):
     import torch
     t = {}
+    sdt = torch.float32 if fp32 else torch.bfloat16
     for key in ("x_q", "x_k", "x_v", "z", "a", "b"):
-        t[key] = torch.from_numpy(inp[key]).to(dev).to(torch.bfloat16)
+        t[key] = torch.from_numpy(inp[key]).to(dev).to(sdt)
     for key in ("conv_w", "A_log", "dt_bias", "norm_w"):
         t[key] = torch.from_numpy(inp[key]).to(dev)
     t["cu_seqlens"] = torch.from_numpy(inp["cu_seqlens"]).to(dev)
@@ -171,14 +179,15 @@ def time_prefill(cfg, steps, warmup, dev, flush, with_e2e=False, trace=False, se
 
     import gateddeltanet_layer_gb300 as gdn
     inp = inputs_of(cfg)
-    t = _device_inputs(inp, dev)
+    fp32 = cfg.dtype == "fp32"
+    t = _device_inputs(inp, dev, fp32)
     T, N = cfg.T, cfg.N
-    out = torch.empty((T, cfg.h_v, cfg.d_v), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, cfg.h_v, cfg.d_v), dtype=torch.float32 if fp32 else torch.bfloat16, device=dev)
     fs = torch.empty((N, cfg.h_v, cfg.d_k, cfg.d_v), dtype=torch.float32, device=dev)
     if seg_chunks:
         ws_bytes = gdn.prefill_segmented_workspace_bytes(T, N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v, seg_chunks)
     else:
-        ws_bytes = gdn.prefill_workspace_bytes(T, N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v, True)
+        ws_bytes = gdn.prefill_workspace_bytes(T, N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v, not fp32)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -385,7 +394,10 @@ HEADLINE = synth.LONG_128K
 # captures; per sequence it does the same work, so its DRAM traffic scales to
 # the headline call by the number of sequences.
 LONG_2X8192 = synth.scaled(synth.LONG_128K, name="prefill_long_T16384", lengths=(8192,) * 2)
-PROFILE_CASES = {LONG_2X8192.name: LONG_2X8192, synth.FEW_CHAINS_16K.name: synth.FEW_CHAINS_16K}
+# the shapes the token-sequential fp32 kernel serves: more than 8 value heads per q/k head, fp32 streams
+GQA16_4K = synth.scaled(synth.SINGLE_4K, name="prefill_T4096_gqa16", h_qk=2)
+FP32_4K = synth.scaled(synth.SINGLE_4K, name="prefill_T4096_fp32", dtype="fp32")
+PROFILE_CASES = {c.name: c for c in (LONG_2X8192, synth.FEW_CHAINS_16K, GQA16_4K, FP32_4K)}
 
 
 def prefill_line(cfg, res, steps, pk, dev):
@@ -482,6 +494,14 @@ def run_ours(args):
             ent["segmented"]["seg_chunks"] = seg
             ent["speedup"] = ent["plain"]["ms"] / ent["segmented"]["ms"]
             extra[f"{c.name}_segmented"] = ent
+        # the token-sequential fp32 kernel (one CTA per chain) on the shapes the chunked path leaves to it
+        for c in (GQA16_4K, FP32_4K, synth.TINY):
+            n_steps = max(3, args.steps // 4)
+            r = time_prefill(c, n_steps, args.warmup, dev, flush, trace=True)
+            m, rl = prefill_line(c, r, n_steps, pk, dev)
+            extra[c.name] = {"tokens_per_s": c.T / (m * 1e-3), "ms": m, "roofline_frac": rl["frac"],
+                             "per_kernel": rl["per_kernel"], "h_qk": c.h_qk, "h_v": c.h_v, "d": c.d_k,
+                             "dtype": c.dtype}
         r = time_backward(synth.SINGLE_4K, max(3, args.steps // 4), args.warmup, dev, flush)
         m, = max_over_ranks([statistics.mean(r["ms"])], dev)
         extra["prefill_backward_T4096"] = {"tokens_per_s": synth.SINGLE_4K.T / (m * 1e-3), "ms": m,

@@ -27,7 +27,7 @@ int check_dims(const gdn_dims *d) {
 }
 
 bool use_tensor_core_prefill(const gdn_dims *d) {
-  return d->io_dtype == GDN_BF16 && d->d_k == 128 && d->d_v == 128 && d->h_v / d->h_qk <= gdn::kTcMaxRep;
+  return d->io_dtype == GDN_BF16 && d->d_k == 128 && d->d_v == 128;
 }
 
 }  // namespace

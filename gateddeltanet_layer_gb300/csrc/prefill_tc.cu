@@ -381,7 +381,10 @@ __device__ __forceinline__ void l2norm_rows(float (&y)[8][4], int lane) {
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const PrefillParams p, const Ws ws) {
-  const int g = blockIdx.x, hq = blockIdx.y;
+  // grid (chunk slots, q/k heads x value-head groups): a CTA takes up to kMaxRep of the value heads
+  // of its q/k head (all of them unless h_v / h_qk > kMaxRep, where each group redoes the q/k part)
+  const int ngrp = (p.h_v / p.h_qk + kMaxRep - 1) / kMaxRep;
+  const int g = blockIdx.x, hq = blockIdx.y / ngrp, vbase = kMaxRep * (blockIdx.y % ngrp);
   tc::grid_dependency_wait();  // the chunk table
   tc::launch_dependents();     // the state pass may be scheduled once every prep CTA has started
   const int total = ws.chunk_base[p.N];
@@ -392,12 +395,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lr = tid & 127, gh = tid >> 7;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-  const int h_v = p.h_v, h_qk = p.h_qk, rep = h_v / h_qk;
+  const int h_v = p.h_v, h_qk = p.h_qk, rep = h_v / h_qk, nrep = min(kMaxRep, rep - vbase);
+  const bool qk_images = vbase == 0;  // the group that writes the per-q/k-head images
   // TMEM: the 256-column W / U' accumulator at column 0; K K^T and Q K^T (64
   // columns) under it when the value heads come as one pair (their A is taken
   // before the first W / U' product), else beside it
-  const uint32_t tmem_cols = rep <= 2 ? 256u : 512u;
-  const int COL_P1 = rep <= 2 ? 0 : 256;
+  const uint32_t tmem_cols = nrep <= 2 ? 256u : 512u;
+  const int COL_P1 = nrep <= 2 ? 0 : 256;
 
   const int4 info = ws.chunk_info[g];
   const int t0 = info.y, s0 = info.z, Lc = info.w;
@@ -439,7 +443,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const int r0 = 8 * warp, c0 = 4 * lane;  // conv: this thread's rows and channels
   const bool compact = ws.compact != 0;
   auto v_slot_of = [&](int vv) {
-    return ws.vs + ((size_t)g * h_v + hq * rep + vv) * (compact ? kCSlot : kVSlot);
+    return ws.vs + ((size_t)g * h_v + hq * rep + vbase + vv) * (compact ? kCSlot : kVSlot);
   };
   uint8_t *const q_slot = ws.qs + ((size_t)g * h_qk + hq) * kQSlot;  // compact only
 
@@ -447,16 +451,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   auto prefetch_v = [&](int vv) {
     const int t = t0 - 3 + tid;
     if (tid < kC + 3 && t >= s0 && t < t0 + Lc)
-      tc::prefetch_l2(xv + (size_t)t * v_stride + (size_t)(hq * rep + vv) * kD, kD * 2);
+      tc::prefetch_l2(xv + (size_t)t * v_stride + (size_t)(hq * rep + vbase + vv) * kD, kD * 2);
   };
   prefetch_v(0);
 
   // ---------------- gates of every value head and their running sums inside the chunk
-  for (int v0 = 0; v0 < rep; v0 += 4) {
+  for (int v0 = 0; v0 < nrep; v0 += 4) {
     const int vv = v0 + (tid >> 6), r = tid & 63;
     float gsum = 0.0f;
-    if (vv < rep) {
-      const int h = hq * rep + vv;
+    if (vv < nrep) {
+      const int h = hq * rep + vbase + vv;
       float gg = 0.0f, be = 0.0f;
       if (r < Lc) {
         const size_t gi = (size_t)(t0 + r) * h_v + h;
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       sG[vv * 256 + 128 + r] = be;
     }
     __syncthreads();
-    if (vv < rep) {
+    if (vv < nrep) {
       if (r >= 32) gsum += carry[vv & 3];
       sG[vv * 256 + r] = gsum;
       const float gm = expf(gsum);
@@ -481,7 +485,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       *reinterpret_cast<float *>(v_slot_of(vv) + (compact ? kCGam : kVGam) + 4 * r) = gm;
     }
     __syncthreads();
-    if (vv < rep) {
+    if (vv < nrep) {
       const float dec = expf(sG[vv * 256 + 63] - sG[vv * 256 + r]);
       sG[vv * 256 + 192 + r] = dec;
       if (compact) *reinterpret_cast<float *>(v_slot_of(vv) + kCDec + 4 * r) = dec;
@@ -497,7 +501,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       uint2 xrq[11];
       load_rows(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(hq * kD + c0), xrq);
       load_rows(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(h_qk * kD + hq * kD + c0), xrk);
-      if (rep > 1) prefetch_v(1);
+      if (nrep > 1) prefetch_v(1);
       conv_silu(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
     }
     l2norm_rows(y, lane);
@@ -512,12 +516,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       *reinterpret_cast<uint2 *>(sm + P_KQL + off) = lo;
     }
     if (compact) {  // Q, once per q/k head: [64 rows] SW128 slabs
+      if (qk_images) {
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
-        *reinterpret_cast<uint2 *>(q_slot + kQQ + tc::sw128_offset(64, r0 + r, c0)) =
-            pack4_f16(y[r][0], y[r][1], y[r][2], y[r][3]);
+        for (int r = 0; r < 8; ++r)
+          *reinterpret_cast<uint2 *>(q_slot + kQQ + tc::sw128_offset(64, r0 + r, c0)) =
+              pack4_f16(y[r][0], y[r][1], y[r][2], y[r][3]);
+      }
     } else {
-      for (int vv = 0; vv < rep; ++vv) {  // Q^ = diag(gamma) Q: rows 0-63 of the [Q^; W] image
+      for (int vv = 0; vv < nrep; ++vv) {  // Q^ = diag(gamma) Q: rows 0-63 of the [Q^; W] image
         const float *gam = sG + vv * 256 + 64;
         uint8_t *dst = v_slot_of(vv) + kVWQ;
 #pragma unroll
@@ -560,8 +566,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   }
 
   // ---------------- the value heads, two at a time
-  for (int grp = 0; grp < rep && !failed; grp += 2) {
-    const int nh = min(2, rep - grp);
+  for (int grp = 0; grp < nrep && !failed; grp += 2) {
+    const int nh = min(2, nrep - grp);
     auto AT = [&](int hh) { return reinterpret_cast<float *>(sm + (hh ? P_AT1 : P_AT0)); };
     auto XF = [&](int hh) { return reinterpret_cast<float *>(sm + P_XF + (hh ? 4096 : 0)); };
 
@@ -569,16 +575,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     {
       uint2 xr[11];
       float y[8][4];
-      load_rows(xv + (size_t)(hq * rep + grp) * kD + c0, v_stride, t0, s0, Lc, r0,
-                hist(2 * h_qk * kD + (hq * rep + grp) * kD + c0), xr);
-      conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + grp) * kD + c0, Lc, r0, y);
+      load_rows(xv + (size_t)(hq * rep + vbase + grp) * kD + c0, v_stride, t0, s0, Lc, r0,
+                hist(2 * h_qk * kD + (hq * rep + vbase + grp) * kD + c0), xr);
+      conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + vbase + grp) * kD + c0, Lc, r0, y);
       // the second head's rows in flight over the first head's stores and the wait below
       if (nh > 1)
-        load_rows(xv + (size_t)(hq * rep + grp + 1) * kD + c0, v_stride, t0, s0, Lc, r0,
-                  hist(2 * h_qk * kD + (hq * rep + grp + 1) * kD + c0), xr);
-      if (grp + 2 < rep) {
+        load_rows(xv + (size_t)(hq * rep + vbase + grp + 1) * kD + c0, v_stride, t0, s0, Lc, r0,
+                  hist(2 * h_qk * kD + (hq * rep + vbase + grp + 1) * kD + c0), xr);
+      if (grp + 2 < nrep) {
         prefetch_v(grp + 2);
-        if (grp + 3 < rep) prefetch_v(grp + 3);
+        if (grp + 3 < nrep) prefetch_v(grp + 3);
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {  // first head: its tile is not under the K K^T / Q K^T operands
@@ -589,7 +595,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       }
       if (grp == 0 && wait_all(bar, phase)) { failed = true; break; }  // K K^T and Q K^T are done
       if (nh > 1) {
-        conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + grp + 1) * kD + c0, Lc, r0, y);
+        conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + vbase + grp + 1) * kD + c0, Lc, r0, y);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float col[8];
@@ -661,7 +667,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       const int hh = tid >> 6, bb = (tid >> 4) & 3, s = tid & 15;
       const bool act = hh < nh;
       if (tid >= 128 && compact) {  // meanwhile: the K^T tile to its image, once per q/k head
-        if (grp == 0) {
+        if (grp == 0 && qk_images) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const int q = tid - 128 + 128 * k;
@@ -888,7 +894,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
             *reinterpret_cast<const uint4 *>(stu + (q >> 8) * 4096 + m * 64 + (((q & 3) ^ ((m >> 1) & 3)) << 4));
       }
     }
-    if (grp + 2 < rep) __syncthreads();  // the stagings are read before the next pair's tiles go there
+    if (grp + 2 < nrep) __syncthreads();  // the stagings are read before the next pair's tiles go there
   }
   if (failed && tid == 0) set_status(p.status, kDevTimeout);
   tc::fence_before_sync();
@@ -2100,7 +2106,7 @@ cudaError_t launch_table_and_prep(const PrefillParams &p, const Ws &ws, cudaStre
     e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ws.max_chunks, (unsigned)p.h_qk);
+    cfg.gridDim = dim3((unsigned)ws.max_chunks, (unsigned)(p.h_qk * ((p.h_v / p.h_qk + kMaxRep - 1) / kMaxRep)));
     cfg.blockDim = dim3(kPrepThreads);
     cfg.dynamicSmemBytes = kPrepSmem;
     cfg.stream = s;

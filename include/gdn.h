@@ -188,7 +188,7 @@ GDN_API int gdn_prefill_carry(const gdn_dims *dims, const void *q, const void *k
  *             fewer sequential steps: it pays when N * h_v chains leave most
  *             SMs idle.
  * Supported shapes: the chunked tensor-core shapes of gdn_prefill (bf16,
- * d_k = d_v = 128, h_v / h_qk <= 8); others return GDN_ERR_UNSUPPORTED.
+ * d_k = d_v = 128); others return GDN_ERR_UNSUPPORTED.
  * Every other argument, the workspace (of
  * gdn_prefill_segmented_workspace_bytes(dims, seg_chunks) bytes; the B, M and
  * start-state buffers add 192 KiB per segment and value head) and the errors

@@ -50,7 +50,7 @@ def test_tiny_fp32_config():
     check(synth.make_prefill(synth.TINY), "fp32")
 
 
-@pytest.mark.parametrize("case", ["ragged_single", "varlen_edges", "long_memory", "gqa4", "gqa8", "gqa16",
+@pytest.mark.parametrize("case", ["ragged_single", "varlen_edges", "long_memory", "gqa4", "gqa8", "gqa12", "gqa16",
                                   "fp32_d128", "gqa1", "gqa3", "chunk_edges", "fast_decay"])
 def test_small_cases(case):
     if case == "ragged_single":      # several chunks plus a ragged tail
@@ -70,9 +70,11 @@ def test_small_cases(case):
         cfg = synth.scaled(synth.VARLEN_32K, lengths=(64, 65, 127, 1, 128), h_qk=1, h_v=2, seed=11)
     elif case == "fast_decay":       # gates near their strongest: A_log up to log 16 and large dt_bias
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(200,), h_qk=1, h_v=2, init_std=0.02, seed=12)
-    elif case == "gqa8":             # the most value heads per q/k head the chunked path takes
+    elif case == "gqa8":             # the most value heads one chunk-prep CTA takes
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(70,), h_qk=1, h_v=8, seed=8)
-    elif case == "gqa16":            # beyond it: served by the token-sequential kernel
+    elif case == "gqa12":            # a group of 8 value heads and one of 4, each redoing the q/k part
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(70, 130), h_qk=1, h_v=12, init_std=0.02, seed=13)
+    elif case == "gqa16":            # two groups of 8 value heads per q/k head
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(70,), h_qk=1, h_v=16, seed=9)
     else:                            # fp32 streams at d = 128 (token-sequential fp32 kernel)
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(130, 7), h_qk=1, h_v=2, dtype="fp32", init_std=0.02)
@@ -89,7 +91,8 @@ def test_small_cases(case):
     ((150, 1, 64), 2, 8),                  # 24 chains: one CTA per SM, a ring of operand sets
     ((65, 1, 128, 30, 64), 4, 8),          # 40 chains: two CTAs per SM, one set per kind
     ((65, 1, 128, 30, 64, 100, 7, 64, 129, 3), 16, 32),  # 320 chains: more CTAs than fit at once
-], ids=["chains24", "chains40", "chains320"])
+    ((200, 64, 1, 90), 2, 32),             # 128 chains, 16 value heads per q/k head (two prep groups)
+], ids=["chains24", "chains40", "chains320", "chains128_gqa16"])
 def test_state_pass_chain_counts(lengths, h_qk, h_v):
     """Few and many (sequence, value head) chains (the state pass runs a ring
     of operand sets at one CTA per SM for few chains, two CTAs per SM
