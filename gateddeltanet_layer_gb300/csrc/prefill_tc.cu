@@ -752,16 +752,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     }
     __syncthreads();
     // (c) the lower-left 32 x 32 block T_21 = -T_2 (A_21 T_1); threads 128 hh .. 128 hh + 127 take
-    //     head hh, a 2 x 4 tile each (T_1 and T_2 are whole lower-triangular blocks: zeros above the diagonal)
+    //     head hh, a 2 x 4 tile each.  T_1 and T_2 are lower triangular: (A_21 T_1)[., c] sums over
+    //     k >= c and (T_2 Y)[r, .] over k <= r, so each warp's loop starts (first product: its columns
+    //     share a lower bound) or stops (second: its rows share an upper bound) where its tile allows
     {
-      const int hh = tid >> 7, t = tid & 127, rr = 2 * (t >> 3), cc = 4 * (t & 7);
+      const int hh = tid >> 7, t = tid & 127;
       const bool act = hh < nh;
       if (act) {
+        const int rr = 2 * (t & 15), cc = 4 * (t >> 4), k0 = 8 * ((t >> 5) & 3);  // k0: the warp's first column
         const float *At = AT(hh);
         const float *a0 = At + (32 + rr) * kPad, *a1 = a0 + kPad;
         float2 y0a = make_float2(0.0f, 0.0f), y0b = y0a, y1a = y0a, y1b = y0a;  // rows rr, rr + 1
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
+#pragma unroll 4
+        for (int k = k0; k < 32; k += 2) {
           const float2 av = *reinterpret_cast<const float2 *>(a0 + k), bv = *reinterpret_cast<const float2 *>(a1 + k);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
@@ -779,11 +782,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       }
       __syncthreads();
       if (act) {
+        const int rr = 2 * (t >> 3), cc = 4 * (t & 7), k1 = 8 * ((t >> 5) & 3) + 8;  // k1: past the warp's last row
         float *At = AT(hh);
         const float *t0r = At + (32 + rr) * kPad + 32, *t1r = t0r + kPad;
         float2 z0a = make_float2(0.0f, 0.0f), z0b = z0a, z1a = z0a, z1b = z0a;
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
+#pragma unroll 4
+        for (int k = 0; k < k1; k += 2) {
           const float2 pv = *reinterpret_cast<const float2 *>(t0r + k), qv = *reinterpret_cast<const float2 *>(t1r + k);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
