@@ -164,13 +164,6 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
   return v[0];
 }
 
-// The hardware reciprocal (rcp.approx: a few ulp of fp32, far below the fp16
-// rounding of the results it feeds; 1 / inf = 0).
-__device__ __forceinline__ float rcp_approx(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 // SiLU of a pair: x sigmoid(x) = h + h tanh(h), h = x / 2, with the hardware
 // tanh (tanh.approx: absolute error about 2^-11, so |error| <= ~2^-11 |h|).
 // Two multi-function-unit operations per pair instead of four (2^x and 1/x
@@ -2075,8 +2068,8 @@ cudaError_t launch_state_ts(const PrefillParams &p, const Ws &ws, cudaStream_t s
   cudaError_t e =
       cudaFuncSetAttribute(state_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ts::kSmem);
   if (e != cudaSuccess) return e;
-  trace_begin(s, GDN_K_STATE);
   if (chains == 0) return cudaSuccess;
+  trace_begin(s, GDN_K_STATE);
   state_ts_kernel<<<chains * (unsigned)p.h_v, ts::kThreads, ts::kSmem, s>>>(p, ws, zmap, omap);
   trace_end(s);
   return cudaGetLastError();
