@@ -60,6 +60,11 @@ struct BwdWs {
   float *hs;     // [N][h_v][slices][kB + 1][kSliceThreads][kSlot]: the block's states, in reverse
   float *wo;     // [T][h_v][d_v]: o (scaled) of every token
   float *wdo;    // [T][h_v][d_v]: its gradient
+  float *xq;     // [T][h_qk][d_k]: q^ = L2-normalised silu(conv(q)), every token (computed once)
+  float *xk;     // [T][h_qk][d_k]: k^
+  float *xv;     // [T][h_v][d_v]: silu(conv(v))
+  float *xal;    // [T][h_v]: alpha = e^g
+  float *xbe;    // [T][h_v]: beta
   float *dqn;    // [T][h_v][d_k]: gradient of the normalised q (per value head; summed over slices)
   float *dkn;    // [T][h_v][d_k]
   float *dvs;    // [T][h_v][d_v]: gradient of silu(conv(v))
@@ -70,7 +75,7 @@ struct BwdWs {
 };
 
 struct BwdLayout {
-  size_t ckpt, hs, wo, wdo, dqn, dkn, dvs, dg, dbeta, acc, total;
+  size_t ckpt, hs, wo, wdo, xq, xk, xv, xal, xbe, dqn, dkn, dvs, dg, dbeta, acc, total;
   int slots, slices;
   BwdLayout(int T, int N, int h_qk, int h_v, int d_k, int d_v) {
     slices = (d_v + kSliceCols - 1) / kSliceCols;
@@ -81,7 +86,12 @@ struct BwdLayout {
     hs = up(ckpt + (size_t)slots * h_v * slices * st);
     wo = up(hs + (size_t)N * h_v * slices * (kB + 1) * st);
     wdo = up(wo + (size_t)T * h_v * d_v * sizeof(float));
-    dqn = up(wdo + (size_t)T * h_v * d_v * sizeof(float));
+    xq = up(wdo + (size_t)T * h_v * d_v * sizeof(float));
+    xk = up(xq + (size_t)T * h_qk * d_k * sizeof(float));
+    xv = up(xk + (size_t)T * h_qk * d_k * sizeof(float));
+    xal = up(xv + (size_t)T * h_v * d_v * sizeof(float));
+    xbe = up(xal + (size_t)T * h_v * sizeof(float));
+    dqn = up(xbe + (size_t)T * h_v * sizeof(float));
     dkn = up(dqn + (size_t)T * h_v * d_k * sizeof(float));
     dvs = up(dkn + (size_t)T * h_v * d_k * sizeof(float));
     dg = up(dvs + (size_t)T * h_v * d_v * sizeof(float));
@@ -91,55 +101,49 @@ struct BwdLayout {
   }
 };
 
-// The block's prologue (as the forward fp32 kernel): conv(4) + SiLU of q, k
-// and of the slice's columns [j0, j0 + kSliceCols) of v, L2 norm of q, k, and
-// the gates, for tokens [t0, t0 + nt) of sequence [s0, s1) into shared memory.
-template <typename IO>
-__device__ void block_prologue(const BwdParams &p, int h, int hq, int s0, int t0, int nt, int j0, float *sq,
-                               float *sk, float *sv, float *salpha, float *sbeta, float A_exp, float dtb) {
+// The block's inputs into shared memory: q^, k^ and the slice's columns
+// [j0, j0 + kSliceCols) of silu(conv(v)) (zeros past d_v), alpha and beta, for
+// tokens [t0, t0 + nt), from the arrays bwd_inputs_kernel wrote.
+__device__ void block_prologue(const BwdParams &p, const BwdWs &ws, int h, int hq, int t0, int nt, int j0,
+                               float *sq, float *sk, float *sv, float *salpha, float *sbeta) {
   const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
-  const int nch = 2 * dk + kSliceCols;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const IO *xq = static_cast<const IO *>(p.q), *xk = static_cast<const IO *>(p.k), *xv = static_cast<const IO *>(p.v);
-  const IO *xa = static_cast<const IO *>(p.a), *xb = static_cast<const IO *>(p.b);
-  for (int idx = threadIdx.x; idx < nt * nch; idx += blockDim.x) {
-    const int tt = idx / nch, c = idx % nch;
-    const int t = t0 + tt;
-    const IO *src;
-    size_t stride;
-    int ch;
-    float *dst;
-    if (c < dk) {
-      src = xq + hq * dk + c; stride = (size_t)h_qk * dk; ch = hq * dk + c; dst = sq + tt * dk + c;
-    } else if (c < 2 * dk) {
-      const int cc = c - dk;
-      src = xk + hq * dk + cc; stride = (size_t)h_qk * dk; ch = h_qk * dk + hq * dk + cc; dst = sk + tt * dk + cc;
-    } else {
-      const int cc = c - 2 * dk, jj = j0 + cc;
-      dst = sv + tt * kSliceCols + cc;
-      if (jj >= dv) { *dst = 0.0f; continue; }
-      src = xv + h * dv + jj; stride = (size_t)h_v * dv; ch = 2 * h_qk * dk + h * dv + jj;
-    }
-    float pre = 0.0f;
+  // float4 copies (d_k, d_v and the row offsets are multiples of 16 floats), kU in flight per thread
+  const int nq = dk / 4, nv = kSliceCols / 4, per_tok = 2 * nq + nv, total = nt * per_tok;
+  const float4 *gq = reinterpret_cast<const float4 *>(ws.xq), *gk = reinterpret_cast<const float4 *>(ws.xk);
+  const float4 *gv = reinterpret_cast<const float4 *>(ws.xv);
+  float4 *sq4 = reinterpret_cast<float4 *>(sq), *sk4 = reinterpret_cast<float4 *>(sk);
+  float4 *sv4 = reinterpret_cast<float4 *>(sv);
+  constexpr int kU = 6;
+  for (int base = threadIdx.x; base < total; base += kU * blockDim.x) {
+    float4 val[kU];
+    float4 *dst[kU];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int tau = t - 3 + j;
-      if (tau >= s0) pre = fmaf(p.conv_w[ch * 4 + j], to_f(src[(size_t)tau * stride]), pre);
+    for (int u = 0; u < kU; ++u) {
+      const int idx = base + u * blockDim.x;
+      dst[u] = nullptr;
+      if (idx < total) {
+        const int tt = idx / per_tok, c = idx % per_tok;
+        const size_t t = (size_t)(t0 + tt);
+        if (c < nq) {
+          val[u] = gq[(t * h_qk + hq) * nq + c];
+          dst[u] = sq4 + tt * nq + c;
+        } else if (c < 2 * nq) {
+          val[u] = gk[(t * h_qk + hq) * nq + c - nq];
+          dst[u] = sk4 + tt * nq + c - nq;
+        } else {
+          const int jj = j0 + 4 * (c - 2 * nq);
+          val[u] = jj < dv ? gv[((t * h_v + h) * dv + jj) / 4] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          dst[u] = sv4 + tt * nv + c - 2 * nq;
+        }
+      }
     }
-    *dst = silu_f(pre);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (dst[u]) *dst[u] = val[u];
   }
   for (int tt = threadIdx.x; tt < nt; tt += blockDim.x) {
-    const size_t t = (size_t)(t0 + tt);
-    salpha[tt] = expf(gate_g(to_f(xa[t * h_v + h]), A_exp, dtb));
-    sbeta[tt] = sigmoid_f(to_f(xb[t * h_v + h]));
-  }
-  __syncthreads();
-  for (int row = warp; row < 2 * nt; row += nwarps) {
-    float *x = row < nt ? sq + row * dk : sk + (row - nt) * dk;
-    float ss = 0.0f;
-    for (int i = lane; i < dk; i += 32) ss = fmaf(x[i], x[i], ss);
-    const float inv = rsqrtf(warp_sum(ss) + kEpsL2);
-    for (int i = lane; i < dk; i += 32) x[i] *= inv;
+    salpha[tt] = ws.xal[(size_t)(t0 + tt) * h_v + h];
+    sbeta[tt] = ws.xbe[(size_t)(t0 + tt) * h_v + h];
   }
   __syncthreads();
 }
@@ -199,23 +203,31 @@ __device__ __forceinline__ void fwd_step(float (&H)[kRows][kCW], int tt, int dk,
     qr[r] = i < dk ? sq[tt * dk + i] : 0.0f;
   }
   const float al = salpha[tt], be = sbeta[tt];
+  // p = H^T k over the warp's columns: the 8 column sums together (a reduce-scatter leaves column
+  // l >> 2 in lane l, then each is broadcast), not one butterfly per column
+  float s[kCW];
 #pragma unroll
   for (int c = 0; c < kCW; ++c) {
-    float s = 0.0f;
+    s[c] = 0.0f;
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) s = fmaf(H[r][c], kr[r], s);
-    const float pc = warp_sum(s);
+    for (int r = 0; r < kRows; ++r) s[c] = fmaf(H[r][c], kr[r], s[c]);
+  }
+  const float ps = reduce_scatter<kCW>(s, lane);
+  float o[kCW];
+#pragma unroll
+  for (int c = 0; c < kCW; ++c) {
+    const float pc = __shfl_sync(0xffffffffu, ps, 4 * c);
     const float u = be * (sv[tt * kSliceCols + jw + c] - al * pc);
-    float o = 0.0f;
+    o[c] = 0.0f;
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
       H[r][c] = fmaf(kr[r], u, al * H[r][c]);
-      o = fmaf(H[r][c], qr[r], o);
+      o[c] = fmaf(H[r][c], qr[r], o[c]);
     }
-    if (wo_row) {
-      o = warp_sum(o);
-      if (lane == c && jw + c < jmax) wo_row[jw + c] = o * scale;
-    }
+  }
+  if (wo_row) {
+    const float os = reduce_scatter<kCW>(o, lane);  // lane l: column l >> 2
+    if ((lane & 3) == 0 && jw + (lane >> 2) < jmax) wo_row[jw + (lane >> 2)] = os * scale;
   }
 }
 
@@ -233,10 +245,10 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_fwd_kernel(const BwdParams 
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, jw = kCW * warp;
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];
   float *sq = smem, *sk = sq + kB * dk, *sv = sk + kB * dk, *salpha = sv + 2 * kB * kSliceCols;
   float *sbeta = salpha + kB;
-  const float A_exp = expf(p.A_log[cx.h]), dtb = p.dt_bias[cx.h], scale = rsqrtf((float)dk);
+  const float scale = rsqrtf((float)dk);
   const size_t chain_off = ((size_t)cx.n * h_v + cx.h) * dk * dv;
   float H[kRows][kCW];
 #pragma unroll
@@ -250,7 +262,7 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_fwd_kernel(const BwdParams 
     const int t0 = cx.s0 + kB * b, nt = min(kB, cx.s1 - t0);
     store_state(slice_ptr(ws.ckpt, ((size_t)(cx.slot0 + b) * h_v + cx.h) * ws.slices + cx.sl), H);
     __syncthreads();  // the previous block's shared memory is consumed
-    block_prologue<IO>(p, cx.h, cx.hq, cx.s0, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta, A_exp, dtb);
+    block_prologue(p, ws, cx.h, cx.hq, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta);
     for (int tt = 0; tt < nt; ++tt)
       fwd_step(H, tt, dk, jw, dv - cx.j0, sq, sk, sv, salpha, sbeta, scale,
                ws.wo + ((size_t)(t0 + tt) * h_v + cx.h) * dv + cx.j0);
@@ -299,13 +311,13 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
   const SliceCtx cx = slice_ctx(p, ws.slices);
   if (!cx.ok) return;  // reported by the forward kernel
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, jw = kCW * warp;
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];
   float *sq = smem, *sk = sq + kB * dk, *sv = sk + kB * dk, *sdo = sv + kB * kSliceCols;
   float *red_q = sdo + kB * kSliceCols;         // [kSliceWarps][128]
   float *red_k = red_q + kSliceWarps * 128;
   float *red_s = red_k + kSliceWarps * 128;     // [kSliceWarps][4]
   float *salpha = red_s + kSliceWarps * 4, *sbeta = salpha + kB;
-  const float A_exp = expf(p.A_log[cx.h]), dtb = p.dt_bias[cx.h], scale = rsqrtf((float)dk);
+  const float scale = rsqrtf((float)dk);
   const size_t chain_off = ((size_t)cx.n * h_v + cx.h) * dk * dv;
   auto elem_ok = [&](int r, int c) { return lane + 32 * r < dk && cx.j0 + jw + c < dv; };
   float G[kRows][kCW], H[kRows][kCW];
@@ -319,10 +331,19 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
   for (int b = cx.nblk - 1; b >= 0; --b) {
     const int t0 = cx.s0 + kB * b, nt = min(kB, cx.s1 - t0);
     __syncthreads();
-    block_prologue<IO>(p, cx.h, cx.hq, cx.s0, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta, A_exp, dtb);
-    for (int e = tid; e < nt * kSliceCols; e += kSliceThreads) {  // do of the slice's columns
-      const int tt = e / kSliceCols, jj = e % kSliceCols;
-      sdo[e] = cx.j0 + jj < dv ? ws.wdo[((size_t)(t0 + tt) * h_v + cx.h) * dv + cx.j0 + jj] : 0.0f;
+    block_prologue(p, ws, cx.h, cx.hq, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta);
+    {  // do of the slice's columns, float4 copies (all of them in flight)
+      constexpr int kPer = kB * kSliceCols / 4 / kSliceThreads;
+      float4 dv4[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int e = tid + kSliceThreads * u, tt = e / (kSliceCols / 4), jj = cx.j0 + 4 * (e % (kSliceCols / 4));
+        dv4[u] = (tt < nt && jj < dv)
+                     ? *reinterpret_cast<const float4 *>(ws.wdo + ((size_t)(t0 + tt) * h_v + cx.h) * dv + jj)
+                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) reinterpret_cast<float4 *>(sdo)[tid + kSliceThreads * u] = dv4[u];
     }
     load_state(slice_ptr(ws.ckpt, ((size_t)(cx.slot0 + b) * h_v + cx.h) * ws.slices + cx.sl), H);
     for (int tt = 0; tt < nt; ++tt) {  // the block's states again (before each token)
@@ -371,16 +392,24 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
         dkp[r] = 0.0f;
       }
       float pc[kCW], du[kCW];
+      {  // the column sums, 8 at a time (reduce-scatter, then broadcast)
+        float a[kCW], d[kCW];
 #pragma unroll
-      for (int c = 0; c < kCW; ++c) {
-        float a = 0.0f, d = 0.0f;
+        for (int c = 0; c < kCW; ++c) {
+          a[c] = 0.0f;
+          d[c] = 0.0f;
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          a = fmaf(Hp[r][c], kr[r], a);
-          d = fmaf(G[r][c], kr[r], d);
+          for (int r = 0; r < kRows; ++r) {
+            a[c] = fmaf(Hp[r][c], kr[r], a[c]);
+            d[c] = fmaf(G[r][c], kr[r], d[c]);
+          }
         }
-        pc[c] = warp_sum(a);
-        du[c] = warp_sum(d);
+        const float as = reduce_scatter<kCW>(a, lane), ds = reduce_scatter<kCW>(d, lane);
+#pragma unroll
+        for (int c = 0; c < kCW; ++c) {
+          pc[c] = __shfl_sync(0xffffffffu, as, 4 * c);
+          du[c] = __shfl_sync(0xffffffffu, ds, 4 * c);
+        }
       }
       float s_db = 0.0f, s_dup = 0.0f, dp[kCW];
 #pragma unroll
@@ -463,6 +492,64 @@ __device__ __forceinline__ int2 seq_of(const int32_t *cu, int N, int t) {
     if (cu[mid] <= t) lo = mid; else hi = mid - 1;
   }
   return make_int2(cu[lo], cu[lo + 1]);
+}
+
+// The forward's per-token inputs, once for every chain and column slice that reads them: one warp per
+// (token, row) with row y < h_qk the q head y, then the k heads, then the value heads; lane l takes
+// channels l, l + 32, ...  conv(4) over the sequence's own tokens, SiLU, the L2 norm of q and k; the
+// value-head rows also write alpha = e^g and beta.
+template <typename IO>
+__global__ void __launch_bounds__(256) bwd_inputs_kernel(const BwdParams p, const BwdWs ws) {
+  const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v, rows = 2 * h_qk + h_v;
+  const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= (size_t)p.T * rows) return;
+  const int t = (int)(row / rows), y = (int)(row % rows);
+  const int s0 = seq_of(p.cu_seqlens, p.N, t).x;
+  const IO *src;
+  size_t stride;
+  int cb, D;
+  float *dst;
+  if (y < 2 * h_qk) {
+    const int hq = y < h_qk ? y : y - h_qk;
+    src = static_cast<const IO *>(y < h_qk ? p.q : p.k) + hq * dk;
+    stride = (size_t)h_qk * dk;
+    cb = y * dk;  // conv channels: [q heads | k heads | v heads]
+    D = dk;
+    dst = (y < h_qk ? ws.xq : ws.xk) + ((size_t)t * h_qk + hq) * dk;
+  } else {
+    const int hv = y - 2 * h_qk;
+    src = static_cast<const IO *>(p.v) + hv * dv;
+    stride = (size_t)h_v * dv;
+    cb = 2 * h_qk * dk + hv * dv;
+    D = dv;
+    dst = ws.xv + ((size_t)t * h_v + hv) * dv;
+    if (lane == 0) {
+      const size_t gi = (size_t)t * h_v + hv;
+      ws.xal[gi] = expf(gate_g(to_f(static_cast<const IO *>(p.a)[gi]), expf(p.A_log[hv]), p.dt_bias[hv]));
+      ws.xbe[gi] = sigmoid_f(to_f(static_cast<const IO *>(p.b)[gi]));
+    }
+  }
+  float x[4];
+  float ss = 0.0f;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int c = lane + 32 * r;
+    float pre = 0.0f;
+    if (c < D) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int tau = t - 3 + j;
+        if (tau >= s0) pre = fmaf(p.conv_w[(size_t)(cb + c) * 4 + j], to_f(src[(size_t)tau * stride + c]), pre);
+      }
+    }
+    x[r] = c < D ? silu_f(pre) : 0.0f;
+    ss = fmaf(x[r], x[r], ss);
+  }
+  const float inv = y < 2 * h_qk ? rsqrtf(warp_sum(ss) + kEpsL2) : 1.0f;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    if (lane + 32 * r < D) dst[lane + 32 * r] = x[r] * inv;
 }
 
 __device__ __forceinline__ float block_sum128(float v, float *red) {
@@ -600,6 +687,11 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
   ws.hs = reinterpret_cast<float *>(p.ws + L.hs);
   ws.wo = reinterpret_cast<float *>(p.ws + L.wo);
   ws.wdo = reinterpret_cast<float *>(p.ws + L.wdo);
+  ws.xq = reinterpret_cast<float *>(p.ws + L.xq);
+  ws.xk = reinterpret_cast<float *>(p.ws + L.xk);
+  ws.xv = reinterpret_cast<float *>(p.ws + L.xv);
+  ws.xal = reinterpret_cast<float *>(p.ws + L.xal);
+  ws.xbe = reinterpret_cast<float *>(p.ws + L.xbe);
   ws.dqn = reinterpret_cast<float *>(p.ws + L.dqn);
   ws.dkn = reinterpret_cast<float *>(p.ws + L.dkn);
   ws.dvs = reinterpret_cast<float *>(p.ws + L.dvs);
@@ -615,13 +707,15 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
   const unsigned rows = (unsigned)(((size_t)p.T * p.h_v + 7) / 8);
   const dim3 pgrid((unsigned)((p.T + kTile - 1) / kTile), (unsigned)(2 * p.h_qk + p.h_v));
   const unsigned ggrid = (unsigned)(((size_t)p.T * p.h_v + 255) / 256);
-  auto run = [&](auto fwd_k, auto norm_k, auto rev_k, auto pro_k, auto gate_k) -> cudaError_t {
+  const unsigned irows = (unsigned)(((size_t)p.T * (2 * p.h_qk + p.h_v) + 7) / 8);
+  auto run = [&](auto in_k, auto fwd_k, auto norm_k, auto rev_k, auto pro_k, auto gate_k) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(fwd_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(rev_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return err;
     if (ctas) {
       trace_begin(s, GDN_K_BWD_CHAIN);
+      if (p.T > 0) in_k<<<irows, 256, 0, s>>>(p, ws);
       fwd_k<<<ctas, kSliceThreads, smem, s>>>(p, ws);
       if (p.T > 0) norm_k<<<rows, 256, 0, s>>>(p, ws);
       rev_k<<<ctas, kSliceThreads, smem, s>>>(p, ws);
@@ -639,10 +733,10 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
     return cudaGetLastError();
   };
   if (bf16)
-    return run(bwd_fwd_kernel<__nv_bfloat16>, bwd_norm_kernel<__nv_bfloat16>, bwd_rev_kernel<__nv_bfloat16>,
-               bwd_prologue_kernel<__nv_bfloat16>, bwd_gate_kernel<__nv_bfloat16>);
-  return run(bwd_fwd_kernel<float>, bwd_norm_kernel<float>, bwd_rev_kernel<float>, bwd_prologue_kernel<float>,
-             bwd_gate_kernel<float>);
+    return run(bwd_inputs_kernel<__nv_bfloat16>, bwd_fwd_kernel<__nv_bfloat16>, bwd_norm_kernel<__nv_bfloat16>,
+               bwd_rev_kernel<__nv_bfloat16>, bwd_prologue_kernel<__nv_bfloat16>, bwd_gate_kernel<__nv_bfloat16>);
+  return run(bwd_inputs_kernel<float>, bwd_fwd_kernel<float>, bwd_norm_kernel<float>, bwd_rev_kernel<float>,
+             bwd_prologue_kernel<float>, bwd_gate_kernel<float>);
 }
 
 }  // namespace gdn

@@ -39,6 +39,29 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Sum over the 32 lanes of the warp of each of the NV values v[i] (NV a power
+// of two <= 32): lane l returns the sum for i = l >> (5 - log2 NV).
+template <int NV>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int off = 16 >> st;
+    const int half = (NV >> st) >> 1;  // values kept after this stage (0: plain butterfly)
+    if (half > 0) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = upper ? v[i] : v[i + half];
+        const float keep = upper ? v[i + half] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    }
+  }
+  return v[0];
+}
+
 // ----------------------------------------------------------------- device status
 // First error wins; 0 = OK.  Codes are the public gdn_status values.
 enum : int { kDevOk = 0, kDevBadSeqlens = 5, kDevTimeout = 6 };

@@ -141,28 +141,6 @@ __device__ __forceinline__ void mma_chain(uint32_t d, uint32_t a, int a_rows, in
               (acc || k > 0) ? 1u : 0u);
 }
 
-// Sum over the 32 lanes of the warp of each of the NV values v[i] (NV a power
-// of two <= 32): lane l returns the sum for i = l >> (5 - log2 NV).
-template <int NV>
-__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
-#pragma unroll
-  for (int st = 0; st < 5; ++st) {
-    const int off = 16 >> st;
-    const int half = (NV >> st) >> 1;  // values kept after this stage (0: plain butterfly)
-    if (half > 0) {
-      const bool upper = (lane & off) != 0;
-#pragma unroll
-      for (int i = 0; i < half; ++i) {
-        const float send = upper ? v[i] : v[i + half];
-        const float keep = upper ? v[i + half] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-      }
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-    }
-  }
-  return v[0];
-}
 
 // SiLU of a pair: x sigmoid(x) = h + h tanh(h), h = x / 2, with the hardware
 // tanh (tanh.approx: absolute error about 2^-11, so |error| <= ~2^-11 |h|).
