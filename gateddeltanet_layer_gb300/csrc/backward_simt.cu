@@ -231,8 +231,9 @@ __device__ __forceinline__ void fwd_step(float (&H)[kRows][kCW], int tt, int dk,
   }
 }
 
+constexpr int kRedFloats = kSliceWarps * (2 * 128 + 4);  // one buffer of the reverse step's column sums
 constexpr size_t slice_smem_floats(int dk) {
-  return (size_t)kB * (2 * dk + 2 * kSliceCols) + (size_t)kSliceWarps * (2 * 128 + 4) + 2 * kB;
+  return (size_t)kB * (2 * dk + 2 * kSliceCols) + 2 * (size_t)kRedFloats + 2 * kB;
 }
 
 // Forward with checkpoints: the slice of the state at each block start, and o of every token.
@@ -313,10 +314,10 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, jw = kCW * warp;
   extern __shared__ __align__(16) float smem[];
   float *sq = smem, *sk = sq + kB * dk, *sv = sk + kB * dk, *sdo = sv + kB * kSliceCols;
-  float *red_q = sdo + kB * kSliceCols;         // [kSliceWarps][128]
-  float *red_k = red_q + kSliceWarps * 128;
-  float *red_s = red_k + kSliceWarps * 128;     // [kSliceWarps][4]
-  float *salpha = red_s + kSliceWarps * 4, *sbeta = salpha + kB;
+  // two buffers (by token parity) of [kSliceWarps][128] q and k sums and [kSliceWarps][4] scalars: a
+  // token's sums are written, then read after one barrier; the buffer is written again two tokens later
+  float *red = sdo + kB * kSliceCols;
+  float *salpha = red + 2 * kRedFloats, *sbeta = salpha + kB;
   const float scale = rsqrtf((float)dk);
   const size_t chain_off = ((size_t)cx.n * h_v + cx.h) * dk * dv;
   auto elem_ok = [&](int r, int c) { return lane + 32 * r < dk && cx.j0 + jw + c < dv; };
@@ -361,6 +362,8 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
     load_state(slice_ptr(hs, nt - 1), Hp);
     for (int tt = nt - 1; tt >= 0; --tt) {
       const size_t tok = (size_t)(t0 + tt) * h_v + cx.h;
+      float *red_q = red + (tt & 1) * kRedFloats, *red_k = red_q + kSliceWarps * 128;
+      float *red_s = red_k + kSliceWarps * 128;
       float Hn[kRows][kCW];  // the state before token tt - 1, in flight over this step
       load_state(slice_ptr(hs, tt > 0 ? tt - 1 : 0), Hn);
       float kr[kRows], qr[kRows];
@@ -465,7 +468,6 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
         atomicAdd(&ws.dg[tok], al * (dal - be * dup));  // linear in the slice's parts
         atomicAdd(&ws.dbeta[tok], db);
       }
-      __syncthreads();
 #pragma unroll
       for (int r = 0; r < kRows; ++r)
 #pragma unroll
