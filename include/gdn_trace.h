@@ -31,7 +31,7 @@ typedef enum {
   GDN_K_STATE = 2,       /* sequential inter-chunk state pass + gated RMSNorm epilogue */
   GDN_K_PREFILL_SIMT = 3,/* token-sequential fp32 prefill (small or fp32 shapes) */
   GDN_K_DECODE = 4,      /* one-token decode step */
-  GDN_K_BWD_CHAIN = 5,   /* backward: forward with checkpoints, RMSNorm and the rule in reverse (3 launches) */
+  GDN_K_BWD_CHAIN = 5,   /* backward: inputs, forward with checkpoints, RMSNorm and the rule in reverse (4 launches) */
   GDN_K_BWD_PROLOGUE = 6,/* backward: L2 norm, SiLU and conv in reverse */
   GDN_K_SEG_SCAN = 7,    /* segment-parallel prefill: segment table and the scan over segments (2 launches) */
   GDN_K_COUNT = 8
