@@ -72,35 +72,54 @@ __global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
   for (int t0 = s0; t0 < s1; t0 += kTB) {
     const int nt = min(kTB, s1 - t0);
     __syncthreads();  // the previous batch's buffers are consumed
-    // conv (width 4; before s0 the carried history, or zeros) + SiLU
-    for (int idx = threadIdx.x; idx < nt * nch; idx += blockDim.x) {
-      const int tt = idx / nch, c = idx % nch;
-      const int t = t0 + tt;
-      const IO *src;
-      size_t stride;
-      int ch;
-      float *dst;
-      if (c < dk) {
-        src = xq + hq * dk + c; stride = (size_t)h_qk * dk; ch = hq * dk + c; dst = sq + tt * dk + c;
-      } else if (c < 2 * dk) {
-        const int cc = c - dk;
-        src = xk + hq * dk + cc; stride = (size_t)h_qk * dk; ch = h_qk * dk + hq * dk + cc;
-        dst = sk + tt * dk + cc;
-      } else {
-        const int cc = c - 2 * dk;
-        src = xv + h * dv + cc; stride = (size_t)h_v * dv; ch = 2 * h_qk * dk + h * dv + cc;
-        dst = sv + tt * dv + cc;
-      }
-      float pre = 0.0f;
+    // conv (width 4; before s0 the carried history, or zeros) + SiLU: kU elements per thread at a time,
+    // their 4 kU input loads issued before any is used
+    constexpr int kU = 4;
+    for (int base = threadIdx.x; base < nt * nch; base += kU * blockDim.x) {
+      float xin[kU][4], w[kU][4];
+      float *dst[kU];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int tau = t - 3 + j;
-        if (tau >= s0)
-          pre = fmaf(p.conv_w[ch * 4 + j], to_f(src[(size_t)tau * stride]), pre);
-        else if (hist)  // the carried input of token tau = s0 - 3 + m sits at m (oldest first)
-          pre = fmaf(p.conv_w[ch * 4 + j], to_f(hist[((size_t)n * Cc + ch) * 3 + (tau - s0 + 3)]), pre);
+      for (int u = 0; u < kU; ++u) {
+        const int idx = base + u * blockDim.x;
+        dst[u] = nullptr;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xin[u][j] = w[u][j] = 0.0f;
+        if (idx < nt * nch) {
+          const int tt = idx / nch, c = idx % nch;
+          const int t = t0 + tt;
+          const IO *src;
+          size_t stride;
+          int ch;
+          if (c < dk) {
+            src = xq + hq * dk + c; stride = (size_t)h_qk * dk; ch = hq * dk + c; dst[u] = sq + tt * dk + c;
+          } else if (c < 2 * dk) {
+            const int cc = c - dk;
+            src = xk + hq * dk + cc; stride = (size_t)h_qk * dk; ch = h_qk * dk + hq * dk + cc;
+            dst[u] = sk + tt * dk + cc;
+          } else {
+            const int cc = c - 2 * dk;
+            src = xv + h * dv + cc; stride = (size_t)h_v * dv; ch = 2 * h_qk * dk + h * dv + cc;
+            dst[u] = sv + tt * dv + cc;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int tau = t - 3 + j;
+            w[u][j] = p.conv_w[ch * 4 + j];
+            if (tau >= s0)
+              xin[u][j] = to_f(src[(size_t)tau * stride]);
+            else if (hist)  // the carried input of token tau = s0 - 3 + m sits at m (oldest first)
+              xin[u][j] = to_f(hist[((size_t)n * Cc + ch) * 3 + (tau - s0 + 3)]);
+          }
+        }
       }
-      *dst = silu_f(pre);
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (dst[u]) {
+          float pre = 0.0f;  // a tap with no input (before s0, no history) adds w * 0
+#pragma unroll
+          for (int j = 0; j < 4; ++j) pre = fmaf(w[u][j], xin[u][j], pre);
+          *dst[u] = silu_f(pre);
+        }
     }
     for (int tt = threadIdx.x; tt < nt; tt += blockDim.x) {
       const size_t t = (size_t)(t0 + tt);
@@ -136,10 +155,11 @@ __global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
           for (int r = 0; r < kRows; ++r) s = fmaf(H[r][c], kr[r], s);
           pc[c] = s;
         }
+        {  // the 8 column sums together: reduce-scatter (lane l: column l / 4), then broadcast
+          const float ps = reduce_scatter<kCW>(pc, lane);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-          for (int c = 0; c < kCW; ++c) pc[c] += __shfl_xor_sync(0xffffffffu, pc[c], o);
+          for (int c = 0; c < kCW; ++c) pc[c] = __shfl_sync(0xffffffffu, ps, 4 * c);
+        }
         float oc[kCW];
 #pragma unroll
         for (int c = 0; c < kCW; ++c) {
@@ -153,13 +173,8 @@ __global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
           }
           oc[c] = s;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-          for (int c = 0; c < kCW; ++c) oc[c] += __shfl_xor_sync(0xffffffffu, oc[c], o);
-#pragma unroll
-        for (int c = 0; c < kCW; ++c)
-          if (lane == c && j0 + c < dv) so[tt * dv + j0 + c] = oc[c] * scale;
+        const float os = reduce_scatter<kCW>(oc, lane);  // lane l: column l / 4
+        if ((lane & 3) == 0 && j0 + (lane >> 2) < dv) so[tt * dv + j0 + (lane >> 2)] = os * scale;
       }
     }
     __syncthreads();
