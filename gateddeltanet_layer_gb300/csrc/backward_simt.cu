@@ -36,8 +36,11 @@
 //   bwd_gate_kernel      per (token, value head): da, db, and the sums into
 //                        dA_log and ddt_bias.
 //
-// The slice layout follows the forward fp32 kernel: warp w owns columns
-// [8w, 8w+8) of the slice, lane l rows l, l+32, l+64, l+96.  Sums into one
+// The slice layout: warp w owns columns [kCW w, kCW w + kCW) of the slice
+// (two, so that a token step's chain of dependent work per warp is short:
+// 16 warps per slice of 32 columns measured 8.2 ms on the 4096-token
+// workload, against 9.4 with 4 columns per warp and 10.9 with 8), lane l rows
+// l, l+32, l+64, l+96.  Sums into one
 // value from several CTAs are atomic adds, so their rounding order is not
 // fixed from run to run: fp32 for the per-token q, k and gate gradients (a
 // few terms each), fp64 for the parameter gradients (conv_w, A_log, dt_bias,
@@ -50,10 +53,11 @@ namespace gdn {
 namespace {
 
 constexpr int kB = 32;        // tokens per block (checkpoint interval, prologue batch)
-constexpr int kCW = 8;        // state columns per warp
+constexpr int kCW = 2;        // state columns per warp
 constexpr int kRows = 4;      // rows per lane (d_k <= 128)
 constexpr int kSlot = kRows * kCW;  // state values per thread
-constexpr int kSliceWarps = 4, kSliceCols = kCW * kSliceWarps, kSliceThreads = 32 * kSliceWarps;
+constexpr int kSliceWarps = 16, kSliceCols = kCW * kSliceWarps, kSliceThreads = 32 * kSliceWarps;
+constexpr int kColLanes = 32 / kCW;  // a reduce-scatter over the warp leaves column c in lanes c kColLanes ..
 
 struct BwdWs {
   float *ckpt;   // [slots][h_v][slices][kSliceThreads][kSlot]: the state slice at each block start
@@ -173,21 +177,23 @@ __device__ __forceinline__ SliceCtx slice_ctx(const BwdParams &p, int slices) {
 __device__ __forceinline__ float *slice_ptr(float *base, size_t slot) {
   return base + (slot * kSliceThreads + threadIdx.x) * kSlot;
 }
+// (the thread's kSlot values row by row, as float4: kSlot is a multiple of 4)
+static_assert(kSlot % 4 == 0, "state slots in float4");
 __device__ __forceinline__ void store_state(float *dst, const float (&H)[kRows][kCW]) {
 #pragma unroll
-  for (int r = 0; r < kRows; ++r)
-#pragma unroll
-    for (int c = 0; c < kCW; c += 4)
-      *reinterpret_cast<float4 *>(dst + r * kCW + c) = make_float4(H[r][c], H[r][c + 1], H[r][c + 2], H[r][c + 3]);
+  for (int e = 0; e < kSlot; e += 4)
+    *reinterpret_cast<float4 *>(dst + e) = make_float4(H[e / kCW][e % kCW], H[(e + 1) / kCW][(e + 1) % kCW],
+                                                       H[(e + 2) / kCW][(e + 2) % kCW], H[(e + 3) / kCW][(e + 3) % kCW]);
 }
 __device__ __forceinline__ void load_state(const float *src, float (&H)[kRows][kCW]) {
 #pragma unroll
-  for (int r = 0; r < kRows; ++r)
-#pragma unroll
-    for (int c = 0; c < kCW; c += 4) {
-      const float4 f = *reinterpret_cast<const float4 *>(src + r * kCW + c);
-      H[r][c] = f.x; H[r][c + 1] = f.y; H[r][c + 2] = f.z; H[r][c + 3] = f.w;
-    }
+  for (int e = 0; e < kSlot; e += 4) {
+    const float4 f = *reinterpret_cast<const float4 *>(src + e);
+    H[e / kCW][e % kCW] = f.x;
+    H[(e + 1) / kCW][(e + 1) % kCW] = f.y;
+    H[(e + 2) / kCW][(e + 2) % kCW] = f.z;
+    H[(e + 3) / kCW][(e + 3) % kCW] = f.w;
+  }
 }
 // One forward step of the rule on this warp's columns (jw = its first column in the slice); o of the
 // token (scaled) to wo_row (the token's row of o, at the slice's first column) if given.
@@ -203,8 +209,8 @@ __device__ __forceinline__ void fwd_step(float (&H)[kRows][kCW], int tt, int dk,
     qr[r] = i < dk ? sq[tt * dk + i] : 0.0f;
   }
   const float al = salpha[tt], be = sbeta[tt];
-  // p = H^T k over the warp's columns: the 8 column sums together (a reduce-scatter leaves column
-  // l >> 2 in lane l, then each is broadcast), not one butterfly per column
+  // p = H^T k over the warp's columns: the column sums together (a reduce-scatter leaves column
+  // l / kColLanes in lane l, then each is broadcast), not one butterfly per column
   float s[kCW];
 #pragma unroll
   for (int c = 0; c < kCW; ++c) {
@@ -216,7 +222,7 @@ __device__ __forceinline__ void fwd_step(float (&H)[kRows][kCW], int tt, int dk,
   float o[kCW];
 #pragma unroll
   for (int c = 0; c < kCW; ++c) {
-    const float pc = __shfl_sync(0xffffffffu, ps, 4 * c);
+    const float pc = __shfl_sync(0xffffffffu, ps, kColLanes * c);
     const float u = be * (sv[tt * kSliceCols + jw + c] - al * pc);
     o[c] = 0.0f;
 #pragma unroll
@@ -226,8 +232,8 @@ __device__ __forceinline__ void fwd_step(float (&H)[kRows][kCW], int tt, int dk,
     }
   }
   if (wo_row) {
-    const float os = reduce_scatter<kCW>(o, lane);  // lane l: column l >> 2
-    if ((lane & 3) == 0 && jw + (lane >> 2) < jmax) wo_row[jw + (lane >> 2)] = os * scale;
+    const float os = reduce_scatter<kCW>(o, lane);  // lane l: column l / kColLanes
+    if (lane % kColLanes == 0 && jw + lane / kColLanes < jmax) wo_row[jw + lane / kColLanes] = os * scale;
   }
 }
 
@@ -334,17 +340,18 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
     __syncthreads();
     block_prologue(p, ws, cx.h, cx.hq, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta);
     {  // do of the slice's columns, float4 copies (all of them in flight)
-      constexpr int kPer = kB * kSliceCols / 4 / kSliceThreads;
+      constexpr int kQuads = kB * kSliceCols / 4, kPer = (kQuads + kSliceThreads - 1) / kSliceThreads;
       float4 dv4[kPer];
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int e = tid + kSliceThreads * u, tt = e / (kSliceCols / 4), jj = cx.j0 + 4 * (e % (kSliceCols / 4));
-        dv4[u] = (tt < nt && jj < dv)
+        dv4[u] = (e < kQuads && tt < nt && jj < dv)
                      ? *reinterpret_cast<const float4 *>(ws.wdo + ((size_t)(t0 + tt) * h_v + cx.h) * dv + jj)
                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) reinterpret_cast<float4 *>(sdo)[tid + kSliceThreads * u] = dv4[u];
+      for (int u = 0; u < kPer; ++u)
+        if (tid + kSliceThreads * u < kQuads) reinterpret_cast<float4 *>(sdo)[tid + kSliceThreads * u] = dv4[u];
     }
     load_state(slice_ptr(ws.ckpt, ((size_t)(cx.slot0 + b) * h_v + cx.h) * ws.slices + cx.sl), H);
     for (int tt = 0; tt < nt; ++tt) {  // the block's states again (before each token)
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
         dkp[r] = 0.0f;
       }
       float pc[kCW], du[kCW];
-      {  // the column sums, 8 at a time (reduce-scatter, then broadcast)
+      {  // the column sums, all of the warp's at once (reduce-scatter, then broadcast)
         float a[kCW], d[kCW];
 #pragma unroll
         for (int c = 0; c < kCW; ++c) {
@@ -410,8 +417,8 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
         const float as = reduce_scatter<kCW>(a, lane), ds = reduce_scatter<kCW>(d, lane);
 #pragma unroll
         for (int c = 0; c < kCW; ++c) {
-          pc[c] = __shfl_sync(0xffffffffu, as, 4 * c);
-          du[c] = __shfl_sync(0xffffffffu, ds, 4 * c);
+          pc[c] = __shfl_sync(0xffffffffu, as, kColLanes * c);
+          du[c] = __shfl_sync(0xffffffffu, ds, kColLanes * c);
         }
       }
       float s_db = 0.0f, s_dup = 0.0f, dp[kCW];
