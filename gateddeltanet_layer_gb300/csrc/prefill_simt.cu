@@ -3,7 +3,7 @@
 // Serves fp32 streams (where a bf16 tensor-core operand would not meet a 1e-4
 // tolerance) and every supported shape other than the d = 128 bf16 case.
 // One CTA per (sequence, value head) chain.  The state H = S^T (d_k x d_v)
-// lives in registers: warp w owns columns [8w, 8w+8) of H, lane l owns rows
+// lives in registers: warp w owns columns [4w, 4w+4) of H, lane l owns rows
 // l, l+32, l+64, l+96.  Columns of H evolve independently under the rule
 // (p_j = H[:,j] . k, u_j = beta (v_j - alpha p_j), H[:,j] <- alpha H[:,j] + k u_j),
 // so each warp advances its columns through the whole sequence without
@@ -17,11 +17,12 @@ namespace gdn {
 namespace {
 
 constexpr int kTB = 32;      // tokens per prologue/epilogue batch
-constexpr int kCW = 8;       // state columns per warp
+constexpr int kCW = 4;       // state columns per warp (d_v / 4 warps: up to 1024 threads)
+constexpr int kColLanes = 32 / kCW;  // a reduce-scatter over the warp leaves column c in lane c kColLanes
 constexpr int kRows = 4;     // rows per lane (d_k <= 128)
 
 template <typename IO>
-__global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillParams p) {
   const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
   const int n = blockIdx.x / h_v;
   const int h = blockIdx.x % h_v;
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
     __syncthreads();  // the previous batch's buffers are consumed
     // conv (width 4; before s0 the carried history, or zeros) + SiLU: kU elements per thread at a time,
     // their 4 kU input loads issued before any is used
-    constexpr int kU = 4;
+    constexpr int kU = 2;
     for (int base = threadIdx.x; base < nt * nch; base += kU * blockDim.x) {
       float xin[kU][4], w[kU][4];
       float *dst[kU];
@@ -155,10 +156,10 @@ __global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
           for (int r = 0; r < kRows; ++r) s = fmaf(H[r][c], kr[r], s);
           pc[c] = s;
         }
-        {  // the 8 column sums together: reduce-scatter (lane l: column l / 4), then broadcast
+        {  // the warp's column sums together: reduce-scatter (lane l: column l / kColLanes), then broadcast
           const float ps = reduce_scatter<kCW>(pc, lane);
 #pragma unroll
-          for (int c = 0; c < kCW; ++c) pc[c] = __shfl_sync(0xffffffffu, ps, 4 * c);
+          for (int c = 0; c < kCW; ++c) pc[c] = __shfl_sync(0xffffffffu, ps, kColLanes * c);
         }
         float oc[kCW];
 #pragma unroll
@@ -173,8 +174,8 @@ __global__ void __launch_bounds__(512) prefill_simt_kernel(PrefillParams p) {
           }
           oc[c] = s;
         }
-        const float os = reduce_scatter<kCW>(oc, lane);  // lane l: column l / 4
-        if ((lane & 3) == 0 && j0 + (lane >> 2) < dv) so[tt * dv + j0 + (lane >> 2)] = os * scale;
+        const float os = reduce_scatter<kCW>(oc, lane);  // lane l: column l / kColLanes
+        if (lane % kColLanes == 0 && j0 + lane / kColLanes < dv) so[tt * dv + j0 + lane / kColLanes] = os * scale;
       }
     }
     __syncthreads();
