@@ -214,6 +214,36 @@ def test_superposition_in_state_and_values():
     np.testing.assert_allclose(H_a, H_s + H_v, rtol=1e-12, atol=1e-14)
 
 
+def test_segments_joined_by_their_affine_state_maps():
+    """The reading behind the segment-parallel prefill: over a stretch of
+    tokens the state map is affine, H_out = M H_in + B, with B the run from a
+    zero state and M the run of the same tokens on the identity with v = 0 (the
+    linear part alone).  Joining segments by H_in(s + 1) = M_s H_in(s) + B_s and
+    rerunning each segment from its H_in gives the single run's outputs and
+    final state (segments of 10 tokens and a ragged 7-token one)."""
+    rng = _rng(12)
+    L, dk, dv = 37, 6, 5
+    q = _unit_rows(rng.standard_normal((L, dk)))
+    k = _unit_rows(rng.standard_normal((L, dk)))
+    g = -rng.uniform(0, 1, L)
+    beta = rng.uniform(0, 1, L)
+    v = rng.standard_normal((L, dv))
+    H0 = rng.standard_normal((dk, dv))
+    o_full, H_full = ref.recurrence(q, k, v, g, beta, H0)
+    cuts = [0, 10, 20, 30, L]
+    H_in, outs = H0, []
+    for s0, s1 in zip(cuts[:-1], cuts[1:]):
+        sl = slice(s0, s1)
+        _, B = ref.recurrence(q[sl], k[sl], v[sl], g[sl], beta[sl], None)
+        _, M = ref.recurrence(q[sl], k[sl], np.zeros((s1 - s0, dk)), g[sl], beta[sl], np.eye(dk))
+        o_seg, H_seg = ref.recurrence(q[sl], k[sl], v[sl], g[sl], beta[sl], H_in)
+        np.testing.assert_allclose(H_seg, M @ H_in + B, rtol=1e-12, atol=1e-13)
+        outs.append(o_seg)
+        H_in = M @ H_in + B
+    np.testing.assert_allclose(np.vstack(outs), o_full, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(H_in, H_full, rtol=1e-12, atol=1e-13)
+
+
 @pytest.mark.parametrize("chunk", [1, 7, 16, 64])
 @pytest.mark.parametrize("memory", ["config", "long"])
 def test_chunked_equals_token_form(chunk, memory):
