@@ -351,7 +351,11 @@ __device__ __forceinline__ void l2norm_rows(float (&y)[8][4], int lane) {
   }
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const PrefillParams p, const Ws ws) {
+// upmap: the U' images as [slot][256 rows][32] fp16 (slot = chunk x h_v + value head), 64-byte swizzle:
+// the staging's 16-byte chunk c of row m sits at c ^ ((m >> 1) & 3), the tensor memory accelerator's
+// 64-byte pattern, so one 3-D store writes a head's 16 KB.
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    chunk_prep_kernel(const PrefillParams p, const Ws ws, const __grid_constant__ CUtensorMap upmap) {
   // grid (chunk slots, q/k heads x value-head groups): a CTA takes up to kMaxRep of the value heads
   // of its q/k head (all of them unless h_v / h_qk > kMaxRep, where each group redoes the q/k part)
   const int ngrp = (p.h_v / p.h_qk + kMaxRep - 1) / kMaxRep;
@@ -851,27 +855,30 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
             tc::st_chunk_f16(stu + (2 * half + c32) * 4096 + m * 64 + ((cc ^ ((m >> 1) & 3)) << 4), u + 8 * cc);
         }
       }
+      tc::fence_async_smem();  // the stagings are read by the tensor memory accelerator
       tc::fence_before_sync();
       __syncthreads();  // staged, and the accumulator is read: the next product may overwrite it
       tc::fence_after_sync();
       if (hh + 1 < nh) issue_wu(hh + 1);
-      uint8_t *v_slot = v_slot_of(grp + hh);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int q = tid + kPrepThreads * k;  // 16-byte chunk q of 1024
-        // W: staged bytes [0, 8K) -> image slab 0 rows 64-127, [8K, 16K) -> slab 1 rows 64-127 (compact: the
-        // two 64-row slabs of the W image, the same bytes in order)
-        *reinterpret_cast<uint4 *>(v_slot + (compact ? kCW + 16 * q : kVWQ + 8192 + 16 * q + (q >= 512 ? 8192 : 0))) =
-            *reinterpret_cast<const uint4 *>(stw + 16 * q);
-        // U': image chunk q = (slice q / 256, row m, chunk q % 4)
-        const int m = (q >> 2) & 63;
-        *reinterpret_cast<uint4 *>(v_slot + (compact ? kCUp : kVUp) + 16 * q) =
-            *reinterpret_cast<const uint4 *>(stu + (q >> 8) * 4096 + m * 64 + (((q & 3) ^ ((m >> 1) & 3)) << 4));
+      if (tid == 0) {  // W: the staged bytes are the image's, in order; U': one swizzled 3-D store
+        uint8_t *v_slot = v_slot_of(grp + hh);
+        if (compact) {
+          tc::bulk_s2g(v_slot + kCW, stw, 16384);
+        } else {  // the W rows 64-127 of the two slabs of [Q^; W]
+          tc::bulk_s2g(v_slot + kVWQ + 8192, stw, 8192);
+          tc::bulk_s2g(v_slot + kVWQ + 24576, stw + 8192, 8192);
+        }
+        tc::tma_store_3d(&upmap, 0, 0, g * h_v + hq * rep + vbase + grp + hh, stu);
+        tc::bulk_commit();
       }
     }
-    if (grp + 2 < nrep) __syncthreads();  // the stagings are read before the next pair's tiles go there
+    if (grp + 2 < nrep) {  // the stagings are read before the next pair's tiles go there
+      if (tid == 0) tc::bulk_wait_read();
+      __syncthreads();
+    }
   }
   if (failed && tid == 0) set_status(p.status, kDevTimeout);
+  if (tid == 0) tc::bulk_wait_all();  // the image stores are done before the CTA's shared memory goes
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
@@ -1970,6 +1977,20 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The U' images of the chunk prep as a 3-D fp16 tensor [slots][256 rows][32] (rows of 64 bytes; slot
+// stride `slot_bytes`), boxes of one slot, 64-byte swizzle.
+bool make_up_map(CUtensorMap *m, const void *base, uint64_t slots, uint64_t slot_bytes) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  cuuint64_t dims[3] = {32, 256, slots};
+  cuuint64_t strides[2] = {64, slot_bytes};
+  cuuint32_t box[3] = {32, 256, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t prefill_tc_workspace_bytes(int T, int N, int h_qk, int h_v) { return WsLayout(T, N, h_qk, h_v).total; }
@@ -2090,8 +2111,13 @@ cudaError_t launch_table_and_prep(const PrefillParams &p, const Ws &ws, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    CUtensorMap upmap;
+    std::memset(&upmap, 0, sizeof(upmap));
+    if (!make_up_map(&upmap, ws.vs + (ws.compact ? kCUp : kVUp), (uint64_t)ws.max_chunks * p.h_v,
+                     ws.compact ? kCSlot : kVSlot))
+      return cudaErrorInvalidValue;
     trace_begin(s, GDN_K_CHUNK_PREP);
-    e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel, p, ws);
+    e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel, p, ws, upmap);
     trace_end(s);
   }
   return e;

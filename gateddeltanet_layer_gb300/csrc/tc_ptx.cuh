@@ -193,6 +193,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, in
 // 2-D tiled TMA store of a shared-memory box to (x = column, y = row) of a
 // tensor map, in this thread's current bulk group; parts of the box outside
 // the tensor are not written.  The coordinates must not be negative.
+// 3-D tiled TMA store of a shared-memory box to (x, y, z) of a tensor map, in
+// this thread's current bulk group; the same rules as tma_store_2d.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int x, int y, int z, const void *src_smem) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z), "r"(smem_u32(src_smem))
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, const void *src_smem) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
