@@ -490,13 +490,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       *reinterpret_cast<uint2 *>(sm + P_KQ + off) = hi;
       *reinterpret_cast<uint2 *>(sm + P_KQL + off) = lo;
     }
-    if (compact) {  // Q, once per q/k head: [64 rows] SW128 slabs
-      if (qk_images) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-          *reinterpret_cast<uint2 *>(q_slot + kQQ + tc::sw128_offset(64, r0 + r, c0)) =
-              pack4_f16(y[r][0], y[r][1], y[r][2], y[r][3]);
-      }
+    if (compact) {
+      // Q, once per q/k head: its two 64-row SW128 slabs are rows 64-127 of the hi tile's slabs (the same
+      // fp16 values, the same swizzle), copied below
     } else {
       for (int vv = 0; vv < nrep; ++vv) {  // Q^ = diag(gamma) Q: rows 0-63 of the [Q^; W] image
         const float *gam = sG + vv * 256 + 64;
@@ -538,6 +534,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     mma_chain(tmem + COL_P1, sbase + P_KQ, 128, 0, sbase + P_KQL, 128, 0, 8, kIdN64, true);
     mma_chain(tmem + COL_P1, sbase + P_KQL, 128, 0, sbase + P_KQ, 128, 0, 8, kIdN64, true);
     tc::mma_commit(bar);
+    if (compact && qk_images) {  // the per-q/k-head images: Q (from the hi tile) and the K^T tile
+      tc::bulk_s2g(q_slot + kQQ, sm + P_KQ + 8192, 8192);
+      tc::bulk_s2g(q_slot + kQQ + 8192, sm + P_KQ + 16384 + 8192, 8192);
+      tc::bulk_s2g(q_slot + kQKt, sm + P_KT, 16384);
+      tc::bulk_commit();
+    }
   }
 
   // ---------------- the value heads, two at a time
@@ -568,6 +570,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         for (int r = 0; r < 8; ++r) col[r] = y[r][c];
         tc::st_chunk_f16(sm + P_VT0 + tc::sw128_chunk(128, c0 + c, warp), col);
       }
+      if (grp == 0 && tid == 0 && compact && qk_images) tc::bulk_wait_read();  // before the tiles are reused
       if (grp == 0 && wait_all(bar, phase)) { failed = true; break; }  // K K^T and Q K^T are done
       if (nh > 1) {
         conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + vbase + grp + 1) * kD + c0, Lc, r0, y);
@@ -619,19 +622,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)  // staged in the image's layout (the inverse's scratch is free)
           tc::st_chunk_f16(sm + P_XF + tc::sw128_chunk(64, r, 4 * gh + cc), v + 8 * cc);
-        // warps 2 and 6 hold rows 0-31 of -A_Q, warps 3 and 7 rows 32-63: each pair stores its 4 KB of the
-        // image in order (512 contiguous bytes per warp store), synchronised among its own 64 threads
+        // warps 2 and 6 hold rows 0-31 of -A_Q, warps 3 and 7 rows 32-63: each pair's 4 KB of the image,
+        // contiguous, goes by one bulk copy once the pair (synchronised among its own 64 threads) has staged it
+        tc::fence_async_smem();
         const int pr = warp & 1, t = 32 * (warp >> 2) + lane;
         tc::named_barrier(1 + pr, 64);
-        uint8_t *dst = v_slot_of(grp + hh) + (compact ? kCAq : kVAq);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int q = 256 * pr + t + 64 * k;
-          *reinterpret_cast<uint4 *>(dst + 16 * q) = *reinterpret_cast<const uint4 *>(sm + P_XF + 16 * q);
+        if (t == 0) {
+          tc::bulk_s2g(v_slot_of(grp + hh) + (compact ? kCAq : kVAq) + 4096 * pr, sm + P_XF + 4096 * pr, 4096);
+          tc::bulk_commit();
         }
-        if (hh + 1 < nh) tc::named_barrier(1 + pr, 64);  // read before the next head's staging
+        if (hh + 1 < nh) {  // read before the next head's staging
+          if (t == 0) tc::bulk_wait_read();
+          tc::named_barrier(1 + pr, 64);
+        }
       }
     }
+    if (lr >= 64 && 32 * (warp >> 2) + lane == 0) tc::bulk_wait_read();  // before the inverse's scratch goes there
     tc::fence_before_sync();
     __syncthreads();
 
@@ -641,15 +647,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       float x[16];
       const int hh = tid >> 6, bb = (tid >> 4) & 3, s = tid & 15;
       const bool act = hh < nh;
-      if (tid >= 128 && compact) {  // meanwhile: the K^T tile to its image, once per q/k head
-        if (grp == 0 && qk_images) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int q = tid - 128 + 128 * k;
-            *reinterpret_cast<uint4 *>(q_slot + kQKt + 16 * q) = *reinterpret_cast<const uint4 *>(sm + P_KT + 16 * q);
-          }
-        }
-      } else if (tid >= 128) {  // meanwhile: the K~^T = (diag(e^(G_C - G)) K)^T images of the pair, from the
+      if (tid >= 128 && !compact) {  // meanwhile: the K~^T = (diag(e^(G_C - G)) K)^T images of the pair, from the
                                 // K^T tile (the image has its SW128 layout), 16-byte chunks in order
         for (int h2 = 0; h2 < nh; ++h2) {
           const float *dec = sGall + (grp + h2) * 256 + 192;
@@ -878,7 +876,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
   }
   if (failed && tid == 0) set_status(p.status, kDevTimeout);
-  if (tid == 0) tc::bulk_wait_all();  // the image stores are done before the CTA's shared memory goes
+  tc::bulk_wait_all();  // this thread's image stores are done before the CTA's shared memory goes
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
