@@ -281,14 +281,18 @@ constexpr uint32_t kIdN256 = tc::idesc_f16(128, 256);
 // pitch `stride` elements) as packed bf16; rows past the chunk's end are 0, and
 // so are the (at most three) rows before the sequence start unless `hist`
 // points at the carried conv history of the 4 channels ([channel][3] bf16,
-// oldest first: token s0 - 3 + m at m).
+// oldest first: token s0 - 3 + m at m).  FULL: a whole chunk starting at
+// least 3 tokens into its sequence (every row is a plain load).
+template <bool FULL>
 __device__ __forceinline__ void load_rows(const __nv_bfloat16 *x, size_t stride, int t0, int s0, int Lc, int r0,
                                           const __nv_bfloat16 *hist, uint2 (&xr)[11]) {
 #pragma unroll
   for (int rr = 0; rr < 11; ++rr) {
     const int row = r0 - 3 + rr;
     const int t = t0 + row;
-    if (t >= s0) {
+    if (FULL) {
+      xr[rr] = *reinterpret_cast<const uint2 *>(x + (size_t)t * stride);
+    } else if (t >= s0) {
       xr[rr] = row < Lc ? *reinterpret_cast<const uint2 *>(x + (size_t)t * stride) : make_uint2(0u, 0u);
     } else if (hist) {  // t >= t0 - 3 >= s0 - 3
       const uint16_t *h = reinterpret_cast<const uint16_t *>(hist) + (t - s0 + 3);
@@ -299,7 +303,8 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16 *x, size_t stride,
   }
 }
 // conv(4) + SiLU of the rows of load_rows, channels from conv_w row `ch`;
-// channels in pairs, one packed fp32 instruction per pair.
+// channels in pairs, one packed fp32 instruction per pair.  FULL: every row is in the chunk.
+template <bool FULL>
 __device__ __forceinline__ void conv_silu(const uint2 (&xr)[11], const float *conv_w, int ch, int Lc, int r0,
                                           float (&y)[8][4]) {
   float4 w[4];
@@ -319,7 +324,7 @@ __device__ __forceinline__ void conv_silu(const uint2 (&xr)[11], const float *co
   };
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    const bool ok = r0 + r < Lc;
+    const bool ok = FULL || r0 + r < Lc;
 #pragma unroll
     for (int pr = 0; pr < 2; ++pr) {
       float2 a = tc::mul2(wp[pr][0], pair(r, pr));
@@ -380,6 +385,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
   const int4 info = ws.chunk_info[g];
   const int t0 = info.y, s0 = info.z, Lc = info.w;
+  const bool full = Lc == kC && t0 - 3 >= s0;  // a whole chunk with no sequence start in its conv window
   // conv history of channel ch for this thread's 4 channels (only the first chunk of a sequence reads it)
   const size_t conv_ch = 2 * (size_t)h_qk * kD + (size_t)h_v * kD;
   const __nv_bfloat16 *hist0 =
@@ -474,10 +480,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     uint2 xrk[11];
     {  // both heads' rows in flight at once
       uint2 xrq[11];
-      load_rows(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(hq * kD + c0), xrq);
-      load_rows(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(h_qk * kD + hq * kD + c0), xrk);
+      if (full) {
+        load_rows<true>(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, nullptr, xrq);
+        load_rows<true>(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, nullptr, xrk);
+      } else {
+        load_rows<false>(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(hq * kD + c0), xrq);
+        load_rows<false>(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(h_qk * kD + hq * kD + c0), xrk);
+      }
       if (nrep > 1) prefetch_v(1);
-      conv_silu(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
+      if (full) conv_silu<true>(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
+      else conv_silu<false>(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
     }
     l2norm_rows(y, lane);
 #pragma unroll
@@ -506,7 +518,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
       }
     }
-    conv_silu(xrk, p.conv_w, h_qk * kD + hq * kD + c0, Lc, r0, kreg);
+    if (full) conv_silu<true>(xrk, p.conv_w, h_qk * kD + hq * kD + c0, Lc, r0, kreg);
+    else conv_silu<false>(xrk, p.conv_w, h_qk * kD + hq * kD + c0, Lc, r0, kreg);
     l2norm_rows(kreg, lane);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -552,13 +565,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     {
       uint2 xr[11];
       float y[8][4];
-      load_rows(xv + (size_t)(hq * rep + vbase + grp) * kD + c0, v_stride, t0, s0, Lc, r0,
-                hist(2 * h_qk * kD + (hq * rep + vbase + grp) * kD + c0), xr);
-      conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + vbase + grp) * kD + c0, Lc, r0, y);
+      const int vch0 = 2 * h_qk * kD + (hq * rep + vbase + grp) * kD + c0;  // conv channel of the first head
+      if (full) {
+        load_rows<true>(xv + (size_t)(hq * rep + vbase + grp) * kD + c0, v_stride, t0, s0, Lc, r0, nullptr, xr);
+        conv_silu<true>(xr, p.conv_w, vch0, Lc, r0, y);
+      } else {
+        load_rows<false>(xv + (size_t)(hq * rep + vbase + grp) * kD + c0, v_stride, t0, s0, Lc, r0, hist(vch0), xr);
+        conv_silu<false>(xr, p.conv_w, vch0, Lc, r0, y);
+      }
       // the second head's rows in flight over the first head's stores and the wait below
-      if (nh > 1)
-        load_rows(xv + (size_t)(hq * rep + vbase + grp + 1) * kD + c0, v_stride, t0, s0, Lc, r0,
-                  hist(2 * h_qk * kD + (hq * rep + vbase + grp + 1) * kD + c0), xr);
+      if (nh > 1) {
+        if (full)
+          load_rows<true>(xv + (size_t)(hq * rep + vbase + grp + 1) * kD + c0, v_stride, t0, s0, Lc, r0, nullptr, xr);
+        else
+          load_rows<false>(xv + (size_t)(hq * rep + vbase + grp + 1) * kD + c0, v_stride, t0, s0, Lc, r0,
+                           hist(vch0 + kD), xr);
+      }
       if (grp + 2 < nrep) {
         prefetch_v(grp + 2);
         if (grp + 3 < nrep) prefetch_v(grp + 3);
@@ -573,7 +595,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       if (grp == 0 && tid == 0 && compact && qk_images) tc::bulk_wait_read();  // before the tiles are reused
       if (grp == 0 && wait_all(bar, phase)) { failed = true; break; }  // K K^T and Q K^T are done
       if (nh > 1) {
-        conv_silu(xr, p.conv_w, 2 * h_qk * kD + (hq * rep + vbase + grp + 1) * kD + c0, Lc, r0, y);
+        if (full) conv_silu<true>(xr, p.conv_w, vch0 + kD, Lc, r0, y);
+        else conv_silu<false>(xr, p.conv_w, vch0 + kD, Lc, r0, y);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float col[8];
