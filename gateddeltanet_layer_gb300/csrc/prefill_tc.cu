@@ -436,6 +436,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   };
   prefetch_v(0);
 
+  // the q and k rows of the conv: loads in flight over the gates below
+  uint2 xrq[11], xrk[11];
+  if (full) {
+    load_rows<true>(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, nullptr, xrq);
+    load_rows<true>(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, nullptr, xrk);
+  } else {
+    load_rows<false>(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(hq * kD + c0), xrq);
+    load_rows<false>(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(h_qk * kD + hq * kD + c0), xrk);
+  }
+
   // ---------------- gates of every value head and their running sums inside the chunk
   for (int v0 = 0; v0 < nrep; v0 += 4) {
     const int vv = v0 + (tid >> 6), r = tid & 63;
@@ -477,16 +487,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   // ---------------- q and k: conv + SiLU + L2 norm -> [K; Q] hi / lo tiles, K^T tile, Q^ images
   {
     float y[8][4], kreg[8][4];
-    uint2 xrk[11];
-    {  // both heads' rows in flight at once
-      uint2 xrq[11];
-      if (full) {
-        load_rows<true>(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, nullptr, xrq);
-        load_rows<true>(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, nullptr, xrk);
-      } else {
-        load_rows<false>(xq + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(hq * kD + c0), xrq);
-        load_rows<false>(xk + hq * kD + c0, qk_stride, t0, s0, Lc, r0, hist(h_qk * kD + hq * kD + c0), xrk);
-      }
+    {
       if (nrep > 1) prefetch_v(1);
       if (full) conv_silu<true>(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
       else conv_silu<false>(xrq, p.conv_w, hq * kD + c0, Lc, r0, y);
