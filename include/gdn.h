@@ -41,6 +41,10 @@
  *    kernel.  Anything else returns GDN_ERR_UNSUPPORTED.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
  *    asynchronous: they enqueue kernels and return without synchronising.
+ *    With a caller-owned workspace (and the trace off) a prefill or decode
+ *    call can be captured in a CUDA graph and replayed, the graph reading
+ *    whatever values the captured buffers hold at replay time; calls on
+ *    different streams with their own workspaces may run concurrently.
  *  - Errors.  Invalid arguments (NULL required pointer, non-positive size,
  *    misalignment, h_v not a multiple of h_qk, short workspace) return a status
  *    before anything is launched.  A failed launch returns GDN_ERR_CUDA.
