@@ -505,7 +505,7 @@ def run_ours(args):
         r = time_backward(synth.SINGLE_4K, max(3, args.steps // 4), args.warmup, dev, flush)
         m, = max_over_ranks([statistics.mean(r["ms"])], dev)
         extra["prefill_backward_T4096"] = {"tokens_per_s": synth.SINGLE_4K.T / (m * 1e-3), "ms": m,
-                                           "kernels": "bwd_inputs_kernel, bwd_fwd_kernel, bwd_norm_kernel, bwd_rev_kernel, bwd_prologue_kernel, bwd_gate_kernel, bwd_param_kernel",
+                                           "kernels": "token_inputs_kernel, bwd_fwd_kernel, bwd_norm_kernel, bwd_rev_kernel, bwd_prologue_kernel, bwd_gate_kernel, bwd_param_kernel",
                                            "kernels_ms_per_step": r["kernels"]}
         dc = synth.DECODE_256
         r = time_decode(dc, args.steps, args.warmup, dev, flush)

@@ -48,6 +48,7 @@
 #include "gdn_common.cuh"
 #include "../../include/gdn_trace.h"
 #include "gdn_internal.h"
+#include "token_inputs.cuh"
 
 namespace gdn {
 namespace {
@@ -107,7 +108,7 @@ struct BwdLayout {
 
 // The block's inputs into shared memory: q^, k^ and the slice's columns
 // [j0, j0 + kSliceCols) of silu(conv(v)) (zeros past d_v), alpha and beta, for
-// tokens [t0, t0 + nt), from the arrays bwd_inputs_kernel wrote.
+// tokens [t0, t0 + nt), from the arrays token_inputs_kernel wrote.
 __device__ void block_prologue(const BwdParams &p, const BwdWs &ws, int h, int hq, int t0, int nt, int j0,
                                float *sq, float *sk, float *sv, float *salpha, float *sbeta) {
   const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
@@ -493,74 +494,6 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
   }
 }
 
-// Sequence [s0, s1) of token t (binary search over cu_seqlens).
-__device__ __forceinline__ int2 seq_of(const int32_t *cu, int N, int t) {
-  int lo = 0, hi = N - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  return make_int2(cu[lo], cu[lo + 1]);
-}
-
-// The forward's per-token inputs, once for every chain and column slice that reads them: one warp per
-// (token, row) with row y < h_qk the q head y, then the k heads, then the value heads; lane l takes
-// channels l, l + 32, ...  conv(4) over the sequence's own tokens, SiLU, the L2 norm of q and k; the
-// value-head rows also write alpha = e^g and beta.
-template <typename IO>
-__global__ void __launch_bounds__(256) bwd_inputs_kernel(const BwdParams p, const BwdWs ws) {
-  const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v, rows = 2 * h_qk + h_v;
-  const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= (size_t)p.T * rows) return;
-  const int t = (int)(row / rows), y = (int)(row % rows);
-  const int s0 = seq_of(p.cu_seqlens, p.N, t).x;
-  const IO *src;
-  size_t stride;
-  int cb, D;
-  float *dst;
-  if (y < 2 * h_qk) {
-    const int hq = y < h_qk ? y : y - h_qk;
-    src = static_cast<const IO *>(y < h_qk ? p.q : p.k) + hq * dk;
-    stride = (size_t)h_qk * dk;
-    cb = y * dk;  // conv channels: [q heads | k heads | v heads]
-    D = dk;
-    dst = (y < h_qk ? ws.xq : ws.xk) + ((size_t)t * h_qk + hq) * dk;
-  } else {
-    const int hv = y - 2 * h_qk;
-    src = static_cast<const IO *>(p.v) + hv * dv;
-    stride = (size_t)h_v * dv;
-    cb = 2 * h_qk * dk + hv * dv;
-    D = dv;
-    dst = ws.xv + ((size_t)t * h_v + hv) * dv;
-    if (lane == 0) {
-      const size_t gi = (size_t)t * h_v + hv;
-      ws.xal[gi] = expf(gate_g(to_f(static_cast<const IO *>(p.a)[gi]), expf(p.A_log[hv]), p.dt_bias[hv]));
-      ws.xbe[gi] = sigmoid_f(to_f(static_cast<const IO *>(p.b)[gi]));
-    }
-  }
-  float x[4];
-  float ss = 0.0f;
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int c = lane + 32 * r;
-    float pre = 0.0f;
-    if (c < D) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int tau = t - 3 + j;
-        if (tau >= s0) pre = fmaf(p.conv_w[(size_t)(cb + c) * 4 + j], to_f(src[(size_t)tau * stride + c]), pre);
-      }
-    }
-    x[r] = c < D ? silu_f(pre) : 0.0f;
-    ss = fmaf(x[r], x[r], ss);
-  }
-  const float inv = y < 2 * h_qk ? rsqrtf(warp_sum(ss) + kEpsL2) : 1.0f;
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-    if (lane + 32 * r < D) dst[lane + 32 * r] = x[r] * inv;
-}
-
 __device__ __forceinline__ float block_sum128(float v, float *red) {
   v = warp_sum(v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -606,13 +539,13 @@ __global__ void __launch_bounds__(128) bwd_prologue_kernel(const BwdParams p, co
   for (int tt = 0; tt < kTile + 3; ++tt) {
     const int t = t0 + tt;
     if (t >= p.T) break;  // uniform over the CTA
-    const int2 sq = seq_of(p.cu_seqlens, p.N, t);
+    const SeqOf sq = seq_of(p.cu_seqlens, p.N, t);
     float pre = 0.0f;
     if (act)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int tau = t - 3 + j;
-        if (tau >= sq.x) pre = fmaf(w[j], to_f(src[(size_t)tau * stride + c]), pre);
+        if (tau >= sq.s0) pre = fmaf(w[j], to_f(src[(size_t)tau * stride + c]), pre);
       }
     const float s = sigmoid_f(pre), xh = pre * s, dsilu = s * (1.0f + pre * (1.0f - s));
     float dxh;
@@ -637,14 +570,14 @@ __global__ void __launch_bounds__(128) bwd_prologue_kernel(const BwdParams p, co
   for (int tt = 0; tt < kTile; ++tt) {
     const int t = t0 + tt;
     if (t >= Tc) break;
-    const int2 sq = seq_of(p.cu_seqlens, p.N, t);
+    const SeqOf sq = seq_of(p.cu_seqlens, p.N, t);
     float acc = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int tp = t + 3 - j;  // the output token that reads input t through tap j
-      if (tp < sq.y) acc = fmaf(sdp[tt + 3 - j][c], w[j], acc);
+      if (tp < sq.s1) acc = fmaf(sdp[tt + 3 - j][c], w[j], acc);
       const int tau = t - 3 + j;  // the input tap j of output t reads
-      if (tau >= sq.x) dw[j] = fmaf(sdp[tt][c], to_f(src[(size_t)tau * stride + c]), dw[j]);
+      if (tau >= sq.s0) dw[j] = fmaf(sdp[tt][c], to_f(src[(size_t)tau * stride + c]), dw[j]);
     }
     dx[(size_t)t * stride + c] = acc;
   }
@@ -716,7 +649,14 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
   const unsigned rows = (unsigned)(((size_t)p.T * p.h_v + 7) / 8);
   const dim3 pgrid((unsigned)((p.T + kTile - 1) / kTile), (unsigned)(2 * p.h_qk + p.h_v));
   const unsigned ggrid = (unsigned)(((size_t)p.T * p.h_v + 255) / 256);
-  const unsigned irows = (unsigned)(((size_t)p.T * (2 * p.h_qk + p.h_v) + 7) / 8);
+  const unsigned irows =
+      (unsigned)(((size_t)p.T * (2 * p.h_qk + p.h_v) + kTokenRowsPerCta - 1) / kTokenRowsPerCta);
+  TokenInputs ti{};
+  ti.q = p.q; ti.k = p.k; ti.v = p.v; ti.a = p.a; ti.b = p.b;
+  ti.conv_w = p.conv_w; ti.A_log = p.A_log; ti.dt_bias = p.dt_bias; ti.cu_seqlens = p.cu_seqlens;
+  ti.init_conv = nullptr;  // the backward's forward starts every sequence from a zero conv history
+  ti.T = p.T; ti.N = p.N; ti.h_qk = p.h_qk; ti.h_v = p.h_v; ti.d_k = p.d_k; ti.d_v = p.d_v;
+  ti.xq = ws.xq; ti.xk = ws.xk; ti.xv = ws.xv; ti.xal = ws.xal; ti.xbe = ws.xbe;
   auto run = [&](auto in_k, auto fwd_k, auto norm_k, auto rev_k, auto pro_k, auto gate_k) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(fwd_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -724,7 +664,7 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
       return err;
     if (ctas) {
       trace_begin(s, GDN_K_BWD_CHAIN);
-      if (p.T > 0) in_k<<<irows, 256, 0, s>>>(p, ws);
+      if (p.T > 0) in_k<<<irows, 32 * kTokenRowsPerCta, 0, s>>>(ti);
       fwd_k<<<ctas, kSliceThreads, smem, s>>>(p, ws);
       if (p.T > 0) norm_k<<<rows, 256, 0, s>>>(p, ws);
       rev_k<<<ctas, kSliceThreads, smem, s>>>(p, ws);
@@ -742,9 +682,9 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
     return cudaGetLastError();
   };
   if (bf16)
-    return run(bwd_inputs_kernel<__nv_bfloat16>, bwd_fwd_kernel<__nv_bfloat16>, bwd_norm_kernel<__nv_bfloat16>,
+    return run(token_inputs_kernel<__nv_bfloat16>, bwd_fwd_kernel<__nv_bfloat16>, bwd_norm_kernel<__nv_bfloat16>,
                bwd_rev_kernel<__nv_bfloat16>, bwd_prologue_kernel<__nv_bfloat16>, bwd_gate_kernel<__nv_bfloat16>);
-  return run(bwd_inputs_kernel<float>, bwd_fwd_kernel<float>, bwd_norm_kernel<float>, bwd_rev_kernel<float>,
+  return run(token_inputs_kernel<float>, bwd_fwd_kernel<float>, bwd_norm_kernel<float>, bwd_rev_kernel<float>,
              bwd_prologue_kernel<float>, bwd_gate_kernel<float>);
 }
 

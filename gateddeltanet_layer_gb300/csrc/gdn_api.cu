@@ -39,6 +39,8 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *d) {
   size_t bytes = kStatusBytes;
   if (use_tensor_core_prefill(d))
     bytes += gdn::prefill_tc_workspace_bytes(d->num_tokens, d->num_seqs, d->h_qk, d->h_v);
+  else
+    bytes += gdn::prefill_simt_workspace_bytes(d->num_tokens, d->h_qk, d->h_v, d->d_k, d->d_v);
   return bytes;
 }
 

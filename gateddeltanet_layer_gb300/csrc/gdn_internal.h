@@ -61,6 +61,8 @@ size_t prefill_backward_workspace_bytes(int T, int N, int h_qk, int h_v, int d_k
 
 // Token-sequential fp32 prefill (any supported shape, bf16 or fp32 streams).
 cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t s);
+// Its workspace (after the status block): the per-token inputs (fp32), computed once.
+size_t prefill_simt_workspace_bytes(int T, int h_qk, int h_v, int d_k, int d_v);
 // Chunked tensor-core prefill (bf16 streams, d_k = d_v = 128).  Its chunk
 // preparation takes up to kTcMaxRep value heads of a q/k head per CTA (more
 // value heads per q/k head: several CTAs, each redoing the q/k part).

@@ -12,6 +12,7 @@
 #include "gdn_common.cuh"
 #include "../../include/gdn_trace.h"
 #include "gdn_internal.h"
+#include "token_inputs.cuh"
 
 namespace gdn {
 namespace {
@@ -22,7 +23,7 @@ constexpr int kColLanes = 32 / kCW;  // a reduce-scatter over the warp leaves co
 constexpr int kRows = 4;     // rows per lane (d_k <= 128)
 
 template <typename IO>
-__global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillParams p, const TokenInputs ti) {
   const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
   const int n = blockIdx.x / h_v;
   const int h = blockIdx.x % h_v;
@@ -36,15 +37,10 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
     return;
   }
 
-  const IO *__restrict__ xq = static_cast<const IO *>(p.q);
-  const IO *__restrict__ xk = static_cast<const IO *>(p.k);
-  const IO *__restrict__ xv = static_cast<const IO *>(p.v);
-  const IO *__restrict__ xa = static_cast<const IO *>(p.a);
-  const IO *__restrict__ xb = static_cast<const IO *>(p.b);
   const IO *__restrict__ xz = static_cast<const IO *>(p.z);
   IO *__restrict__ out = static_cast<IO *>(p.out);
 
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];
   float *sq = smem;               // [kTB][dk]
   float *sk = sq + kTB * dk;      // [kTB][dk]
   float *sv = sk + kTB * dk;      // [kTB][dv]
@@ -63,78 +59,50 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
       H[r][c] = (p.init_state && i < dk && j < dv) ? p.init_state[state_off + (size_t)i * dv + j] : 0.0f;
     }
 
-  const float A_exp = expf(p.A_log[h]);
-  const float dtb = p.dt_bias[h];
   const float scale = rsqrtf((float)dk);
-  const int nch = 2 * dk + dv;
-  const int Cc = 2 * h_qk * dk + h_v * dv;
-  const IO *__restrict__ hist = static_cast<const IO *>(p.init_conv);  // conv history, or null (zeros)
 
   for (int t0 = s0; t0 < s1; t0 += kTB) {
     const int nt = min(kTB, s1 - t0);
     __syncthreads();  // the previous batch's buffers are consumed
-    // conv (width 4; before s0 the carried history, or zeros) + SiLU: kU elements per thread at a time,
-    // their 4 kU input loads issued before any is used
-    constexpr int kU = 2;
-    for (int base = threadIdx.x; base < nt * nch; base += kU * blockDim.x) {
-      float xin[kU][4], w[kU][4];
-      float *dst[kU];
+    // the batch's inputs (q^, k^, silu(conv(v)), alpha, beta) from the token-inputs pass: float4 copies
+    // (head dims are multiples of 16), kU of them in flight per thread
+    {
+      const int nq = dk / 4, nv = dv / 4, per_tok = 2 * nq + nv, total = nt * per_tok;
+      const float4 *gq = reinterpret_cast<const float4 *>(ti.xq), *gk = reinterpret_cast<const float4 *>(ti.xk);
+      const float4 *gv = reinterpret_cast<const float4 *>(ti.xv);
+      float4 *sq4 = reinterpret_cast<float4 *>(sq), *sk4 = reinterpret_cast<float4 *>(sk);
+      float4 *sv4 = reinterpret_cast<float4 *>(sv);
+      constexpr int kU = 4;
+      for (int base = threadIdx.x; base < total; base += kU * blockDim.x) {
+        float4 val[kU];
+        float4 *dst[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int idx = base + u * blockDim.x;
-        dst[u] = nullptr;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) xin[u][j] = w[u][j] = 0.0f;
-        if (idx < nt * nch) {
-          const int tt = idx / nch, c = idx % nch;
-          const int t = t0 + tt;
-          const IO *src;
-          size_t stride;
-          int ch;
-          if (c < dk) {
-            src = xq + hq * dk + c; stride = (size_t)h_qk * dk; ch = hq * dk + c; dst[u] = sq + tt * dk + c;
-          } else if (c < 2 * dk) {
-            const int cc = c - dk;
-            src = xk + hq * dk + cc; stride = (size_t)h_qk * dk; ch = h_qk * dk + hq * dk + cc;
-            dst[u] = sk + tt * dk + cc;
-          } else {
-            const int cc = c - 2 * dk;
-            src = xv + h * dv + cc; stride = (size_t)h_v * dv; ch = 2 * h_qk * dk + h * dv + cc;
-            dst[u] = sv + tt * dv + cc;
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int tau = t - 3 + j;
-            w[u][j] = p.conv_w[ch * 4 + j];
-            if (tau >= s0)
-              xin[u][j] = to_f(src[(size_t)tau * stride]);
-            else if (hist)  // the carried input of token tau = s0 - 3 + m sits at m (oldest first)
-              xin[u][j] = to_f(hist[((size_t)n * Cc + ch) * 3 + (tau - s0 + 3)]);
+        for (int u = 0; u < kU; ++u) {
+          const int idx = base + u * blockDim.x;
+          dst[u] = nullptr;
+          if (idx < total) {
+            const int tt = idx / per_tok, c = idx % per_tok;
+            const size_t t = (size_t)(t0 + tt);
+            if (c < nq) {
+              val[u] = gq[(t * h_qk + hq) * nq + c];
+              dst[u] = sq4 + tt * nq + c;
+            } else if (c < 2 * nq) {
+              val[u] = gk[(t * h_qk + hq) * nq + c - nq];
+              dst[u] = sk4 + tt * nq + c - nq;
+            } else {
+              val[u] = gv[(t * h_v + h) * nv + c - 2 * nq];
+              dst[u] = sv4 + tt * nv + c - 2 * nq;
+            }
           }
         }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (dst[u]) *dst[u] = val[u];
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-        if (dst[u]) {
-          float pre = 0.0f;  // a tap with no input (before s0, no history) adds w * 0
-#pragma unroll
-          for (int j = 0; j < 4; ++j) pre = fmaf(w[u][j], xin[u][j], pre);
-          *dst[u] = silu_f(pre);
-        }
-    }
-    for (int tt = threadIdx.x; tt < nt; tt += blockDim.x) {
-      const size_t t = (size_t)(t0 + tt);
-      salpha[tt] = expf(gate_g(to_f(xa[t * h_v + h]), A_exp, dtb));
-      sbeta[tt] = sigmoid_f(to_f(xb[t * h_v + h]));
-    }
-    __syncthreads();
-    // L2-normalise the q and k rows (one warp per row)
-    for (int row = warp; row < 2 * nt; row += nwarps) {
-      float *x = row < nt ? sq + row * dk : sk + (row - nt) * dk;
-      float ss = 0.0f;
-      for (int i = lane; i < dk; i += 32) ss = fmaf(x[i], x[i], ss);
-      const float inv = rsqrtf(warp_sum(ss) + kEpsL2);
-      for (int i = lane; i < dk; i += 32) x[i] *= inv;
+      for (int tt = threadIdx.x; tt < nt; tt += blockDim.x) {
+        salpha[tt] = ti.xal[(size_t)(t0 + tt) * h_v + h];
+        sbeta[tt] = ti.xbe[(size_t)(t0 + tt) * h_v + h];
+      }
     }
     __syncthreads();
     // the rule, token by token, on this warp's columns
@@ -205,28 +173,36 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
 
 }  // namespace
 
+size_t prefill_simt_workspace_bytes(int T, int h_qk, int h_v, int d_k, int d_v) {
+  return token_inputs_bytes(T, h_qk, h_v, d_k, d_v);
+}
+
 cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t s) {
   const int warps = (p.d_v + kCW - 1) / kCW;
   const int threads = 32 * warps;
   const size_t smem = sizeof(float) * (size_t)(kTB * (2 * p.d_k + 2 * p.d_v) + 2 * kTB);
   const unsigned grid = (unsigned)p.N * (unsigned)p.h_v;
   if (grid == 0) return cudaSuccess;
-  if (bf16) {
-    auto kern = prefill_simt_kernel<__nv_bfloat16>;
+  if (p.ws_bytes < prefill_simt_workspace_bytes(p.T, p.h_qk, p.h_v, p.d_k, p.d_v)) return cudaErrorInvalidValue;
+  TokenInputs ti{};
+  ti.q = p.q; ti.k = p.k; ti.v = p.v; ti.a = p.a; ti.b = p.b;
+  ti.conv_w = p.conv_w; ti.A_log = p.A_log; ti.dt_bias = p.dt_bias; ti.cu_seqlens = p.cu_seqlens;
+  ti.init_conv = p.init_conv;
+  ti.T = p.T; ti.N = p.N; ti.h_qk = p.h_qk; ti.h_v = p.h_v; ti.d_k = p.d_k; ti.d_v = p.d_v;
+  token_inputs_carve(ti, p.ws);
+  const unsigned irows =
+      (unsigned)(((size_t)p.T * (2 * p.h_qk + p.h_v) + kTokenRowsPerCta - 1) / kTokenRowsPerCta);
+  auto run = [&](auto in_k, auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     trace_begin(s, GDN_K_PREFILL_SIMT);
-    kern<<<grid, threads, smem, s>>>(p);
+    if (p.T > 0) in_k<<<irows, 32 * kTokenRowsPerCta, 0, s>>>(ti);
+    kern<<<grid, threads, smem, s>>>(p, ti);
     trace_end(s);
-  } else {
-    auto kern = prefill_simt_kernel<float>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    trace_begin(s, GDN_K_PREFILL_SIMT);
-    kern<<<grid, threads, smem, s>>>(p);
-    trace_end(s);
-  }
-  return cudaGetLastError();
+    return cudaGetLastError();
+  };
+  if (bf16) return run(token_inputs_kernel<__nv_bfloat16>, prefill_simt_kernel<__nv_bfloat16>);
+  return run(token_inputs_kernel<float>, prefill_simt_kernel<float>);
 }
 
 }  // namespace gdn
