@@ -2,13 +2,15 @@
 //
 // Serves fp32 streams (where a bf16 tensor-core operand would not meet a 1e-4
 // tolerance) and every supported shape other than the d = 128 bf16 case.
-// One CTA per (sequence, value head) chain.  The state H = S^T (d_k x d_v)
-// lives in registers: warp w owns columns [4w, 4w+4) of H, lane l owns rows
-// l, l+32, l+64, l+96.  Columns of H evolve independently under the rule
-// (p_j = H[:,j] . k, u_j = beta (v_j - alpha p_j), H[:,j] <- alpha H[:,j] + k u_j),
-// so each warp advances its columns through the whole sequence without
-// waiting for the others; only the RMSNormGated epilogue needs every column,
-// and it runs once per batch of kTB tokens.
+// Three launches: the per-token inputs once (token_inputs.cuh); then one CTA
+// per (sequence, value head, slice of 32 state columns) with the state
+// H = S^T (d_k x d_v) in registers: warp w owns columns [2w, 2w+2) of the
+// slice, lane l rows l, l+32, l+64, l+96.  Columns of H evolve independently
+// under the rule (p_j = H[:,j] . k, u_j = beta (v_j - alpha p_j),
+// H[:,j] <- alpha H[:,j] + k u_j), so each warp advances its columns through
+// the whole sequence without waiting for the others, writing o of every
+// token; the RMSNormGated, which needs whole rows, runs after, one warp per
+// (token, value head).
 #include "gdn_common.cuh"
 #include "../../include/gdn_trace.h"
 #include "gdn_internal.h"
@@ -17,19 +19,22 @@
 namespace gdn {
 namespace {
 
-constexpr int kTB = 32;      // tokens per prologue/epilogue batch
-constexpr int kCW = 4;       // state columns per warp (d_v / 4 warps: up to 1024 threads)
+constexpr int kTB = 32;      // tokens per batch of copied inputs
+constexpr int kCW = 2;       // state columns per warp
 constexpr int kColLanes = 32 / kCW;  // a reduce-scatter over the warp leaves column c in lane c kColLanes
 constexpr int kRows = 4;     // rows per lane (d_k <= 128)
+constexpr int kSliceCols = 32, kSliceWarps = kSliceCols / kCW, kSliceThreads = 32 * kSliceWarps;
 
+// One CTA per (chain, slice of kSliceCols state columns): the rule token by
+// token on the slice's columns, o (scaled) of every token to `wo`.
 template <typename IO>
-__global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillParams p, const TokenInputs ti) {
+__global__ void __launch_bounds__(kSliceThreads, 1) prefill_simt_kernel(PrefillParams p, const TokenInputs ti,
+                                                                     float *wo) {
   const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
-  const int n = blockIdx.x / h_v;
-  const int h = blockIdx.x % h_v;
-  const int hq = h / (h_v / h_qk);
+  const int slices = (dv + kSliceCols - 1) / kSliceCols;
+  const int sl = blockIdx.x % slices, chain = blockIdx.x / slices;
+  const int n = chain / h_v, h = chain % h_v, hq = h / (h_v / h_qk), jsl = kSliceCols * sl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
 
   const int s0 = p.cu_seqlens[n], s1 = p.cu_seqlens[n + 1];
   if (s0 < 0 || s1 < s0 || s1 > p.T) {
@@ -37,19 +42,15 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
     return;
   }
 
-  const IO *__restrict__ xz = static_cast<const IO *>(p.z);
-  IO *__restrict__ out = static_cast<IO *>(p.out);
-
   extern __shared__ __align__(16) float smem[];
-  float *sq = smem;               // [kTB][dk]
-  float *sk = sq + kTB * dk;      // [kTB][dk]
-  float *sv = sk + kTB * dk;      // [kTB][dv]
-  float *so = sv + kTB * dv;      // [kTB][dv]
-  float *salpha = so + kTB * dv;  // [kTB]
-  float *sbeta = salpha + kTB;    // [kTB]
+  float *sq = smem;                    // [kTB][dk]
+  float *sk = sq + kTB * dk;           // [kTB][dk]
+  float *sv = sk + kTB * dk;           // [kTB][kSliceCols]
+  float *salpha = sv + kTB * kSliceCols;  // [kTB]
+  float *sbeta = salpha + kTB;         // [kTB]
 
   const size_t state_off = ((size_t)n * h_v + h) * dk * dv;
-  const int j0 = warp * kCW;
+  const int j0 = jsl + warp * kCW;     // this warp's first column
   float H[kRows][kCW];
 #pragma unroll
   for (int r = 0; r < kRows; ++r)
@@ -58,18 +59,16 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
       const int i = lane + 32 * r, j = j0 + c;
       H[r][c] = (p.init_state && i < dk && j < dv) ? p.init_state[state_off + (size_t)i * dv + j] : 0.0f;
     }
-
   const float scale = rsqrtf((float)dk);
 
   for (int t0 = s0; t0 < s1; t0 += kTB) {
     const int nt = min(kTB, s1 - t0);
     __syncthreads();  // the previous batch's buffers are consumed
-    // the batch's inputs (q^, k^, silu(conv(v)), alpha, beta) from the token-inputs pass: float4 copies
-    // (head dims are multiples of 16), kU of them in flight per thread
+    // the batch's inputs (q^, k^, the slice's columns of silu(conv(v)), alpha, beta) from the token-inputs
+    // pass: float4 copies (head dims and slices are multiples of 16 floats), kU in flight per thread
     {
-      const int nq = dk / 4, nv = dv / 4, per_tok = 2 * nq + nv, total = nt * per_tok;
+      const int nq = dk / 4, nv = kSliceCols / 4, per_tok = 2 * nq + nv, total = nt * per_tok;
       const float4 *gq = reinterpret_cast<const float4 *>(ti.xq), *gk = reinterpret_cast<const float4 *>(ti.xk);
-      const float4 *gv = reinterpret_cast<const float4 *>(ti.xv);
       float4 *sq4 = reinterpret_cast<float4 *>(sq), *sk4 = reinterpret_cast<float4 *>(sk);
       float4 *sv4 = reinterpret_cast<float4 *>(sv);
       constexpr int kU = 4;
@@ -90,7 +89,9 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
               val[u] = gk[(t * h_qk + hq) * nq + c - nq];
               dst[u] = sk4 + tt * nq + c - nq;
             } else {
-              val[u] = gv[(t * h_v + h) * nv + c - 2 * nq];
+              const int j = jsl + 4 * (c - 2 * nq);
+              val[u] = j < dv ? *reinterpret_cast<const float4 *>(ti.xv + (t * h_v + h) * dv + j)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
               dst[u] = sv4 + tt * nv + c - 2 * nq;
             }
           }
@@ -119,10 +120,10 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
         float pc[kCW];
 #pragma unroll
         for (int c = 0; c < kCW; ++c) {
-          float s = 0.0f;
+          float s_ = 0.0f;
 #pragma unroll
-          for (int r = 0; r < kRows; ++r) s = fmaf(H[r][c], kr[r], s);
-          pc[c] = s;
+          for (int r = 0; r < kRows; ++r) s_ = fmaf(H[r][c], kr[r], s_);
+          pc[c] = s_;
         }
         {  // the warp's column sums together: reduce-scatter (lane l: column l / kColLanes), then broadcast
           const float ps = reduce_scatter<kCW>(pc, lane);
@@ -132,30 +133,19 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
         float oc[kCW];
 #pragma unroll
         for (int c = 0; c < kCW; ++c) {
-          const int j = j0 + c;
-          const float u = be * ((j < dv ? sv[tt * dv + j] : 0.0f) - al * pc[c]);
-          float s = 0.0f;
+          const int jj = warp * kCW + c;  // column within the slice
+          const float u = be * (sv[tt * kSliceCols + jj] - al * pc[c]);
+          float s_ = 0.0f;
 #pragma unroll
           for (int r = 0; r < kRows; ++r) {
             H[r][c] = fmaf(kr[r], u, al * H[r][c]);
-            s = fmaf(H[r][c], qr[r], s);
+            s_ = fmaf(H[r][c], qr[r], s_);
           }
-          oc[c] = s;
+          oc[c] = s_;
         }
         const float os = reduce_scatter<kCW>(oc, lane);  // lane l: column l / kColLanes
-        if (lane % kColLanes == 0 && j0 + lane / kColLanes < dv) so[tt * dv + j0 + lane / kColLanes] = os * scale;
-      }
-    }
-    __syncthreads();
-    // RMSNormGated epilogue (one warp per token)
-    for (int tt = warp; tt < nt; tt += nwarps) {
-      float ss = 0.0f;
-      for (int j = lane; j < dv; j += 32) ss = fmaf(so[tt * dv + j], so[tt * dv + j], ss);
-      const float inv = rsqrtf(warp_sum(ss) / (float)dv + kEpsRms);
-      const size_t row = ((size_t)(t0 + tt) * h_v + h) * dv;
-      for (int j = lane; j < dv; j += 32) {
-        const float y = so[tt * dv + j] * inv * p.norm_w[j] * silu_f(to_f(xz[row + j]));
-        out[row + j] = from_f<IO>(y);
+        if (lane % kColLanes == 0 && j0 + lane / kColLanes < dv)
+          wo[((size_t)(t0 + tt) * h_v + h) * dv + j0 + lane / kColLanes] = os * scale;
       }
     }
   }
@@ -171,17 +161,31 @@ __global__ void __launch_bounds__(32 * 128 / kCW) prefill_simt_kernel(PrefillPar
   }
 }
 
+// RMSNormGated, one warp per (token, value head) row, from o of every token.
+template <typename IO>
+__global__ void __launch_bounds__(256) simt_norm_kernel(const PrefillParams p, const float *wo) {
+  const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, dv = p.d_v;
+  if (row >= (size_t)p.T * p.h_v) return;
+  const float *o = wo + row * dv;
+  const IO *xz = static_cast<const IO *>(p.z) + row * dv;
+  IO *out = static_cast<IO *>(p.out) + row * dv;
+  float ss = 0.0f;
+  for (int j = lane; j < dv; j += 32) ss = fmaf(o[j], o[j], ss);
+  const float inv = rsqrtf(warp_sum(ss) / (float)dv + kEpsRms);
+  for (int j = lane; j < dv; j += 32) out[j] = from_f<IO>(o[j] * inv * p.norm_w[j] * silu_f(to_f(xz[j])));
+}
+
 }  // namespace
 
 size_t prefill_simt_workspace_bytes(int T, int h_qk, int h_v, int d_k, int d_v) {
-  return token_inputs_bytes(T, h_qk, h_v, d_k, d_v);
+  return token_inputs_bytes(T, h_qk, h_v, d_k, d_v) + (size_t)T * h_v * d_v * sizeof(float);
 }
 
 cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t s) {
-  const int warps = (p.d_v + kCW - 1) / kCW;
-  const int threads = 32 * warps;
-  const size_t smem = sizeof(float) * (size_t)(kTB * (2 * p.d_k + 2 * p.d_v) + 2 * kTB);
-  const unsigned grid = (unsigned)p.N * (unsigned)p.h_v;
+  const int slices = (p.d_v + kSliceCols - 1) / kSliceCols;
+  const size_t smem = sizeof(float) * (size_t)(kTB * (2 * p.d_k + kSliceCols) + 2 * kTB);
+  const unsigned grid = (unsigned)p.N * (unsigned)p.h_v * (unsigned)slices;
   if (grid == 0) return cudaSuccess;
   if (p.ws_bytes < prefill_simt_workspace_bytes(p.T, p.h_qk, p.h_v, p.d_k, p.d_v)) return cudaErrorInvalidValue;
   TokenInputs ti{};
@@ -190,19 +194,24 @@ cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t 
   ti.init_conv = p.init_conv;
   ti.T = p.T; ti.N = p.N; ti.h_qk = p.h_qk; ti.h_v = p.h_v; ti.d_k = p.d_k; ti.d_v = p.d_v;
   token_inputs_carve(ti, p.ws);
+  float *wo = reinterpret_cast<float *>(p.ws + token_inputs_bytes(p.T, p.h_qk, p.h_v, p.d_k, p.d_v));
   const unsigned irows =
       (unsigned)(((size_t)p.T * (2 * p.h_qk + p.h_v) + kTokenRowsPerCta - 1) / kTokenRowsPerCta);
-  auto run = [&](auto in_k, auto kern) -> cudaError_t {
+  const unsigned nrows = (unsigned)(((size_t)p.T * p.h_v + 7) / 8);
+  auto run = [&](auto in_k, auto kern, auto norm_k) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     trace_begin(s, GDN_K_PREFILL_SIMT);
     if (p.T > 0) in_k<<<irows, 32 * kTokenRowsPerCta, 0, s>>>(ti);
-    kern<<<grid, threads, smem, s>>>(p, ti);
+    kern<<<grid, kSliceThreads, smem, s>>>(p, ti, wo);
+    if (p.T > 0) norm_k<<<nrows, 256, 0, s>>>(p, wo);
     trace_end(s);
     return cudaGetLastError();
   };
-  if (bf16) return run(token_inputs_kernel<__nv_bfloat16>, prefill_simt_kernel<__nv_bfloat16>);
-  return run(token_inputs_kernel<float>, prefill_simt_kernel<float>);
+  if (bf16)
+    return run(token_inputs_kernel<__nv_bfloat16>, prefill_simt_kernel<__nv_bfloat16>,
+               simt_norm_kernel<__nv_bfloat16>);
+  return run(token_inputs_kernel<float>, prefill_simt_kernel<float>, simt_norm_kernel<float>);
 }
 
 }  // namespace gdn

@@ -29,7 +29,7 @@ typedef enum {
   GDN_K_CHUNK_TABLE = 0, /* varlen bookkeeping: chunk table from cu_seqlens */
   GDN_K_CHUNK_PREP = 1,  /* per-chunk conv, gates, intra-chunk WY/UT terms */
   GDN_K_STATE = 2,       /* sequential inter-chunk state pass + gated RMSNorm epilogue */
-  GDN_K_PREFILL_SIMT = 3,/* token-sequential fp32 prefill (small or fp32 shapes) */
+  GDN_K_PREFILL_SIMT = 3,/* token-sequential fp32 prefill (inputs, the rule per column slice, the norm: 3 launches) */
   GDN_K_DECODE = 4,      /* one-token decode step */
   GDN_K_BWD_CHAIN = 5,   /* backward: inputs, forward with checkpoints, RMSNorm and the rule in reverse (4 launches) */
   GDN_K_BWD_PROLOGUE = 6,/* backward: L2 norm, SiLU and conv in reverse */
