@@ -551,15 +551,20 @@ def headline_config(cfg, world):
             "parallelism": f"replicas x{world}"}
 
 
+# The sources of the chunked prefill's kernels (the ones the DRAM summary measures): its translation
+# unit and the headers it includes.
+PREFILL_TC_SOURCES = ("gateddeltanet_layer_gb300/csrc/prefill_tc.cu", "gateddeltanet_layer_gb300/csrc/tc_ptx.cuh",
+                      "gateddeltanet_layer_gb300/csrc/gdn_common.cuh", "gateddeltanet_layer_gb300/csrc/gdn_internal.h",
+                      "include/gdn.h", "include/gdn_trace.h")
+
+
 def _source_digest():
-    """sha256 over the library's CUDA sources (csrc/*.cu, *.cuh, *.h), in name order."""
+    """sha256 over the chunked prefill's sources (PREFILL_TC_SOURCES, in that order)."""
     import hashlib
-    csrc = os.path.join(ROOT, "gateddeltanet_layer_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in PREFILL_TC_SOURCES:
+        h.update(f.encode())
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()
 
 
