@@ -1,0 +1,75 @@
+"""A seeded sweep of small random workloads through the chunked prefill, the
+segment-parallel prefill and the carried-conv prefill, every chain against the
+oracle: random sequence counts and lengths (empty, 1-token, chunk-edge and
+multi-chunk sequences), q/k and value head counts (1 to 16 value heads per q/k
+head, so one or several chunk-prep groups and both state-pass forms), initial
+states present or not, the final state written over the initial one, and
+random segment lengths."""
+import numpy as np
+import pytest
+
+from gateddeltanet_layer_gb300 import synth
+from oracle import oracle as ref
+from tests.helpers import parity, to_torch
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+EDGE_LENGTHS = (0, 1, 2, 3, 63, 64, 65, 127, 128, 129)
+
+
+def _draw(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 7))
+    lengths = tuple(int(rng.choice(EDGE_LENGTHS)) if rng.random() < 0.5 else int(rng.integers(0, 400))
+                    for _ in range(n))
+    if sum(lengths) == 0:
+        lengths = lengths[:-1] + (70,)
+    h_qk = int(rng.choice([1, 2, 4]))
+    rep = int(rng.choice([1, 2, 3, 4, 8, 12, 16]))
+    init_std = float(rng.choice([0.0, 0.02]))
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=lengths, h_qk=h_qk, h_v=h_qk * rep, init_std=init_std,
+                       seed=1000 + seed)
+    return cfg, rng
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_workload(seed):
+    import gateddeltanet_layer_gb300 as gdn
+    gdn.library()
+    cfg, rng = _draw(seed)
+    inp = synth.make_prefill(cfg)
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"])
+    t = to_torch(inp, True)
+    args = (t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"], t["dt_bias"],
+            t["norm_w"], t["cu_seqlens"])
+    what = f"seed {seed} (lengths {cfg.lengths}, {cfg.h_qk}/{cfg.h_v} heads)"
+
+    # the chunked prefill; with an initial state, in place every other seed
+    init = t.get("init_state")
+    in_place = init is not None and seed % 2 == 0
+    out, fs = gdn.prefill(*args, None if init is None else init.clone() if not in_place else init,
+                          final_state=init if in_place else None)
+    torch.cuda.synchronize()
+    parity(out.float().cpu().numpy(), r["y"], "bf16", f"{what} out")
+    parity(fs.cpu().numpy(), r["final_state"], "bf16", f"{what} final_state")
+
+    # the segment-parallel prefill with a random segment length
+    seg = int(rng.choice([1, 2, 3, 5]))
+    init2 = None if inp["init_state"] is None else to_torch({"init_state": inp["init_state"]}, True)["init_state"]
+    out2, fs2 = gdn.prefill_segmented(*args, init2, seg_chunks=seg)
+    torch.cuda.synchronize()
+    parity(out2.float().cpu().numpy(), r["y"], "bf16", f"{what} segmented({seg}) out")
+    parity(fs2.cpu().numpy(), r["final_state"], "bf16", f"{what} segmented({seg}) final_state")
+
+    # the carried-conv prefill with a random conv history, against the oracle given the same history
+    Cc = 2 * cfg.h_qk * cfg.d_k + cfg.h_v * cfg.d_v
+    hist = synth.round_bf16(np.random.default_rng(seed + 500).standard_normal((cfg.N, Cc, 3)).astype(np.float32))
+    r3 = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], init_conv=hist)
+    init3 = None if inp["init_state"] is None else to_torch({"init_state": inp["init_state"]}, True)["init_state"]
+    out3, fs3, fc3 = gdn.prefill_carry(*args, init3, torch.from_numpy(hist).to("cuda", torch.bfloat16))
+    torch.cuda.synchronize()
+    parity(out3.float().cpu().numpy(), r3["y"], "bf16", f"{what} carry out")
+    parity(fs3.cpu().numpy(), r3["final_state"], "bf16", f"{what} carry final_state")
+    np.testing.assert_array_equal(fc3.float().cpu().numpy(),
+                                  ref.conv_cache_after_prefill(inp, inp["cu_seqlens"], init_conv=hist))
