@@ -4,7 +4,7 @@ oracle: random sequence counts and lengths (empty, 1-token, chunk-edge and
 multi-chunk sequences), q/k and value head counts (1 to 16 value heads per q/k
 head, so one or several chunk-prep groups and both state-pass forms), initial
 states present or not, the final state written over the initial one, and
-random segment lengths."""
+random segment lengths; and the backward on random small workloads."""
 import numpy as np
 import pytest
 
@@ -73,3 +73,42 @@ def test_random_workload(seed):
     parity(fs3.cpu().numpy(), r3["final_state"], "bf16", f"{what} carry final_state")
     np.testing.assert_array_equal(fc3.float().cpu().numpy(),
                                   ref.conv_cache_after_prefill(inp, inp["cu_seqlens"], init_conv=hist))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_backward(seed):
+    """The backward on random small workloads (head dims 16 to 128, 1 to 4
+    value heads per q/k head, bf16 or fp32 streams, with or without an initial
+    state and a final-state gradient), every gradient at the fp32 bar."""
+    import gateddeltanet_layer_gb300 as gdn
+    gdn.library()
+    rng = np.random.default_rng(seed + 200)
+    n = int(rng.integers(1, 4))
+    lengths = tuple(int(rng.choice(EDGE_LENGTHS)) if rng.random() < 0.5 else int(rng.integers(0, 150))
+                    for _ in range(n))
+    if sum(lengths) == 0:
+        lengths = lengths[:-1] + (40,)
+    d = int(rng.choice([16, 32, 128]))
+    h_qk = int(rng.choice([1, 2]))
+    rep = int(rng.choice([1, 2, 4]))
+    dtype = str(rng.choice(["bf16", "fp32"]))
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=lengths, h_qk=h_qk, h_v=h_qk * rep, d_k=d, d_v=d, dtype=dtype,
+                       init_std=float(rng.choice([0.0, 0.02])), seed=2000 + seed)
+    bf16 = dtype == "bf16"
+    inp = synth.make_prefill(cfg)
+    dy = rng.standard_normal((cfg.T, cfg.h_v, cfg.d_v)).astype(np.float32)
+    if bf16:
+        dy = synth.round_bf16(dy)
+    dfinal = rng.standard_normal((cfg.N, cfg.h_v, d, d)).astype(np.float32) if rng.random() < 0.5 else None
+    t = to_torch(inp, bf16)
+    g = gdn.prefill_backward(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                             t["dt_bias"], t["norm_w"], t["cu_seqlens"],
+                             torch.from_numpy(dy).to("cuda", torch.bfloat16 if bf16 else torch.float32),
+                             t.get("init_state"), None if dfinal is None else torch.from_numpy(dfinal).cuda())
+    torch.cuda.synchronize()
+    r = ref.prefill_backward(inp, inp["cu_seqlens"], dy, inp["init_state"], dfinal)
+    what = f"seed {seed} (lengths {lengths}, {h_qk}/{h_qk * rep} heads, d {d}, {dtype})"
+    for name, key in (("q", "x_q"), ("k", "x_k"), ("v", "x_v"), ("a", "a"), ("b", "b"), ("z", "z"),
+                      ("conv_w", "conv_w"), ("A_log", "A_log"), ("dt_bias", "dt_bias"), ("norm_w", "norm_w"),
+                      ("init_state", "init_state")):
+        parity(g[name].cpu().numpy(), r[key], "fp32", f"{what} d{name}")
