@@ -316,8 +316,10 @@ def time_backward(cfg, steps, warmup, dev, flush):
 
     import gateddeltanet_layer_gb300 as gdn
     inp = inputs_of(cfg)
-    t = _device_inputs(inp, dev)
-    dy = torch.randn((cfg.T, cfg.h_v, cfg.d_v), generator=torch.Generator().manual_seed(1)).to(dev, torch.bfloat16)
+    fp32 = cfg.dtype == "fp32"
+    t = _device_inputs(inp, dev, fp32)
+    dy = torch.randn((cfg.T, cfg.h_v, cfg.d_v), generator=torch.Generator().manual_seed(1)).to(
+        dev, torch.float32 if fp32 else torch.bfloat16)
     ws = torch.empty(gdn.prefill_backward_workspace_bytes(cfg.T, cfg.N, cfg.h_qk, cfg.h_v, cfg.d_k, cfg.d_v),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -669,9 +671,12 @@ def run_case(args):
     cfg = {**synth.CONFIGS, **PROFILE_CASES}[args.case]
     if isinstance(cfg, synth.DecodeConfig):
         r = time_decode(cfg, args.steps, args.warmup, dev, flush)
+    elif args.backward:
+        r = time_backward(cfg, args.steps, args.warmup, dev, flush)
     else:
         r = time_prefill(cfg, args.steps, args.warmup, dev, flush, seg_chunks=args.seg_chunks)
-    print(json.dumps({"case": args.case, "seg_chunks": args.seg_chunks, "ms": r["ms"]}), flush=True)
+    print(json.dumps({"case": args.case, "backward": args.backward, "seg_chunks": args.seg_chunks, "ms": r["ms"]}),
+          flush=True)
 
 
 def main():
@@ -685,6 +690,7 @@ def main():
                     help="run only this workload's GPU call")
     ap.add_argument("--seg-chunks", type=int, default=0,
                     help="with --case: time the segment-parallel prefill with segments of this many chunks")
+    ap.add_argument("--backward", action="store_true", help="with --case: time the backward of that prefill")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
