@@ -184,6 +184,41 @@ def test_bad_cu_seqlens_sets_device_status():
     assert gdn.workspace_status(ws) == 0  # reading clears it
 
 
+@pytest.mark.parametrize("path", ["segmented", "carry", "fp32"])
+def test_bad_cu_seqlens_sets_device_status_on_every_path(path):
+    """The same decreasing cu_seqlens through the segment-parallel prefill,
+    the carried-conv prefill (the chunk table and the conv-cache pass) and the
+    fp32 token-sequential prefill: each reports status 5 through its workspace."""
+    gdn = _gdn()
+    fp32 = path == "fp32"
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=(64, 64), h_qk=1, h_v=2, dtype="fp32" if fp32 else "bf16", seed=13)
+    inp = synth.make_prefill(cfg)
+    inp["cu_seqlens"] = np.array([0, 100, 64], dtype=np.int32)  # sequence 1 has negative length
+    t = to_torch(inp, not fp32)
+    args = (t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"], t["dt_bias"],
+            t["norm_w"], t["cu_seqlens"])
+    if path == "segmented":
+        nbytes = gdn.prefill_segmented_workspace_bytes(cfg.T, cfg.N, 1, 2, 128, 128, 1)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+        gdn.prefill_segmented(*args, seg_chunks=1, workspace=ws)
+    elif path == "carry":
+        ws = torch.zeros(gdn.prefill_workspace_bytes(cfg.T, cfg.N, 1, 2, 128, 128, True), dtype=torch.uint8,
+                         device="cuda")
+        _, _, fc = gdn.prefill_carry(*args, workspace=ws)
+    else:
+        ws = torch.zeros(gdn.prefill_workspace_bytes(cfg.T, cfg.N, 1, 2, 128, 128, False), dtype=torch.uint8,
+                         device="cuda")
+        gdn.prefill(*args, workspace=ws)
+    torch.cuda.synchronize()
+    assert gdn.workspace_status(ws) == 5
+    assert gdn.workspace_status(ws) == 0  # reading clears it
+    if path == "carry":  # the invalid sequence's conv history is zeros; the valid one's is its last 3 inputs
+        fcn = fc.float().cpu().numpy()
+        assert not fcn[1].any()
+        Cq = cfg.h_qk * cfg.d_k
+        np.testing.assert_array_equal(fcn[0, :Cq], inp["x_q"][97:100].reshape(3, Cq).T)
+
+
 def test_invalid_arguments_raise():
     gdn = _gdn()
     t = to_torch(synth.make_prefill(synth.scaled(synth.SINGLE_4K, lengths=(8,), h_qk=2, h_v=3)), True)
