@@ -184,11 +184,12 @@ def test_bad_cu_seqlens_sets_device_status():
     assert gdn.workspace_status(ws) == 0  # reading clears it
 
 
-@pytest.mark.parametrize("path", ["segmented", "carry", "fp32"])
+@pytest.mark.parametrize("path", ["segmented", "carry", "fp32", "backward"])
 def test_bad_cu_seqlens_sets_device_status_on_every_path(path):
     """The same decreasing cu_seqlens through the segment-parallel prefill,
-    the carried-conv prefill (the chunk table and the conv-cache pass) and the
-    fp32 token-sequential prefill: each reports status 5 through its workspace."""
+    the carried-conv prefill (the chunk table and the conv-cache pass), the
+    fp32 token-sequential prefill and the backward: each reports status 5
+    through its workspace."""
     gdn = _gdn()
     fp32 = path == "fp32"
     cfg = synth.scaled(synth.VARLEN_32K, lengths=(64, 64), h_qk=1, h_v=2, dtype="fp32" if fp32 else "bf16", seed=13)
@@ -205,10 +206,15 @@ def test_bad_cu_seqlens_sets_device_status_on_every_path(path):
         ws = torch.zeros(gdn.prefill_workspace_bytes(cfg.T, cfg.N, 1, 2, 128, 128, True), dtype=torch.uint8,
                          device="cuda")
         _, _, fc = gdn.prefill_carry(*args, workspace=ws)
-    else:
+    elif path == "fp32":
         ws = torch.zeros(gdn.prefill_workspace_bytes(cfg.T, cfg.N, 1, 2, 128, 128, False), dtype=torch.uint8,
                          device="cuda")
         gdn.prefill(*args, workspace=ws)
+    else:
+        ws = torch.zeros(gdn.prefill_backward_workspace_bytes(cfg.T, cfg.N, 1, 2, 128, 128), dtype=torch.uint8,
+                         device="cuda")
+        dy = torch.randn((cfg.T, 2, 128), generator=torch.Generator().manual_seed(3)).to("cuda", torch.bfloat16)
+        gdn.prefill_backward(*args, dy, workspace=ws)
     torch.cuda.synchronize()
     assert gdn.workspace_status(ws) == 5
     assert gdn.workspace_status(ws) == 0  # reading clears it
@@ -245,6 +251,43 @@ def test_kernel_trace_counts_each_launch():
         assert n == 2 and ms > 0, (name, n, ms)
     run_gpu(inp, True)
     assert gdn.trace_read() == {}
+
+
+def test_kernel_trace_of_the_other_paths():
+    """The trace of a segment-parallel prefill (chunk table, prep, the two
+    state passes, the segment table and scan), of an fp32 prefill (one record
+    around its three launches) and of a backward (one record around the
+    inputs, forward, norm and reverse kernels, one around the conv / norm
+    prologue), each with positive device times."""
+    gdn = _gdn()
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=(300, 70), h_qk=2, h_v=4, seed=15)
+    inp = synth.make_prefill(cfg)
+    t = to_torch(inp, True)
+    args = (t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"], t["dt_bias"],
+            t["norm_w"], t["cu_seqlens"])
+    gdn.trace_enable(True)
+    try:
+        gdn.trace_read()
+        gdn.prefill_segmented(*args, seg_chunks=2)
+        torch.cuda.synchronize()
+        rec = gdn.trace_read()
+        assert {k: v[0] for k, v in rec.items()} == {"chunk_table_kernel": 1, "chunk_prep_kernel": 1,
+                                                      "state_kernel": 2, "seg_scan_kernels": 2}, rec
+        assert all(v[1] > 0 for v in rec.values()), rec
+        f = to_torch(synth.make_prefill(synth.scaled(cfg, dtype="fp32")), False)
+        gdn.prefill(f["x_q"], f["x_k"], f["x_v"], f["a"], f["b"], f["z"], f["conv_w"], f["A_log"], f["dt_bias"],
+                    f["norm_w"], f["cu_seqlens"])
+        torch.cuda.synchronize()
+        rec = gdn.trace_read()
+        assert list(rec) == ["prefill_simt_kernel"] and rec["prefill_simt_kernel"][0] == 1, rec
+        dy = torch.randn((cfg.T, cfg.h_v, cfg.d_v), generator=torch.Generator().manual_seed(4)).to("cuda", torch.bfloat16)
+        gdn.prefill_backward(*args, dy)
+        torch.cuda.synchronize()
+        rec = gdn.trace_read()
+        assert {k: v[0] for k, v in rec.items()} == {"bwd_state_kernels": 1, "bwd_prologue_kernel": 1}, rec
+        assert all(v[1] > 0 for v in rec.values()), rec
+    finally:
+        gdn.trace_enable(False)
 
 
 def _segment(inp, cu, bounds):
