@@ -33,8 +33,8 @@ class Parity:
     full-size output can be compared sequence by sequence without holding the
     whole fp64 reference), then asserts the tolerances once."""
 
-    def __init__(self, dtype: str, what: str = ""):
-        self.dtype, self.what = dtype, what
+    def __init__(self, dtype: str, what: str = "", normwise: bool = False):
+        self.dtype, self.what, self.normwise = dtype, what, normwise
         self.max_rel = 0.0
         self.max_abs = 0.0
         self.max_abs_rounded = 0.0      # |g - bf16(r)|
@@ -53,7 +53,10 @@ class Parity:
             return self
         assert np.all(np.isfinite(g)), f"{self.what}: non-finite values"
         err = np.abs(g - r)
-        self.max_rel = max(self.max_rel, float(np.max(err / np.maximum(1.0, np.abs(r)))))
+        if self.normwise:  # relative to the tensor's largest magnitude (see parity_sum)
+            self.max_rel = max(self.max_rel, float(err.max()) / max(1.0, float(np.abs(r).max())))
+        else:
+            self.max_rel = max(self.max_rel, float(np.max(err / np.maximum(1.0, np.abs(r)))))
         self.max_abs = max(self.max_abs, float(err.max()))
         if self.dtype == "bf16":
             er = np.abs(g - _round_bf16(r))
@@ -85,6 +88,16 @@ class Parity:
 def parity(got, ref, dtype: str, what: str = ""):
     """Assert the per-tensor tolerances; returns (max_rel, rel_l2, max_abs)."""
     return Parity(dtype, what).add(got, ref).check()
+
+
+def parity_sum(got, ref, dtype: str, what: str = ""):
+    """The tolerances for a tensor each of whose elements is a sum over every
+    token and head (the parameter gradients): the max-abs measure is taken
+    relative to max(1, the tensor's largest |r|) instead of each element's own
+    |r|.  An element summed from n terms in fp32 carries an error of order
+    n * 2^-24 * sum |term|, which is of the tensor's scale, not of an element
+    that the signs of its terms cancel down; the rel-L2 bound is unchanged."""
+    return Parity(dtype, what, normwise=True).add(got, ref).check()
 
 
 def to_torch(inp: dict, bf16: bool, device="cuda"):
