@@ -115,3 +115,37 @@ def test_random_backward(seed):
                       ("init_state", "init_state")):
         check = parity_sum if name in ("conv_w", "A_log", "dt_bias", "norm_w") else parity
         check(g[name].cpu().numpy(), r[key], "fp32", f"{what} d{name}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("seed", range(6))
+def test_random_medium_workload(seed):
+    """Packed batches of 1 to 40 sequences of 0 to 2000 tokens at the graded
+    head counts (16/32 heads, d = 128, nonzero initial states): many chunk-prep
+    waves and several state-pass rounds, through the plain prefill and the
+    segment-parallel one with a random segment length, every chain against the
+    oracle."""
+    import os
+
+    import gateddeltanet_layer_gb300 as gdn
+    gdn.library()
+    rng = np.random.default_rng(seed + 5000)
+    n = int(rng.integers(1, 41))
+    lengths = tuple(int(x) for x in rng.integers(0, 2000, size=n))
+    if sum(lengths) == 0:
+        lengths = (100,)
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=lengths, init_std=0.02, seed=6000 + seed)
+    inp = synth.make_prefill(cfg)
+    t = to_torch(inp, True)
+    args = (t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"], t["dt_bias"],
+            t["norm_w"], t["cu_seqlens"], t["init_state"])
+    out, fs = gdn.prefill(*args)
+    seg = int(rng.integers(1, 17))
+    out2, fs2 = gdn.prefill_segmented(*args, seg_chunks=seg)
+    torch.cuda.synchronize()
+    r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"], threads=os.cpu_count())
+    what = f"seed {seed} ({n} sequences, {cfg.T} tokens)"
+    parity(out.float().cpu().numpy(), r["y"], "bf16", f"{what} out")
+    parity(fs.cpu().numpy(), r["final_state"], "bf16", f"{what} final_state")
+    parity(out2.float().cpu().numpy(), r["y"], "bf16", f"{what} segmented({seg}) out")
+    parity(fs2.cpu().numpy(), r["final_state"], "bf16", f"{what} segmented({seg}) final_state")
