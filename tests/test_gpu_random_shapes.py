@@ -4,7 +4,8 @@ oracle: random sequence counts and lengths (empty, 1-token, chunk-edge and
 multi-chunk sequences), q/k and value head counts (1 to 16 value heads per q/k
 head, so one or several chunk-prep groups and both state-pass forms), initial
 states present or not, the final state written over the initial one, and
-random segment lengths; and the backward on random small workloads."""
+random segment lengths; the backward and the decode step on random small
+workloads; and (slow) random medium packed batches at the graded head counts."""
 import numpy as np
 import pytest
 
@@ -149,3 +150,31 @@ def test_random_medium_workload(seed):
     parity(fs.cpu().numpy(), r["final_state"], "bf16", f"{what} final_state")
     parity(out2.float().cpu().numpy(), r["y"], "bf16", f"{what} segmented({seg}) out")
     parity(fs2.cpu().numpy(), r["final_state"], "bf16", f"{what} segmented({seg}) final_state")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_decode(seed):
+    """The decode step on random batches (1 to 300 sequences), q/k and value
+    head counts (1 to 16 value heads per q/k head), head dims (16 to 128, d_k
+    and d_v drawn apart) and stream dtypes: output and state against the
+    oracle, the conv cache exactly."""
+    import gateddeltanet_layer_gb300 as gdn
+    gdn.library()
+    rng = np.random.default_rng(seed + 7000)
+    h_qk = int(rng.choice([1, 2, 4, 16]))
+    rep = int(rng.choice([1, 2, 3, 8, 16]))
+    dtype = str(rng.choice(["bf16", "fp32"]))
+    cfg = synth.scaled(synth.DECODE_256, batch=int(rng.integers(1, 301)), h_qk=h_qk, h_v=h_qk * rep,
+                       d_k=int(rng.choice([16, 32, 64, 128])), d_v=int(rng.choice([16, 32, 64, 128])), dtype=dtype,
+                       seed=8000 + seed)
+    bf16 = dtype == "bf16"
+    inp = synth.make_decode(cfg)
+    t = to_torch(inp, bf16)
+    out = gdn.decode_step(t["x_q"], t["x_k"], t["x_v"], t["a"], t["b"], t["z"], t["conv_w"], t["A_log"],
+                          t["dt_bias"], t["norm_w"], t["conv_state"], t["state"])
+    torch.cuda.synchronize()
+    r = ref.decode_step(inp, inp["conv_state"], inp["state"])
+    what = f"seed {seed} (B {cfg.batch}, {h_qk}/{h_qk * rep} heads, d {cfg.d_k}/{cfg.d_v}, {dtype})"
+    parity(out.float().cpu().numpy(), r["y"], dtype, f"{what} out")
+    parity(t["state"].cpu().numpy(), r["state"], dtype, f"{what} state")
+    np.testing.assert_array_equal(t["conv_state"].float().cpu().numpy(), r["conv_state"])
