@@ -7,7 +7,7 @@ import pytest
 
 from gateddeltanet_layer_gb300 import synth
 from oracle import oracle as ref
-from tests.helpers import parity, to_torch
+from tests.helpers import parity, parity_sum, to_torch
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -127,3 +127,81 @@ def test_two_prefills_on_two_streams():
         r = ref.prefill(inp, inp["cu_seqlens"], inp["init_state"])
         parity(out.float().cpu().numpy(), r["y"], "bf16", "two streams out")
         parity(fs.cpu().numpy(), r["final_state"], "bf16", "two streams final_state")
+
+
+@pytest.mark.parametrize("path", ["segmented", "carry", "fp32", "backward"])
+def test_other_paths_replayed_from_a_cuda_graph(path):
+    """The segment-parallel prefill, the carried-conv prefill, the fp32 prefill
+    and the backward, each captured once with a caller-owned workspace and
+    replayed on new values copied into the captured tensors: each replay
+    equals the oracle on the values it saw."""
+    gdn = _gdn()
+    fp32 = path == "fp32"
+    cfg = synth.scaled(synth.VARLEN_32K, lengths=(200, 1, 97), h_qk=2, h_v=4, init_std=0.02,
+                       dtype="fp32" if fp32 else "bf16", seed=91)
+    sdt = torch.float32 if fp32 else torch.bfloat16
+    inp = synth.make_prefill(cfg)
+    t = to_torch(inp, not fp32)
+    Cc = 2 * cfg.h_qk * cfg.d_k + cfg.h_v * cfg.d_v
+    hist = torch.zeros((cfg.N, Cc, 3), dtype=sdt, device="cuda")
+    dy = torch.zeros((cfg.T, cfg.h_v, cfg.d_v), dtype=sdt, device="cuda")
+    if path == "segmented":
+        nbytes = gdn.prefill_segmented_workspace_bytes(cfg.T, cfg.N, cfg.h_qk, cfg.h_v, 128, 128, 2)
+    elif path == "backward":
+        nbytes = gdn.prefill_backward_workspace_bytes(cfg.T, cfg.N, cfg.h_qk, cfg.h_v, 128, 128, not fp32)
+    else:
+        nbytes = gdn.prefill_workspace_bytes(cfg.T, cfg.N, cfg.h_qk, cfg.h_v, 128, 128, not fp32)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((cfg.T, cfg.h_v, 128), dtype=sdt, device="cuda")
+    fs = torch.empty((cfg.N, cfg.h_v, 128, 128), dtype=torch.float32, device="cuda")
+    fc = torch.empty((cfg.N, Cc, 3), dtype=sdt, device="cuda")
+    res = {}
+
+    def call():
+        args = _prefill_args(t)
+        if path == "segmented":
+            gdn.prefill_segmented(*args, seg_chunks=2, out=out, final_state=fs, workspace=ws)
+        elif path == "carry":
+            gdn.prefill_carry(*args, hist, out=out, final_state=fs, final_conv=fc, workspace=ws)
+        elif path == "fp32":
+            gdn.prefill(*args, out=out, final_state=fs, workspace=ws)
+        else:
+            res["g"] = gdn.prefill_backward(*args[:-1], dy, args[-1], workspace=ws)
+
+    call()  # first call outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for seed in (92, 93):
+        new = synth.make_prefill(synth.scaled(cfg, seed=seed))
+        tn = to_torch(new, not fp32)
+        for key in ("x_q", "x_k", "x_v", "a", "b", "z", "init_state", "conv_w", "A_log", "dt_bias", "norm_w"):
+            t[key].copy_(tn[key])
+        rng = np.random.default_rng(seed)
+        h_new = synth.round_bf16(rng.standard_normal((cfg.N, Cc, 3)).astype(np.float32))
+        dy_new = rng.standard_normal((cfg.T, cfg.h_v, 128)).astype(np.float32)
+        if not fp32:
+            dy_new = synth.round_bf16(dy_new)
+        hist.copy_(torch.from_numpy(h_new))
+        dy.copy_(torch.from_numpy(dy_new))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gdn.workspace_status(ws) == 0
+        what = f"{path} graph replay {seed}"
+        if path == "backward":
+            r = ref.prefill_backward(new, new["cu_seqlens"], dy_new, new["init_state"])
+            g = res["g"]
+            for name, key in (("q", "x_q"), ("k", "x_k"), ("v", "x_v"), ("a", "a"), ("b", "b"), ("z", "z"),
+                              ("init_state", "init_state")):
+                parity(g[name].cpu().numpy(), r[key], "fp32", f"{what} d{name}")
+            for name in ("conv_w", "A_log", "dt_bias", "norm_w"):
+                parity_sum(g[name].cpu().numpy(), r[name], "fp32", f"{what} d{name}")
+            continue
+        r = ref.prefill(new, new["cu_seqlens"], new["init_state"], init_conv=h_new if path == "carry" else None)
+        dt = "fp32" if fp32 else "bf16"
+        parity(out.float().cpu().numpy(), r["y"], dt, f"{what} out")
+        parity(fs.cpu().numpy(), r["final_state"], dt, f"{what} final_state")
+        if path == "carry":
+            np.testing.assert_array_equal(fc.float().cpu().numpy(),
+                                          ref.conv_cache_after_prefill(new, new["cu_seqlens"], init_conv=h_new))
