@@ -109,9 +109,10 @@ struct BwdLayout {
 // The block's inputs into shared memory: q^, k^ and the slice's columns
 // [j0, j0 + kSliceCols) of silu(conv(v)) (zeros past d_v), alpha and beta, for
 // tokens [t0, t0 + nt), from the arrays token_inputs_kernel wrote.
-__device__ void block_prologue(const BwdParams &p, const BwdWs &ws, int h, int hq, int t0, int nt, int j0,
+__device__ __forceinline__ void block_prologue(const BwdParams &p, const BwdWs &ws, int dk, int h, int hq, int t0,
+                                               int nt, int j0,
                                float *sq, float *sk, float *sv, float *salpha, float *sbeta) {
-  const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
+  const int h_v = p.h_v, h_qk = p.h_qk, dv = p.d_v;
   // float4 copies (d_k, d_v and the row offsets are multiples of 16 floats), kU in flight per thread
   const int nq = dk / 4, nv = kSliceCols / 4, per_tok = 2 * nq + nv, total = nt * per_tok;
   const float4 *gq = reinterpret_cast<const float4 *>(ws.xq), *gk = reinterpret_cast<const float4 *>(ws.xk);
@@ -244,9 +245,9 @@ constexpr size_t slice_smem_floats(int dk) {
 }
 
 // Forward with checkpoints: the slice of the state at each block start, and o of every token.
-template <typename IO>
+template <typename IO, int DK>
 __global__ void __launch_bounds__(kSliceThreads) bwd_fwd_kernel(const BwdParams p, const BwdWs ws) {
-  const int h_v = p.h_v, dk = p.d_k, dv = p.d_v;
+  const int h_v = p.h_v, dk = DK ? DK : p.d_k, dv = p.d_v;
   const SliceCtx cx = slice_ctx(p, ws.slices);
   if (!cx.ok) {
     if (threadIdx.x == 0) set_status(p.status, kDevBadSeqlens);
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_fwd_kernel(const BwdParams 
     const int t0 = cx.s0 + kB * b, nt = min(kB, cx.s1 - t0);
     store_state(slice_ptr(ws.ckpt, ((size_t)(cx.slot0 + b) * h_v + cx.h) * ws.slices + cx.sl), H);
     __syncthreads();  // the previous block's shared memory is consumed
-    block_prologue(p, ws, cx.h, cx.hq, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta);
+    block_prologue(p, ws, dk, cx.h, cx.hq, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta);
     for (int tt = 0; tt < nt; ++tt)
       fwd_step(H, tt, dk, jw, dv - cx.j0, sq, sk, sv, salpha, sbeta, scale,
                ws.wo + ((size_t)(t0 + tt) * h_v + cx.h) * dv + cx.j0);
@@ -313,9 +314,9 @@ __global__ void __launch_bounds__(256) bwd_norm_kernel(const BwdParams p, const 
 }
 
 // The rule in reverse, per (chain, column slice).
-template <typename IO>
+template <typename IO, int DK>
 __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams p, const BwdWs ws) {
-  const int h_v = p.h_v, dk = p.d_k, dv = p.d_v;
+  const int h_v = p.h_v, dk = DK ? DK : p.d_k, dv = p.d_v;
   const SliceCtx cx = slice_ctx(p, ws.slices);
   if (!cx.ok) return;  // reported by the forward kernel
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, jw = kCW * warp;
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
   for (int b = cx.nblk - 1; b >= 0; --b) {
     const int t0 = cx.s0 + kB * b, nt = min(kB, cx.s1 - t0);
     __syncthreads();
-    block_prologue(p, ws, cx.h, cx.hq, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta);
+    block_prologue(p, ws, dk, cx.h, cx.hq, t0, nt, cx.j0, sq, sk, sv, salpha, sbeta);
     {  // do of the slice's columns, float4 copies (all of them in flight)
       constexpr int kQuads = kB * kSliceCols / 4, kPer = (kQuads + kSliceThreads - 1) / kSliceThreads;
       float4 dv4[kPer];
@@ -657,7 +658,13 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
   ti.init_conv = nullptr;  // the backward's forward starts every sequence from a zero conv history
   ti.T = p.T; ti.N = p.N; ti.h_qk = p.h_qk; ti.h_v = p.h_v; ti.d_k = p.d_k; ti.d_v = p.d_v;
   ti.xq = ws.xq; ti.xk = ws.xk; ti.xv = ws.xv; ti.xal = ws.xal; ti.xbe = ws.xbe;
-  auto run = [&](auto in_k, auto fwd_k, auto norm_k, auto rev_k, auto pro_k, auto gate_k) -> cudaError_t {
+  // the token-sequential kernels come in two forms: d_k = 128 fixed at compile time, and any d_k
+  auto run = [&](auto in_k, auto fwd_k128, auto fwd_k, auto norm_k, auto rev_k128, auto rev_k, auto pro_k,
+                 auto gate_k) -> cudaError_t {
+    if (p.d_k == 128) {
+      fwd_k = fwd_k128;
+      rev_k = rev_k128;
+    }
     cudaError_t err = cudaFuncSetAttribute(fwd_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(rev_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
@@ -682,10 +689,12 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
     return cudaGetLastError();
   };
   if (bf16)
-    return run(token_inputs_kernel<__nv_bfloat16>, bwd_fwd_kernel<__nv_bfloat16>, bwd_norm_kernel<__nv_bfloat16>,
-               bwd_rev_kernel<__nv_bfloat16>, bwd_prologue_kernel<__nv_bfloat16>, bwd_gate_kernel<__nv_bfloat16>);
-  return run(token_inputs_kernel<float>, bwd_fwd_kernel<float>, bwd_norm_kernel<float>, bwd_rev_kernel<float>,
-             bwd_prologue_kernel<float>, bwd_gate_kernel<float>);
+    return run(token_inputs_kernel<__nv_bfloat16>, bwd_fwd_kernel<__nv_bfloat16, 128>, bwd_fwd_kernel<__nv_bfloat16, 0>,
+               bwd_norm_kernel<__nv_bfloat16>, bwd_rev_kernel<__nv_bfloat16, 128>, bwd_rev_kernel<__nv_bfloat16, 0>,
+               bwd_prologue_kernel<__nv_bfloat16>, bwd_gate_kernel<__nv_bfloat16>);
+  return run(token_inputs_kernel<float>, bwd_fwd_kernel<float, 128>, bwd_fwd_kernel<float, 0>, bwd_norm_kernel<float>,
+             bwd_rev_kernel<float, 128>, bwd_rev_kernel<float, 0>, bwd_prologue_kernel<float>,
+             bwd_gate_kernel<float>);
 }
 
 }  // namespace gdn

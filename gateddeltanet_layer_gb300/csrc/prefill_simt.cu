@@ -26,11 +26,12 @@ constexpr int kRows = 4;     // rows per lane (d_k <= 128)
 constexpr int kSliceCols = 32, kSliceWarps = kSliceCols / kCW, kSliceThreads = 32 * kSliceWarps;
 
 // One CTA per (chain, slice of kSliceCols state columns): the rule token by
-// token on the slice's columns, o (scaled) of every token to `wo`.
-template <typename IO>
+// token on the slice's columns, o (scaled) of every token to `wo`.  DK: the
+// head dim d_k when it is fixed at compile time (128), else 0 (read from p).
+template <typename IO, int DK>
 __global__ void __launch_bounds__(kSliceThreads, 1) prefill_simt_kernel(PrefillParams p, const TokenInputs ti,
                                                                      float *wo) {
-  const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v;
+  const int h_v = p.h_v, h_qk = p.h_qk, dk = DK ? DK : p.d_k, dv = p.d_v;
   const int slices = (dv + kSliceCols - 1) / kSliceCols;
   const int sl = blockIdx.x % slices, chain = blockIdx.x / slices;
   const int n = chain / h_v, h = chain % h_v, hq = h / (h_v / h_qk), jsl = kSliceCols * sl;
@@ -198,7 +199,8 @@ cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t 
   const unsigned irows =
       (unsigned)(((size_t)p.T * (2 * p.h_qk + p.h_v) + kTokenRowsPerCta - 1) / kTokenRowsPerCta);
   const unsigned nrows = (unsigned)(((size_t)p.T * p.h_v + 7) / 8);
-  auto run = [&](auto in_k, auto kern, auto norm_k) -> cudaError_t {
+  auto run = [&](auto in_k, auto kern128, auto kern, auto norm_k) -> cudaError_t {
+    if (p.d_k == 128) kern = kern128;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     trace_begin(s, GDN_K_PREFILL_SIMT);
@@ -209,9 +211,10 @@ cudaError_t launch_prefill_simt(const PrefillParams &p, bool bf16, cudaStream_t 
     return cudaGetLastError();
   };
   if (bf16)
-    return run(token_inputs_kernel<__nv_bfloat16>, prefill_simt_kernel<__nv_bfloat16>,
-               simt_norm_kernel<__nv_bfloat16>);
-  return run(token_inputs_kernel<float>, prefill_simt_kernel<float>, simt_norm_kernel<float>);
+    return run(token_inputs_kernel<__nv_bfloat16>, prefill_simt_kernel<__nv_bfloat16, 128>,
+               prefill_simt_kernel<__nv_bfloat16, 0>, simt_norm_kernel<__nv_bfloat16>);
+  return run(token_inputs_kernel<float>, prefill_simt_kernel<float, 128>, prefill_simt_kernel<float, 0>,
+             simt_norm_kernel<float>);
 }
 
 }  // namespace gdn
