@@ -39,7 +39,8 @@
 // The slice layout: warp w owns columns [kCW w, kCW w + kCW) of the slice
 // (two, so that a token step's chain of dependent work per warp is short:
 // 16 warps per slice of 32 columns measured 8.2 ms on the 4096-token
-// workload, against 9.4 with 4 columns per warp and 10.9 with 8), lane l rows
+// workload, against 9.4 with 4 columns per warp and 10.9 with 8; 7.2 with the
+// head dim fixed at 128 at compile time), lane l rows
 // l, l+32, l+64, l+96.  Sums into one
 // value from several CTAs are atomic adds, so their rounding order is not
 // fixed from run to run: fp32 for the per-token q, k and gate gradients (a
