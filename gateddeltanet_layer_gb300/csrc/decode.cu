@@ -22,9 +22,10 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxRows = 16;  // d_k / kWarps for d_k <= 128
 
-template <typename IO>
+// D: the head dims when both are fixed at compile time (128), else 0 (read from p).
+template <typename IO, int D>
 __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
-  const int h_qk = p.h_qk, h_v = p.h_v, dk = p.d_k, dv = p.d_v;
+  const int h_qk = p.h_qk, h_v = p.h_v, dk = D ? D : p.d_k, dv = D ? D : p.d_v;
   const int rep = h_v / h_qk;
   const int b = blockIdx.x / h_qk;
   const int hq = blockIdx.x % h_qk;
@@ -244,10 +245,14 @@ cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s) {
   const unsigned grid = (unsigned)p.B * (unsigned)p.h_qk;
   if (grid == 0) return cudaSuccess;
   trace_begin(s, GDN_K_DECODE);
-  if (bf16)
-    decode_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(p);
-  else
-    decode_kernel<float><<<grid, kThreads, 0, s>>>(p);
+  const bool d128 = p.d_k == 128 && p.d_v == 128;
+  if (bf16) {
+    if (d128) decode_kernel<__nv_bfloat16, 128><<<grid, kThreads, 0, s>>>(p);
+    else decode_kernel<__nv_bfloat16, 0><<<grid, kThreads, 0, s>>>(p);
+  } else {
+    if (d128) decode_kernel<float, 128><<<grid, kThreads, 0, s>>>(p);
+    else decode_kernel<float, 0><<<grid, kThreads, 0, s>>>(p);
+  }
   trace_end(s);
   return cudaGetLastError();
 }
