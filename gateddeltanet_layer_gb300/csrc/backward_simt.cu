@@ -46,6 +46,8 @@
 // fixed from run to run: fp32 for the per-token q, k and gate gradients (a
 // few terms each), fp64 for the parameter gradients (conv_w, A_log, dt_bias,
 // norm_w: sums over every token and head, converted to fp32 at the end).
+#include <algorithm>
+
 #include "gdn_common.cuh"
 #include "../../include/gdn_trace.h"
 #include "gdn_internal.h"
@@ -283,35 +285,51 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_fwd_kernel(const BwdParams 
 template <typename IO>
 __global__ void __launch_bounds__(256) bwd_norm_kernel(const BwdParams p, const BwdWs ws) {
   const int dv = p.d_v, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ double snw[128];
-  for (int j = threadIdx.x; j < dv; j += blockDim.x) snw[j] = 0.0;
-  __syncthreads();
+  __shared__ double snw[8][128];
+  double acc[4] = {0.0, 0.0, 0.0, 0.0};  // this lane's dnorm_w terms, columns lane + 32 m (d_v <= 128)
   const size_t rows = (size_t)p.T * p.h_v;
-  const size_t rw = (size_t)blockIdx.x * 8 + warp;
-  if (rw < rows) {
+  // a grid of a few waves: each warp takes rows rw, rw + 8 gridDim.x, ... and keeps its dnorm_w sums in
+  // registers, so each CTA adds to the global sums once
+  for (size_t rw = (size_t)blockIdx.x * 8 + warp; rw < rows; rw += (size_t)gridDim.x * 8) {
     const IO *xz = static_cast<const IO *>(p.z) + rw * dv;
     const IO *gy = static_cast<const IO *>(p.dy) + rw * dv;
     const float *o = ws.wo + rw * dv;
     float ss = 0.0f, dot = 0.0f;
-    for (int j = lane; j < dv; j += 32) {
-      const float z = to_f(xz[j]);
-      ss = fmaf(o[j], o[j], ss);
-      dot = fmaf(to_f(gy[j]) * o[j], p.norm_w[j] * silu_f(z), dot);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int j = lane + 32 * m;
+      if (j < dv) {
+        const float z = to_f(xz[j]);
+        ss = fmaf(o[j], o[j], ss);
+        dot = fmaf(to_f(gy[j]) * o[j], p.norm_w[j] * silu_f(z), dot);
+      }
     }
     ss = warp_sum(ss);
     dot = warp_sum(dot);
     const float r = rsqrtf(ss / (float)dv + kEpsRms);
-    for (int j = lane; j < dv; j += 32) {
-      const float z = to_f(xz[j]), g = to_f(gy[j]);
-      const float s = sigmoid_f(z), silu = z * s, w = p.norm_w[j];
-      ws.wdo[rw * dv + j] = r * w * silu * g - o[j] * r * r * r * dot / (float)dv;
-      p.dz[rw * dv + j] = g * o[j] * r * w * s * (1.0f + z * (1.0f - s));
-      atomicAdd(&snw[j], (double)(g * o[j] * r * silu));
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int j = lane + 32 * m;
+      if (j < dv) {
+        const float z = to_f(xz[j]), g = to_f(gy[j]);
+        const float s = sigmoid_f(z), silu = z * s, w = p.norm_w[j];
+        ws.wdo[rw * dv + j] = r * w * silu * g - o[j] * r * r * r * dot / (float)dv;
+        p.dz[rw * dv + j] = g * o[j] * r * w * s * (1.0f + z * (1.0f - s));
+        acc[m] += (double)(g * o[j] * r * silu);
+      }
     }
   }
+#pragma unroll
+  for (int m = 0; m < 4; ++m)
+    if (lane + 32 * m < dv) snw[warp][lane + 32 * m] = acc[m];
   __syncthreads();
   double *acc_nw = ws.acc + (size_t)(2 * p.h_qk * p.d_k + p.h_v * dv) * 4 + 2 * p.h_v;
-  for (int j = threadIdx.x; j < dv; j += blockDim.x) atomicAdd(&acc_nw[j], snw[j]);
+  for (int j = threadIdx.x; j < dv; j += blockDim.x) {
+    double t = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += snw[w][j];
+    atomicAdd(&acc_nw[j], t);
+  }
 }
 
 // The rule in reverse, per (chain, column slice).
@@ -496,16 +514,6 @@ __global__ void __launch_bounds__(kSliceThreads) bwd_rev_kernel(const BwdParams 
   }
 }
 
-__device__ __forceinline__ float block_sum128(float v, float *red) {
-  v = warp_sum(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  const float s = red[0] + red[1] + red[2] + red[3];
-  __syncthreads();
-  return s;
-}
-
 constexpr int kTile = 64;
 
 // per (token tile, conv head): conv head y < h_qk is q head y, then the k
@@ -515,7 +523,6 @@ __global__ void __launch_bounds__(128) bwd_prologue_kernel(const BwdParams p, co
   const int h_v = p.h_v, h_qk = p.h_qk, dk = p.d_k, dv = p.d_v, rep = h_v / h_qk;
   const int t0 = blockIdx.x * kTile, y = blockIdx.y, c = threadIdx.x;
   __shared__ float sdp[kTile + 3][128];
-  __shared__ float red[4];
   const bool is_q = y < h_qk, is_k = !is_q && y < 2 * h_qk;
   const int D = (is_q || is_k) ? dk : dv;
   const int hq = is_q ? y : y - h_qk, hvv = y - 2 * h_qk;
@@ -537,33 +544,64 @@ __global__ void __launch_bounds__(128) bwd_prologue_kernel(const BwdParams p, co
   if (act)
 #pragma unroll
     for (int j = 0; j < 4; ++j) w[j] = p.conv_w[(size_t)(cb + c) * 4 + j];
-  // d pre of tokens [t0, t0 + kTile + 3) (the ones the tile's inputs feed)
-  for (int tt = 0; tt < kTile + 3; ++tt) {
-    const int t = t0 + tt;
-    if (t >= p.T) break;  // uniform over the CTA
-    const SeqOf sq = seq_of(p.cu_seqlens, p.N, t);
-    float pre = 0.0f;
-    if (act)
+  // d pre of tokens [t0, t0 + kTile + 3) (the ones the tile's inputs feed): one warp per token, lane l
+  // taking channels l + 32 m, so the L2 norm's two sums over the head are warp sums (no block barrier)
+  {
+    const int warp = c >> 5, lane = c & 31;
+    float wm[4][4];  // conv taps of this lane's channels
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int tau = t - 3 + j;
-        if (tau >= sq.s0) pre = fmaf(w[j], to_f(src[(size_t)tau * stride + c]), pre);
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wm[m][j] = lane + 32 * m < D ? p.conv_w[(size_t)(cb + lane + 32 * m) * 4 + j] : 0.f;
+    for (int tt = warp; tt < kTile + 3; tt += 4) {
+      const int t = t0 + tt;
+      if (t >= p.T) break;  // uniform over the warp
+      const SeqOf sq = seq_of(p.cu_seqlens, p.N, t);
+      float pre[4], xh[4], dsl[4];
+      float ss = 0.0f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        pre[m] = 0.0f;
+        if (ch < D)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int tau = t - 3 + j;
+            if (tau >= sq.s0) pre[m] = fmaf(wm[m][j], to_f(src[(size_t)tau * stride + ch]), pre[m]);
+          }
+        const float sg = sigmoid_f(pre[m]);
+        xh[m] = ch < D ? pre[m] * sg : 0.0f;
+        dsl[m] = sg * (1.0f + pre[m] * (1.0f - sg));
+        ss = fmaf(xh[m], xh[m], ss);
       }
-    const float s = sigmoid_f(pre), xh = pre * s, dsilu = s * (1.0f + pre * (1.0f - s));
-    float dxh;
-    if (is_q || is_k) {
-      const float *gsrc = is_q ? ws.dqn : ws.dkn;
-      float gsum = 0.0f;
-      if (act)
-        for (int r = 0; r < rep; ++r) gsum += gsrc[((size_t)t * h_v + hq * rep + r) * dk + c];
-      const float nrm = sqrtf(block_sum128(act ? xh * xh : 0.0f, red) + kEpsL2);
-      const float yv = xh / nrm;
-      const float yg = block_sum128(act ? yv * gsum : 0.0f, red);
-      dxh = (gsum - yv * yg) / nrm;
-    } else {
-      dxh = act ? ws.dvs[((size_t)t * h_v + hvv) * dv + c] : 0.0f;
+      float dxh[4];
+      if (is_q || is_k) {
+        const float *gsrc = is_q ? ws.dqn : ws.dkn;
+        float gsum[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int ch = lane + 32 * m;
+          gsum[m] = 0.0f;
+          if (ch < D)
+            for (int r = 0; r < rep; ++r) gsum[m] += gsrc[((size_t)t * h_v + hq * rep + r) * dk + ch];
+        }
+        const float nrm = sqrtf(warp_sum(ss) + kEpsL2);
+        float yg = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) yg = fmaf(xh[m] / nrm, gsum[m], yg);
+        yg = warp_sum(yg);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) dxh[m] = (gsum[m] - (xh[m] / nrm) * yg) / nrm;
+      } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int ch = lane + 32 * m;
+          dxh[m] = ch < D ? ws.dvs[((size_t)t * h_v + hvv) * dv + ch] : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) sdp[tt][lane + 32 * m] = lane + 32 * m < D ? dxh[m] * dsl[m] : 0.0f;
     }
-    sdp[tt][c] = act ? dxh * dsilu : 0.0f;
   }
   __syncthreads();
   if (!act) return;
@@ -648,7 +686,9 @@ cudaError_t launch_prefill_backward(const BwdParams &p, bool bf16, cudaStream_t 
   if ((e = cudaMemsetAsync(p.ws + L.dqn, 0, L.total - L.dqn, s)) != cudaSuccess) return e;
   const size_t smem = sizeof(float) * slice_smem_floats(p.d_k);
   const unsigned ctas = (unsigned)p.N * (unsigned)p.h_v * (unsigned)L.slices;
-  const unsigned rows = (unsigned)(((size_t)p.T * p.h_v + 7) / 8);
+  // the RMSNormGated reverse: 8 rows per CTA at a time, at most 8 CTAs per SM on 152 SMs (each CTA adds
+  // its dnorm_w sums once)
+  const unsigned rows = (unsigned)std::min<size_t>(((size_t)p.T * p.h_v + 7) / 8, (size_t)152 * 8);
   const dim3 pgrid((unsigned)((p.T + kTile - 1) / kTile), (unsigned)(2 * p.h_qk + p.h_v));
   const unsigned ggrid = (unsigned)(((size_t)p.T * p.h_v + 255) / 256);
   const unsigned irows =
