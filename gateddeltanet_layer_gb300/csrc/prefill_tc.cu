@@ -359,11 +359,13 @@ __device__ __forceinline__ void l2norm_rows(float (&y)[8][4], int lane) {
 // upmap: the U' images as [slot][256 rows][32] fp16 (slot = chunk x h_v + value head), 64-byte swizzle:
 // the staging's 16-byte chunk c of row m sits at c ^ ((m >> 1) & 3), the tensor memory accelerator's
 // 64-byte pattern, so one 3-D store writes a head's 16 KB.
+// NREP: the value heads per q/k head when fixed at compile time (2), else 0 (from p).
+template <int NREP>
 __global__ void __launch_bounds__(kPrepThreads, 2)
     chunk_prep_kernel(const PrefillParams p, const Ws ws, const __grid_constant__ CUtensorMap upmap) {
   // grid (chunk slots, q/k heads x value-head groups): a CTA takes up to kMaxRep of the value heads
   // of its q/k head (all of them unless h_v / h_qk > kMaxRep, where each group redoes the q/k part)
-  const int ngrp = (p.h_v / p.h_qk + kMaxRep - 1) / kMaxRep;
+  const int ngrp = NREP ? 1 : (p.h_v / p.h_qk + kMaxRep - 1) / kMaxRep;
   const int g = blockIdx.x, hq = blockIdx.y / ngrp, vbase = kMaxRep * (blockIdx.y % ngrp);
   tc::grid_dependency_wait();  // the chunk table
   tc::launch_dependents();     // the state pass may be scheduled once every prep CTA has started
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lr = tid & 127, gh = tid >> 7;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-  const int h_v = p.h_v, h_qk = p.h_qk, rep = h_v / h_qk, nrep = min(kMaxRep, rep - vbase);
+  const int h_v = p.h_v, h_qk = p.h_qk, rep = NREP ? NREP : h_v / h_qk, nrep = NREP ? NREP : min(kMaxRep, rep - vbase);
   const bool qk_images = vbase == 0;  // the group that writes the per-q/k-head images
   // TMEM: the 256-column W / U' accumulator at column 0; K K^T and Q K^T (64
   // columns) under it when the value heads come as one pair (their A is taken
@@ -2121,7 +2123,9 @@ cudaError_t launch_table_and_prep(const PrefillParams &p, const Ws &ws, cudaStre
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.T > 0) {
-    e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+    // the common two value heads per q/k head with its head counts fixed at compile time
+    auto prep = p.h_v == 2 * p.h_qk ? chunk_prep_kernel<2> : chunk_prep_kernel<0>;
+    e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ws.max_chunks, (unsigned)(p.h_qk * ((p.h_v / p.h_qk + kMaxRep - 1) / kMaxRep)));
@@ -2139,7 +2143,7 @@ cudaError_t launch_table_and_prep(const PrefillParams &p, const Ws &ws, cudaStre
                      ws.compact ? kCSlot : kVSlot))
       return cudaErrorInvalidValue;
     trace_begin(s, GDN_K_CHUNK_PREP);
-    e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel, p, ws, upmap);
+    e = cudaLaunchKernelEx(&cfg, prep, p, ws, upmap);
     trace_end(s);
   }
   return e;
