@@ -44,7 +44,8 @@ def _check_backward(cfg, with_dfinal=True, slow_decay=False):
         check(g[name].cpu().numpy(), r[key], "fp32", f"d{name}")
 
 
-@pytest.mark.parametrize("case", ["tiny_fp32", "bf16_d128_varlen", "fp32_d32_gqa4", "bf16_slow_decay"])
+@pytest.mark.parametrize("case", ["tiny_fp32", "bf16_d128_varlen", "fp32_d32_gqa4", "bf16_slow_decay",
+                                  "bf16_dk128_dv64", "fp32_dk64_dv128"])
 def test_backward_matches_oracle(case):
     if case == "tiny_fp32":
         cfg = synth.scaled(synth.TINY, init_std=0.05)
@@ -56,9 +57,17 @@ def test_backward_matches_oracle(case):
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(70, 5), h_qk=1, h_v=4, d_k=32, d_v=32, dtype="fp32",
                            init_std=0.02, seed=62)
         _check_backward(cfg, with_dfinal=False)
-    else:
+    elif case == "bf16_slow_decay":
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(160,), h_qk=1, h_v=2, init_std=0.02, seed=63)
         _check_backward(cfg, slow_decay=True)
+    elif case == "bf16_dk128_dv64":          # the d_k = 128 forms of the forward and reverse kernels, 2 slices
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(100, 37), h_qk=1, h_v=2, d_k=128, d_v=64, init_std=0.02,
+                           seed=64)
+        _check_backward(cfg)
+    else:                                    # their general forms with d_v = 128 (4 slices)
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(70,), h_qk=1, h_v=2, d_k=64, d_v=128, dtype="fp32",
+                           init_std=0.02, seed=65)
+        _check_backward(cfg)
 
 
 @pytest.mark.slow

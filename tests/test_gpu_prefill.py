@@ -51,7 +51,8 @@ def test_tiny_fp32_config():
 
 
 @pytest.mark.parametrize("case", ["ragged_single", "varlen_edges", "long_memory", "gqa4", "gqa8", "gqa12", "gqa16",
-                                  "fp32_d128", "gqa1", "gqa3", "chunk_edges", "fast_decay"])
+                                  "fp32_d128", "gqa1", "gqa3", "chunk_edges", "fast_decay", "bf16_dk128_dv64",
+                                  "fp32_dk64_dv128"])
 def test_small_cases(case):
     if case == "ragged_single":      # several chunks plus a ragged tail
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(200,), h_qk=2, h_v=4)
@@ -76,6 +77,11 @@ def test_small_cases(case):
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(70, 130), h_qk=1, h_v=12, init_std=0.02, seed=13)
     elif case == "gqa16":            # two groups of 8 value heads per q/k head
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(70,), h_qk=1, h_v=16, seed=9)
+    elif case == "bf16_dk128_dv64":  # the token-sequential kernel's d_k = 128 form with two 32-column slices
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(90, 41), h_qk=1, h_v=2, d_k=128, d_v=64, init_std=0.02, seed=14)
+    elif case == "fp32_dk64_dv128":  # its general form with four slices
+        cfg = synth.scaled(synth.SINGLE_4K, lengths=(77,), h_qk=2, h_v=4, d_k=64, d_v=128, dtype="fp32",
+                           init_std=0.02, seed=15)
     else:                            # fp32 streams at d = 128 (token-sequential fp32 kernel)
         cfg = synth.scaled(synth.SINGLE_4K, lengths=(130, 7), h_qk=1, h_v=2, dtype="fp32", init_std=0.02)
     inp = synth.make_prefill(cfg)
