@@ -70,3 +70,19 @@ def test_reference_arm_prints_one_line():
     assert d["ms_per_step"] > 0 and "chains" in d["cpu_baseline"]["sample"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("name", ["LONG_128K", "VARLEN_32K", "SINGLE_4K"])
+def test_dram_summaries_match_the_sources(name):
+    """Each committed DRAM-traffic summary the bench reports from was taken on
+    the chunked prefill's current sources (its sha256 over them matches), its
+    kernels add up to the call and the traffic is at least the algorithmic
+    bytes; a change to those sources without a new capture fails here."""
+    sys.path.insert(0, ROOT)
+    import bench
+    cfg = getattr(bench.synth, name)
+    tr = bench.profiled_traffic(cfg)
+    assert tr is not None, f"profiles/dram_{cfg.name}.md is missing or was taken on other sources"
+    assert sum(tr["kernels"].values()) == tr["call"]
+    nbytes, _ = bench.prefill_work(cfg)
+    assert tr["call"] >= nbytes
