@@ -50,10 +50,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
   IO *__restrict__ cache = static_cast<IO *>(p.conv_state);
   IO *__restrict__ out = static_cast<IO *>(p.out);
 
-  __shared__ float sq[128], sk[128], sv[128], su[128], so[128];
-  __shared__ float red_p[kWarps][128], red_s[kWarps][128];
-  __shared__ float sred[kWarps];
-  __shared__ float s_kq, s_alpha, s_beta, s_inv;
+  // per value head, two buffers by head parity: a head's buffer is written only after every thread has
+  // passed the previous head's second barrier, so every read of it two heads back is done (no barrier
+  // at the end of a head)
+  __shared__ float sq[128], sk[128];
+  __shared__ float sv[2][128], su[2][128];
+  __shared__ float red_p[2][kWarps][128], red_s[2][kWarps][128];
+  __shared__ float sred[2][kWarps];
+  __shared__ float s_kq, s_alpha[2], s_beta[2];
 
   // conv with the cache + SiLU for the q and k channels of this head
   for (int c = tid; c < 2 * dk; c += kThreads) {
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
   const float scale = rsqrtf((float)dk);
 
   for (int vv = 0; vv < rep; ++vv) {
-    const int h = hq * rep + vv;
+    const int h = hq * rep + vv, bf = vv & 1;
     float *Hg = p.state + ((size_t)sb * h_v + h) * dk * dv;
     // issue the state loads first: they are the stream this kernel exists for
     float4 Hr[kMaxRows];
@@ -116,15 +120,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
       cc[0] = cc[1];
       cc[1] = cc[2];
       cc[2] = xv[xi];
-      sv[j] = silu_f(pre);
+      sv[bf][j] = silu_f(pre);
     }
     if (tid == 0) {
       const size_t gi = (size_t)b * h_v + h;
-      s_alpha = expf(gate_g(to_f(xa[gi]), expf(p.A_log[h]), p.dt_bias[h]));
-      s_beta = sigmoid_f(to_f(xb[gi]));
+      s_alpha[bf] = expf(gate_g(to_f(xa[gi]), expf(p.A_log[h]), p.dt_bias[h]));
+      s_beta[bf] = sigmoid_f(to_f(xb[gi]));
     }
-    __syncthreads();
-    // partial H^T k and H^T q over this warp's rows
+    // partial H^T k and H^T q over this warp's rows (sv, alpha and beta are read after the next barrier)
     float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) {
@@ -139,42 +142,39 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
     if (col_ok) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        red_p[warp][j0 + c] = pk[c];
-        red_s[warp][j0 + c] = pq[c];
+        red_p[bf][warp][j0 + c] = pk[c];
+        red_s[bf][warp][j0 + c] = pq[c];
       }
     }
     __syncthreads();
-    const float al = s_alpha, be = s_beta;
+    const float al = s_alpha[bf], be = s_beta[bf];
     float o_j = 0.0f;
     if (tid < dv) {
       float pj = 0.f, sj = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        pj += red_p[w][tid];
-        sj += red_s[w][tid];
+        pj += red_p[bf][w][tid];
+        sj += red_s[bf][w][tid];
       }
-      const float u = be * (sv[tid] - al * pj);
-      su[tid] = u;
+      const float u = be * (sv[bf][tid] - al * pj);
+      su[bf][tid] = u;
       o_j = scale * fmaf(al, sj, s_kq * u);
-      so[tid] = o_j;
     }
-    // RMSNormGated needs sum_j o_j^2
+    // RMSNormGated needs sum_j o_j^2: the warps' sums, then each thread adds them up itself
     float ss = warp_sum(tid < dv ? o_j * o_j : 0.0f);
-    if (lane == 0) sred[warp] = ss;
-    __syncthreads();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < kWarps; ++w) t += sred[w];
-      s_inv = rsqrtf(t / (float)dv + kEpsRms);
-    }
+    if (lane == 0) sred[bf][warp] = ss;
     __syncthreads();
     if (tid < dv) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) t += sred[bf][w];
+      const float inv = rsqrtf(t / (float)dv + kEpsRms);
       const size_t oi = ((size_t)b * h_v + h) * dv + tid;
-      out[oi] = from_f<IO>(so[tid] * s_inv * p.norm_w[tid] * silu_f(to_f(xz[oi])));
+      out[oi] = from_f<IO>(o_j * inv * p.norm_w[tid] * silu_f(to_f(xz[oi])));
     }
     // H <- alpha H + k u^T, written back in place
     if (col_ok) {
-      const float u0 = su[j0], u1 = su[j0 + 1], u2 = su[j0 + 2], u3 = su[j0 + 3];
+      const float u0 = su[bf][j0], u1 = su[bf][j0 + 1], u2 = su[bf][j0 + 2], u3 = su[bf][j0 + 3];
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r) {
         const int i = i0 + r;
@@ -189,7 +189,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         }
       }
     }
-    __syncthreads();  // sv, su, so, red_* are reused by the next value head
   }
 }
 
